@@ -1,0 +1,254 @@
+/*
+ * Gated Residual (GR) oracle: the plain definition, in fp64, on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may call, link or load this file;
+ * only the tests, the smoke check and the bench's CPU-baseline leg use it. It shares no code
+ * with the CUDA library.
+ *
+ * Sources (page, section, equation):
+ *   "【论文解读】 Qwen3.8 Flash Next" (wkq9411.github.io), §二.4 Gated Residual:
+ *     eq rms      R̂_i = RMSNorm(R_i; γ_i)
+ *     eq gate     G = unvec σ(W_u SiLU((1/n_r) W_d vec R̂)),  W_d: r×n_r·d,  W_u: n_r·d×r
+ *     eq use_gate x = (1/n_r) Σ_i G_i ⊙ R̂_i
+ *     eq s        s = 2σ((1/n_r) W_w vec R̂),  W_w: n_r×n_r·d
+ *     eq write    R'_i = R_i + s_i y
+ *   "Qwen3.8-Flash-Next 架构笔记 · 06 / RESIDUAL" (cbphcr.github.io), §2 and §3 (same
+ *   formulas at n_r = 4).
+ * Readings where the pages leave a point open (eps placement, multiplicative gain,
+ * branch-major vec) are listed in the repository's SPEC file; eps is a parameter here.
+ *
+ * Layouts, all row-major:
+ *   R, R_out  [n][nb][D]      token, branch, channel
+ *   y, x      [n][D]
+ *   s         [n][nb]
+ *   gamma     [nb][D]
+ *   Wd        [r][nb*D]       vec index j = i*D + c (branches stacked)
+ *   Wu        [nb*D][r]
+ *   Ww        [nb][nb*D]
+ *   G (opt.)  [n][nb][D]      the read gates, for tests of eq auv
+ *   inv (opt.)[n][nb]         1/sqrt(mean(R_i^2) + eps)
+ *
+ * Every function loops over tokens independently (OpenMP over tokens when available).
+ * Return value: 0, or -1 on a bad argument, or -2 when scratch memory could not be had.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Logistic function 1/(1+e^{-a}), written so that neither branch overflows. */
+static double sigmoid(double a)
+{
+    if (a >= 0.0)
+        return 1.0 / (1.0 + exp(-a));
+    double e = exp(a);
+    return e / (1.0 + e);
+}
+
+/* SiLU(a) = a·σ(a) (the activation inside eq gate). */
+static double silu(double a) { return a * sigmoid(a); }
+
+/* Group RMSNorm of one token, eq rms: per branch i, inv_i = 1/sqrt(mean_c R_i[c]^2 + eps),
+ * Rh[i*D+c] = R_i[c] · inv_i · gamma_i[c]. */
+static void group_rmsnorm(int nb, int D, double eps, const double *R, const double *gamma,
+                          double *Rh, double *inv)
+{
+    for (int i = 0; i < nb; ++i) {
+        const double *Ri = R + (size_t)i * D;
+        double ss = 0.0;
+        for (int c = 0; c < D; ++c)
+            ss += Ri[c] * Ri[c];
+        double ms = ss / (double)D;
+        inv[i] = 1.0 / sqrt(ms + eps);
+        for (int c = 0; c < D; ++c)
+            Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];
+    }
+}
+
+/* The read of one token given its normalised state Rh (= vec R̂, length nb*D):
+ * eq gate, eq use_gate and eq s. h (length r) and g (length nb*D) are scratch. */
+static void read_from_normalised(int nb, int D, int r, const double *Rh, const double *Wd,
+                                 const double *Wu, const double *Ww, double *h, double *g,
+                                 double *x, double *s, double *G_out)
+{
+    const size_t K = (size_t)nb * D;
+    const double inv_nb = 1.0 / (double)nb;
+
+    /* z = (1/n_r) W_d vec R̂ ; h = SiLU(z) */
+    for (int k = 0; k < r; ++k) {
+        const double *w = Wd + (size_t)k * K;
+        double acc = 0.0;
+        for (size_t j = 0; j < K; ++j)
+            acc += w[j] * Rh[j];
+        h[k] = silu(inv_nb * acc);
+    }
+    /* G = unvec σ(W_u h) */
+    for (size_t j = 0; j < K; ++j) {
+        const double *w = Wu + j * (size_t)r;
+        double acc = 0.0;
+        for (int k = 0; k < r; ++k)
+            acc += w[k] * h[k];
+        g[j] = sigmoid(acc);
+    }
+    /* x = (1/n_r) Σ_i G_i ⊙ R̂_i */
+    for (int c = 0; c < D; ++c) {
+        double acc = 0.0;
+        for (int i = 0; i < nb; ++i)
+            acc += g[(size_t)i * D + c] * Rh[(size_t)i * D + c];
+        x[c] = inv_nb * acc;
+    }
+    /* s = 2σ((1/n_r) W_w vec R̂) */
+    for (int i = 0; i < nb; ++i) {
+        const double *w = Ww + (size_t)i * K;
+        double acc = 0.0;
+        for (size_t j = 0; j < K; ++j)
+            acc += w[j] * Rh[j];
+        s[i] = 2.0 * sigmoid(inv_nb * acc);
+    }
+    if (G_out)
+        memcpy(G_out, g, K * sizeof(double));
+}
+
+static int bad_dims(int64_t n, int nb, int D, int r)
+{
+    return n < 0 || nb < 1 || D < 1 || r < 1;
+}
+
+/* gr_read: eq rms → eq gate → eq use_gate, and eq s, for n tokens. */
+int gro_read(int64_t n, int nb, int D, int r, double eps, const double *R, const double *gamma,
+             const double *Wd, const double *Wu, const double *Ww, double *x, double *s,
+             double *G_out, double *inv_out)
+{
+    if (bad_dims(n, nb, D, r) || !R || !gamma || !Wd || !Wu || !Ww || !x || !s)
+        return -1;
+    const size_t K = (size_t)nb * D;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *Rh = malloc(K * sizeof(double));
+        double *g = malloc(K * sizeof(double));
+        double *h = malloc((size_t)r * sizeof(double));
+        double *inv = malloc((size_t)nb * sizeof(double));
+        if (!Rh || !g || !h || !inv) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < n; ++t) {
+                group_rmsnorm(nb, D, eps, R + (size_t)t * K, gamma, Rh, inv);
+                read_from_normalised(nb, D, r, Rh, Wd, Wu, Ww, h, g, x + (size_t)t * D,
+                                     s + (size_t)t * nb, G_out ? G_out + (size_t)t * K : NULL);
+                if (inv_out)
+                    memcpy(inv_out + (size_t)t * nb, inv, (size_t)nb * sizeof(double));
+            }
+        }
+        free(Rh);
+        free(g);
+        free(h);
+        free(inv);
+    }
+    return failed ? -2 : 0;
+}
+
+/* gr_write: eq write, R'_i = R_i + s_i y, for n tokens. R_out may equal R. */
+int gro_write(int64_t n, int nb, int D, const double *R, const double *y, const double *s,
+              double *R_out)
+{
+    if (n < 0 || nb < 1 || D < 1 || !R || !y || !s || !R_out)
+        return -1;
+    const size_t K = (size_t)nb * D;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        for (int i = 0; i < nb; ++i) {
+            const double si = s[(size_t)t * nb + i];
+            for (int c = 0; c < D; ++c) {
+                size_t e = (size_t)t * K + (size_t)i * D + c;
+                R_out[e] = R[e] + si * y[(size_t)t * D + c];
+            }
+        }
+    }
+    return 0;
+}
+
+/* gr_write_then_read: eq write with the previous sublayer's s, then the read of the next
+ * sublayer on the written state (kept in fp64, not rounded). */
+int gro_write_then_read(int64_t n, int nb, int D, int r, double eps, const double *R,
+                        const double *y, const double *s_prev, const double *gamma,
+                        const double *Wd, const double *Wu, const double *Ww, double *R_out,
+                        double *x, double *s_next)
+{
+    int st = gro_write(n, nb, D, R, y, s_prev, R_out);
+    if (st)
+        return st;
+    return gro_read(n, nb, D, r, eps, R_out, gamma, Wd, Wu, Ww, x, s_next, NULL, NULL);
+}
+
+/* The combine of eq use_gate with the gates given instead of predicted:
+ * x = (1/n_r) Σ_i G_i ⊙ RMSNorm(R_i; γ_i). G is [nb][D], the same for every token. */
+int gro_read_fixed_gates(int64_t n, int nb, int D, double eps, const double *R,
+                         const double *gamma, const double *G, double *x)
+{
+    if (n < 0 || nb < 1 || D < 1 || !R || !gamma || !G || !x)
+        return -1;
+    const size_t K = (size_t)nb * D;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *Rh = malloc(K * sizeof(double));
+        double *inv = malloc((size_t)nb * sizeof(double));
+        if (!Rh || !inv) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < n; ++t) {
+                group_rmsnorm(nb, D, eps, R + (size_t)t * K, gamma, Rh, inv);
+                for (int c = 0; c < D; ++c) {
+                    double acc = 0.0;
+                    for (int i = 0; i < nb; ++i)
+                        acc += G[(size_t)i * D + c] * Rh[(size_t)i * D + c];
+                    x[(size_t)t * D + c] = acc / (double)nb;
+                }
+            }
+        }
+        free(Rh);
+        free(inv);
+    }
+    return failed ? -2 : 0;
+}
+
+/* Single-stream residual add x += y (the bandwidth reference path), n elements. */
+int gro_residual_add(int64_t n, const double *y, double *x)
+{
+    if (n < 0 || !y || !x)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < n; ++e)
+        x[e] += y[e];
+    return 0;
+}
+
+/* Number of threads the parallel loops above use (1 without OpenMP). */
+int gro_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Set the thread count of the parallel loops (no-op without OpenMP). */
+void gro_set_num_threads(int k)
+{
+#ifdef _OPENMP
+    if (k > 0)
+        omp_set_num_threads(k);
+#else
+    (void)k;
+#endif
+}

@@ -1,0 +1,178 @@
+"""ctypes binding of the fp64 C oracle (gr_oracle.c). Test infrastructure only."""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gr_oracle.c")
+_SO = os.path.join(_HERE, "libgr_oracle.so")
+_LOCK = threading.Lock()
+_LIB = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gr_oracle.c into a shared library beside it (gcc, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load(path: str) -> ctypes.CDLL:
+    L = ctypes.CDLL(path)
+    P = ctypes.POINTER(ctypes.c_double)
+    i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    L.gro_read.argtypes = [i64, i32, i32, i32, f64, P, P, P, P, P, P, P, P, P]
+    L.gro_write.argtypes = [i64, i32, i32, P, P, P, P]
+    L.gro_write_then_read.argtypes = [i64, i32, i32, i32, f64, P, P, P, P, P, P, P, P, P, P]
+    L.gro_read_fixed_gates.argtypes = [i64, i32, i32, f64, P, P, P, P]
+    L.gro_residual_add.argtypes = [i64, P, P]
+    L.gro_num_threads.argtypes = []
+    L.gro_set_num_threads.argtypes = [i32]
+    L.gro_set_num_threads.restype = None
+    for f in ("gro_read", "gro_write", "gro_write_then_read", "gro_read_fixed_gates",
+              "gro_residual_add", "gro_num_threads"):
+        getattr(L, f).restype = ctypes.c_int
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            build()
+            _LIB = _load(_SO)
+    return _LIB
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Run the functions of this module against another build of the oracle source (the
+    tests use it to check that deliberately broken copies fail the pins)."""
+    global _LIB
+    old = lib()
+    _LIB = _load(path)
+    try:
+        yield
+    finally:
+        _LIB = old
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _check(st: int, what: str) -> None:
+    if st != 0:
+        raise RuntimeError(f"oracle {what} failed with status {st}")
+
+
+def num_threads() -> int:
+    return int(lib().gro_num_threads())
+
+
+def set_num_threads(k: int) -> None:
+    lib().gro_set_num_threads(int(k))
+
+
+def read(R, gamma, w_down, w_up, w_write, eps: float = 1e-6, return_internals: bool = False):
+    """gr_read. R [n, nb, D] -> x [n, D], s [n, nb] (and G [n, nb, D], inv [n, nb])."""
+    R = _f64(R)
+    n, nb, D = R.shape
+    Wd = _f64(w_down)
+    r = Wd.shape[0]
+    gamma, Wu, Ww = _f64(gamma), _f64(w_up), _f64(w_write)
+    assert gamma.shape == (nb, D) and Wd.shape == (r, nb * D)
+    assert Wu.shape == (nb * D, r) and Ww.shape == (nb, nb * D)
+    x = np.empty((n, D))
+    s = np.empty((n, nb))
+    G = np.empty((n, nb, D)) if return_internals else None
+    inv = np.empty((n, nb)) if return_internals else None
+    _check(lib().gro_read(n, nb, D, r, float(eps), _p(R), _p(gamma), _p(Wd), _p(Wu), _p(Ww),
+                          _p(x), _p(s), _p(G), _p(inv)), "read")
+    if return_internals:
+        return x, s, G, inv
+    return x, s
+
+
+def write(R, y, s):
+    """gr_write. R' = R + s_i y for every branch i."""
+    R, y, s = _f64(R), _f64(y), _f64(s)
+    n, nb, D = R.shape
+    assert y.shape == (n, D) and s.shape == (n, nb)
+    out = np.empty_like(R)
+    _check(lib().gro_write(n, nb, D, _p(R), _p(y), _p(s), _p(out)), "write")
+    return out
+
+
+def write_then_read(R, y, s_prev, params: dict, eps: float = 1e-6):
+    """Fused step: the write with s_prev, then the read with ``params`` (keys gamma, w_down,
+    w_up, w_write). Returns (R', x, s_next); R' stays in fp64."""
+    R, y, s_prev = _f64(R), _f64(y), _f64(s_prev)
+    n, nb, D = R.shape
+    gamma, Wd, Wu, Ww = (_f64(params[k]) for k in ("gamma", "w_down", "w_up", "w_write"))
+    r = Wd.shape[0]
+    R_out = np.empty_like(R)
+    x = np.empty((n, D))
+    s = np.empty((n, nb))
+    _check(lib().gro_write_then_read(n, nb, D, r, float(eps), _p(R), _p(y), _p(s_prev),
+                                     _p(gamma), _p(Wd), _p(Wu), _p(Ww), _p(R_out), _p(x), _p(s)),
+           "write_then_read")
+    return R_out, x, s
+
+
+def read_fixed_gates(R, gamma, G, eps: float = 1e-6):
+    """x = (1/nb) sum_i G_i * RMSNorm(R_i; gamma_i) with given gates G [nb, D]."""
+    R, gamma, G = _f64(R), _f64(gamma), _f64(G)
+    n, nb, D = R.shape
+    assert gamma.shape == (nb, D) and G.shape == (nb, D)
+    x = np.empty((n, D))
+    _check(lib().gro_read_fixed_gates(n, nb, D, float(eps), _p(R), _p(gamma), _p(G), _p(x)),
+           "read_fixed_gates")
+    return x
+
+
+def residual_add(x, y):
+    """Single-stream x + y."""
+    x = _f64(x).copy()
+    y = _f64(y)
+    assert x.shape == y.shape
+    _check(lib().gro_residual_add(x.size, _p(y), _p(x)), "residual_add")
+    return x
+
+
+def chain(R0, ys, params_list, eps: float = 1e-6):
+    """A stack of sublayers: read with params_list[0], then for l = 1..L-1 the fused write of
+    y_{l-1} with s_{l-1} followed by the read with params_list[l], then the final write of
+    y_{L-1}. Returns the states before every read and after the last write (L+1 states,
+    fp64), the block inputs x_l and the write strengths s_l."""
+    L = len(params_list)
+    assert len(ys) == L
+    states = [_f64(R0)]
+    xs, ss = [], []
+    p0 = params_list[0]
+    x, s = read(states[0], p0["gamma"], p0["w_down"], p0["w_up"], p0["w_write"], eps)
+    xs.append(x)
+    ss.append(s)
+    for l in range(1, L):
+        R, x, s = write_then_read(states[-1], ys[l - 1], ss[-1], params_list[l], eps)
+        states.append(R)
+        xs.append(x)
+        ss.append(s)
+    states.append(write(states[-1], ys[L - 1], ss[-1]))
+    return states, xs, ss

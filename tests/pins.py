@@ -1,0 +1,301 @@
+"""Pins of the fp64 oracle: checks against facts fixed by the pages and by mathematics, none of
+which re-types the oracle's own loops.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees. They go through the
+``oracle`` package, so ``oracle.use_library`` can point them at a deliberately broken build
+(tests/test_oracle_mutants.py).
+
+Sources: "【论文解读】 Qwen3.8 Flash Next" (wkq9411.github.io) §二.2 (HC, eq block: the widened
+network equals Pre-Norm for static one-hot read/write), §二.4 (GatedNorm; GR eq rms, gate,
+use_gate, s, write), §二.6 (eq rcv, eq auv; branches exchangeable at init);
+"Qwen3.8-Flash-Next 架构笔记 · 06 / RESIDUAL" (cbphcr.github.io), two-branch example;
+"Residual" (rainlin-net.pages.dev) §2.2 Pre-Norm.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as Fnn
+
+import oracle
+from oracle import dense
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rel(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def _params(rng, nb, D, r, std=0.3, gamma_random=True):
+    gamma = (1.0 + 0.3 * rng.standard_normal((nb, D))) if gamma_random else np.ones((nb, D))
+    return {
+        "gamma": gamma,
+        "w_down": std * rng.standard_normal((r, nb * D)),
+        "w_up": std * rng.standard_normal((nb * D, r)),
+        "w_write": std * rng.standard_normal((nb, nb * D)),
+    }
+
+
+def _read(R, p, eps=1e-6, internals=False):
+    return oracle.read(R, p["gamma"], p["w_down"], p["w_up"], p["w_write"], eps,
+                       return_internals=internals)
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+
+
+def _torch_rmsnorm(u, gamma, eps):
+    """Textbook RMSNorm over the last axis (torch library routine)."""
+    return Fnn.rms_norm(_t(u), (u.shape[-1],), weight=_t(gamma), eps=eps).numpy()
+
+
+def _torch_gatednorm(u, gamma, W1, W2, eps):
+    """GatedNorm(u) = RMSNorm(u) ⊙ σ(W2 SiLU(W1 RMSNorm(u))), Digest §二.4, from torch ops."""
+    un = Fnn.rms_norm(_t(u), (u.shape[-1],), weight=_t(gamma), eps=eps)
+    gate = torch.sigmoid(Fnn.linear(Fnn.silu(Fnn.linear(un, _t(W1))), _t(W2)))
+    return (un * gate).numpy(), un.numpy()
+
+
+# ---------------------------------------------------------------------------------------------
+
+def pin_dense_bruteforce():
+    """Loop formulation (C) == matrix formulation (numpy) on tiny shapes, incl. n_r != 4."""
+    rng = np.random.default_rng(101)
+    for (n, nb, D, r, eps) in [(1, 1, 1, 1, 1e-6), (3, 2, 3, 2, 1e-6), (4, 4, 8, 3, 0.3),
+                               (2, 4, 17, 5, 1e-6), (5, 3, 16, 4, 1e-2), (2, 4, 32, 8, 0.0)]:
+        R = rng.standard_normal((n, nb, D)) * rng.uniform(0.1, 10, size=(1, nb, 1))
+        p = _params(rng, nb, D, r, std=0.5)
+        x, s = _read(R, p, eps)
+        x2, s2 = dense.read(R, p["gamma"], p["w_down"], p["w_up"], p["w_write"], eps)
+        assert _rel(x, x2) < 1e-12 and _rel(s, s2) < 1e-12, (n, nb, D, r)
+        y = rng.standard_normal((n, D))
+        assert _rel(oracle.write(R, y, s), dense.write(R, y, s)) < 1e-14
+
+
+def pin_zero_down_projection():
+    """W_d = 0 ⇒ z = 0 ⇒ h = SiLU(0) = 0 ⇒ every gate is σ(0) = 1/2 exactly, so
+    x = (1/(2 n_r)) Σ_i RMSNorm(R_i; γ_i) with RMSNorm from torch."""
+    rng = np.random.default_rng(102)
+    for nb in (4, 2):
+        n, D, r, eps = 5, 24, 4, 1e-6
+        R = rng.standard_normal((n, nb, D))
+        p = _params(rng, nb, D, r)
+        p["w_down"] = np.zeros_like(p["w_down"])
+        x, s, G, inv = _read(R, p, eps, internals=True)
+        assert np.all(G == 0.5)
+        expect = sum(_torch_rmsnorm(R[:, i, :], p["gamma"][i], eps) for i in range(nb)) / (2 * nb)
+        assert _rel(x, expect) < 1e-13
+
+
+def pin_zero_up_projection():
+    """W_u = 0 ⇒ G ≡ σ(0) = 1/2 whatever W_d does."""
+    rng = np.random.default_rng(103)
+    R = rng.standard_normal((3, 4, 16))
+    p = _params(rng, 4, 16, 3, std=2.0)
+    p["w_up"] = np.zeros_like(p["w_up"])
+    _, _, G, _ = _read(R, p, internals=True)
+    assert np.all(G == 0.5)
+
+
+def pin_zero_write_projection():
+    """W_w = 0 ⇒ s ≡ 2σ(0) = 1 exactly (eq s)."""
+    rng = np.random.default_rng(104)
+    R = rng.standard_normal((4, 4, 16))
+    p = _params(rng, 4, 16, 3)
+    p["w_write"] = np.zeros_like(p["w_write"])
+    _, s = _read(R, p)
+    assert np.all(s == 1.0)
+
+
+def pin_gatednorm_single_branch():
+    """n_r = 1: eq gate and eq use_gate collapse to GatedNorm (the 1/n_r factors are 1), and
+    eq s to 2σ(W_w RMSNorm(u)). Compared with torch's rms_norm/linear/silu/sigmoid."""
+    rng = np.random.default_rng(105)
+    n, D, r, eps = 6, 20, 5, 1e-6
+    u = rng.standard_normal((n, D)) * 3.0
+    p = _params(rng, 1, D, r, std=0.5)
+    x, s = _read(u[:, None, :], p, eps)
+    gn, un = _torch_gatednorm(u, p["gamma"][0], p["w_down"], p["w_up"], eps)
+    assert _rel(x, gn) < 1e-13
+    s_t = (2.0 * torch.sigmoid(Fnn.linear(_t(un), _t(p["w_write"])))).numpy()
+    assert _rel(s, s_t) < 1e-13
+
+
+def pin_replicated_branches():
+    """n_r = 4 copies of one stream u with equal gains and weights tiled over the branch
+    blocks: (1/n_r) W_d vec R̂ = W_1 R̂, every G_i = σ(W_2 h), so x = GatedNorm(u) and
+    s_j = 2σ(w_j · RMSNorm(u)). Fails if a 1/n_r is dropped or moved, or vec is mis-ordered."""
+    rng = np.random.default_rng(106)
+    n, D, r, eps, nb = 4, 12, 3, 1e-6, 4
+    u = rng.standard_normal((n, D)) * 2.0
+    gamma1 = 1.0 + 0.3 * rng.standard_normal(D)
+    W1 = 0.6 * rng.standard_normal((r, D))
+    W2 = 0.6 * rng.standard_normal((D, r))
+    w = 0.6 * rng.standard_normal((nb, D))
+    p = {"gamma": np.tile(gamma1, (nb, 1)), "w_down": np.tile(W1, (1, nb)),
+         "w_up": np.tile(W2, (nb, 1)), "w_write": np.tile(w, (1, nb))}
+    R = np.repeat(u[:, None, :], nb, axis=1)
+    x, s = _read(R, p, eps)
+    gn, un = _torch_gatednorm(u, gamma1, W1, W2, eps)
+    assert _rel(x, gn) < 1e-13
+    assert _rel(s, (2.0 * torch.sigmoid(Fnn.linear(_t(un), _t(w)))).numpy()) < 1e-13
+
+
+def pin_prenorm_reduction():
+    """One-hot read gates (G_0 = 1, others 0) with γ_0 = n_r·γ_pre and write strengths
+    (1, 0, 0, 0) turn a GR stack into the Pre-Norm residual x ← x + F(RMSNorm(x)) on branch 0
+    (Digest §二.2: static one-hot read, write e_0, identity mixing equals Pre-Norm; §二.4: GR
+    replaces the pre-norm). The reference loop uses torch's rms_norm."""
+    rng = np.random.default_rng(107)
+    n, D, nb, L, eps = 3, 16, 4, 6, 1e-6
+    gamma_pre = 1.0 + 0.2 * rng.standard_normal(D)
+    Ms = [rng.standard_normal((D, D)) / math.sqrt(D) for _ in range(L)]
+    x_pre = rng.standard_normal((n, D))
+    R = rng.standard_normal((n, nb, D))
+    R[:, 0, :] = x_pre
+    others = R[:, 1:, :].copy()
+    gamma = np.ones((nb, D))
+    gamma[0] = nb * gamma_pre
+    G = np.zeros((nb, D))
+    G[0] = 1.0
+    s = np.zeros((n, nb))
+    s[:, 0] = 1.0
+    for l in range(L):
+        xin = oracle.read_fixed_gates(R, gamma, G, eps)
+        R = oracle.write(R, xin @ Ms[l], s)
+        x_pre = x_pre + _torch_rmsnorm(x_pre, gamma_pre, eps) @ Ms[l]
+    assert _rel(R[:, 0, :], x_pre) < 1e-13
+    assert np.array_equal(R[:, 1:, :], others)
+
+
+def pin_two_branch_toy():
+    """The two-branch example of the GR notes (tests/golden/two_branch_toy.json)."""
+    with open(os.path.join(GOLDEN, "two_branch_toy.json")) as f:
+        g = json.load(f)
+    R = np.asarray(g["R"])[None]
+    x = oracle.read_fixed_gates(R, np.asarray(g["gamma"]), np.asarray(g["G"]), g["eps"])
+    exp = g["expected"]
+    assert np.allclose(x[0], exp["x"], rtol=0, atol=1e-12)
+    assert np.all(np.abs(x[0]) > 0.1)  # the sublayer input mixes both streams
+    y = x @ np.asarray(g["F_matrix_rows_out"]).T
+    assert np.allclose(y[0], exp["y"], rtol=0, atol=1e-12)
+    Rp = oracle.write(R, y, np.asarray(g["s"])[None])
+    assert np.allclose(Rp[0], exp["R_prime"], rtol=0, atol=1e-12)
+
+
+def pin_two_branch_learned_gate():
+    """The same two branches with a predicted gate, in closed form. r = 1, eps = 0,
+    γ = 1/√2 (so R̂ = R), W_d = [2, 0, 0, 2]: z = (1/2)(2 + 2) = 2, h = SiLU(2) = 2σ(2).
+    W_u = [1, -1, -1, 1]ᵀ: G_1 = (σ(h), σ(-h)), G_2 = (σ(-h), σ(h)) — branch 1 read mostly in
+    dimension 1, branch 2 in dimension 2 — so x = (σ(h)/2, σ(h)/2).
+    W_w = [[2,0,0,0],[0,0,0,-2]]: s = (2σ(1), 2σ(-1))."""
+    sig = lambda a: 1.0 / (1.0 + math.exp(-a))  # noqa: E731
+    R = np.array([[[1.0, 0.0], [0.0, 1.0]]])
+    p = {"gamma": np.full((2, 2), 1.0 / math.sqrt(2.0)), "w_down": np.array([[2.0, 0, 0, 2.0]]),
+         "w_up": np.array([[1.0], [-1.0], [-1.0], [1.0]]),
+         "w_write": np.array([[2.0, 0, 0, 0], [0, 0, 0, -2.0]])}
+    x, s, G, _ = _read(R, p, eps=0.0, internals=True)
+    h = 2.0 * sig(2.0)
+    assert np.allclose(G[0], [[sig(h), sig(-h)], [sig(-h), sig(h)]], rtol=0, atol=1e-14)
+    assert np.allclose(x[0], [sig(h) / 2, sig(h) / 2], rtol=0, atol=1e-14)
+    assert np.allclose(s[0], [2 * sig(1.0), 2 * sig(-1.0)], rtol=0, atol=1e-14)
+
+
+def pin_chain_closed_form():
+    """eq rcv: with no branch mixing, R_c^(v) = R_c^(0) + Σ_{u<v} s_c^(u) y^(u)."""
+    rng = np.random.default_rng(108)
+    n, nb, D, r, L = 3, 4, 16, 4, 7
+    R0 = rng.standard_normal((n, nb, D))
+    ys = [0.5 * rng.standard_normal((n, D)) for _ in range(L)]
+    ps = [_params(rng, nb, D, r, std=0.4) for _ in range(L)]
+    states, xs, ss = oracle.chain(R0, ys, ps)
+    for v in range(L + 1):
+        acc = R0.copy()
+        for u in range(v):
+            acc = acc + ss[u][:, :, None] * ys[u][:, None, :]
+        assert _rel(states[v], acc) < 1e-13
+    assert not np.allclose(ss[0], ss[1])  # strengths are data dependent
+
+
+def pin_decomposition():
+    """eq auv: x^(v) = a_{0→v} + Σ_{u<v} a_{u→v}, with
+    a_{u→v} = (1/n_r) Σ_c G_c^(v) ⊙ γ_c ⊙ s_c^(u) y^(u) / rms(R_c^(v)) (and a_{0→v} the same
+    with R_c^(0)); exact up to round-off, so the fractions π_uv sum to 1."""
+    rng = np.random.default_rng(109)
+    n, nb, D, r, L, eps = 2, 4, 16, 4, 5, 1e-6
+    R0 = rng.standard_normal((n, nb, D))
+    ys = [0.7 * rng.standard_normal((n, D)) for _ in range(L)]
+    ps = [_params(rng, nb, D, r, std=0.4) for _ in range(L)]
+    states, xs, ss = oracle.chain(R0, ys, ps, eps)
+    v = L - 1
+    p = ps[v]
+    x, _, G, inv = _read(states[v], p, eps, internals=True)
+    assert _rel(x, xs[v]) < 1e-14
+    coef = G * p["gamma"][None] * inv[:, :, None]            # G_c γ_c / rms(R_c^(v))
+    a0 = (coef * R0).sum(axis=1) / nb
+    a = [(coef * (ss[u][:, :, None] * ys[u][:, None, :])).sum(axis=1) / nb for u in range(v)]
+    assert _rel(a0 + sum(a), x) < 1e-13
+    norms = np.array([np.linalg.norm(au, axis=1) for au in a])  # [v, n]
+    pi = norms / norms.sum(axis=0, keepdims=True)
+    assert np.allclose(pi.sum(axis=0), 1.0, atol=3e-8)
+
+
+def pin_branch_permutation():
+    """Branches are exchangeable (Digest §二.6): permuting branches together with γ rows, W_d
+    column blocks, W_u row blocks and W_w rows and column blocks permutes s and leaves x."""
+    rng = np.random.default_rng(110)
+    n, nb, D, r = 4, 4, 12, 3
+    R = rng.standard_normal((n, nb, D))
+    p = _params(rng, nb, D, r, std=0.5)
+    perm = np.array([2, 0, 3, 1])
+    blocks = np.concatenate([np.arange(i * D, (i + 1) * D) for i in perm])
+    q = {"gamma": p["gamma"][perm], "w_down": p["w_down"][:, blocks],
+         "w_up": p["w_up"][blocks, :], "w_write": p["w_write"][perm][:, blocks]}
+    x, s = _read(R, p)
+    x2, s2 = _read(R[:, perm, :], q)
+    assert _rel(x2, x) < 1e-13 and _rel(s2, s[:, perm]) < 1e-13
+
+
+def pin_branch_scale_invariance():
+    """With eps = 0, RMSNorm removes any positive per-branch scale: x and s are unchanged."""
+    rng = np.random.default_rng(111)
+    R = rng.standard_normal((3, 4, 16))
+    p = _params(rng, 4, 16, 3, std=0.5)
+    x, s = _read(R, p, eps=0.0)
+    c = np.array([0.1, 1.0, 10.0, 100.0])[None, :, None]
+    x2, s2 = _read(R * c, p, eps=0.0)
+    assert _rel(x2, x) < 1e-13 and _rel(s2, s) < 1e-13
+
+
+def pin_ranges_and_saturation():
+    """G ∈ (0,1) and s ∈ (0,2) (bounded positive gates); huge logits stay finite."""
+    rng = np.random.default_rng(112)
+    R = rng.standard_normal((3, 4, 16))
+    p = _params(rng, 4, 16, 3, std=0.5)
+    x, s, G, _ = _read(R, p, internals=True)
+    assert np.all((G > 0) & (G < 1)) and np.all((s > 0) & (s < 2))
+    big = {k: (v * 1e4 if k != "gamma" else v) for k, v in p.items()}
+    x, s, G, _ = _read(R, big, internals=True)
+    assert np.all(np.isfinite(x)) and np.all(np.isfinite(s)) and np.all(np.isfinite(G))
+    assert np.all((G >= 0) & (G <= 1)) and np.all((s >= 0) & (s <= 2))
+
+
+def pin_residual_add():
+    rng = np.random.default_rng(113)
+    a, b = rng.standard_normal(1000), rng.standard_normal(1000)
+    assert np.array_equal(oracle.residual_add(a, b), a + b)
+
+
+ALL_PINS = [pin_dense_bruteforce, pin_zero_down_projection, pin_zero_up_projection,
+            pin_zero_write_projection, pin_gatednorm_single_branch, pin_replicated_branches,
+            pin_prenorm_reduction, pin_two_branch_toy, pin_two_branch_learned_gate,
+            pin_chain_closed_form, pin_decomposition, pin_branch_permutation,
+            pin_branch_scale_invariance, pin_ranges_and_saturation, pin_residual_add]

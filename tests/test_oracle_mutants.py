@@ -1,0 +1,60 @@
+"""The pins catch plausible mistakes: each mutant below is a copy of the oracle source with one
+planted error (a dropped term, a wrong sign or index, a transposed operand), built on the CPU
+into a temporary directory. Every mutant must fail at least one pin other than the matrix-form
+cross-check, so the pins constrain the oracle independently of any second formulation."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gr_oracle.c")
+
+MUTANTS = {
+    "drop_1/n_r_inside_silu": ("h[k] = silu(inv_nb * acc);", "h[k] = silu(acc);"),
+    "drop_1/n_r_in_combine": ("x[c] = inv_nb * acc;", "x[c] = acc;"),
+    "drop_2_in_s": ("s[i] = 2.0 * sigmoid(inv_nb * acc);", "s[i] = sigmoid(inv_nb * acc);"),
+    "drop_1/n_r_in_s": ("s[i] = 2.0 * sigmoid(inv_nb * acc);", "s[i] = 2.0 * sigmoid(acc);"),
+    "drop_gamma": ("Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];",
+                   "Rh[(size_t)i * D + c] = Ri[c] * inv[i];"),
+    "sigmoid_sign": ("return 1.0 / (1.0 + exp(-a));", "return 1.0 / (1.0 + exp(a));"),
+    "eps_outside_sqrt": ("inv[i] = 1.0 / sqrt(ms + eps);", "inv[i] = 1.0 / (sqrt(ms) + eps);"),
+    "norm_over_all_branches": ("double ms = ss / (double)D;", "double ms = ss / (double)(D * nb);"),
+    "transposed_w_up": ("acc += w[k] * h[k];", "acc += Wu[(size_t)k * K + j] * h[k];"),
+    "write_uses_s0": ("const double si = s[(size_t)t * nb + i];",
+                      "const double si = s[(size_t)t * nb];"),
+    "silu_is_sigmoid": ("static double silu(double a) { return a * sigmoid(a); }",
+                        "static double silu(double a) { return sigmoid(a); }"),
+    "write_sign": ("R_out[e] = R[e] + si * y[(size_t)t * D + c];",
+                   "R_out[e] = R[e] - si * y[(size_t)t * D + c];"),
+    "vec_channel_major": ("Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];",
+                          "Rh[(size_t)c * nb + i] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];"),
+    "fixed_gate_no_1/n_r": ("x[(size_t)t * D + c] = acc / (double)nb;",
+                            "x[(size_t)t * D + c] = acc;"),
+    "gamma_wrong_branch": ("Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];",
+                           "Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[c];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(oracle_mod, tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not found once: {old}"
+    mpath = tmp_path / "gr_oracle_mutant.c"
+    mpath.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", str(mpath), "-o",
+                    str(so), "-lm"], check=True)
+    caught = []
+    with oracle.use_library(str(so)):
+        for pin in pins.ALL_PINS:
+            if pin is pins.pin_dense_bruteforce:
+                continue
+            try:
+                pin()
+            except AssertionError:
+                caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every invariant pin"
