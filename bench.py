@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Throughput of the fused Gated Residual write→read on GB300.
+
+One step = one fused gr_write_then_read over the whole workload (default: prefill, N=16384
+tokens, D=4096, 4 branches, r=16, bf16 states), with the write strengths ping-ponged from step
+to step like a chain of sublayers. The state (512 MiB) is larger than L2, so no flush is
+needed between steps. Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gr|reference] [--workload NAME]
+
+For N > 1 (torchrun, one process per GPU) every rank processes its own token shard of the
+same size (weak scaling); there is no data-path collective, only the timing barrier and a
+max over ranks. `--impl reference` times the fp64 CPU oracle on this host's cores on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GR fused read/write tokens/s & HBM GB/s vs GB300 peak (4 branches, D=4096)"
+UNIT = "tokens/s"
+BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[1])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gr", "reference"], default="gr")
+    ap.add_argument("--workload", default="prefill")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------------------------
+# accounting
+
+def bytes_per_token(w) -> int:
+    """Algorithmic HBM bytes of one token in the fused step: R read and written (4·D each),
+    y read, x written (D each), s_prev read and s_next written (4 fp32 each)."""
+    b = w.state_bytes_per_elem()
+    return 2 * 4 * w.d_model * b + 2 * w.d_model * b + 2 * 4 * 4
+
+
+def weight_bytes(w) -> int:
+    """Parameter bytes a fused launch reads once: W_d, W_w, W_u in the state dtype, gamma fp32."""
+    b = w.state_bytes_per_elem()
+    K = 4 * w.d_model
+    return (2 * w.rank + 4) * K * b + K * 4
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: fused GR write->read, N={w.n_tokens} tokens, D={w.d_model}, 4 branches, "
+            f"r={w.rank}, {w.dtype} states, fp32 accumulation")
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_sha(kernel_path: str) -> str:
+    from stream_gated_residual_gb300 import build as gbuild
+    name = {"fused_bf16": "gr_fused_bf16.cu", "generic": "gr_generic.cu"}[kernel_path]
+    h = hashlib.sha256()
+    for p in (os.path.join(gbuild.CSRC, name), os.path.join(gbuild.CSRC, "gr_internal.h")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel_path: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and workload, if the
+    kernel source has not changed since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_path}__{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"^dram_bytes_per_launch:\s*(\d+)", text, re.M)
+    m_s = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
+    if not (m_b and m_s) or m_s.group(1) != kernel_source_sha(kernel_path):
+        return None
+    return int(m_b.group(1))
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = (uuid or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="gr_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and self.uuid not in parts[1].lower():
+                    continue
+                rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k] == "Active"})
+        loaded = [v for v in sm if mx and v >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+
+class OracleInputs:
+    """The workload's inputs in fp64 for the first n tokens (generated once)."""
+
+    def __init__(self, w, n_tokens: int):
+        from stream_gated_residual_gb300 import workloads as wl
+        self.w = w
+        self.n = n_tokens
+        self.R = wl.to_f64(wl.make_state(w, n_tokens))
+        self.y = wl.to_f64(wl.make_y(w, 0, n_tokens))
+        self.sp = wl.make_s_prev(w, n_tokens)
+        self.p = wl.make_params(w, 1)
+
+    def run(self, a: int, b: int) -> float:
+        """Seconds of one fused oracle step on tokens a..b-1."""
+        import oracle
+        t0 = time.perf_counter()
+        oracle.write_then_read(self.R[a:b], self.y[a:b], self.sp[a:b], self.p, self.w.eps)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(w, target_s: float = 12.0) -> dict:
+    import oracle
+    oracle.build()
+    probe = 64
+    t = OracleInputs(w, probe).run(0, probe)
+    n = int(max(probe, min(w.n_tokens, target_s * probe / max(t, 1e-9))))
+    t = OracleInputs(w, n).run(0, n)
+    return {"value": n / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {n} of {w.n_tokens} tokens of the {w.name} workload, one fused "
+                      f"write->read in fp64 ({t:.1f} s)"}
+
+
+def run_reference(args, w) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    steps, warmup = max(1, args.steps), max(0, args.warmup)
+    probe = OracleInputs(w, 32)
+    probe_t = probe.run(0, 32)
+    budget_s = 150.0
+    per_step = int(max(1, min(w.n_tokens, budget_s * 32 / probe_t / (steps + warmup))))
+    pool = min(w.n_tokens, max(per_step, 2048))
+    inp = OracleInputs(w, pool)
+
+    def window(i):
+        a = (i * per_step) % max(1, pool - per_step + 1)
+        return a, a + per_step
+
+    for i in range(warmup):
+        inp.run(*window(i))
+    total = 0.0
+    for i in range(steps):
+        total += inp.run(*window(i))
+    value = steps * per_step / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * total / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": workload_desc(w), "n_tokens": w.n_tokens, "d_model": w.d_model,
+                   "rank": w.rank, "n_branch": 4, "step_sample_tokens": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} of the first {pool} tokens of the {w.name} "
+                                   f"workload per step (fused write->read, fp64)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+
+def run_gr(args, w) -> None:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from stream_gated_residual_gb300 import gr
+    from stream_gated_residual_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    gr.load()
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    # each rank owns its own shard of tokens (a different seed), same size on every rank
+    wr = w.scaled(seed=w.seed + rank)
+
+    def dev_tensor(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    R_h, y_h, sp_h = wl.make_state(wr), wl.make_y(wr), wl.make_s_prev(wr)
+    p = wl.make_params(wr, 1)
+    R, y = dev_tensor(R_h), dev_tensor(y_h)
+    s_a = torch.from_numpy(sp_h).to(dev)
+    s_b = torch.empty_like(s_a)
+    x = torch.empty((w.n_tokens, w.d_model), dtype=tdt, device=dev)
+    pt = {k: torch.from_numpy(v).to(dev) for k, v in p.items()}
+    P = gr.pack_params(pt["gamma"], pt["w_down"], pt["w_up"], pt["w_write"], tdt, w.eps)
+    path = gr.kernel_path(w.n_tokens, w.d_model, w.rank, tdt)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1
+
+    def step(i):
+        sp, sn = (s_a, s_b) if i % 2 == 0 else (s_b, s_a)
+        gr.write_then_read(R, y, sp, P, x=x, s_next=sn, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+
+    def timed():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(uuid)
+        sampler.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks = sampler.stop()
+        if world > 1:
+            dist.barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, clocks
+
+    ms, clocks = timed()
+    if BAD_REASONS & set(clocks["reasons"]):
+        ms, clocks = timed()  # one re-measurement
+        clocks["remeasured"] = True
+    ms_step = ms / args.steps
+    tokens_per_s = world * w.n_tokens * args.steps / (ms / 1e3)
+
+    # roofline of the one kernel of the step
+    peaks = load_peaks()
+    alg_bytes = w.n_tokens * bytes_per_token(w) + weight_bytes(w)
+    achieved = alg_bytes / (ms_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                "kernel": path, "algorithmic_bytes_per_launch": alg_bytes,
+                "traffic": profiled_traffic(path, w.name)}
+
+    # bandwidth reference: single-stream x += y on [N, D]
+    xr = torch.zeros((w.n_tokens, w.d_model), dtype=tdt, device=dev)
+    yr = y.clone()
+    for _ in range(5):
+        gr.residual_add_ref(xr, yr, stream=stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    nref = 50
+    e0.record(stream)
+    for _ in range(nref):
+        gr.residual_add_ref(xr, yr, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ref_gbs = 3 * xr.numel() * xr.element_size() / (e0.elapsed_time(e1) / nref / 1e3) / 1e9
+    del xr, yr
+
+    # end to end through the host-buffer C entry: H2D of R, y, s_prev; D2H of R', x, s_next
+    Rh = torch.from_numpy(R_h.view(np.int16) if R_h.dtype == np.uint16 else R_h)
+    yh = torch.from_numpy(y_h.view(np.int16) if y_h.dtype == np.uint16 else y_h)
+    if tdt == torch.bfloat16:
+        Rh, yh = Rh.view(torch.bfloat16), yh.view(torch.bfloat16)
+    Rh, yh = Rh.pin_memory(), yh.pin_memory()
+    sph = torch.from_numpy(sp_h).pin_memory()
+    xh = torch.empty((w.n_tokens, w.d_model), dtype=tdt).pin_memory()
+    snh = torch.empty((w.n_tokens, 4), dtype=torch.float32).pin_memory()
+    nws = gr.host_workspace_size(w.n_tokens, w.d_model, tdt)
+    del R, y, x, s_a, s_b
+    torch.cuda.empty_cache()
+    wsb = torch.empty(nws + 256, dtype=torch.uint8, device=dev)
+    ws = wsb[(-wsb.data_ptr()) % 256:][:nws]
+    gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)  # warm-up
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    es = w.state_bytes_per_elem()
+    h2d = w.n_tokens * (4 * w.d_model * es + w.d_model * es + 16)
+    d2h = h2d
+    e2e = {"value": world * w.n_tokens * args.e2e_steps / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "api": "gr_write_then_read_host (pinned host buffers)"}
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded numpy PCG64; no dataset)",
+            "config": {"workload": workload_desc(w), "n_tokens_per_gpu": w.n_tokens,
+                       "d_model": w.d_model, "rank": w.rank, "n_branch": 4,
+                       "state_dtype": w.dtype, "accumulate": "fp32", "parallelism": f"dp{world}",
+                       "l2": f"inputs larger than L2 (state {R_h.nbytes >> 20} MiB), no flush"},
+            "hbm_gbs": achieved,
+            "roofline": roofline,
+            "bandwidth_reference": {"kernel": "gr_residual_add_ref (x += y, single stream)",
+                                    "gbs": ref_gbs, "frac": ref_gbs / peaks["hbm_gbs"]},
+            "cpu_baseline": base,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from stream_gated_residual_gb300 import workloads as wl
+    if args.workload not in wl.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(wl.WORKLOADS)}")
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gr(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+/*
+ * gr.h — C ABI of the GB300 Gated Residual (GR) read/write library (libgr_gb300.so).
+ *
+ * What the calls compute (all per token t, branch i, channel c; n_r = 4 branches):
+ *   "【论文解读】 Qwen3.8 Flash Next" (wkq9411.github.io), §二.4 Gated Residual:
+ *     eq rms      R̂_i = RMSNorm(R_i; γ_i) = R_i · γ_i / sqrt(mean_c R_i[c]^2 + eps)
+ *     eq gate     G = unvec σ(W_u SiLU((1/n_r) W_d vec R̂))
+ *     eq use_gate x = (1/n_r) Σ_i G_i ⊙ R̂_i
+ *     eq s        s = 2σ((1/n_r) W_w vec R̂)
+ *     eq write    R'_i = R_i + s_i · y
+ *   "Qwen3.8-Flash-Next 架构笔记 · 06 / RESIDUAL" (cbphcr.github.io) §2–§3 give the same
+ *   formulas at n_r = 4, and §5 asks that the read and the write each traverse the widened
+ *   state once; gr_write_then_read fuses one sublayer's write with the next sublayer's read so
+ *   that each state byte crosses HBM once per sublayer.
+ *
+ * Conventions shared by every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller (unless a call says HOST). The
+ *     library never allocates or frees memory.
+ *   - Calls are asynchronous on the caller's CUDA stream, passed as `void*` (cudaStream_t;
+ *     NULL = the legacy default stream). Results are ready when the stream has reached them.
+ *   - Layouts are row-major and dense:
+ *       R   [N][4][D]  state (token, branch, channel), dtype shape->state_dtype
+ *       y   [N][D]     sublayer output F(x), state dtype
+ *       x   [N][D]     block input for the next sublayer, state dtype
+ *       s   [N][4]     write strengths, fp32
+ *       gamma [4][D], W_d [r][4D], W_u [4D][r], W_w [4][4D], fp32 (vec index = i*D + c)
+ *   - Arithmetic is fp32. bf16 stores round to nearest even. On the bf16 path the weights are
+ *     used as bf16 with gamma folded into W_d and W_w (see gr_pack_params); the combine uses
+ *     gamma in fp32. The read after a fused write uses the stored (rounded) state.
+ *   - Every call validates its arguments on the host first. On any validation error it returns
+ *     a negative status, launches nothing and touches no output. A status of GR_E_CUDA means a
+ *     launch or copy failed; the CUDA error is not cleared from the runtime.
+ *   - n_tokens == 0 is valid and does nothing.
+ */
+#ifndef GR_GB300_H
+#define GR_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GR_API_VERSION 1
+#define GR_MAX_D 12288   /* largest d_model (one token's fp32 state row must fit on chip) */
+#define GR_MAX_RANK 64
+
+/* Status codes. */
+enum {
+    GR_OK = 0,
+    GR_E_NULL = -1,        /* a required pointer is NULL                                        */
+    GR_E_SHAPE = -2,       /* n_tokens < 0, d_model not a multiple of 8 in [8, GR_MAX_D],      */
+                           /* or n_branch != 4                                                 */
+    GR_E_DTYPE = -3,       /* unknown state dtype                                               */
+    GR_E_ALIGN = -4,       /* a device pointer is not 16-byte aligned                           */
+    GR_E_RANK = -5,        /* rank outside [1, 64]                                              */
+    GR_E_PARAMS = -6,      /* params not packed by gr_pack_params, or packed for another shape  */
+    GR_E_SIZE = -7,        /* a caller-provided buffer is smaller than the call needs           */
+    GR_E_ALIAS = -8,       /* an output overlaps an input in a way the call forbids             */
+    GR_E_CUDA = -9,        /* a CUDA launch or copy failed                                      */
+    GR_E_DEVICE = -10,     /* no usable CUDA device (this build runs on sm_103a only)           */
+    GR_E_EPS = -11         /* eps negative or not finite                                        */
+};
+
+/* Storage dtype of R, y and x. */
+typedef enum { GR_F32 = 0, GR_BF16 = 1 } gr_dtype;
+
+/* Problem shape. n_branch must be 4; d_model a multiple of 8 in [8, GR_MAX_D]; 1 <= rank <= 64. */
+typedef struct gr_shape {
+    int64_t n_tokens;    /* N: flattened tokens ([B,S,D] or [B,1,D] -> N rows) */
+    int32_t d_model;     /* D: block width */
+    int32_t n_branch;    /* n_r: must be 4 */
+    int32_t rank;        /* r: gate bottleneck rank */
+    int32_t state_dtype; /* gr_dtype of R, y, x */
+    float eps;           /* RMSNorm epsilon (the pages give none; 1e-6 is the usual value) */
+} gr_shape;
+
+/* Packed parameters of one sublayer's GR module. Filled by gr_pack_params; the caller owns the
+ * device buffer `packed` and keeps it alive while calls that use these params are in flight. */
+typedef struct gr_params {
+    const void* packed;  /* device buffer written by gr_pack_params */
+    int32_t d_model, n_branch, rank, state_dtype;
+    uint64_t tag;        /* GR_PARAMS_TAG once packed */
+} gr_params;
+
+#define GR_PARAMS_TAG 0x47523330304B5031ull
+
+/* Version of this ABI (GR_API_VERSION). */
+int gr_api_version(void);
+
+/* Human-readable text for a status code (static storage; never NULL). */
+const char* gr_status_string(int status);
+
+/* Name of the kernel path a read or fused step takes for `shape` (static string, never NULL):
+ * "fused_bf16" (tensor-core kernel), "generic" (one CTA per token), or "invalid". Host only. */
+const char* gr_kernel_path(const gr_shape* shape);
+
+/* Bytes of device memory gr_pack_params needs for `shape` (host only; no CUDA call).
+ * Returns GR_OK and sets *bytes, or a validation status. shape->n_tokens is ignored. */
+int gr_packed_size(const gr_shape* shape, size_t* bytes);
+
+/* Lay the fp32 parameters of one GR module out for the kernels (Digest §二.4 shapes:
+ * gamma [4][D], W_d [r][4D], W_u [4D][r], W_w [4][4D]; all DEVICE pointers, fp32, 16-byte
+ * aligned). `packed` is a DEVICE buffer of at least gr_packed_size() bytes, 256-byte aligned.
+ * On the bf16 path the packed weights are bf16 (nearest even) with gamma folded into W_d and
+ * W_w (W[k][i*D+c]·gamma[i][c] in fp32, then rounded); gamma is also kept in fp32 for the combine. On
+ * the fp32 path the weights stay fp32 and nothing is folded. Runs on `stream`; the inputs may
+ * be freed once the stream has passed the call. Fills *out on success. */
+int gr_pack_params(const gr_shape* shape, const float* gamma, const float* w_down,
+                   const float* w_up, const float* w_write, void* packed, size_t packed_bytes,
+                   gr_params* out, void* stream);
+
+/* The read (eq rms, eq gate, eq use_gate, eq s) of a chain's first sublayer:
+ * R [N][4][D] -> x [N][D] and s [N][4]. R is only read. x and s must not overlap R. */
+int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
+            void* stream);
+
+/* The write (eq write) of a chain's last sublayer: R[t][i][:] += s[t][i] · y[t][:], in place. */
+int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void* stream);
+
+/* One sublayer's write fused with the next sublayer's read, in one traversal of the state:
+ *   R[t][i][:] = R[t][i][:] + s_prev[t][i] · y[t][:]            (eq write, in place)
+ *   x, s_next  = read of the written (stored) R with `next`       (eq rms … eq s)
+ * y and x may be the same buffer (F's input/output buffer), and s_prev and s_next may be the
+ * same buffer: each token's y and s_prev are read before its x and s_next are written. Apart
+ * from those two exact matches, x and s_next must not overlap R, y, s_prev or each other. */
+int gr_write_then_read(const gr_shape* shape, void* R, const void* y, const float* s_prev,
+                       const gr_params* next, void* x, float* s_next, void* stream);
+
+/* The combine of eq use_gate with caller-given gates: x = (1/4) Σ_i G_i ⊙ RMSNorm(R_i; γ_i),
+ * G [4][D] fp32 broadcast over tokens, gamma [4][D] fp32. No gate prediction, no s. Used to
+ * check reductions that need gates σ cannot produce (one-hot reads: GR as Pre-Norm,
+ * Digest §二.2 and §二.4). */
+int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma,
+                        const float* G, void* x, void* stream);
+
+/* Single-stream residual add x[e] += y[e], e < n, in `dtype` (the plain residual
+ * x_{l+1} = x_l + F(x_l) of "Residual" §1): the bandwidth reference for the GR kernels.
+ * n >= 0; pointers 16-byte aligned. */
+int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* stream);
+
+/* Bytes of device workspace gr_write_then_read_host needs for `shape`. */
+int gr_host_workspace_size(const gr_shape* shape, size_t* bytes);
+
+/* gr_write_then_read on HOST buffers (pinned memory gives asynchronous copies): copies R, y and
+ * s_prev into `workspace` (DEVICE, >= gr_host_workspace_size bytes, 256-byte aligned), runs the
+ * fused step there, copies R', x and s_next back into R_host, x_host and s_next_host, and
+ * synchronises `stream` before returning. Host buffers must not overlap. */
+int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_host,
+                            const float* s_prev_host, const gr_params* next, void* x_host,
+                            float* s_next_host, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GR_GB300_H */

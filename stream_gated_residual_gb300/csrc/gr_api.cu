@@ -1,0 +1,304 @@
+// C ABI of the GR library: host-side validation, dispatch to the kernels, status codes.
+// Declarations and the contract of every entry point are in include/gr.h.
+#include <math.h>
+#include <string.h>
+
+#include "gr_internal.h"
+
+namespace gr {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];        // 0 = not queried yet
+int g_device_ok[kMaxDevices];       // 0 = unknown, 1 = sm_103, -1 = unusable
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return (d >= 0 && d < kMaxDevices) ? d : -1;
+}
+
+// The build targets sm_103a only; refuse other devices before launching anything.
+int check_device() {
+    const int d = current_device();
+    if (d < 0) return GR_E_DEVICE;
+    if (g_device_ok[d] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) {
+            return GR_E_DEVICE;
+        }
+        g_sm_count[d] = sms;
+        g_device_ok[d] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_device_ok[d] == 1 ? GR_OK : GR_E_DEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return na && nb && a0 < b0 + nb && b0 < a0 + na;
+}
+
+int validate_shape(const gr_shape* s) {
+    if (!s) return GR_E_NULL;
+    if (s->n_tokens < 0 || s->n_branch != kBranches || s->d_model < 8 || s->d_model % 8 != 0 ||
+        s->d_model > GR_MAX_D)
+        return GR_E_SHAPE;
+    if (s->state_dtype != GR_F32 && s->state_dtype != GR_BF16) return GR_E_DTYPE;
+    if (s->rank < 1 || s->rank > GR_MAX_RANK) return GR_E_RANK;
+    if (!(s->eps >= 0.0f) || !isfinite(s->eps)) return GR_E_EPS;
+    return GR_OK;
+}
+
+int validate_params(const gr_shape* s, const gr_params* p) {
+    if (!p) return GR_E_NULL;
+    if (p->tag != GR_PARAMS_TAG || !p->packed) return GR_E_PARAMS;
+    if (p->d_model != s->d_model || p->n_branch != s->n_branch || p->rank != s->rank ||
+        p->state_dtype != s->state_dtype)
+        return GR_E_PARAMS;
+    return GR_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == GR_BF16 ? 2 : 4; }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? GR_OK : GR_E_CUDA; }
+
+// Which kernel runs a read (or fused step) for this shape.
+bool use_fused(const gr_shape* s) {
+    return s->state_dtype == GR_BF16 && fused_supported(s->d_model, s->rank);
+}
+
+int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
+             const gr_params* p, void* x, float* s_out, cudaStream_t st) {
+    if (s->n_tokens == 0) return GR_OK;
+    cudaError_t e;
+    if (use_fused(s))
+        e = launch_fused_bf16(s->n_tokens, s->d_model, s->rank, s->eps, R, y, s_prev, p->packed,
+                              x, s_out, st);
+    else
+        e = launch_generic(s->n_tokens, s->d_model, s->rank, s->state_dtype, s->eps, R, y,
+                           s_prev, p->packed, x, s_out, st);
+    return status_of(e);
+}
+
+}  // namespace
+
+int sm_count() {
+    const int d = current_device();
+    if (d < 0) return 1;
+    if (g_sm_count[d] == 0) {
+        int sms = 1;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+        g_sm_count[d] = sms > 0 ? sms : 1;
+    }
+    return g_sm_count[d];
+}
+
+}  // namespace gr
+
+using namespace gr;
+
+extern "C" {
+
+int gr_api_version(void) { return GR_API_VERSION; }
+
+const char* gr_status_string(int status) {
+    switch (status) {
+        case GR_OK: return "ok";
+        case GR_E_NULL: return "a required pointer is NULL";
+        case GR_E_SHAPE: return "bad shape (n_tokens < 0, d_model not a multiple of 8 in [8, 12288], or n_branch != 4)";
+        case GR_E_DTYPE: return "unknown state dtype";
+        case GR_E_ALIGN: return "a pointer is not aligned as the call requires";
+        case GR_E_RANK: return "rank outside [1, 64]";
+        case GR_E_PARAMS: return "params not packed by gr_pack_params or packed for another shape";
+        case GR_E_SIZE: return "a caller-provided buffer is too small";
+        case GR_E_ALIAS: return "an output overlaps an input";
+        case GR_E_CUDA: return "a CUDA launch or copy failed";
+        case GR_E_DEVICE: return "no usable sm_103 CUDA device";
+        case GR_E_EPS: return "eps negative or not finite";
+        default: return "unknown status";
+    }
+}
+
+const char* gr_kernel_path(const gr_shape* shape) {
+    if (validate_shape(shape) != GR_OK) return "invalid";
+    return use_fused(shape) ? "fused_bf16" : "generic";
+}
+
+int gr_packed_size(const gr_shape* shape, size_t* bytes) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (!bytes) return GR_E_NULL;
+    *bytes = make_layout(shape->d_model, shape->rank, shape->state_dtype).total;
+    return GR_OK;
+}
+
+int gr_pack_params(const gr_shape* shape, const float* gamma, const float* w_down,
+                   const float* w_up, const float* w_write, void* packed, size_t packed_bytes,
+                   gr_params* out, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (!gamma || !w_down || !w_up || !w_write || !packed || !out) return GR_E_NULL;
+    if (!aligned16(gamma) || !aligned16(w_down) || !aligned16(w_up) || !aligned16(w_write) ||
+        !aligned256(packed))
+        return GR_E_ALIGN;
+    const Layout L = make_layout(shape->d_model, shape->rank, shape->state_dtype);
+    if (packed_bytes < L.total) return GR_E_SIZE;
+    const size_t K = size_t(kBranches) * shape->d_model;
+    const size_t r = size_t(shape->rank);
+    if (overlaps(packed, L.total, gamma, K * 4) || overlaps(packed, L.total, w_down, r * K * 4) ||
+        overlaps(packed, L.total, w_up, r * K * 4) ||
+        overlaps(packed, L.total, w_write, kBranches * K * 4))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    cudaError_t e = launch_pack(shape->d_model, shape->rank, shape->state_dtype, gamma, w_down,
+                                w_up, w_write, packed, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return GR_E_CUDA;
+    out->packed = packed;
+    out->d_model = shape->d_model;
+    out->n_branch = shape->n_branch;
+    out->rank = shape->rank;
+    out->state_dtype = shape->state_dtype;
+    out->tag = GR_PARAMS_TAG;
+    return GR_OK;
+}
+
+int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
+            void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if ((st = validate_params(shape, params))) return st;
+    if (!R || !x || !s) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(x) || !aligned16(s)) return GR_E_ALIGN;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es, nx = N * D * es, ns = N * kBranches * 4;
+    if (overlaps(x, nx, R, nR) || overlaps(s, ns, R, nR) || overlaps(x, nx, s, ns))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return run_step(shape, const_cast<void*>(R), nullptr, nullptr, params, x, s,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (!R || !y || !s) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(y) || !aligned16(s)) return GR_E_ALIGN;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es;
+    if (overlaps(R, nR, y, N * D * es) || overlaps(R, nR, s, N * kBranches * 4))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_write(shape->n_tokens, shape->d_model, shape->state_dtype, R, y, s,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int gr_write_then_read(const gr_shape* shape, void* R, const void* y, const float* s_prev,
+                       const gr_params* next, void* x, float* s_next, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if ((st = validate_params(shape, next))) return st;
+    if (!R || !y || !s_prev || !x || !s_next) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(y) || !aligned16(s_prev) || !aligned16(x) ||
+        !aligned16(s_next))
+        return GR_E_ALIGN;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es, ny = N * D * es, ns = N * kBranches * 4;
+    if (overlaps(R, nR, y, ny) || overlaps(R, nR, s_prev, ns) || overlaps(x, ny, R, nR) ||
+        overlaps(s_next, ns, R, nR) || overlaps(x, ny, s_next, ns) ||
+        overlaps(x, ny, s_prev, ns) || overlaps(s_next, ns, y, ny) ||
+        (x != y && overlaps(x, ny, y, ny)) || (s_next != s_prev && overlaps(s_next, ns, s_prev, ns)))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return run_step(shape, R, y, s_prev, next, x, s_next, static_cast<cudaStream_t>(stream));
+}
+
+int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma,
+                        const float* G, void* x, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (!R || !gamma || !G || !x) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(x)) return GR_E_ALIGN;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    if (overlaps(x, N * D * es, R, N * kBranches * D * es)) return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_fixed_gates(shape->n_tokens, shape->d_model, shape->state_dtype,
+                                        shape->eps, R, gamma, G, x,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* stream) {
+    if (n < 0) return GR_E_SHAPE;
+    if (dtype != GR_F32 && dtype != GR_BF16) return GR_E_DTYPE;
+    if (!y || !x) return GR_E_NULL;
+    if (!aligned16(y) || !aligned16(x)) return GR_E_ALIGN;
+    if (overlaps(x, size_t(n) * elem_size(dtype), y, size_t(n) * elem_size(dtype)))
+        return GR_E_ALIAS;
+    int st = check_device();
+    if (st) return st;
+    return status_of(launch_residual_add(n, dtype, y, x, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_host_workspace_size(const gr_shape* shape, size_t* bytes) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (!bytes) return GR_E_NULL;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    *bytes = align256(N * kBranches * D * es) + align256(N * D * es) * 2 +
+             align256(N * kBranches * 4) * 2;
+    return GR_OK;
+}
+
+int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_host,
+                            const float* s_prev_host, const gr_params* next, void* x_host,
+                            float* s_next_host, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if ((st = validate_params(shape, next))) return st;
+    if (!R_host || !y_host || !s_prev_host || !x_host || !s_next_host || !workspace)
+        return GR_E_NULL;
+    if (!aligned256(workspace)) return GR_E_ALIGN;
+    size_t need = 0;
+    gr_host_workspace_size(shape, &need);
+    if (workspace_bytes < need) return GR_E_SIZE;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es, ny = N * D * es, ns = N * kBranches * 4;
+    if (overlaps(R_host, nR, y_host, ny) || overlaps(R_host, nR, x_host, ny) ||
+        overlaps(x_host, ny, y_host, ny) || overlaps(s_prev_host, ns, s_next_host, ns) ||
+        overlaps(R_host, nR, s_next_host, ns) || overlaps(x_host, ny, s_next_host, ns))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    if (N == 0) return GR_OK;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(workspace);
+    void* dR = w;
+    void* dy = w + align256(nR);
+    void* dx = w + align256(nR) + align256(ny);
+    float* dsp = reinterpret_cast<float*>(w + align256(nR) + 2 * align256(ny));
+    float* dsn = reinterpret_cast<float*>(w + align256(nR) + 2 * align256(ny) + align256(ns));
+    if (cudaMemcpyAsync(dR, R_host, nR, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dy, y_host, ny, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dsp, s_prev_host, ns, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return GR_E_CUDA;
+    st = run_step(shape, dR, dy, dsp, next, dx, dsn, cs);
+    if (st) return st;
+    if (cudaMemcpyAsync(R_host, dR, nR, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaMemcpyAsync(x_host, dx, ny, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaMemcpyAsync(s_next_host, dsn, ns, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return GR_E_CUDA;
+    return status_of(cudaStreamSynchronize(cs));
+}
+
+}  // extern "C"

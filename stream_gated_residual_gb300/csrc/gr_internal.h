@@ -1,0 +1,100 @@
+// Internal declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gr.h"
+
+namespace gr {
+
+constexpr int kBranches = 4;
+
+// Layout of the packed parameter buffer written by gr_pack_params. Every section starts on a
+// 256-byte boundary. `w` is the weight element size (2 for bf16, 4 for fp32).
+//   gamma32 : fp32 [4][D]                      gains, used by the combine
+//   wdw     : W    [r+4][4D]                   rows 0..r-1 = W_d, rows r..r+3 = W_w
+//                                              (gamma folded on the bf16 path)
+//   wut     : W    [r][4D]                     W_u transposed
+//   frag    : bf16 fragment-ordered copies for the fused tensor-core kernel (bf16 path,
+//             d_model a multiple of 256, rank <= 32); see gr_fused_bf16.cu
+struct Layout {
+    size_t gamma32, wdw, wut, frag_down, frag_up, total;
+    size_t frag_down_bytes, frag_up_bytes;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Fragment-section sizes of the fused bf16 kernel (0 when the shape does not use it).
+size_t fused_frag_down_bytes(int D, int r);
+size_t fused_frag_up_bytes(int D, int r);
+bool fused_supported(int D, int r);
+
+inline Layout make_layout(int D, int r, int dtype) {
+    Layout L{};
+    const size_t K = size_t(kBranches) * D;
+    const size_t w = dtype == GR_BF16 ? 2 : 4;
+    size_t off = 0;
+    L.gamma32 = off;
+    off = align256(off + K * 4);
+    L.wdw = off;
+    off = align256(off + size_t(r + kBranches) * K * w);
+    L.wut = off;
+    off = align256(off + size_t(r) * K * w);
+    L.frag_down_bytes = (dtype == GR_BF16 && fused_supported(D, r)) ? fused_frag_down_bytes(D, r) : 0;
+    L.frag_up_bytes = (dtype == GR_BF16 && fused_supported(D, r)) ? fused_frag_up_bytes(D, r) : 0;
+    L.frag_down = off;
+    off = align256(off + L.frag_down_bytes);
+    L.frag_up = off;
+    off = align256(off + L.frag_up_bytes);
+    L.total = off;
+    return L;
+}
+
+// ---- launchers (return a cudaError_t from the launch) --------------------------------------
+
+// Pack fp32 parameters into `packed` following make_layout.
+cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float* wd,
+                        const float* wu, const float* ww, void* packed, cudaStream_t st);
+
+// Generic per-token kernel: optional write (y != nullptr) then optional read (x != nullptr).
+cudaError_t launch_generic(int64_t N, int D, int r, int dtype, float eps, void* R,
+                           const void* y, const float* s_prev, const void* packed, void* x,
+                           float* s_out, cudaStream_t st);
+
+// Fused bf16 tensor-core kernel (write then read, or read only when y == nullptr).
+cudaError_t launch_fused_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
+                              const float* s_prev, const void* packed, void* x, float* s_out,
+                              cudaStream_t st);
+
+// Streaming write R += s_i * y (no read).
+cudaError_t launch_write(int64_t N, int D, int dtype, void* R, const void* y, const float* s,
+                         cudaStream_t st);
+
+// Combine with given gates.
+cudaError_t launch_fixed_gates(int64_t N, int D, int dtype, float eps, const void* R,
+                               const float* gamma, const float* G, void* x, cudaStream_t st);
+
+// Single-stream x += y.
+cudaError_t launch_residual_add(int64_t n, int dtype, const void* y, void* x, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// ---- device helpers ------------------------------------------------------------------------
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Logistic function with the accurate expf (the fp32 path's 1e-5 budget).
+__device__ __forceinline__ float sigmoid_accurate(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+}  // namespace gr

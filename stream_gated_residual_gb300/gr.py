@@ -1,0 +1,263 @@
+"""Python binding of libgr_gb300.so: argument marshalling only.
+
+Every step of the Gated Residual read/write runs in the library's CUDA kernels; this module
+checks tensor devices, dtypes and contiguity, takes ``data_ptr()`` and the current CUDA stream,
+calls the C entry point of the same name and raises ``GRError`` on a non-zero status. PyTorch
+supplies device memory and streams. There is no fallback: if the library is missing, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+GR_F32, GR_BF16 = 0, 1
+GR_PARAMS_TAG = 0x47523330304B5031
+
+_DTYPES = {torch.float32: GR_F32, torch.bfloat16: GR_BF16}
+
+
+class GRError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int64), ("d_model", ctypes.c_int32),
+                ("n_branch", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("state_dtype", ctypes.c_int32), ("eps", ctypes.c_float)]
+
+
+class ParamsStruct(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("d_model", ctypes.c_int32),
+                ("n_branch", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("state_dtype", ctypes.c_int32), ("tag", ctypes.c_uint64)]
+
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libgr_gb300.so (built by ``__graft_entry__.build()``); raise if it is absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"{_build.LIB} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(_build.LIB)
+    P, S, V = ctypes.POINTER(ParamsStruct), ctypes.POINTER(Shape), ctypes.c_void_p
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "gr_api_version": ([], ctypes.c_int),
+        "gr_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "gr_kernel_path": ([S], ctypes.c_char_p),
+        "gr_packed_size": ([S, sz], ctypes.c_int),
+        "gr_pack_params": ([S, V, V, V, V, V, ctypes.c_size_t, P, V], ctypes.c_int),
+        "gr_read": ([S, V, P, V, V, V], ctypes.c_int),
+        "gr_write": ([S, V, V, V, V], ctypes.c_int),
+        "gr_write_then_read": ([S, V, V, V, P, V, V, V], ctypes.c_int),
+        "gr_read_fixed_gates": ([S, V, V, V, V, V], ctypes.c_int),
+        "gr_residual_add_ref": ([ctypes.c_int64, ctypes.c_int32, V, V, V], ctypes.c_int),
+        "gr_host_workspace_size": ([S, sz], ctypes.c_int),
+        "gr_write_then_read_host": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _LIB = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return load().gr_status_string(int(status)).decode()
+
+
+def kernel_path(n_tokens: int, d_model: int, rank: int, dtype: torch.dtype) -> str:
+    """Which kernel a read or fused step of this shape runs ("fused_bf16" or "generic")."""
+    return load().gr_kernel_path(ctypes.byref(make_shape(n_tokens, d_model, rank, dtype))).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise GRError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(None if t is None else t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_shape(n_tokens: int, d_model: int, rank: int, dtype: torch.dtype,
+               eps: float = 1e-6) -> Shape:
+    if dtype not in _DTYPES:
+        raise ValueError(f"state dtype must be float32 or bfloat16, got {dtype}")
+    return Shape(int(n_tokens), int(d_model), 4, int(rank), _DTYPES[dtype], float(eps))
+
+
+class Params:
+    """One GR module's packed parameters: the device buffer and its ``gr_params`` record."""
+
+    def __init__(self, buf: torch.Tensor, st: ParamsStruct, dtype: torch.dtype, eps: float):
+        self.buffer = buf
+        self.struct = st
+        self.dtype = dtype
+        self.eps = eps
+        self.d_model = st.d_model
+        self.rank = st.rank
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+def packed_size(d_model: int, rank: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().gr_packed_size(ctypes.byref(make_shape(0, d_model, rank, dtype)),
+                                 ctypes.byref(n)), "gr_packed_size")
+    return n.value
+
+
+def pack_params(gamma: torch.Tensor, w_down: torch.Tensor, w_up: torch.Tensor,
+                w_write: torch.Tensor, dtype: torch.dtype, eps: float = 1e-6,
+                stream=None) -> Params:
+    """gr_pack_params: fp32 CUDA tensors gamma [4,D], W_d [r,4D], W_u [4D,r], W_w [4,4D]."""
+    for t, n in ((gamma, "gamma"), (w_down, "w_down"), (w_up, "w_up"), (w_write, "w_write")):
+        _dev(t, n)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{n} must be float32")
+    r, K = w_down.shape
+    D = K // 4
+    if tuple(gamma.shape) != (4, D) or tuple(w_up.shape) != (K, r) or \
+            tuple(w_write.shape) != (4, K):
+        raise ValueError("parameter shapes must be gamma [4,D], W_d [r,4D], W_u [4D,r], "
+                         "W_w [4,4D]")
+    shape = make_shape(0, D, r, dtype, eps)
+    nbytes = packed_size(D, r, dtype)
+    buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=gamma.device)
+    off = (-buf.data_ptr()) % 256
+    view = buf[off:off + nbytes]
+    st = ParamsStruct()
+    _check(load().gr_pack_params(ctypes.byref(shape), _ptr(gamma), _ptr(w_down), _ptr(w_up),
+                                 _ptr(w_write), _ptr(view), nbytes, ctypes.byref(st),
+                                 _stream(stream)), "gr_pack_params")
+    p = Params(view, st, dtype, eps)
+    p._keep = buf
+    return p
+
+
+def _state_shape(R: torch.Tensor, params_or_rank, eps: float) -> Shape:
+    _dev(R, "R")
+    if R.dim() != 3 or R.shape[1] != 4:
+        raise ValueError("R must have shape [N, 4, D]")
+    rank = params_or_rank.rank if isinstance(params_or_rank, Params) else int(params_or_rank)
+    return make_shape(R.shape[0], R.shape[2], rank, R.dtype, eps)
+
+
+def read(R: torch.Tensor, params: Params, x: torch.Tensor | None = None,
+         s: torch.Tensor | None = None, stream=None):
+    """gr_read: R [N,4,D] -> (x [N,D], s [N,4] fp32)."""
+    shape = _state_shape(R, params, params.eps)
+    N, _, D = R.shape
+    x = torch.empty((N, D), dtype=R.dtype, device=R.device) if x is None else x
+    s = torch.empty((N, 4), dtype=torch.float32, device=R.device) if s is None else s
+    _dev(x, "x")
+    _dev(s, "s")
+    _check(load().gr_read(ctypes.byref(shape), _ptr(R), params.ref(), _ptr(x), _ptr(s),
+                          _stream(stream)), "gr_read")
+    return x, s
+
+
+def write(R: torch.Tensor, y: torch.Tensor, s: torch.Tensor, stream=None) -> torch.Tensor:
+    """gr_write: R += s_i y in place; returns R."""
+    shape = _state_shape(R, 1, 1e-6)
+    _dev(y, "y")
+    _dev(s, "s")
+    _check(load().gr_write(ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s), _stream(stream)),
+           "gr_write")
+    return R
+
+
+def write_then_read(R: torch.Tensor, y: torch.Tensor, s_prev: torch.Tensor, params: Params,
+                    x: torch.Tensor | None = None, s_next: torch.Tensor | None = None,
+                    stream=None):
+    """gr_write_then_read: R += s_prev_i y in place, then (x, s_next) = read(R, params)."""
+    shape = _state_shape(R, params, params.eps)
+    N, _, D = R.shape
+    x = torch.empty((N, D), dtype=R.dtype, device=R.device) if x is None else x
+    s_next = torch.empty((N, 4), dtype=torch.float32, device=R.device) if s_next is None \
+        else s_next
+    for t, n in ((y, "y"), (s_prev, "s_prev"), (x, "x"), (s_next, "s_next")):
+        _dev(t, n)
+    _check(load().gr_write_then_read(ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev),
+                                     params.ref(), _ptr(x), _ptr(s_next), _stream(stream)),
+           "gr_write_then_read")
+    return x, s_next
+
+
+def read_fixed_gates(R: torch.Tensor, gamma: torch.Tensor, G: torch.Tensor, eps: float = 1e-6,
+                     x: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gr_read_fixed_gates: x = (1/4) sum_i G_i * RMSNorm(R_i; gamma_i)."""
+    shape = _state_shape(R, 1, eps)
+    N, _, D = R.shape
+    x = torch.empty((N, D), dtype=R.dtype, device=R.device) if x is None else x
+    for t, n in ((gamma, "gamma"), (G, "G"), (x, "x")):
+        _dev(t, n)
+    _check(load().gr_read_fixed_gates(ctypes.byref(shape), _ptr(R), _ptr(gamma), _ptr(G),
+                                      _ptr(x), _stream(stream)), "gr_read_fixed_gates")
+    return x
+
+
+def residual_add_ref(x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:
+    """gr_residual_add_ref: x += y (single stream), in place."""
+    _dev(x, "x")
+    _dev(y, "y")
+    if x.dtype not in _DTYPES or y.dtype != x.dtype or x.numel() != y.numel():
+        raise ValueError("x and y must have the same size and dtype (float32 or bfloat16)")
+    _check(load().gr_residual_add_ref(x.numel(), _DTYPES[x.dtype], _ptr(y), _ptr(x),
+                                      _stream(stream)), "gr_residual_add_ref")
+    return x
+
+
+def host_workspace_size(n_tokens: int, d_model: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().gr_host_workspace_size(ctypes.byref(make_shape(n_tokens, d_model, 1, dtype)),
+                                         ctypes.byref(n)), "gr_host_workspace_size")
+    return n.value
+
+
+def write_then_read_host(R: torch.Tensor, y: torch.Tensor, s_prev: torch.Tensor,
+                         params: Params, x: torch.Tensor, s_next: torch.Tensor,
+                         workspace: torch.Tensor, stream=None):
+    """gr_write_then_read_host on CPU tensors (pinned for asynchronous copies); `workspace` is
+    a CUDA uint8 tensor of at least host_workspace_size() bytes, 256-byte aligned."""
+    for t, n in ((R, "R"), (y, "y"), (s_prev, "s_prev"), (x, "x"), (s_next, "s_next")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    N, _, D = R.shape
+    shape = make_shape(N, D, params.rank, R.dtype, params.eps)
+    _check(load().gr_write_then_read_host(
+        ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev), params.ref(), _ptr(x), _ptr(s_next),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "gr_write_then_read_host")
+    return x, s_next

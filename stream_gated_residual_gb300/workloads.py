@@ -14,14 +14,16 @@ W_d ``[r, 4D]``, W_u ``[4D, r]``, W_w ``[4, 4D]``.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 
 import numpy as np
 
 N_BRANCH = 4
 
-# independent random streams per array kind: default_rng([seed, kind, layer])
+# independent random streams per array kind: default_rng([seed, kind, layer(, chunk)])
 _K_STATE, _K_Y, _K_PARAMS, _K_S, _K_OUTLIER = 1, 2, 3, 4, 5
 
 
@@ -108,17 +110,37 @@ def to_f64(a: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------------------------
 # generators
 
-def _rng(w: Workload, kind: int, layer: int = 0) -> np.random.Generator:
-    return np.random.default_rng([w.seed, kind, layer])
+CHUNK_ROWS = 1024  # rows per independent random stream (part of the recipe)
 
 
-def _normal_f32(rng, shape, chunk_rows: int = 4096) -> np.ndarray:
-    """Standard normal float32 array drawn row-chunk by row-chunk (bounded host memory)."""
-    out = np.empty(shape, dtype=np.float32)
-    flat = out.reshape(shape[0], -1)
-    for a in range(0, shape[0], chunk_rows):
-        b = min(shape[0], a + chunk_rows)
-        flat[a:b] = rng.standard_normal((b - a, flat.shape[1]), dtype=np.float32)
+def _rng(w: Workload, kind: int, layer: int = 0, chunk: int | None = None):
+    key = [w.seed, kind, layer] if chunk is None else [w.seed, kind, layer, chunk]
+    return np.random.default_rng(key)
+
+
+def _draw_rows(w: Workload, kind: int, layer: int, n_rows: int, row_shape: tuple, fill,
+               dtype: str) -> np.ndarray:
+    """Draw an [n_rows, *row_shape] array chunk by chunk: chunk q (rows q*CHUNK_ROWS ...) comes
+    from its own stream default_rng([seed, kind, layer, q]) through ``fill(rng, rows)``
+    (float32), then is rounded to the storage dtype. Chunks run on a thread pool; the result
+    does not depend on the thread count, and the first n rows do not depend on n_rows."""
+    itemsize = 2 if dtype == "bf16" else 4
+    out = np.empty((n_rows,) + tuple(row_shape), dtype=np.uint16 if itemsize == 2 else np.float32)
+
+    def one(q):
+        a = q * CHUNK_ROWS
+        b = min(n_rows, a + CHUNK_ROWS)
+        vals = fill(_rng(w, kind, layer, q), b - a)
+        out[a:b] = to_storage(vals, dtype)
+
+    nchunks = (n_rows + CHUNK_ROWS - 1) // CHUNK_ROWS
+    if nchunks <= 1:
+        for q in range(nchunks):
+            one(q)
+    else:
+        workers = min(nchunks, os.cpu_count() or 1, 32)
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(one, range(nchunks)))
     return out
 
 
@@ -134,37 +156,37 @@ def make_state(w: Workload, n_tokens: int | None = None) -> np.ndarray:
     """Initial residual state R [N, 4, D] in storage dtype: N(0,1) per branch, times the
     branch scale, times outlier_mult on the outlier channels (all tokens and branches)."""
     n = w.n_tokens if n_tokens is None else n_tokens
-    rng = _rng(w, _K_STATE)
-    R = _normal_f32(rng, (n, N_BRANCH, w.d_model))
     scales = np.asarray(w.branch_scales, dtype=np.float32)
-    if np.any(scales != 1.0):
-        R *= scales[None, :, None]
     ch = outlier_channels(w)
-    if ch.size:
-        R[:, :, ch] *= np.float32(w.outlier_mult)
-    return to_storage(R, w.dtype)
+
+    def fill(rng, rows):
+        R = rng.standard_normal((rows, N_BRANCH, w.d_model), dtype=np.float32)
+        if np.any(scales != 1.0):
+            R *= scales[None, :, None]
+        if ch.size:
+            R[:, :, ch] *= np.float32(w.outlier_mult)
+        return R
+
+    return _draw_rows(w, _K_STATE, 0, n, (N_BRANCH, w.d_model), fill, w.dtype)
 
 
 def make_y(w: Workload, layer: int = 0, n_tokens: int | None = None) -> np.ndarray:
     """Sublayer output y [N, D] in storage dtype: y_std * N(0,1), or y_std * Student-t(3)."""
     n = w.n_tokens if n_tokens is None else n_tokens
-    rng = _rng(w, _K_Y, layer)
-    if w.y_kind == "normal":
-        y = _normal_f32(rng, (n, w.d_model))
-        y *= np.float32(w.y_std)
-    elif w.y_kind == "t3":
-        y = np.empty((n, w.d_model), dtype=np.float32)
-        for a in range(0, n, 4096):
-            b = min(n, a + 4096)
-            y[a:b] = (w.y_std * rng.standard_t(3, size=(b - a, w.d_model))).astype(np.float32)
-    else:
+    if w.y_kind not in ("normal", "t3"):
         raise ValueError(w.y_kind)
-    return to_storage(y, w.dtype)
+
+    def fill(rng, rows):
+        if w.y_kind == "normal":
+            return rng.standard_normal((rows, w.d_model), dtype=np.float32) * np.float32(w.y_std)
+        return (w.y_std * rng.standard_t(3, size=(rows, w.d_model))).astype(np.float32)
+
+    return _draw_rows(w, _K_Y, layer, n, (w.d_model,), fill, w.dtype)
 
 
 def make_params(w: Workload, layer: int = 0, weight_mult: float = 1.0) -> dict:
-    """Per-sublayer parameters: gains 1 (times the branch scale factors of the config are
-    applied to the state, not here), W_d, W_u, W_w ~ N(0, weight_std) * weight_mult.
+    """Per-sublayer parameters: gains 1 (the workloads' branch scales act on the state, see
+    make_state), W_d, W_u, W_w ~ N(0, weight_std) * weight_mult.
     On bf16 workloads the weights are rounded to bf16-representable float32 values."""
     rng = _rng(w, _K_PARAMS, layer)
     K = N_BRANCH * w.d_model

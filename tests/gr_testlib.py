@@ -1,0 +1,58 @@
+"""Shared helpers of the tests: moving workload arrays to torch, per-row error metrics."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from stream_gated_residual_gb300 import workloads as wl
+
+# tolerances on the per-row relative L2 error (max over rows): fp32 path, bf16 path
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def to_torch(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """Storage array (bf16 bits as uint16, or float32) -> torch tensor with the same bytes."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(
+            device)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def params_to_torch(p: dict, device="cuda") -> dict:
+    return {k: torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(device)
+            for k, v in p.items()}
+
+
+def rel_rows(a, b) -> float:
+    """max over rows of ||a_row - b_row||_2 / ||b_row||_2 (rows = all but the last axis)."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    a2 = a.reshape(-1, a.shape[-1])
+    b2 = b.reshape(-1, b.shape[-1])
+    num = np.linalg.norm(a2 - b2, axis=1)
+    den = np.maximum(np.linalg.norm(b2, axis=1), 1e-30)
+    return float(np.max(num / den)) if len(num) else 0.0
+
+
+def max_abs(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:
+    """A seeded sorted sample of k token rows, always including the first and last."""
+    if n <= k:
+        return np.arange(n)
+    rng = np.random.default_rng([seed, 99])
+    pick = rng.choice(np.arange(1, n - 1), size=k - 2, replace=False)
+    return np.sort(np.concatenate([[0, n - 1], pick]))
+
+
+__all__ = ["TOL", "TORCH_DTYPE", "to_torch", "to_f64", "params_to_torch", "rel_rows", "max_abs",
+           "sample_rows", "wl"]

@@ -1,0 +1,119 @@
+"""The C-ABI library loads on the CPU host and exports every symbol include/gr.h declares; the
+host-side validation rejects bad arguments before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from stream_gated_residual_gb300 import build as gbuild
+from stream_gated_residual_gb300 import gr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gr.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(gr_\w+)\s*\(", text, re.M)))
+
+
+def header_constant(name):
+    text = open(HEADER).read()
+    m = re.search(rf"{name}\s*=\s*(-?\d+)", text) or re.search(rf"#define {name}\s+(\w+)", text)
+    return int(m.group(1), 0)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in gr.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gr_api_version() == header_constant("GR_API_VERSION")
+    for code in range(0, -12, -1):
+        s = gr.status_string(code)
+        assert s and s != "unknown status", code
+    assert gr.status_string(-99) == "unknown status"
+
+
+def _shape(n=4, d=64, nb=4, r=8, dt=gr.GR_BF16, eps=1e-6):
+    return gr.Shape(n, d, nb, r, dt, eps)
+
+
+FAKE = ctypes.c_void_p(0x10000)          # 16-byte aligned, never dereferenced on the host
+FAKE2 = ctypes.c_void_p(0x20000000)
+FAKE3 = ctypes.c_void_p(0x40000000)
+FAKE4 = ctypes.c_void_p(0x60000000)
+FAKE5 = ctypes.c_void_p(0x70000000)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), "GR_E_SHAPE"), (dict(d=12), "GR_E_SHAPE"), (dict(d=0), "GR_E_SHAPE"),
+    (dict(d=12296), "GR_E_SHAPE"), (dict(nb=3), "GR_E_SHAPE"), (dict(r=0), "GR_E_RANK"),
+    (dict(r=65), "GR_E_RANK"), (dict(dt=7), "GR_E_DTYPE"), (dict(eps=-1.0), "GR_E_EPS"),
+    (dict(eps=float("inf")), "GR_E_EPS")])
+def test_packed_size_rejects_bad_shapes(lib, kw, code):
+    n = ctypes.c_size_t(0)
+    st = lib.gr_packed_size(ctypes.byref(_shape(**kw)), ctypes.byref(n))
+    assert st == header_constant(code)
+
+
+def test_packed_size_grows_with_shape(lib):
+    def size(d, r, dt):
+        n = ctypes.c_size_t(0)
+        assert lib.gr_packed_size(ctypes.byref(_shape(d=d, r=r, dt=dt)), ctypes.byref(n)) == 0
+        return n.value
+    assert size(256, 8, gr.GR_F32) > size(256, 8, gr.GR_BF16) > 0
+    assert size(512, 8, gr.GR_BF16) > size(256, 8, gr.GR_BF16)
+    assert size(256, 16, gr.GR_BF16) > size(256, 8, gr.GR_BF16)
+    assert size(256, 8, gr.GR_BF16) % 256 == 0
+
+
+def test_calls_validate_before_any_launch(lib):
+    sh = ctypes.byref(_shape())
+    null = ctypes.c_void_p(None)
+    E = header_constant
+    p = gr.ParamsStruct()
+    # params never packed
+    assert lib.gr_read(sh, FAKE, ctypes.byref(p), FAKE2, FAKE3, null) == E("GR_E_PARAMS")
+    p.tag = gr.GR_PARAMS_TAG
+    p.packed = 0x1000
+    p.d_model, p.n_branch, p.rank, p.state_dtype = 64, 4, 8, gr.GR_BF16
+    pr = ctypes.byref(p)
+    assert lib.gr_read(None, FAKE, pr, FAKE2, FAKE3, null) == E("GR_E_NULL")
+    assert lib.gr_read(sh, null, pr, FAKE2, FAKE3, null) == E("GR_E_NULL")
+    assert lib.gr_read(sh, ctypes.c_void_p(0x10008), pr, FAKE2, FAKE3, null) == E("GR_E_ALIGN")
+    assert lib.gr_read(sh, FAKE, pr, FAKE, FAKE3, null) == E("GR_E_ALIAS")
+    # params packed for another shape
+    p.rank = 16
+    assert lib.gr_read(sh, FAKE, pr, FAKE2, FAKE3, null) == E("GR_E_PARAMS")
+    p.rank = 8
+    assert lib.gr_write(sh, FAKE, FAKE, FAKE3, null) == E("GR_E_ALIAS")
+    assert lib.gr_write(sh, null, FAKE2, FAKE3, null) == E("GR_E_NULL")
+    # x may equal y; x may not overlap R
+    assert lib.gr_write_then_read(sh, FAKE, FAKE2, FAKE3, pr, FAKE, FAKE4, null) == E("GR_E_ALIAS")
+    assert lib.gr_write_then_read(sh, FAKE, FAKE2, FAKE3, pr, FAKE4, FAKE2, null) == \
+        E("GR_E_ALIAS")
+    # pack: misaligned packed buffer, too small a buffer
+    out = gr.ParamsStruct()
+    assert lib.gr_pack_params(sh, FAKE, FAKE2, FAKE3, FAKE4, ctypes.c_void_p(0x70000010), 1 << 30,
+                              ctypes.byref(out), null) == E("GR_E_ALIGN")
+    assert lib.gr_pack_params(sh, FAKE, FAKE2, FAKE3, FAKE4, FAKE5, 16, ctypes.byref(out),
+                              null) == E("GR_E_SIZE")
+    assert out.tag == 0  # untouched on error
+    assert lib.gr_residual_add_ref(-1, gr.GR_BF16, FAKE, FAKE2, null) == E("GR_E_SHAPE")
+    assert lib.gr_residual_add_ref(16, 5, FAKE, FAKE2, null) == E("GR_E_DTYPE")
+    assert lib.gr_residual_add_ref(64, gr.GR_BF16, FAKE, FAKE, null) == E("GR_E_ALIAS")
+    ws = ctypes.c_size_t(0)
+    assert lib.gr_host_workspace_size(sh, ctypes.byref(ws)) == 0 and ws.value > 0
+    assert lib.gr_write_then_read_host(sh, FAKE, FAKE2, FAKE3, pr, FAKE4, FAKE5, FAKE, 16,
+                                       null) == E("GR_E_SIZE")

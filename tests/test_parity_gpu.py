@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 oracle, element by element
+on seeded inputs, per-row relative L2 error within 1e-5 (fp32 states) / 2e-2 (bf16 states)."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gr_testlib import TOL, TORCH_DTYPE, max_abs, params_to_torch, rel_rows, sample_rows, \
+    to_f64, to_torch
+from stream_gated_residual_gb300 import gr
+from stream_gated_residual_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    gr.load()
+    oracle.build()
+
+
+def _pack(p: dict, dtype: str, eps: float):
+    t = params_to_torch(p)
+    return gr.pack_params(t["gamma"], t["w_down"], t["w_up"], t["w_write"], TORCH_DTYPE[dtype],
+                          eps)
+
+
+def fused_case(w: wl.Workload, n_tokens=None, weight_mult=1.0, random_gamma=False,
+               rows=None, chunk=2048):
+    """One fused write→read on the GPU; the oracle on `rows` (all rows if None)."""
+    N = w.n_tokens if n_tokens is None else n_tokens
+    R = wl.make_state(w, N)
+    y = wl.make_y(w, 0, N)
+    s_prev = wl.make_s_prev(w, N)
+    p = wl.make_params(w, 1, weight_mult)
+    if random_gamma:
+        p["gamma"] = wl.make_random_gamma(w, 1)
+    Rt, yt, st = to_torch(R), to_torch(y), torch.from_numpy(s_prev).cuda()
+    P = _pack(p, w.dtype, w.eps)
+    x, s = gr.write_then_read(Rt, yt, st, P)
+    torch.cuda.synchronize()
+    rows = np.arange(N) if rows is None else rows
+    err = {"R": 0.0, "x": 0.0, "s": 0.0}
+    for a in range(0, len(rows), chunk):
+        idx = rows[a:a + chunk]
+        Ro, xo, so = oracle.write_then_read(wl.to_f64(R[idx]), wl.to_f64(y[idx]), s_prev[idx], p,
+                                            w.eps)
+        sel = torch.from_numpy(idx).cuda()
+        err["R"] = max(err["R"], rel_rows(to_f64(Rt[sel]), Ro))
+        err["x"] = max(err["x"], rel_rows(to_f64(x[sel]), xo))
+        err["s"] = max(err["s"], rel_rows(to_f64(s[sel]), so))
+    assert torch.isfinite(x.float()).all() and torch.isfinite(Rt.float()).all()
+    assert bool(((s > 0) & (s < 2)).all())
+    return err
+
+
+def test_tiny_fp32_read_then_write():
+    """Tiny fp32 GR step: one read, then one write with the read's s (tol 1e-5)."""
+    w = wl.WORKLOADS["tiny_fp32"]
+    R = wl.make_state(w)
+    y = wl.make_y(w)
+    p = wl.make_params(w)
+    Rt = to_torch(R)
+    P = _pack(p, "f32", w.eps)
+    x, s = gr.read(Rt, P)
+    xo, so = oracle.read(wl.to_f64(R), p["gamma"], p["w_down"], p["w_up"], p["w_write"], w.eps)
+    assert rel_rows(to_f64(x), xo) < TOL["f32"]
+    assert rel_rows(to_f64(s), so) < TOL["f32"]
+    gr.write(Rt, to_torch(y), s)
+    Ro = oracle.write(wl.to_f64(R), wl.to_f64(y), to_f64(s))
+    assert rel_rows(to_f64(Rt), Ro) < TOL["f32"]
+
+
+def test_tiny_fp32_fused():
+    e = fused_case(wl.WORKLOADS["tiny_fp32"])
+    assert max(e.values()) < TOL["f32"], e
+
+
+@pytest.mark.parametrize("N,D,r", [(1, 8, 1), (3, 8, 3), (17, 264, 5), (33, 520, 64),
+                                   (5, 4104, 16)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_odd_shapes(N, D, r, dtype):
+    w = wl.Workload("odd", N, D, r, dtype, y_std=0.5, seed=7)
+    e = fused_case(w, random_gamma=True)
+    assert max(e.values()) < TOL[dtype], e
+
+
+def test_decode_full():
+    """N=128, D=4096, r=16, bf16: all rows."""
+    e = fused_case(wl.WORKLOADS["decode"])
+    assert max(e.values()) < TOL["bf16"], e
+
+
+def test_decode_sharp_gates_and_random_gamma():
+    """Weights x50 (gate logits far from 0, so G and s leave 1/2 and 1) and non-unit gains."""
+    e = fused_case(wl.WORKLOADS["decode"], weight_mult=50.0, random_gamma=True)
+    assert max(e.values()) < TOL["bf16"], e
+
+
+def test_prefill_full():
+    """N=16384, D=4096, r=16, bf16: every row against the oracle (in chunks)."""
+    e = fused_case(wl.WORKLOADS["prefill"])
+    assert max(e.values()) < TOL["bf16"], e
+
+
+def test_large_skewed_subset():
+    """The skewed distribution (branch scales 0.1/1/10/100, 1% outlier channels x50, y from
+    Student-t(3)), D=7168, r=32, on the first 1024 tokens."""
+    e = fused_case(wl.WORKLOADS["large_skewed"], n_tokens=1024)
+    assert max(e.values()) < TOL["bf16"], e
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_equals_write_then_read_separately(dtype):
+    """The fused call reads the stored state, so it equals gr_write followed by gr_read."""
+    w = wl.Workload("sep", 64, 512, 16, dtype, y_std=0.5, seed=3)
+    R = wl.make_state(w)
+    y = to_torch(wl.make_y(w))
+    sp = torch.from_numpy(wl.make_s_prev(w)).cuda()
+    P = _pack(wl.make_params(w, 1), dtype, w.eps)
+    R1, R2 = to_torch(R), to_torch(R)
+    x1, s1 = gr.write_then_read(R1, y, sp, P)
+    gr.write(R2, y, sp)
+    x2, s2 = gr.read(R2, P)
+    assert torch.equal(R1, R2)
+    tol = 0 if dtype == "f32" else 2e-3
+    assert rel_rows(to_f64(x1), to_f64(x2)) <= tol and rel_rows(to_f64(s1), to_f64(s2)) <= tol
+
+
+def test_empty_and_in_place_aliases():
+    w = wl.Workload("alias", 8, 256, 8, "bf16", y_std=0.5, seed=5)
+    P = _pack(wl.make_params(w), "bf16", w.eps)
+    R0 = to_torch(wl.make_state(w))
+    y = to_torch(wl.make_y(w))
+    sp = torch.from_numpy(wl.make_s_prev(w)).cuda()
+    # N = 0 is a valid no-op
+    x0, s0 = gr.write_then_read(R0[:0], y[:0], sp[:0], P)
+    assert x0.shape == (0, 256)
+    # x may be y's buffer and s_next may be s_prev's buffer
+    Ra, Rb = R0.clone(), R0.clone()
+    xa, sa = gr.write_then_read(Ra, y.clone(), sp.clone(), P)
+    yb, spb = y.clone(), sp.clone()
+    gr.write_then_read(Rb, yb, spb, P, x=yb, s_next=spb)
+    assert torch.equal(Ra, Rb) and torch.equal(xa, yb) and torch.equal(sa, spb)
+
+
+def test_host_entry_matches_device_entry():
+    w = wl.Workload("host", 256, 1024, 16, "bf16", y_std=0.5, seed=11)
+    R, y, sp = wl.make_state(w), wl.make_y(w), wl.make_s_prev(w)
+    P = _pack(wl.make_params(w, 1), "bf16", w.eps)
+    Rd = to_torch(R)
+    xd, sd = gr.write_then_read(Rd, to_torch(y), torch.from_numpy(sp).cuda(), P)
+    Rh = to_torch(R, "cpu").pin_memory()
+    yh = to_torch(y, "cpu").pin_memory()
+    sph = torch.from_numpy(sp).pin_memory()
+    xh = torch.empty((w.n_tokens, w.d_model), dtype=torch.bfloat16).pin_memory()
+    sh = torch.empty((w.n_tokens, 4), dtype=torch.float32).pin_memory()
+    nws = gr.host_workspace_size(w.n_tokens, w.d_model, torch.bfloat16)
+    buf = torch.empty(nws + 256, dtype=torch.uint8, device="cuda")
+    ws = buf[(-buf.data_ptr()) % 256:][:nws]
+    gr.write_then_read_host(Rh, yh, sph, P, xh, sh, ws)
+    assert torch.equal(Rh, Rd.cpu()) and torch.equal(xh, xd.cpu()) and torch.equal(sh, sd.cpu())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prenorm_reduction_on_gpu(dtype):
+    """One-hot read gates with γ_0 = 4·γ_pre and writes (1,0,0,0): branch 0 follows the
+    Pre-Norm residual x ← x + F(RMSNorm(x)) (Digest §二.2 and §二.4). F is a seeded linear map
+    applied with torch; the reference loop runs in fp64 on the CPU."""
+    rng = np.random.default_rng(21)
+    N, D, L, eps = 64, 256, 8, 1e-6
+    dt = TORCH_DTYPE[dtype]
+    gamma_pre = (1.0 + 0.2 * rng.standard_normal(D))
+    Ms = [rng.standard_normal((D, D)) / math.sqrt(D) for _ in range(L)]
+    R0 = wl.make_state(wl.Workload("pn", N, D, 8, dtype, y_std=1.0, seed=21))
+    R = to_torch(R0)
+    gamma = np.ones((4, D))
+    gamma[0] = 4 * gamma_pre
+    G = np.zeros((4, D))
+    G[0] = 1.0
+    g_t = torch.tensor(gamma, dtype=torch.float32, device="cuda")
+    G_t = torch.tensor(G, dtype=torch.float32, device="cuda")
+    s = torch.zeros((N, 4), dtype=torch.float32, device="cuda")
+    s[:, 0] = 1.0
+    x_ref = wl.to_f64(R0)[:, 0, :].copy()
+    others = R[:, 1:, :].clone()
+    for l in range(L):
+        xin = gr.read_fixed_gates(R, g_t, G_t, eps)
+        y = (xin.float() @ torch.tensor(Ms[l], dtype=torch.float32, device="cuda")).to(dt)
+        gr.write(R, y.contiguous(), s)
+        rn = x_ref / np.sqrt(np.mean(x_ref ** 2, axis=1, keepdims=True) + eps) * gamma_pre
+        x_ref = x_ref + rn @ Ms[l]
+    tol = 1e-5 if dtype == "f32" else 5e-2
+    assert rel_rows(to_f64(R[:, 0, :]), x_ref) < tol
+    assert torch.equal(R[:, 1:, :], others)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_residual_add_reference(dtype):
+    n = 1_000_003  # not a multiple of 8: vector body plus scalar tail
+    rng = np.random.default_rng(4)
+    xs = wl.to_storage(rng.standard_normal(n).astype(np.float32), dtype)
+    ys = wl.to_storage(rng.standard_normal(n).astype(np.float32), dtype)
+    x, y = to_torch(xs), to_torch(ys)
+    gr.residual_add_ref(x, y)
+    expect = oracle.residual_add(wl.to_f64(xs), wl.to_f64(ys))
+    if dtype == "bf16":
+        expect = wl.to_f64(wl.to_storage(expect.astype(np.float32), "bf16"))
+        # fp32 sum of two bf16 values is exact; one rounding to bf16 on both sides
+        assert np.array_equal(to_f64(x), expect)
+    else:
+        assert max_abs(to_f64(x), expect) <= 1e-6 * np.max(np.abs(expect))
+
+
+def test_calls_reject_cpu_tensors():
+    w = wl.Workload("cpu", 4, 64, 8, "bf16", y_std=0.5)
+    P = _pack(wl.make_params(w), "bf16", w.eps)
+    with pytest.raises(ValueError):
+        gr.read(to_torch(wl.make_state(w), "cpu"), P)
