@@ -30,7 +30,7 @@
  *   - Every call validates its arguments on the host first. On any validation error it returns
  *     a negative status, launches nothing and touches no output. A status of GR_E_CUDA means a
  *     launch or copy failed; the CUDA error is not cleared from the runtime.
- *   - n_tokens == 0 is valid and does nothing.
+ *   - n_tokens == 0 is valid and does nothing; the tensor pointers may then be NULL.
  */
 #ifndef GR_GB300_H
 #define GR_GB300_H

@@ -9,7 +9,7 @@ The functions here take numpy arrays of any float dtype, convert them exactly to
 return float64 arrays.
 """
 from .oracle import (build, chain, lib, num_threads, read, read_fixed_gates, residual_add,
-                     set_num_threads, use_library, write, write_then_read)
+                     round_to_storage, set_num_threads, use_library, write, write_then_read)
 
 __all__ = ["build", "chain", "lib", "num_threads", "read", "read_fixed_gates", "residual_add",
-           "set_num_threads", "use_library", "write", "write_then_read"]
+           "round_to_storage", "set_num_threads", "use_library", "write", "write_then_read"]

@@ -221,6 +221,30 @@ int gro_read_fixed_gates(int64_t n, int nb, int D, double eps, const double *R,
     return failed ? -2 : 0;
 }
 
+/* Round v to the nearest value with `bits` significant bits, ties to even (normal range).
+ * bits = 8 is bfloat16 (7 stored fraction bits), bits = 24 is IEEE binary32. Used to model a
+ * state stored in that format: the read after a write sees the stored value. */
+static double round_significand(double v, int bits)
+{
+    if (v == 0.0 || !isfinite(v))
+        return v;
+    int e;
+    frexp(v, &e);                       /* v = m·2^e, 0.5 <= |m| < 1 */
+    double scale = ldexp(1.0, bits - e); /* |v|·scale in [2^(bits-1), 2^bits) */
+    return nearbyint(v * scale) / scale; /* default rounding mode: nearest, ties to even */
+}
+
+/* In place: v[e] = round_significand(v[e], bits) for e < n. */
+int gro_round_significand(int64_t n, int bits, double *v)
+{
+    if (n < 0 || bits < 2 || bits > 52 || !v)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < n; ++e)
+        v[e] = round_significand(v[e], bits);
+    return 0;
+}
+
 /* Single-stream residual add x += y (the bandwidth reference path), n elements. */
 int gro_residual_add(int64_t n, const double *y, double *x)
 {

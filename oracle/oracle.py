@@ -36,11 +36,12 @@ def _load(path: str) -> ctypes.CDLL:
     L.gro_write_then_read.argtypes = [i64, i32, i32, i32, f64, P, P, P, P, P, P, P, P, P, P]
     L.gro_read_fixed_gates.argtypes = [i64, i32, i32, f64, P, P, P, P]
     L.gro_residual_add.argtypes = [i64, P, P]
+    L.gro_round_significand.argtypes = [i64, i32, P]
     L.gro_num_threads.argtypes = []
     L.gro_set_num_threads.argtypes = [i32]
     L.gro_set_num_threads.restype = None
     for f in ("gro_read", "gro_write", "gro_write_then_read", "gro_read_fixed_gates",
-              "gro_residual_add", "gro_num_threads"):
+              "gro_residual_add", "gro_num_threads", "gro_round_significand"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -120,13 +121,32 @@ def write(R, y, s):
     return out
 
 
-def write_then_read(R, y, s_prev, params: dict, eps: float = 1e-6):
+_STORE_BITS = {"bf16": 8, "f32": 24}
+
+
+def round_to_storage(a, dtype: str):
+    """Nearest value representable in the storage format (bf16: 8 significant bits, f32: 24),
+    ties to even, as a new float64 array."""
+    out = _f64(a).copy()
+    _check(lib().gro_round_significand(out.size, _STORE_BITS[dtype], _p(out)), "round")
+    return out
+
+
+def write_then_read(R, y, s_prev, params: dict, eps: float = 1e-6, store: str | None = None):
     """Fused step: the write with s_prev, then the read with ``params`` (keys gamma, w_down,
-    w_up, w_write). Returns (R', x, s_next); R' stays in fp64."""
+    w_up, w_write). Returns (R', x, s_next).
+
+    store=None keeps R' in fp64 and reads it as is (the plain definition). store="bf16" or
+    "f32" rounds R' to that storage format first and reads the stored value, as the library
+    does (a fused write→read reads the state it has just stored)."""
     R, y, s_prev = _f64(R), _f64(y), _f64(s_prev)
     n, nb, D = R.shape
     gamma, Wd, Wu, Ww = (_f64(params[k]) for k in ("gamma", "w_down", "w_up", "w_write"))
     r = Wd.shape[0]
+    if store is not None:
+        Rw = round_to_storage(write(R, y, s_prev), store)
+        x, s = read(Rw, gamma, Wd, Wu, Ww, eps)
+        return Rw, x, s
     R_out = np.empty_like(R)
     x = np.empty((n, D))
     s = np.empty((n, nb))

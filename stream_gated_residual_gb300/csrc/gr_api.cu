@@ -173,6 +173,7 @@ int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void*
     int st = validate_shape(shape);
     if (st) return st;
     if ((st = validate_params(shape, params))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
     if (!R || !x || !s) return GR_E_NULL;
     if (!aligned16(R) || !aligned16(x) || !aligned16(s)) return GR_E_ALIGN;
     const size_t es = elem_size(shape->state_dtype);
@@ -188,6 +189,7 @@ int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void*
 int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void* stream) {
     int st = validate_shape(shape);
     if (st) return st;
+    if (shape->n_tokens == 0) return GR_OK;
     if (!R || !y || !s) return GR_E_NULL;
     if (!aligned16(R) || !aligned16(y) || !aligned16(s)) return GR_E_ALIGN;
     const size_t es = elem_size(shape->state_dtype);
@@ -205,6 +207,7 @@ int gr_write_then_read(const gr_shape* shape, void* R, const void* y, const floa
     int st = validate_shape(shape);
     if (st) return st;
     if ((st = validate_params(shape, next))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
     if (!R || !y || !s_prev || !x || !s_next) return GR_E_NULL;
     if (!aligned16(R) || !aligned16(y) || !aligned16(s_prev) || !aligned16(x) ||
         !aligned16(s_next))
@@ -225,6 +228,7 @@ int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma
                         const float* G, void* x, void* stream) {
     int st = validate_shape(shape);
     if (st) return st;
+    if (shape->n_tokens == 0) return GR_OK;
     if (!R || !gamma || !G || !x) return GR_E_NULL;
     if (!aligned16(R) || !aligned16(x)) return GR_E_ALIGN;
     const size_t es = elem_size(shape->state_dtype);
@@ -239,6 +243,7 @@ int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma
 int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* stream) {
     if (n < 0) return GR_E_SHAPE;
     if (dtype != GR_F32 && dtype != GR_BF16) return GR_E_DTYPE;
+    if (n == 0) return GR_OK;
     if (!y || !x) return GR_E_NULL;
     if (!aligned16(y) || !aligned16(x)) return GR_E_ALIGN;
     if (overlaps(x, size_t(n) * elem_size(dtype), y, size_t(n) * elem_size(dtype)))
@@ -266,6 +271,7 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
     int st = validate_shape(shape);
     if (st) return st;
     if ((st = validate_params(shape, next))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
     if (!R_host || !y_host || !s_prev_host || !x_host || !s_next_host || !workspace)
         return GR_E_NULL;
     if (!aligned256(workspace)) return GR_E_ALIGN;

@@ -45,6 +45,24 @@ def max_abs(a, b) -> float:
     return float(np.max(np.abs(a - b))) if a.size else 0.0
 
 
+def bf16_path_params(p: dict) -> dict:
+    """The parameters the bf16 path computes with, written as oracle inputs: W_d and W_w with
+    gamma folded in and rounded to bf16 (fp32 product, nearest even), divided back by gamma in
+    fp64 so that the oracle's W·(γ ⊙ R) reproduces the folded weight; W_u rounded to bf16.
+    Computed here from the fp32 inputs, never read back from the GPU."""
+    K = p["w_down"].shape[1]
+    g = np.asarray(p["gamma"], dtype=np.float32).reshape(-1)
+    assert g.size == K and np.all(g != 0)
+
+    def fold(W):
+        Wf = wl.round_to_bf16((np.asarray(W, dtype=np.float32) * g[None, :]).astype(np.float32))
+        return Wf.astype(np.float64) / g.astype(np.float64)[None, :]
+
+    return {"gamma": np.asarray(p["gamma"], dtype=np.float64), "w_down": fold(p["w_down"]),
+            "w_up": wl.round_to_bf16(np.asarray(p["w_up"], dtype=np.float32)).astype(np.float64),
+            "w_write": fold(p["w_write"])}
+
+
 def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:
     """A seeded sorted sample of k token rows, always including the first and last."""
     if n <= k:
@@ -55,4 +73,4 @@ def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:
 
 
 __all__ = ["TOL", "TORCH_DTYPE", "to_torch", "to_f64", "params_to_torch", "rel_rows", "max_abs",
-           "sample_rows", "wl"]
+           "sample_rows", "bf16_path_params", "wl"]

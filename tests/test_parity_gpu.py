@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gr_testlib import TOL, TORCH_DTYPE, max_abs, params_to_torch, rel_rows, sample_rows, \
-    to_f64, to_torch
+from gr_testlib import TOL, TORCH_DTYPE, bf16_path_params, max_abs, params_to_torch, \
+    rel_rows, to_f64, to_torch
 from stream_gated_residual_gb300 import gr
 from stream_gated_residual_gb300 import workloads as wl
 
@@ -31,9 +31,19 @@ def _pack(p: dict, dtype: str, eps: float):
                           eps)
 
 
+# Per-row tolerances against the oracle that models the library's storage (the read sees the
+# stored state; bf16-path weights are bf16 with gamma folded): what is left is fp32 accumulation
+# order, the transcendental approximations and the final rounding of x (and of R', where the
+# library rounds its fp32 sum while the oracle rounds the exact sum).
+MODELED_TOL = {"f32": {"R": 1e-6, "x": 1e-5, "s": 1e-5},
+               "bf16": {"R": 4e-3, "x": 4e-3, "s": 1e-3}}
+
+
 def fused_case(w: wl.Workload, n_tokens=None, weight_mult=1.0, random_gamma=False,
                rows=None, chunk=2048):
-    """One fused write→read on the GPU; the oracle on `rows` (all rows if None)."""
+    """One fused write→read on the GPU against the oracle on `rows` (all rows if None).
+    Returns (plain, modeled): per-row errors against the plain fp64 definition, and against the
+    oracle run on the stored state with the weights the bf16 path uses."""
     N = w.n_tokens if n_tokens is None else n_tokens
     R = wl.make_state(w, N)
     y = wl.make_y(w, 0, N)
@@ -41,23 +51,35 @@ def fused_case(w: wl.Workload, n_tokens=None, weight_mult=1.0, random_gamma=Fals
     p = wl.make_params(w, 1, weight_mult)
     if random_gamma:
         p["gamma"] = wl.make_random_gamma(w, 1)
+    pm = bf16_path_params(p) if w.dtype == "bf16" else p
     Rt, yt, st = to_torch(R), to_torch(y), torch.from_numpy(s_prev).cuda()
     P = _pack(p, w.dtype, w.eps)
     x, s = gr.write_then_read(Rt, yt, st, P)
     torch.cuda.synchronize()
     rows = np.arange(N) if rows is None else rows
-    err = {"R": 0.0, "x": 0.0, "s": 0.0}
+    plain = {"R": 0.0, "x": 0.0, "s": 0.0}
+    modeled = {"R": 0.0, "x": 0.0, "s": 0.0}
     for a in range(0, len(rows), chunk):
         idx = rows[a:a + chunk]
-        Ro, xo, so = oracle.write_then_read(wl.to_f64(R[idx]), wl.to_f64(y[idx]), s_prev[idx], p,
-                                            w.eps)
+        Rf, yf, sp = wl.to_f64(R[idx]), wl.to_f64(y[idx]), s_prev[idx]
         sel = torch.from_numpy(idx).cuda()
-        err["R"] = max(err["R"], rel_rows(to_f64(Rt[sel]), Ro))
-        err["x"] = max(err["x"], rel_rows(to_f64(x[sel]), xo))
-        err["s"] = max(err["s"], rel_rows(to_f64(s[sel]), so))
+        got = {"R": to_f64(Rt[sel]), "x": to_f64(x[sel]), "s": to_f64(s[sel])}
+        for ref, res in ((oracle.write_then_read(Rf, yf, sp, p, w.eps), plain),
+                         (oracle.write_then_read(Rf, yf, sp, pm, w.eps, store=w.dtype), modeled)):
+            for k, v in zip(("R", "x", "s"), ref):
+                res[k] = max(res[k], rel_rows(got[k], v))
     assert torch.isfinite(x.float()).all() and torch.isfinite(Rt.float()).all()
-    assert bool(((s > 0) & (s < 2)).all())
-    return err
+    assert bool(((s >= 0) & (s <= 2)).all())  # 2σ(u) saturates to exactly 0 or 2 in fp32
+    print(f"{w.name} N={N} D={w.d_model} r={w.rank} {w.dtype} x{weight_mult}: plain {plain} "
+          f"modeled {modeled}")
+    return plain, modeled
+
+
+def check(w, plain, modeled, plain_too=True):
+    tol = MODELED_TOL[w.dtype]
+    assert all(modeled[k] < tol[k] for k in tol), modeled
+    if plain_too:
+        assert max(plain.values()) < TOL[w.dtype], plain
 
 
 def test_tiny_fp32_read_then_write():
@@ -78,8 +100,8 @@ def test_tiny_fp32_read_then_write():
 
 
 def test_tiny_fp32_fused():
-    e = fused_case(wl.WORKLOADS["tiny_fp32"])
-    assert max(e.values()) < TOL["f32"], e
+    w = wl.WORKLOADS["tiny_fp32"]
+    check(w, *fused_case(w))
 
 
 @pytest.mark.parametrize("N,D,r", [(1, 8, 1), (3, 8, 3), (17, 264, 5), (33, 520, 64),
@@ -87,33 +109,36 @@ def test_tiny_fp32_fused():
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_odd_shapes(N, D, r, dtype):
     w = wl.Workload("odd", N, D, r, dtype, y_std=0.5, seed=7)
-    e = fused_case(w, random_gamma=True)
-    assert max(e.values()) < TOL[dtype], e
+    check(w, *fused_case(w, random_gamma=True))
 
 
 def test_decode_full():
     """N=128, D=4096, r=16, bf16: all rows."""
-    e = fused_case(wl.WORKLOADS["decode"])
-    assert max(e.values()) < TOL["bf16"], e
+    w = wl.WORKLOADS["decode"]
+    check(w, *fused_case(w))
 
 
-def test_decode_sharp_gates_and_random_gamma():
-    """Weights x50 (gate logits far from 0, so G and s leave 1/2 and 1) and non-unit gains."""
-    e = fused_case(wl.WORKLOADS["decode"], weight_mult=50.0, random_gamma=True)
-    assert max(e.values()) < TOL["bf16"], e
+@pytest.mark.parametrize("mult", [10.0, 50.0])
+def test_decode_sharp_gates_and_random_gamma(mult):
+    """Weights x10 (gate logits spread over several units, G and s far from 1/2 and 1) and x50
+    (gates saturated at 0 or 1), with non-unit gains. Against the plain definition the rounding
+    of the stored state moves a saturated s by a relative amount equal to the absolute error of
+    its logit, so only the storage-modelled comparison bounds these cases."""
+    w = wl.WORKLOADS["decode"]
+    check(w, *fused_case(w, weight_mult=mult, random_gamma=True), plain_too=False)
 
 
 def test_prefill_full():
     """N=16384, D=4096, r=16, bf16: every row against the oracle (in chunks)."""
-    e = fused_case(wl.WORKLOADS["prefill"])
-    assert max(e.values()) < TOL["bf16"], e
+    w = wl.WORKLOADS["prefill"]
+    check(w, *fused_case(w))
 
 
 def test_large_skewed_subset():
     """The skewed distribution (branch scales 0.1/1/10/100, 1% outlier channels x50, y from
     Student-t(3)), D=7168, r=32, on the first 1024 tokens."""
-    e = fused_case(wl.WORKLOADS["large_skewed"], n_tokens=1024)
-    assert max(e.values()) < TOL["bf16"], e
+    w = wl.WORKLOADS["large_skewed"]
+    check(w, *fused_case(w, n_tokens=1024))
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
