@@ -137,14 +137,15 @@ def write_then_read(R, y, s_prev, params: dict, eps: float = 1e-6, store: str | 
     w_up, w_write). Returns (R', x, s_next).
 
     store=None keeps R' in fp64 and reads it as is (the plain definition). store="bf16" or
-    "f32" rounds R' to that storage format first and reads the stored value, as the library
-    does (a fused write→read reads the state it has just stored)."""
+    "f32" models the library's storage: the sum R + s·y is formed in fp32 (one rounding, as a
+    fused multiply-add does), stored in that format (a second rounding for bf16), and the read
+    sees the stored value."""
     R, y, s_prev = _f64(R), _f64(y), _f64(s_prev)
     n, nb, D = R.shape
     gamma, Wd, Wu, Ww = (_f64(params[k]) for k in ("gamma", "w_down", "w_up", "w_write"))
     r = Wd.shape[0]
     if store is not None:
-        Rw = round_to_storage(write(R, y, s_prev), store)
+        Rw = round_to_storage(round_to_storage(write(R, y, s_prev), "f32"), store)
         x, s = read(Rw, gamma, Wd, Wu, Ww, eps)
         return Rw, x, s
     R_out = np.empty_like(R)

@@ -31,12 +31,13 @@ def _pack(p: dict, dtype: str, eps: float):
                           eps)
 
 
-# Per-row tolerances against the oracle that models the library's storage (the read sees the
-# stored state; bf16-path weights are bf16 with gamma folded): what is left is fp32 accumulation
-# order, the transcendental approximations and the final rounding of x (and of R', where the
-# library rounds its fp32 sum while the oracle rounds the exact sum).
-MODELED_TOL = {"f32": {"R": 1e-6, "x": 1e-5, "s": 1e-5},
-               "bf16": {"R": 4e-3, "x": 4e-3, "s": 1e-3}}
+# Per-row tolerances against the oracle that models the library's storage (the write's sum is
+# one fp32 fused multiply-add, then stored; the read sees the stored state; bf16-path weights
+# are bf16 with gamma folded). R' then matches to the last bit; what is left for x and s is fp32
+# accumulation order, the transcendental approximations, and the final rounding of x to the
+# state dtype (at most 2^-9 relative per element for bf16, so 4e-3 leaves 2x for the rest).
+MODELED_TOL = {"f32": {"R": 1e-7, "x": 1e-5, "s": 1e-5},
+               "bf16": {"R": 1e-7, "x": 4e-3, "s": 1e-4}}
 
 
 def fused_case(w: wl.Workload, n_tokens=None, weight_mult=1.0, random_gamma=False,
