@@ -60,7 +60,8 @@ enum {
     GR_E_ALIAS = -8,       /* an output overlaps an input in a way the call forbids             */
     GR_E_CUDA = -9,        /* a CUDA launch or copy failed                                      */
     GR_E_DEVICE = -10,     /* no usable CUDA device (this build runs on sm_103a only)           */
-    GR_E_EPS = -11         /* eps negative or not finite                                        */
+    GR_E_EPS = -11,        /* eps negative or not finite                                        */
+    GR_E_TIMEOUT = -12     /* a kernel's bounded device-side wait ran out (see gr_device_status) */
 };
 
 /* Storage dtype of R, y and x. */
@@ -139,6 +140,12 @@ int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma
  * x_{l+1} = x_l + F(x_l) of "Residual" §1): the bandwidth reference for the GR kernels.
  * n >= 0; pointers 16-byte aligned. */
 int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* stream);
+
+/* Device-side status of the kernels that use bounded waits (the fused kernel waits on its own
+ * bulk copies with an iteration limit instead of spinning forever). Synchronises the current
+ * device, then returns GR_OK, GR_E_TIMEOUT if a wait ran out since the last clear (the outputs of
+ * that call are not valid), or GR_E_CUDA. `clear` != 0 resets the status. */
+int gr_device_status(int clear);
 
 /* Bytes of device workspace gr_write_then_read_host needs for `shape`. */
 int gr_host_workspace_size(const gr_shape* shape, size_t* bytes);

@@ -121,6 +121,7 @@ const char* gr_status_string(int status) {
         case GR_E_CUDA: return "a CUDA launch or copy failed";
         case GR_E_DEVICE: return "no usable sm_103 CUDA device";
         case GR_E_EPS: return "eps negative or not finite";
+        case GR_E_TIMEOUT: return "a bounded device-side wait ran out";
         default: return "unknown status";
     }
 }
@@ -251,6 +252,15 @@ int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* 
     int st = check_device();
     if (st) return st;
     return status_of(launch_residual_add(n, dtype, y, x, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_device_status(int clear) {
+    int st = check_device();
+    if (st) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GR_E_CUDA;
+    const int v = fused_status(clear != 0);
+    if (v < 0) return GR_E_CUDA;
+    return v ? GR_E_TIMEOUT : GR_OK;
 }
 
 int gr_host_workspace_size(const gr_shape* shape, size_t* bytes) {

@@ -18,19 +18,19 @@ constexpr int kBranches = 4;
 //   wdw     : W    [r+4][4D]                   rows 0..r-1 = W_d, rows r..r+3 = W_w
 //                                              (gamma folded on the bf16 path)
 //   wut     : W    [r][4D]                     W_u transposed
-//   frag    : bf16 fragment-ordered copies for the fused tensor-core kernel (bf16 path,
-//             d_model a multiple of 256, rank <= 32); see gr_fused_bf16.cu
+//   frag    : per-CTA slices for the fused tensor-core kernel (bf16 path, shapes that
+//             fused_supported() accepts): mma fragments of the weights and fp32 gains,
+//             laid out in gr_fused_bf16.cu; 0 bytes otherwise
 struct Layout {
-    size_t gamma32, wdw, wut, frag_down, frag_up, total;
-    size_t frag_down_bytes, frag_up_bytes;
+    size_t gamma32, wdw, wut, frag, total;
+    size_t frag_bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Fragment-section sizes of the fused bf16 kernel (0 when the shape does not use it).
-size_t fused_frag_down_bytes(int D, int r);
-size_t fused_frag_up_bytes(int D, int r);
+// Fused-kernel support and the size of its fragment section (gr_fused_bf16.cu).
 bool fused_supported(int D, int r);
+size_t fused_frag_bytes(int D, int r);
 
 inline Layout make_layout(int D, int r, int dtype) {
     Layout L{};
@@ -43,12 +43,9 @@ inline Layout make_layout(int D, int r, int dtype) {
     off = align256(off + size_t(r + kBranches) * K * w);
     L.wut = off;
     off = align256(off + size_t(r) * K * w);
-    L.frag_down_bytes = (dtype == GR_BF16 && fused_supported(D, r)) ? fused_frag_down_bytes(D, r) : 0;
-    L.frag_up_bytes = (dtype == GR_BF16 && fused_supported(D, r)) ? fused_frag_up_bytes(D, r) : 0;
-    L.frag_down = off;
-    off = align256(off + L.frag_down_bytes);
-    L.frag_up = off;
-    off = align256(off + L.frag_up_bytes);
+    L.frag_bytes = (dtype == GR_BF16 && fused_supported(D, r)) ? fused_frag_bytes(D, r) : 0;
+    L.frag = off;
+    off = align256(off + L.frag_bytes);
     L.total = off;
     return L;
 }
@@ -79,6 +76,9 @@ cudaError_t launch_fixed_gates(int64_t N, int D, int dtype, float eps, const voi
 
 // Single-stream x += y.
 cudaError_t launch_residual_add(int64_t n, int dtype, const void* y, void* x, cudaStream_t st);
+
+// Status bits recorded by device-side bounded waits (0 = none; -1 = could not be read).
+int fused_status(bool clear);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -45,9 +45,9 @@ __global__ void pack_generic_kernel(int D, int r, const float* __restrict__ gamm
 
 }  // namespace
 
-// Fragment sections of the fused kernel (defined in gr_fused_bf16.cu).
+// Fragment section of the fused kernel (defined in gr_fused_bf16.cu).
 cudaError_t launch_pack_fused(int D, int r, const float* gamma, const float* wd, const float* wu,
-                              const float* ww, void* frag_down, void* frag_up, cudaStream_t st);
+                              const float* ww, void* frag, cudaStream_t st);
 
 cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float* wd,
                         const float* wu, const float* ww, void* packed, cudaStream_t st) {
@@ -71,9 +71,7 @@ cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (L.frag_down_bytes) {
-        e = launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag_down, base + L.frag_up, st);
-    }
+    if (L.frag_bytes) e = launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag, st);
     return e;
 }
 

@@ -69,6 +69,7 @@ def load() -> ctypes.CDLL:
         "gr_read_fixed_gates": ([S, V, V, V, V, V], ctypes.c_int),
         "gr_residual_add_ref": ([ctypes.c_int64, ctypes.c_int32, V, V, V], ctypes.c_int),
         "gr_host_workspace_size": ([S, sz], ctypes.c_int),
+        "gr_device_status": ([ctypes.c_int], ctypes.c_int),
         "gr_write_then_read_host": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -238,6 +239,11 @@ def residual_add_ref(x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Ten
     _check(load().gr_residual_add_ref(x.numel(), _DTYPES[x.dtype], _ptr(y), _ptr(x),
                                       _stream(stream)), "gr_residual_add_ref")
     return x
+
+
+def device_status(clear: bool = False) -> int:
+    """gr_device_status: 0, or the status code of a bounded device-side wait that ran out."""
+    return int(load().gr_device_status(1 if clear else 0))
 
 
 def host_workspace_size(n_tokens: int, d_model: int, dtype: torch.dtype) -> int:

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.gr_api_version() == header_constant("GR_API_VERSION")
-    for code in range(0, -12, -1):
+    for code in range(0, -13, -1):
         s = gr.status_string(code)
         assert s and s != "unknown status", code
     assert gr.status_string(-99) == "unknown status"
@@ -72,7 +72,8 @@ def test_packed_size_grows_with_shape(lib):
         n = ctypes.c_size_t(0)
         assert lib.gr_packed_size(ctypes.byref(_shape(d=d, r=r, dt=dt)), ctypes.byref(n)) == 0
         return n.value
-    assert size(256, 8, gr.GR_F32) > size(256, 8, gr.GR_BF16) > 0
+    assert size(256, 8, gr.GR_F32) > 0 and size(256, 8, gr.GR_BF16) > 0
+    assert size(264, 8, gr.GR_F32) > size(264, 8, gr.GR_BF16)  # no fragment section at D=264
     assert size(512, 8, gr.GR_BF16) > size(256, 8, gr.GR_BF16)
     assert size(256, 16, gr.GR_BF16) > size(256, 8, gr.GR_BF16)
     assert size(256, 8, gr.GR_BF16) % 256 == 0
@@ -117,3 +118,18 @@ def test_calls_validate_before_any_launch(lib):
     assert lib.gr_host_workspace_size(sh, ctypes.byref(ws)) == 0 and ws.value > 0
     assert lib.gr_write_then_read_host(sh, FAKE, FAKE2, FAKE3, pr, FAKE4, FAKE5, FAKE, 16,
                                        null) == E("GR_E_SIZE")
+
+
+@pytest.mark.parametrize("D,r,dtype,path", [
+    (4096, 16, gr.GR_BF16, "fused_bf16"), (2048, 16, gr.GR_BF16, "fused_bf16"),
+    (256, 8, gr.GR_BF16, "fused_bf16"), (512, 1, gr.GR_BF16, "fused_bf16"),
+    (1024, 12, gr.GR_BF16, "fused_bf16"), (7168, 32, gr.GR_BF16, "generic"),
+    (4096, 32, gr.GR_BF16, "generic"), (4104, 16, gr.GR_BF16, "generic"),
+    (768, 16, gr.GR_BF16, "generic"), (8192, 16, gr.GR_BF16, "generic"),
+    (4096, 16, gr.GR_F32, "generic"), (8, 4, gr.GR_BF16, "generic")])
+def test_kernel_path_selection(lib, D, r, dtype, path):
+    """The fused tensor-core kernel takes bf16 shapes whose width splits into 1..16 CTAs of 256
+    channels (a power of two) with rank <= 16; every other valid shape runs the generic kernel."""
+    sh = _shape(n=100, d=D, r=r, dt=dtype)
+    assert lib.gr_kernel_path(ctypes.byref(sh)).decode() == path
+    assert lib.gr_kernel_path(ctypes.byref(_shape(d=12))).decode() == "invalid"

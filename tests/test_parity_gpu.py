@@ -249,3 +249,78 @@ def test_calls_reject_cpu_tensors():
     P = _pack(wl.make_params(w), "bf16", w.eps)
     with pytest.raises(ValueError):
         gr.read(to_torch(wl.make_state(w), "cpu"), P)
+
+
+@pytest.mark.parametrize("D,r,N", [(256, 8, 1), (256, 16, 17), (512, 16, 33), (1024, 12, 100),
+                                   (2048, 16, 250), (4096, 16, 15), (4096, 1, 16),
+                                   (4096, 4, 1000), (2048, 8, 4099)])
+def test_fused_kernel_shapes(D, r, N):
+    """Every cluster size (D = 256 … 4096 → 1 … 16 CTAs), ranks 1 … 16, ragged last tiles."""
+    w = wl.Workload("fused", N, D, r, "bf16", y_std=0.5, seed=13)
+    assert gr.kernel_path(N, D, r, torch.bfloat16) == "fused_bf16"
+    check(w, *fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    assert gr.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("D,r,N", [(2048, 16, 77), (4096, 16, 300)])
+def test_fused_read_only(D, r, N):
+    """gr_read on the fused path: R untouched, x and s against the oracle's read."""
+    w = wl.Workload("read", N, D, r, "bf16", y_std=0.5, seed=17)
+    R = wl.make_state(w)
+    p = wl.make_params(w, 1, weight_mult=5.0)
+    p["gamma"] = wl.make_random_gamma(w, 1)
+    Rt = to_torch(R)
+    x, s = gr.read(Rt, _pack(p, "bf16", w.eps))
+    torch.cuda.synchronize()
+    assert torch.equal(Rt, to_torch(R))
+    pm = bf16_path_params(p)
+    xo, so = oracle.read(wl.to_f64(R), pm["gamma"], pm["w_down"], pm["w_up"], pm["w_write"],
+                         w.eps)
+    tol = MODELED_TOL["bf16"]
+    assert rel_rows(to_f64(x), xo) < tol["x"] and rel_rows(to_f64(s), so) < tol["s"]
+    assert gr.device_status(clear=True) == 0
+
+
+def test_deep_stack_chain():
+    """96 chained sublayers (48 layers × token mixer, MLP) at N=8192, D=2048, r=16, bf16, fresh
+    seeded y_l and weights per sublayer: gr_read, 95 fused steps, gr_write. Every sublayer's
+    state, x and s are compared with the oracle's free-running fp64 chain on 256 sampled token
+    rows (the whole chain of those rows: tokens are independent)."""
+    w = wl.WORKLOADS["deep_stack"]
+    L, N = w.n_sublayers, w.n_tokens
+    rows = np.sort(np.random.default_rng(5).choice(N, 256, replace=False))
+    sel = torch.from_numpy(rows).cuda()
+    R0 = wl.make_state(w)
+    R = to_torch(R0)
+    ps = [wl.make_params(w, l) for l in range(L)]
+    s_a = torch.empty((N, 4), dtype=torch.float32, device="cuda")
+    s_b = torch.empty_like(s_a)
+    x = torch.empty((N, w.d_model), dtype=torch.bfloat16, device="cuda")
+    got = {"R": [], "x": [], "s": []}
+    ys_rows = []
+    P = _pack(ps[0], "bf16", w.eps)
+    gr.read(R, P, x=x, s=s_a)
+    got["R"].append(to_f64(R[sel]))
+    got["x"].append(to_f64(x[sel]))
+    got["s"].append(to_f64(s_a[sel]))
+    for l in range(1, L + 1):
+        y = wl.make_y(w, l - 1)
+        ys_rows.append(wl.to_f64(y[rows]))
+        yt = to_torch(y)
+        if l < L:
+            P = _pack(ps[l], "bf16", w.eps)
+            gr.write_then_read(R, yt, s_a, P, x=x, s_next=s_b)
+            s_a, s_b = s_b, s_a
+            got["x"].append(to_f64(x[sel]))
+            got["s"].append(to_f64(s_a[sel]))
+        else:
+            gr.write(R, yt, s_a)
+        got["R"].append(to_f64(R[sel]))
+    assert gr.device_status(clear=True) == 0
+    states, xs, ss = oracle.chain(wl.to_f64(R0[rows]), ys_rows, ps, w.eps)
+    curve = [max(rel_rows(got["R"][l], states[l]),
+                 rel_rows(got["x"][l], xs[l]) if l < L else 0.0,
+                 rel_rows(got["s"][l], ss[l]) if l < L else 0.0) for l in range(L + 1)]
+    print("deep stack per-sublayer max per-row rel. error:",
+          " ".join(f"{e:.2e}" for e in curve[::8]), "... final", f"{curve[-1]:.2e}")
+    assert max(curve) < TOL["bf16"], curve
