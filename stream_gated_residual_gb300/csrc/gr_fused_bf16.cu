@@ -66,11 +66,12 @@ struct FusedShape {
     int nb4;          // broadcast row per token: h (r values) then inv (4), padded to 4 floats
     int down_bytes, up_bytes, gam_bytes, slice_bytes;
     int stage_bytes, recv_bytes, bcast_bytes;
-    int off_up, off_gam, off_stage, off_recv, off_bcast, off_mbar, smem_bytes;
+    int off_up, off_gam, off_stage, off_recv, off_bcast, off_out, off_mbar, smem_bytes;
 };
 
 // Shared-memory layout: down | up | gamma | kStages stages (1024-aligned) | recv[2] | bcast[2]
-// | mbarriers (stage_full[kStages], weights_full, recv_full[2], bcast_full[2]).
+// | out (an owner's outgoing h/inv rows) | mbarriers (stage_full[kStages], weights_full,
+// recv_full[2], bcast_full[2]).
 // The first three form one CTA's slice of the packed fragment section, in the same order.
 __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     FusedShape s{};
@@ -94,7 +95,8 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     s.off_stage = round_up(s.off_gam + s.gam_bytes, 1024);
     s.off_recv = s.off_stage + kStages * s.stage_bytes;
     s.off_bcast = s.off_recv + 2 * round_up(s.recv_bytes, 16);
-    s.off_mbar = s.off_bcast + 2 * round_up(s.bcast_bytes, 16);
+    s.off_out = s.off_bcast + 2 * round_up(s.bcast_bytes, 16);
+    s.off_mbar = s.off_out + round_up(s.bcast_bytes, 16);
     s.smem_bytes = s.off_mbar + 8 * (kStages + 5);
     return s;
 }
@@ -178,7 +180,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank) {
     uint32_t ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
     return ra;
 }
 // 16 bytes into CTA `rank`'s shared memory at the same offset as `local_addr`, completing
@@ -194,7 +196,7 @@ __device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_
 }
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -265,8 +267,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     }
     __syncthreads();
 
-    // Stage fill for the k-th tile of this cluster (warp 0): 4 R boxes [16 tok][4 br][64 ch],
-    // 4 y boxes [16 tok][64 ch], s_prev rows. Rows past N are zero-filled by the TMA unit.
+    // Stage fill for the k-th tile of this cluster: 4 R boxes [16 tok][4 br][64 ch] (lane 0 of
+    // warps 0..3), 4 y boxes [16 tok][64 ch] (lane 0 of warps 4..7), s_prev rows (warp 0,
+    // lane 1); warp 0 lane 0 arms the stage barrier. Rows past N are zero-filled by the TMA
+    // unit. Spreading the copies over warps keeps each warp's issue latency short.
     auto issue_tile = [&](int64_t k) {
         const int64_t tile = cid + k * ncl;
         if (tile >= ntiles) return;
@@ -275,19 +279,18 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         const int t0 = int(tile * kT);
         const int nv = int(N - t0 < kT ? N - t0 : kT);
         const int c0 = int(crank) * kDq;
-        if (lane == 0)
+        if (warp == 0 && lane == 0)
             mbar_expect_tx(&stage_full[st],
                            uint32_t(kColBlocks * kRBoxBytes +
                                     (WRITE ? kColBlocks * kYBoxBytes + nv * 16 : 0)));
-        __syncwarp();
-        if (lane < kColBlocks) {
-            tma_load_3d(sb + lane * kRBoxBytes, &tm_R, c0 + lane * kBoxCh, 0, t0,
+        if (lane == 0 && warp < kColBlocks) {
+            tma_load_3d(sb + warp * kRBoxBytes, &tm_R, c0 + warp * kBoxCh, 0, t0,
                         &stage_full[st]);
-        } else if (WRITE && lane < 2 * kColBlocks) {
-            const int cb = lane - kColBlocks;
-            tma_load_2d(sb + kYOff + cb * kYBoxBytes, &tm_y, c0 + cb * kBoxCh, t0,
+        } else if (WRITE && lane == 0 && warp < 2 * kColBlocks) {
+            const int yb = warp - kColBlocks;
+            tma_load_2d(sb + kYOff + yb * kYBoxBytes, &tm_y, c0 + yb * kBoxCh, t0,
                         &stage_full[st]);
-        } else if (WRITE && lane == 2 * kColBlocks) {
+        } else if (WRITE && lane == 1 && warp == 0) {
             bulk_g2s(sb + kSOff, s_prev + size_t(t0) * 4, uint32_t(nv) * 16, &stage_full[st]);
         }
     };
@@ -297,8 +300,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         bulk_g2s(smem, frag + size_t(crank) * S.slice_bytes, uint32_t(S.slice_bytes),
                  weights_full);
     }
-    if (warp == 0)
-        for (int k = 0; k < kStages; ++k) issue_tile(k);
+    for (int k = 0; k < kStages; ++k) issue_tile(k);
     cluster_sync();  // every CTA of the cluster runs before any shared::cluster access
     mbar_wait(weights_full, 0);
 
@@ -471,7 +473,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();  // the stage is free: refill it with tile k + kStages
-        if (warp == 0) issue_tile(k + kStages);
+        issue_tile(k + kStages);
 
         // ---- B(k-1) -------------------------------------------------------------------------
         if (k > 0) phase_b(k - 1, t0_prev);
@@ -484,11 +486,52 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         mbar_wait(&recv_full[p], uint32_t((k >> 1) & 1));
         {
             float* recv = recv_ptr(p);              // [C][tpc][4][rw]
-            const int nown = tpc * 4 * rw;
+            const int nown = tpc * 4 * rw;          // a multiple of 4
+            // sum over the C sources: 4 threads per 4-value group, each a quarter of the sources
             for (int v = tid; v < nown; v += kThreads) {
-                float a = 0.f;
-                for (int src = 0; src < C; ++src) a += recv[src * nown + v];
-                recv[v] = a;
+                const int grp = v >> 2, qtr = v & 3;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int src = qtr; src < C; src += 4) {
+                    const float4 b =
+                        *reinterpret_cast<const float4*>(recv + src * nown + 4 * grp);
+                    a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+                }
+                // nown is a multiple of 4, so the four lanes of a group are active together
+                const unsigned mask = __activemask();
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    a.x += __shfl_xor_sync(mask, a.x, o);
+                    a.y += __shfl_xor_sync(mask, a.y, o);
+                    a.z += __shfl_xor_sync(mask, a.z, o);
+                    a.w += __shfl_xor_sync(mask, a.w, o);
+                }
+                if (qtr == 0) *reinterpret_cast<float4*>(recv + 4 * grp) = a;
+            }
+            __syncthreads();
+            // one output per thread: h_k = SiLU(z_k) (k < r), else s written and inv kept
+            float* outrow = reinterpret_cast<float*>(smem + S.off_out);   // [tpc][nb4]
+            for (int v = tid; v < tpc * nb4; v += kThreads) {
+                const int slot = v / nb4, kk = v - slot * nb4;
+                const int tok = int(crank) * tpc + slot;
+                const float* P = recv + slot * 4 * rw;
+                float out = 0.f;
+                if (kk < nk) {
+                    float inv[4], a = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        inv[i] = rsqrtf(P[i * rw + nk] / float(D) + eps);
+                        a = fmaf(inv[i], P[i * rw + kk], a);
+                    }
+                    a *= 0.25f;
+                    if (kk < r) {
+                        out = a * sigmoid_accurate(a);
+                    } else {
+                        if (t0 + tok < N)
+                            s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sigmoid_accurate(a);
+                        out = inv[kk - r];
+                    }
+                }
+                outrow[v] = out;
             }
             __syncthreads();
             const uint32_t bc_u32 = smem_u32(bcast_ptr(p));
@@ -498,32 +541,9 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 const int dst = v % C, rem = v / C;
                 const int slot = rem / ngrp, g4 = rem - slot * ngrp;
                 const int tok = int(crank) * tpc + slot;
-                const float* P = recv + slot * 4 * rw;
-                float inv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) inv[i] = rsqrtf(P[i * rw + nk] / float(D) + eps);
-                float out[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kk = 4 * g4 + e;
-                    out[e] = 0.f;
-                    if (kk < nk) {
-                        float a = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) a = fmaf(inv[i], P[i * rw + kk], a);
-                        a *= 0.25f;
-                        if (kk < r) {
-                            out[e] = a * sigmoid_accurate(a);  // h = SiLU(z)
-                        } else {
-                            if (dst == 0 && t0 + tok < N)
-                                s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sigmoid_accurate(a);
-                            out[e] = inv[kk - r];
-                        }
-                    }
-                }
+                const float4 o4 = *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
                 st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
-                            smem_u32(&bcast_full[p]), uint32_t(dst), out[0], out[1], out[2],
-                            out[3]);
+                            smem_u32(&bcast_full[p]), uint32_t(dst), o4.x, o4.y, o4.z, o4.w);
             }
         }
 #pragma unroll
