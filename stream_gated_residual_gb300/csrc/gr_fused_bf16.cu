@@ -11,23 +11,24 @@
 // traverse the widened state once; here write and read share one traversal: every byte of R,
 // y, R', x crosses HBM once.
 //
-// Organisation (GB300: 152 SMs, 227 KB shared memory per CTA):
+// Organisation (GB300: 152 SMs, 227 KB shared memory and 64 K registers per SM):
 //   * A thread-block cluster of C = D/256 CTAs splits the channels: CTA q owns channels
-//     [256q, 256q+256) of every branch and keeps that slice of the packed weights (mma
-//     fragments, gamma folded into W_d and W_w) and of gamma resident in shared memory.
-//   * Tiles of 16 tokens (the mma M dimension) stream through a 3-stage ring of shared-memory
-//     buffers filled by TMA tensor copies (128-byte swizzle, 9 copies per tile) completing on
-//     mbarriers.
-//   * 8 warps per CTA; warp w owns 32 channels of each branch. A thread holds 8 channels of two
-//     token rows per branch; those registers are directly the A fragments of mma.m16n8k16 once
-//     the K index is permuted consistently with the packed B fragments. The same registers as
-//     B operand give R'·R'ᵀ, whose diagonal is the per-branch sum of squares.
-//   * The per-token row reductions (4 sums of squares and 4·(r+4) partial projections) are
-//     summed over warps in shared memory, then sent with st.async to the token's owner CTA
-//     (completing on the owner's mbarrier), which forms inv, h and s and sends h and inv to
-//     every CTA of the cluster the same way. No cluster-wide barrier in the steady state.
-//   * The up-projection runs on the tensor cores with h split into bf16 hi + lo parts (about 16
-//     significant bits), and σ(a) = ½ + ½·tanh(a/2) with W_u pre-scaled by ½ (exact in bf16).
+//     [256q, 256q+256) of every branch.
+//   * Tiles of 16 tokens (the mma M dimension) arrive by TMA (128-byte swizzle, zero fill past
+//     N): R into a 4-buffer ring, y and s_prev into a 3-buffer ring.
+//   * 16 warps in two roles that run concurrently on different tiles:
+//     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (stored
+//       to HBM and written back in place into the R buffer), the per-branch sums of squares
+//       (diagonal of R'·R'ᵀ on the tensor cores) and the down projections (W_d, W_w with gamma
+//       folded, mma fragments resident in shared memory); sum the two halves; send each token's
+//       row sums with st.async to the token's owner CTA; and, as owners, form inv, h and s and
+//       send h and inv to every CTA of the cluster.
+//     - B warps (8): warp b owns 32 channels of all four branches and keeps its W_u fragments in
+//       registers. For each tile they wait for h and inv, run the up projection on the tensor
+//       cores (h split into bf16 hi + lo parts), form σ(a) = ½ + ½·tanh(a/2) (W_u pre-scaled by
+//       ½), combine the branches from the in-place R', store x, and release the R buffer.
+//   * mbarriers carry every hand-off (TMA completion, R' ready, R buffer empty, row sums and h
+//     arriving from other CTAs); there is no cluster-wide barrier in the steady state.
 #include <cuda.h>
 #include <string.h>
 
@@ -38,17 +39,18 @@ namespace gr {
 namespace {
 
 constexpr int kT = 16;                      // tokens per tile (mma M)
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kDq = kWarps * 32;            // channels per branch per CTA
-constexpr int kStages = 3;
+constexpr int kAW = 8, kBW = 8;             // A warps, B warps
+constexpr int kThreads = (kAW + kBW) * 32;
+constexpr int kAThreads = kAW * 32;
+constexpr int kDq = 256;                    // channels per branch per CTA
+constexpr int kRStages = 4, kYStages = 3;
 constexpr int kBoxCh = 64;                  // channels per TMA box (128 bytes: the swizzle span)
 constexpr int kColBlocks = kDq / kBoxCh;    // 4 boxes per row slice
-constexpr int kRBoxBytes = kBoxCh * 4 * kT * 2;   // [16 tok][4 br][64 ch] bf16 = 8 KB
-constexpr int kYBoxBytes = kBoxCh * kT * 2;       // [16 tok][64 ch] bf16 = 2 KB
-constexpr int kYOff = kColBlocks * kRBoxBytes;    // 32 KB
-constexpr int kSOff = kYOff + kColBlocks * kYBoxBytes;  // 40 KB
-constexpr int kLoadBytes = kSOff + kT * 16;
+constexpr int kRBoxBytes = kBoxCh * 4 * kT * 2;        // [16 tok][4 br][64 ch] bf16 = 8 KB
+constexpr int kRBufBytes = kColBlocks * kRBoxBytes;     // 32 KB
+constexpr int kYBoxBytes = kBoxCh * kT * 2;             // [16 tok][64 ch] bf16 = 2 KB
+constexpr int kSOff = kColBlocks * kYBoxBytes;          // s_prev rows after the y boxes
+constexpr int kYBufBytes = 9 * 1024;                    // 8 KB of y + 256 B of s_prev, padded
 constexpr int kMaxCluster = 16;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles before a wait gives up (~2 s)
 
@@ -61,18 +63,18 @@ struct FusedShape {
     int C;            // cluster size = D / kDq
     int ntd;          // n-tiles of the down projection: ceil((r + 4) / 8)
     int half_last;    // 1 if the last down n-tile has <= 4 real rows (only lanes 0..15 stored)
-    int upb;          // down-fragment units (16 B) per (warp, branch)
-    int rw;           // reduction row per (token, branch): r+4 projections, sum of squares; even
+    int upb;          // down-fragment units (16 B) per (A warp, 32-channel chunk)
+    int rw;           // row-sum record per (token, branch): r+4 projections, sum of squares,
+                      // padded to a multiple of 4 floats (16-byte records)
     int nb4;          // broadcast row per token: h (r values) then inv (4), padded to 4 floats
     int down_bytes, up_bytes, gam_bytes, slice_bytes;
-    int stage_bytes, recv_bytes, bcast_bytes;
-    int off_up, off_gam, off_stage, off_recv, off_bcast, off_out, off_mbar, smem_bytes;
+    int red_bytes, recv_bytes, bcast_bytes;
+    int off_gam, off_r, off_y, off_red, off_recv, off_bcast, off_out, off_mbar, smem_bytes;
 };
 
-// Shared-memory layout: down | up | gamma | kStages stages (1024-aligned) | recv[2] | bcast[2]
-// | out (an owner's outgoing h/inv rows) | mbarriers (stage_full[kStages], weights_full,
-// recv_full[2], bcast_full[2]).
-// The first three form one CTA's slice of the packed fragment section, in the same order.
+// Packed fragment slice of one CTA: down | up | gamma. Shared memory: down | gamma | R ring
+// (1024-aligned) | y ring | red | recv[2] | bcast[2] | out | mbarriers. The up fragments go to
+// the B warps' registers straight from global memory.
 __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     FusedShape s{};
     s.C = D / kDq;
@@ -80,26 +82,37 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     const int last_rows = r + 4 - 8 * (s.ntd - 1);
     s.half_last = last_rows <= 4 ? 1 : 0;
     s.upb = (s.ntd - 1) * 32 + (s.half_last ? 16 : 32);
-    s.rw = round_up(r + 5, 2);
+    s.rw = round_up(r + 5, 4);
     s.nb4 = round_up(r + 4, 4);
-    s.down_bytes = kWarps * 4 * s.upb * 16;
-    s.up_bytes = kWarps * 4 * 4 * 32 * 8;
+    s.down_bytes = kAW * 4 * s.upb * 16;
+    s.up_bytes = kBW * 32 * 16 * 8;
     s.gam_bytes = 4 * kDq * 4;
     s.slice_bytes = s.down_bytes + s.up_bytes + s.gam_bytes;
-    const int red_bytes = kWarps * kT * 4 * s.rw * 4;        // cross-warp partials
-    s.stage_bytes = round_up(kLoadBytes > red_bytes ? kLoadBytes : red_bytes, 1024);
+    s.red_bytes = kAW * kT * s.rw * 4;
     s.recv_bytes = kT * 4 * s.rw * 4;
     s.bcast_bytes = kT * s.nb4 * 4;
-    s.off_up = s.down_bytes;
-    s.off_gam = s.off_up + s.up_bytes;
-    s.off_stage = round_up(s.off_gam + s.gam_bytes, 1024);
-    s.off_recv = s.off_stage + kStages * s.stage_bytes;
+    s.off_gam = s.down_bytes;
+    s.off_r = round_up(s.off_gam + s.gam_bytes, 1024);
+    s.off_y = s.off_r + kRStages * kRBufBytes;
+    s.off_red = s.off_y + kYStages * kYBufBytes;
+    s.off_recv = s.off_red + round_up(s.red_bytes, 16);
     s.off_bcast = s.off_recv + 2 * round_up(s.recv_bytes, 16);
     s.off_out = s.off_bcast + 2 * round_up(s.bcast_bytes, 16);
     s.off_mbar = s.off_out + round_up(s.bcast_bytes, 16);
-    s.smem_bytes = s.off_mbar + 8 * (kStages + 5);
+    s.smem_bytes = s.off_mbar + round_up(8 * 24, 16);
     return s;
 }
+
+// mbarrier indices
+constexpr int kMbRFull = 0;                        // [4] R tile landed (TMA)
+constexpr int kMbRReady = kMbRFull + kRStages;     // [4] R' written back (8 A-warp arrivals)
+constexpr int kMbREmpty = kMbRReady + kRStages;    // [4] B warps done with the R buffer (8)
+constexpr int kMbYFull = kMbREmpty + kRStages;     // [3] y and s_prev landed (TMA)
+constexpr int kMbWeights = kMbYFull + kYStages;    // weights landed
+constexpr int kMbRecv = kMbWeights + 1;            // [2] row sums from every CTA (owner)
+constexpr int kMbBcast = kMbRecv + 2;              // [2] h and inv from every owner
+constexpr int kMbCount = kMbBcast + 2;
+static_assert(kMbCount <= 24, "mbarrier area holds 24");
 
 // ---- PTX wrappers ---------------------------------------------------------------------------
 
@@ -125,6 +138,10 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Named barrier among the A warps only.
+__device__ __forceinline__ void a_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kAThreads) : "memory");
+}
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
@@ -132,6 +149,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
 // Bounded wait on phase `parity` (acquire at cluster scope, so data that remote CTAs delivered
@@ -196,8 +217,7 @@ __device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_
 }
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -213,20 +233,10 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
 }
+// Byte offset of the 16-byte chunk `cch` (0..7) of 128-byte row `row` in a swizzled box.
+__device__ __forceinline__ int swz(int row, int cch) { return row * 128 + ((cch ^ (row & 7)) << 4); }
 
 // ---- the kernel -----------------------------------------------------------------------------
-//
-// Per tile k of this cluster, every CTA runs
-//   A(k)  wait for the stage; write R' (eq write); sums of squares and down projections on
-//         the tensor cores; sum the partials over the 8 warps; st.async each token's sums
-//         to its owner CTA (completing on the owner's recv_full mbarrier); refill the stage.
-//   B(k-1) wait for h and inv of tile k-1 (bcast_full); up projection, gates, combine, x.
-//   C(k)  as owner: wait for the partial sums of its tokens from all CTAs; form inv, h and s
-//         (eq rms, gate, s); write s; st.async h and inv to every CTA of the cluster.
-// B trails A by one tile so that the owners' round trip of tile k is hidden behind A(k+1);
-// the R' registers of tile k-1 stay live across A(k). recv and bcast are double-buffered by
-// tile parity: a CTA can run at most one tile ahead of the slowest CTA in its cluster, because
-// C(k) needs every CTA's A(k).
 
 template <bool WRITE, int NTD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -243,17 +253,13 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     const int tpc = kT / C;                     // tokens owned per CTA and tile
     const int64_t ncl = ncluster_x(), cid = cluster_id_x();
     const int64_t ntiles = (N + kT - 1) / kT;
+    const int64_t nlocal = ntiles > cid ? (ntiles - cid + ncl - 1) / ncl : 0;
     const int nk = r + 4, rw = S.rw, nb4 = S.nb4;
+    const char* slice = frag + size_t(crank) * S.slice_bytes;
 
-    const uint4* s_down = reinterpret_cast<const uint4*>(smem);
-    const uint2* s_up = reinterpret_cast<const uint2*>(smem + S.off_up);
-    const float* s_gam = reinterpret_cast<const float*>(smem + S.off_gam);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S.off_mbar);
-    uint64_t* stage_full = mbar;                 // [kStages]
-    uint64_t* weights_full = mbar + kStages;
-    uint64_t* recv_full = mbar + kStages + 1;    // [2]
-    uint64_t* bcast_full = mbar + kStages + 3;   // [2]
-    auto stage_ptr = [&](int st) { return smem + S.off_stage + st * S.stage_bytes; };
+    auto rbuf = [&](int64_t k) { return smem + S.off_r + int(k % kRStages) * kRBufBytes; };
+    auto ybuf = [&](int64_t k) { return smem + S.off_y + int(k % kYStages) * kYBufBytes; };
     auto recv_ptr = [&](int p) {
         return reinterpret_cast<float*>(smem + S.off_recv + p * round_up(S.recv_bytes, 16));
     };
@@ -262,310 +268,352 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     };
 
     if (tid == 0) {
-        for (int i = 0; i < kStages + 5; ++i) mbar_init(&mbar[i], 1);
+        for (int i = 0; i < kMbCount; ++i) {
+            const bool eight = (i >= kMbRReady && i < kMbRReady + kRStages) ||
+                               (i >= kMbREmpty && i < kMbREmpty + kRStages);
+            mbar_init(&mbar[i], eight ? 8u : 1u);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    // Stage fill for the k-th tile of this cluster: 4 R boxes [16 tok][4 br][64 ch] (lane 0 of
-    // warps 0..3), 4 y boxes [16 tok][64 ch] (lane 0 of warps 4..7), s_prev rows (warp 0,
-    // lane 1); warp 0 lane 0 arms the stage barrier. Rows past N are zero-filled by the TMA
-    // unit. Spreading the copies over warps keeps each warp's issue latency short.
-    auto issue_tile = [&](int64_t k) {
-        const int64_t tile = cid + k * ncl;
-        if (tile >= ntiles) return;
-        const int st = int(k % kStages);
-        char* sb = stage_ptr(st);
-        const int t0 = int(tile * kT);
+    // TMA of the k-th local tile's R boxes (lane 0 of A warps 0..3, one box each).
+    auto issue_r = [&](int64_t k, int a) {
+        if (k >= nlocal) return;
+        const int t0 = int((cid + k * ncl) * kT);
+        uint64_t* bar = &mbar[kMbRFull + int(k % kRStages)];
+        if (a == 0) mbar_expect_tx(bar, uint32_t(kRBufBytes));
+        tma_load_3d(rbuf(k) + a * kRBoxBytes, &tm_R, int(crank) * kDq + a * kBoxCh, 0, t0, bar);
+    };
+    // TMA of the k-th local tile's y boxes (lane 0 of A warps 4..7) and s_prev rows (warp 0,
+    // lane 1); warp 0 lane 0 arms the barrier.
+    auto issue_y = [&](int64_t k, int a, int ln) {
+        if (!WRITE || k >= nlocal) return;
+        const int t0 = int((cid + k * ncl) * kT);
         const int nv = int(N - t0 < kT ? N - t0 : kT);
-        const int c0 = int(crank) * kDq;
-        if (warp == 0 && lane == 0)
-            mbar_expect_tx(&stage_full[st],
-                           uint32_t(kColBlocks * kRBoxBytes +
-                                    (WRITE ? kColBlocks * kYBoxBytes + nv * 16 : 0)));
-        if (lane == 0 && warp < kColBlocks) {
-            tma_load_3d(sb + warp * kRBoxBytes, &tm_R, c0 + warp * kBoxCh, 0, t0,
-                        &stage_full[st]);
-        } else if (WRITE && lane == 0 && warp < 2 * kColBlocks) {
-            const int yb = warp - kColBlocks;
-            tma_load_2d(sb + kYOff + yb * kYBoxBytes, &tm_y, c0 + yb * kBoxCh, t0,
-                        &stage_full[st]);
-        } else if (WRITE && lane == 1 && warp == 0) {
-            bulk_g2s(sb + kSOff, s_prev + size_t(t0) * 4, uint32_t(nv) * 16, &stage_full[st]);
+        uint64_t* bar = &mbar[kMbYFull + int(k % kYStages)];
+        if (a == 0 && ln == 0) mbar_expect_tx(bar, uint32_t(kColBlocks * kYBoxBytes + nv * 16));
+        if (ln == 0 && a >= 4) {
+            const int yb = a - 4;
+            tma_load_2d(ybuf(k) + yb * kYBoxBytes, &tm_y, int(crank) * kDq + yb * kBoxCh, t0, bar);
         }
+        if (a == 0 && ln == 1)
+            bulk_g2s(ybuf(k) + kSOff, s_prev + size_t(t0) * 4, uint32_t(nv) * 16, bar);
     };
 
     if (tid == 0) {
-        mbar_expect_tx(weights_full, uint32_t(S.slice_bytes));
-        bulk_g2s(smem, frag + size_t(crank) * S.slice_bytes, uint32_t(S.slice_bytes),
-                 weights_full);
+        mbar_expect_tx(&mbar[kMbWeights], uint32_t(S.down_bytes + S.gam_bytes));
+        bulk_g2s(smem, slice, uint32_t(S.down_bytes), &mbar[kMbWeights]);
+        bulk_g2s(smem + S.off_gam, slice + S.down_bytes + S.up_bytes, uint32_t(S.gam_bytes),
+                 &mbar[kMbWeights]);
     }
-    for (int k = 0; k < kStages; ++k) issue_tile(k);
+    if (warp < kAW && lane < 2) {
+        for (int k = 0; k < kRStages - 1; ++k) {
+            if (lane == 0 && warp < 4) issue_r(k, warp);
+        }
+        for (int k = 0; k < kYStages; ++k) issue_y(k, warp, lane);
+    }
     cluster_sync();  // every CTA of the cluster runs before any shared::cluster access
-    mbar_wait(weights_full, 0);
 
-    // This thread's 16-byte chunk in the swizzled boxes: column block cb, chunk cch (channels
-    // 32·warp + 8·q4 ... +7 of the CTA slice); box row `row` keeps chunk c at c ^ (row & 7).
-    const int cb = warp >> 1, cch = ((warp & 1) << 2) | q4;
+    if (warp < kAW) {
+        // =============================== A warps ===========================================
+        const int a = warp, ib = a & 3, hh = a >> 2;
+        mbar_wait(&mbar[kMbWeights], 0);
+        const uint4* s_down = reinterpret_cast<const uint4*>(smem);
+        float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kAW][kT][rw]
+        float* outrow = reinterpret_cast<float*>(smem + S.off_out);
+        for (int64_t k = 0; k < nlocal; ++k) {
+            const int64_t t0 = (cid + k * ncl) * kT;
+            const int nv = int(N - t0 < kT ? N - t0 : kT);
+            const int p = int(k & 1);
+            char* rb = rbuf(k);
+            const char* yb = ybuf(k);
+            mbar_wait(&mbar[kMbRFull + int(k % kRStages)], uint32_t((k / kRStages) & 1));
+            if (WRITE) mbar_wait(&mbar[kMbYFull + int(k % kYStages)], uint32_t((k / kYStages) & 1));
 
-    uint32_t Rp[4][2][4];      // R' of the current tile (bf16 pairs): [branch][row][pair]
-    uint32_t Rq[4][2][4];      // R' of the previous tile, for its phase B
-    int64_t t0_prev = 0;
-
-    // Phase B of a tile: up projection (eq gate), gates, combine (eq use_gate), store x.
-    auto phase_b = [&](int64_t kb, int64_t t0b) {
-        const int p = int(kb & 1);
-        mbar_wait(&bcast_full[p], uint32_t((kb >> 1) & 1));
-        const float* bc = bcast_ptr(p);
-        uint32_t ahi[4], alo[4];
+            // write (eq write) for this warp's branch and 128 channels; R' back in place
+            uint32_t Rp[2][4][4];  // [row g / g+8][chunk][channel pair]
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int tk = g + 8 * (m & 1), kc = 2 * q4 + 8 * (m >> 1);
-            const float h0 = kc < r ? bc[tk * nb4 + kc] : 0.f;
-            const float h1 = kc + 1 < r ? bc[tk * nb4 + kc + 1] : 0.f;
-            const float h0h = __bfloat162float(__float2bfloat16_rn(h0));
-            const float h1h = __bfloat162float(__float2bfloat16_rn(h1));
-            ahi[m] = pack_bf2(h0h, h1h);
-            alo[m] = pack_bf2(h0 - h0h, h1 - h1h);
-        }
-        float xacc[2][8];
+            for (int row = 0; row < 2; ++row) {
+                const int tok = g + 8 * row, brow = tok * 4 + ib;
+                float sp = 0.f;
+                if (WRITE) sp = *reinterpret_cast<const float*>(yb + kSOff + tok * 16 + ib * 4);
 #pragma unroll
-        for (int row = 0; row < 2; ++row)
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const int cb = hh * 2 + (j4 >> 1), cch = ((j4 & 1) << 2) | q4;
+                    char* rp = rb + cb * kRBoxBytes + swz(brow, cch);
+                    const uint4 rv = *reinterpret_cast<const uint4*>(rp);
+                    uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
+                    if (WRITE) {
+                        const uint4 yv = *reinterpret_cast<const uint4*>(
+                            yb + cb * kYBoxBytes + swz(tok, cch));
+                        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xacc[row][e] = 0.f;
+                        for (int m = 0; m < 4; ++m)
+                            w[m] = pack_bf2(fmaf(sp, bf_lo(yw[m]), bf_lo(w[m])),
+                                            fmaf(sp, bf_hi(yw[m]), bf_hi(w[m])));
+                        const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(rp) = o;
+                        if (tok < nv)
+                            *reinterpret_cast<uint4*>(
+                                R + (size_t(t0 + tok) * 4 + ib) * size_t(D) + size_t(crank) * kDq +
+                                hh * 128 + j4 * 32 + q4 * 8) = o;
+                    }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float inv0 = bc[g * nb4 + r + i], inv1 = bc[(g + 8) * nb4 + r + i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint2 b = s_up[((warp * 4 + i) * 4 + j) * 32 + lane];
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_bf16(c, ahi[0], ahi[1], ahi[2], ahi[3], b.x, b.y);
-                mma_bf16(c, alo[0], alo[1], alo[2], alo[3], b.x, b.y);
-                const float2 gm =
-                    *reinterpret_cast<const float2*>(s_gam + i * kDq + warp * 32 + q4 * 8 + 2 * j);
-                const float a00 = gm.x * inv0 * bf_lo(Rq[i][0][j]);
-                const float a01 = gm.y * inv0 * bf_hi(Rq[i][0][j]);
-                const float a10 = gm.x * inv1 * bf_lo(Rq[i][1][j]);
-                const float a11 = gm.y * inv1 * bf_hi(Rq[i][1][j]);
-                // G·a = ½a + ½·tanh(·)·a; the ½ is applied once at the end
-                xacc[0][2 * j] += fmaf(tanh_approx(c[0]), a00, a00);
-                xacc[0][2 * j + 1] += fmaf(tanh_approx(c[1]), a01, a01);
-                xacc[1][2 * j] += fmaf(tanh_approx(c[2]), a10, a10);
-                xacc[1][2 * j + 1] += fmaf(tanh_approx(c[3]), a11, a11);
-            }
-        }
-#pragma unroll
-        for (int row = 0; row < 2; ++row) {
-            const int tok = g + 8 * row;
-            if (t0b + tok < N) {
-                __nv_bfloat16* dst =
-                    x + size_t(t0b + tok) * D + size_t(crank) * kDq + warp * 32 + q4 * 8;
-                *reinterpret_cast<uint4*>(dst) = make_uint4(
-                    pack_bf2(0.125f * xacc[row][0], 0.125f * xacc[row][1]),
-                    pack_bf2(0.125f * xacc[row][2], 0.125f * xacc[row][3]),
-                    pack_bf2(0.125f * xacc[row][4], 0.125f * xacc[row][5]),
-                    pack_bf2(0.125f * xacc[row][6], 0.125f * xacc[row][7]));
-            }
-        }
-    };
-
-    int64_t k = 0;
-    for (;; ++k) {
-        const int64_t tile = cid + k * ncl;
-        if (tile >= ntiles) break;
-        const int st = int(k % kStages);
-        const int p = int(k & 1);
-        char* sb = stage_ptr(st);
-        const int64_t t0 = tile * kT;
-        const int nv = int(N - t0 < kT ? N - t0 : kT);
-        mbar_wait(&stage_full[st], uint32_t((k / kStages) & 1));
-
-        // ---- A(k): write (eq write), sums of squares, down projections ----------------------
-#pragma unroll
-        for (int row = 0; row < 2; ++row) {
-            const int tok = g + 8 * row;
-            float yf[8], sp[4] = {0.f, 0.f, 0.f, 0.f};
-            if (WRITE) {
-                const float4 s4 = *reinterpret_cast<const float4*>(sb + kSOff + tok * 16);
-                sp[0] = s4.x, sp[1] = s4.y, sp[2] = s4.z, sp[3] = s4.w;
-                const uint4 yv = *reinterpret_cast<const uint4*>(
-                    sb + kYOff + cb * kYBoxBytes + tok * 128 + ((cch ^ (tok & 7)) << 4));
-                const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m) yf[2 * m] = bf_lo(yw[m]), yf[2 * m + 1] = bf_hi(yw[m]);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int brow = tok * 4 + i;
-                const uint4 rv = *reinterpret_cast<const uint4*>(
-                    sb + cb * kRBoxBytes + brow * 128 + ((cch ^ (brow & 7)) << 4));
-                const uint32_t rw4[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t v = rw4[m];
-                    if (WRITE)
-                        v = pack_bf2(fmaf(sp[i], yf[2 * m], bf_lo(v)),
-                                     fmaf(sp[i], yf[2 * m + 1], bf_hi(v)));
-                    Rp[i][row][m] = v;
-                }
-                if (WRITE && tok < nv) {
-                    __nv_bfloat16* dst = R + (size_t(t0 + tok) * 4 + i) * size_t(D) +
-                                         size_t(crank) * kDq + warp * 32 + q4 * 8;
-                    *reinterpret_cast<uint4*>(dst) =
-                        make_uint4(Rp[i][row][0], Rp[i][row][1], Rp[i][row][2], Rp[i][row][3]);
+                    for (int m = 0; m < 4; ++m) Rp[row][j4][m] = w[m];
                 }
             }
-        }
-        __syncthreads();  // every warp has read the stage; it becomes the partial-sum buffer
-        float* red = reinterpret_cast<float*>(sb);  // [kWarps][kT][4][rw]
+            if (WRITE) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mbar[kMbRReady + int(k % kRStages)]);
+
+            // sums of squares (diagonal of R'·R'ᵀ) and down projections over 128 channels
+            float acc[NTD][4], sq0[4] = {0.f, 0.f, 0.f, 0.f}, sq1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float* r0 = red + ((warp * kT + g) * 4 + i) * rw;
-            float* r1 = red + ((warp * kT + g + 8) * 4 + i) * rw;
-            // down projections (rows: W_d then W_w, gamma folded)
+            for (int j = 0; j < NTD; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint32_t a0 = Rp[0][j4][2 * ks], a1 = Rp[1][j4][2 * ks];
+                    const uint32_t a2 = Rp[0][j4][2 * ks + 1], a3 = Rp[1][j4][2 * ks + 1];
+                    mma_bf16(sq0, a0, a1, a2, a3, a0, a2);   // columns: tokens 0..7
+                    mma_bf16(sq1, a0, a1, a2, a3, a1, a3);   // columns: tokens 8..15
+                }
+#pragma unroll
+                for (int j = 0; j < NTD; ++j) {
+                    uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                    const bool last_half = (j == NTD - 1) && S.half_last;
+                    if (!last_half || lane < 16) b = s_down[(a * 4 + j4) * S.upb + j * 32 + lane];
+                    mma_bf16(acc[j], Rp[0][j4][0], Rp[1][j4][0], Rp[0][j4][1], Rp[1][j4][1], b.x,
+                             b.y);
+                    mma_bf16(acc[j], Rp[0][j4][2], Rp[1][j4][2], Rp[0][j4][3], Rp[1][j4][3], b.z,
+                             b.w);
+                }
+            }
+            // before the row sums of tile k leave, tile k-2's h/inv buffer must be consumed
+            if (k >= 2)
+                mbar_wait(&mbar[kMbREmpty + int((k - 2) % kRStages)],
+                          uint32_t(((k - 2) / kRStages) & 1));
+            float* r0 = red + (a * kT + g) * rw;
+            float* r1 = red + (a * kT + g + 8) * rw;
 #pragma unroll
             for (int j = 0; j < NTD; ++j) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                const bool last_half = (j == NTD - 1) && S.half_last;
-                if (!last_half || lane < 16) b = s_down[(warp * 4 + i) * S.upb + j * 32 + lane];
-                mma_bf16(acc, Rp[i][0][0], Rp[i][1][0], Rp[i][0][1], Rp[i][1][1], b.x, b.y);
-                mma_bf16(acc, Rp[i][0][2], Rp[i][1][2], Rp[i][0][3], Rp[i][1][3], b.z, b.w);
                 const int o = 8 * j + 2 * q4;
                 if (o + 1 < nk) {
-                    *reinterpret_cast<float2*>(r0 + o) = make_float2(acc[0], acc[1]);
-                    *reinterpret_cast<float2*>(r1 + o) = make_float2(acc[2], acc[3]);
+                    *reinterpret_cast<float2*>(r0 + o) = make_float2(acc[j][0], acc[j][1]);
+                    *reinterpret_cast<float2*>(r1 + o) = make_float2(acc[j][2], acc[j][3]);
                 } else if (o < nk) {
-                    r0[o] = acc[0], r1[o] = acc[2];
+                    r0[o] = acc[j][0], r1[o] = acc[j][2];
                 }
-            }
-            // sums of squares: diagonal of R'·R'ᵀ over this warp's 32 channels
-            float sq0[4] = {0.f, 0.f, 0.f, 0.f}, sq1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const uint32_t a0 = Rp[i][0][2 * ks], a1 = Rp[i][1][2 * ks];
-                const uint32_t a2 = Rp[i][0][2 * ks + 1], a3 = Rp[i][1][2 * ks + 1];
-                mma_bf16(sq0, a0, a1, a2, a3, a0, a2);   // columns: tokens 0..7
-                mma_bf16(sq1, a0, a1, a2, a3, a1, a3);   // columns: tokens 8..15
             }
             if (q4 == (g >> 1)) {
                 r0[nk] = (g & 1) ? sq0[1] : sq0[0];
                 r1[nk] = (g & 1) ? sq1[3] : sq1[2];
             }
-        }
-        __syncthreads();
-        {
-            const int nval = kT * 4 * rw;            // a multiple of 4
-            const uint32_t recv_u32 = smem_u32(recv_ptr(p));
-            for (int v = 4 * tid; v < nval; v += 4 * kThreads) {
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float4 b = *reinterpret_cast<const float4*>(red + w * nval + v);
-                    a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+            a_sync();
+            {
+                // value (tok, branch, o) = red[branch][tok][o] + red[branch + 4][tok][o]
+                const int nval = kT * 4 * rw;            // a multiple of 4
+                const uint32_t recv_u32 = smem_u32(recv_ptr(p));
+                for (int v = 4 * tid; v < nval; v += 4 * kAThreads) {
+                    const int tok = v / (4 * rw), rest = v - tok * 4 * rw;
+                    const int bi = rest / rw, o = rest - bi * rw;
+                    const float4 u0 =
+                        *reinterpret_cast<const float4*>(red + (bi * kT + tok) * rw + o);
+                    const float4 u1 =
+                        *reinterpret_cast<const float4*>(red + ((bi + 4) * kT + tok) * rw + o);
+                    const int owner = tok / tpc, slot = tok - owner * tpc;
+                    st_async_v4(recv_u32 + uint32_t(((int(crank) * tpc + slot) * 4 * rw + rest) * 4),
+                                smem_u32(&mbar[kMbRecv + p]), uint32_t(owner), u0.x + u1.x,
+                                u0.y + u1.y, u0.z + u1.z, u0.w + u1.w);
                 }
-                const int tok = v / (4 * rw), rest = v - tok * 4 * rw;
-                const int owner = tok / tpc, slot = tok - owner * tpc;
-                st_async_v4(recv_u32 + uint32_t(((int(crank) * tpc + slot) * 4 * rw + rest) * 4),
-                            smem_u32(&recv_full[p]), uint32_t(owner), a.x, a.y, a.z, a.w);
             }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();  // the stage is free: refill it with tile k + kStages
-        issue_tile(k + kStages);
+            a_sync();  // red and this tile's y buffer are free again
+            // refill: y of tile k+3 into this y buffer; R of tile k+3 into the buffer that
+            // tile k-1 used, once the B warps are done with it
+            if (lane < 2) {
+                issue_y(k + kYStages, a, lane);
+                if (lane == 0 && a < 4 && k + kRStages - 1 < nlocal) {
+                    if (k >= 1)
+                        mbar_wait(&mbar[kMbREmpty + int((k - 1) % kRStages)],
+                                  uint32_t(((k - 1) / kRStages) & 1));
+                    issue_r(k + kRStages - 1, a);
+                }
+            }
 
-        // ---- B(k-1) -------------------------------------------------------------------------
-        if (k > 0) phase_b(k - 1, t0_prev);
-
-        // ---- C(k): owner ---------------------------------------------------------------------
-        if (tid == 0) {
-            mbar_expect_tx(&recv_full[p], uint32_t(C * tpc * 4 * rw * 4));
-            mbar_expect_tx(&bcast_full[p], uint32_t(kT * nb4 * 4));
-        }
-        mbar_wait(&recv_full[p], uint32_t((k >> 1) & 1));
-        {
+            // ---- owner: inv, h (eq gate), s (eq s) for its tokens; send h and inv ----------
+            if (tid == 0) {
+                mbar_expect_tx(&mbar[kMbRecv + p], uint32_t(C * tpc * 4 * rw * 4));
+                mbar_expect_tx(&mbar[kMbBcast + p], uint32_t(kT * nb4 * 4));
+            }
+            mbar_wait(&mbar[kMbRecv + p], uint32_t((k >> 1) & 1));
             float* recv = recv_ptr(p);              // [C][tpc][4][rw]
             const int nown = tpc * 4 * rw;          // a multiple of 4
-            // sum over the C sources: 4 threads per 4-value group, each a quarter of the sources
-            for (int v = tid; v < nown; v += kThreads) {
+            for (int v = tid; v < nown; v += kAThreads) {
                 const int grp = v >> 2, qtr = v & 3;
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int src = qtr; src < C; src += 4) {
                     const float4 b =
                         *reinterpret_cast<const float4*>(recv + src * nown + 4 * grp);
-                    a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+                    s4.x += b.x, s4.y += b.y, s4.z += b.z, s4.w += b.w;
                 }
                 // nown is a multiple of 4, so the four lanes of a group are active together
                 const unsigned mask = __activemask();
 #pragma unroll
                 for (int o = 1; o < 4; o <<= 1) {
-                    a.x += __shfl_xor_sync(mask, a.x, o);
-                    a.y += __shfl_xor_sync(mask, a.y, o);
-                    a.z += __shfl_xor_sync(mask, a.z, o);
-                    a.w += __shfl_xor_sync(mask, a.w, o);
+                    s4.x += __shfl_xor_sync(mask, s4.x, o);
+                    s4.y += __shfl_xor_sync(mask, s4.y, o);
+                    s4.z += __shfl_xor_sync(mask, s4.z, o);
+                    s4.w += __shfl_xor_sync(mask, s4.w, o);
                 }
-                if (qtr == 0) *reinterpret_cast<float4*>(recv + 4 * grp) = a;
+                if (qtr == 0) *reinterpret_cast<float4*>(recv + 4 * grp) = s4;
             }
-            __syncthreads();
-            // one output per thread: h_k = SiLU(z_k) (k < r), else s written and inv kept
-            float* outrow = reinterpret_cast<float*>(smem + S.off_out);   // [tpc][nb4]
-            for (int v = tid; v < tpc * nb4; v += kThreads) {
+            a_sync();
+            for (int v = tid; v < tpc * nb4; v += kAThreads) {
                 const int slot = v / nb4, kk = v - slot * nb4;
                 const int tok = int(crank) * tpc + slot;
                 const float* P = recv + slot * 4 * rw;
                 float out = 0.f;
                 if (kk < nk) {
-                    float inv[4], a = 0.f;
+                    float inv[4], z = 0.f;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         inv[i] = rsqrtf(P[i * rw + nk] / float(D) + eps);
-                        a = fmaf(inv[i], P[i * rw + kk], a);
+                        z = fmaf(inv[i], P[i * rw + kk], z);
                     }
-                    a *= 0.25f;
+                    z *= 0.25f;
                     if (kk < r) {
-                        out = a * sigmoid_accurate(a);
+                        out = z * sigmoid_accurate(z);  // h = SiLU(z)
                     } else {
                         if (t0 + tok < N)
-                            s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sigmoid_accurate(a);
+                            s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sigmoid_accurate(z);
                         out = inv[kk - r];
                     }
                 }
                 outrow[v] = out;
             }
-            __syncthreads();
-            const uint32_t bc_u32 = smem_u32(bcast_ptr(p));
-            const int ngrp = nb4 / 4;
-            // one thread per (owned token, group of 4 outputs, destination CTA)
-            for (int v = tid; v < tpc * ngrp * C; v += kThreads) {
-                const int dst = v % C, rem = v / C;
-                const int slot = rem / ngrp, g4 = rem - slot * ngrp;
-                const int tok = int(crank) * tpc + slot;
-                const float4 o4 = *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
-                st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
-                            smem_u32(&bcast_full[p]), uint32_t(dst), o4.x, o4.y, o4.z, o4.w);
+            a_sync();
+            {
+                const uint32_t bc_u32 = smem_u32(bcast_ptr(p));
+                const int ngrp = nb4 / 4;
+                // one thread per (owned token, group of 4 outputs, destination CTA)
+                for (int v = tid; v < tpc * ngrp * C; v += kAThreads) {
+                    const int dst = v % C, rem = v / C;
+                    const int slot = rem / ngrp, g4 = rem - slot * ngrp;
+                    const int tok = int(crank) * tpc + slot;
+                    const float4 o4 =
+                        *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
+                    st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
+                                smem_u32(&mbar[kMbBcast + p]), uint32_t(dst), o4.x, o4.y, o4.z,
+                                o4.w);
+                }
             }
         }
+    } else {
+        // =============================== B warps ===========================================
+        const int b = warp - kAW;
+        const int cb = b >> 1, cch = ((b & 1) << 2) | q4;
+        // W_u fragments (pre-scaled by ½) for this warp's 32 channels: [branch*4 + n-tile]
+        uint2 wu[16];
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(slice + S.down_bytes) +
+                               (b * 32 + lane) * 8;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+            for (int m = 0; m < 8; ++m) {
+                const uint4 v = src[m];
+                wu[2 * m] = make_uint2(v.x, v.y);
+                wu[2 * m + 1] = make_uint2(v.z, v.w);
+            }
+        }
+        mbar_wait(&mbar[kMbWeights], 0);
+        const float* s_gam = reinterpret_cast<const float*>(smem + S.off_gam);
+        for (int64_t k = 0; k < nlocal; ++k) {
+            const int64_t t0 = (cid + k * ncl) * kT;
+            const int p = int(k & 1);
+            const char* rb = rbuf(k);
+            mbar_wait(&mbar[kMbBcast + p], uint32_t((k >> 1) & 1));
+            mbar_wait(&mbar[kMbRReady + int(k % kRStages)], uint32_t((k / kRStages) & 1));
+            const float* bc = bcast_ptr(p);
+            uint32_t ahi[4], alo[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int tk = g + 8 * (m & 1), kc = 2 * q4 + 8 * (m >> 1);
+                const float h0 = kc < r ? bc[tk * nb4 + kc] : 0.f;
+                const float h1 = kc + 1 < r ? bc[tk * nb4 + kc + 1] : 0.f;
+                const float h0h = __bfloat162float(__float2bfloat16_rn(h0));
+                const float h1h = __bfloat162float(__float2bfloat16_rn(h1));
+                ahi[m] = pack_bf2(h0h, h1h);
+                alo[m] = pack_bf2(h0 - h0h, h1 - h1h);
+            }
+            float xacc[2][8];
 #pragma unroll
             for (int row = 0; row < 2; ++row)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) Rq[i][row][m] = Rp[i][row][m];
-        t0_prev = t0;
+                for (int e = 0; e < 8; ++e) xacc[row][e] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float inv0 = bc[g * nb4 + r + i], inv1 = bc[(g + 8) * nb4 + r + i];
+                const uint4 r0 = *reinterpret_cast<const uint4*>(rb + cb * kRBoxBytes +
+                                                                 swz(g * 4 + i, cch));
+                const uint4 r1 = *reinterpret_cast<const uint4*>(rb + cb * kRBoxBytes +
+                                                                 swz((g + 8) * 4 + i, cch));
+                const uint32_t q0[4] = {r0.x, r0.y, r0.z, r0.w};
+                const uint32_t q1[4] = {r1.x, r1.y, r1.z, r1.w};
+                const float4 gA = *reinterpret_cast<const float4*>(s_gam + i * kDq + b * 32 + q4 * 8);
+                const float4 gB =
+                    *reinterpret_cast<const float4*>(s_gam + i * kDq + b * 32 + q4 * 8 + 4);
+                const float gm[8] = {gA.x, gA.y, gA.z, gA.w, gB.x, gB.y, gB.z, gB.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_bf16(c, ahi[0], ahi[1], ahi[2], ahi[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
+                    mma_bf16(c, alo[0], alo[1], alo[2], alo[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
+                    const float a00 = gm[2 * j] * inv0 * bf_lo(q0[j]);
+                    const float a01 = gm[2 * j + 1] * inv0 * bf_hi(q0[j]);
+                    const float a10 = gm[2 * j] * inv1 * bf_lo(q1[j]);
+                    const float a11 = gm[2 * j + 1] * inv1 * bf_hi(q1[j]);
+                    // G·a = ½a + ½·tanh(·)·a; the ½ is applied once at the end
+                    xacc[0][2 * j] += fmaf(tanh_approx(c[0]), a00, a00);
+                    xacc[0][2 * j + 1] += fmaf(tanh_approx(c[1]), a01, a01);
+                    xacc[1][2 * j] += fmaf(tanh_approx(c[2]), a10, a10);
+                    xacc[1][2 * j + 1] += fmaf(tanh_approx(c[3]), a11, a11);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mbar[kMbREmpty + int(k % kRStages)]);
+#pragma unroll
+            for (int row = 0; row < 2; ++row) {
+                const int tok = g + 8 * row;
+                if (t0 + tok < N) {
+                    __nv_bfloat16* dst =
+                        x + size_t(t0 + tok) * D + size_t(crank) * kDq + b * 32 + q4 * 8;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(
+                        pack_bf2(0.125f * xacc[row][0], 0.125f * xacc[row][1]),
+                        pack_bf2(0.125f * xacc[row][2], 0.125f * xacc[row][3]),
+                        pack_bf2(0.125f * xacc[row][4], 0.125f * xacc[row][5]),
+                        pack_bf2(0.125f * xacc[row][6], 0.125f * xacc[row][7]));
+                }
+            }
+        }
     }
-    if (k > 0) phase_b(k - 1, t0_prev);
     cluster_sync();  // no CTA leaves while shared::cluster traffic to it may be in flight
 }
 
-// Fragment section: for CTA slice q, [down | up | gamma] (the kernel's shared-memory order).
+// Fragment section: for CTA slice q, [down | up | gamma].
+//   down: [A warp a][32-channel chunk j4][upb units of 16 B]: unit (n-tile j, lane) holds
+//         W'[8j + lane/4][8 channels 128·(a/4) + 32·j4 + 8·(lane%4) ...] of branch a%4, where
+//         rows 0..r-1 are W_d, rows r..r+3 are W_w (gamma folded) and the rest are zero.
+//   up:   [B warp b][lane][branch i][n-tile j] 8 B: ½·W_u[i·D + c][k] for the channel
+//         c = 256q + 32b + 8·(g/2) + 2j + g%2 (g = lane/4) and k = 2·(lane%4) + {0, 1, 8, 9}.
+//   gamma: fp32 [4][256] of this CTA's channels.
 __global__ void pack_fused_kernel(int D, int r, const float* __restrict__ gamma,
                                   const float* __restrict__ wd, const float* __restrict__ wu,
                                   const float* __restrict__ ww, char* __restrict__ frag) {
     const FusedShape S = fused_shape(D, r);
     const int K = 4 * D;
-    const int n_down = kWarps * 4 * S.upb;        // 16-byte units per slice
-    const int n_up = kWarps * 4 * 4 * 32;         // 8-byte units per slice
+    const int n_down = kAW * 4 * S.upb;           // 16-byte units per slice
+    const int n_up = kBW * 32 * 16;               // 8-byte units per slice
     const int n_gam = 4 * kDq;                    // floats per slice
     const int per_slice = n_down + n_up + n_gam;
     const int64_t total = int64_t(S.C) * per_slice;
@@ -575,33 +623,35 @@ __global__ void pack_fused_kernel(int D, int r, const float* __restrict__ gamma,
         int u = int(e - int64_t(q) * per_slice);
         char* slice = frag + size_t(q) * S.slice_bytes;
         if (u < n_down) {
-            const int wi = u / S.upb, rest = u - wi * S.upb;   // wi = warp*4 + branch
+            const int aj = u / S.upb, rest = u - aj * S.upb;   // aj = A warp * 4 + chunk
             const int j = rest >> 5, lane = rest & 31;
-            const int w = wi >> 2, i = wi & 3;
+            const int a = aj >> 2, j4 = aj & 3;
+            const int i = a & 3, hh = a >> 2;
             const int n = 8 * j + (lane >> 2);
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(slice + size_t(u) * 16);
             for (int c8 = 0; c8 < 8; ++c8) {
-                const int m = i * D + q * kDq + w * 32 + (lane & 3) * 8 + c8;
+                const int m = i * D + q * kDq + hh * 128 + j4 * 32 + (lane & 3) * 8 + c8;
                 float v = 0.f;
                 if (n < r) v = wd[size_t(n) * K + m] * gamma[m];
                 else if (n < r + 4) v = ww[size_t(n - r) * K + m] * gamma[m];
                 dst[c8] = __float2bfloat16_rn(v);
             }
         } else if ((u -= n_down) < n_up) {
-            const int lane = u & 31, rest = u >> 5;
-            const int j = rest & 3, wi = rest >> 2;
-            const int w = wi >> 2, i = wi & 3;
+            const int nt = u & 15, rest = u >> 4;       // nt = branch*4 + n-tile
+            const int lane = rest & 31, bw = rest >> 5;
+            const int i = nt >> 2, j = nt & 3;
             const int gg = lane >> 2, qq = lane & 3;
-            const int m = i * D + q * kDq + w * 32 + 8 * (gg >> 1) + 2 * j + (gg & 1);
+            const int m = i * D + q * kDq + bw * 32 + 8 * (gg >> 1) + 2 * j + (gg & 1);
             const int kk[4] = {2 * qq, 2 * qq + 1, 2 * qq + 8, 2 * qq + 9};
             __nv_bfloat16* dst =
-                reinterpret_cast<__nv_bfloat16*>(slice + S.off_up + size_t(u) * 8);
+                reinterpret_cast<__nv_bfloat16*>(slice + S.down_bytes + size_t(u) * 8);
             for (int t = 0; t < 4; ++t)
                 dst[t] = __float2bfloat16_rn(kk[t] < r ? 0.5f * wu[size_t(m) * r + kk[t]] : 0.f);
         } else {
             u -= n_up;
             const int i = u / kDq, cl = u - i * kDq;
-            reinterpret_cast<float*>(slice + S.off_gam)[u] = gamma[i * D + q * kDq + cl];
+            reinterpret_cast<float*>(slice + S.down_bytes + S.up_bytes)[u] =
+                gamma[i * D + q * kDq + cl];
         }
     }
 }
