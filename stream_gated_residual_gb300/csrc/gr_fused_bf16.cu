@@ -20,13 +20,14 @@
 //     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (stored
 //       to HBM and written back in place into the R buffer), the per-branch sums of squares
 //       (diagonal of R'·R'ᵀ on the tensor cores) and the down projections (W_d, W_w with gamma
-//       folded, mma fragments resident in shared memory); sum the two halves; send each token's
-//       row sums with st.async to the token's owner CTA; and, as owners, form inv, h and s and
-//       send h and inv to every CTA of the cluster.
-//     - B warps (8): warp b owns 32 channels of all four branches and keeps its W_u fragments in
-//       registers. For each tile they wait for h and inv, run the up projection on the tensor
-//       cores (h split into bf16 hi + lo parts), form σ(a) = ½ + ½·tanh(a/2) (W_u pre-scaled by
-//       ½), combine the branches from the in-place R', store x, and release the R buffer.
+//       folded, mma fragments resident in shared memory); sum the two halves; and send each
+//       token's row sums with st.async to the token's owner CTA.
+//     - B warps (8): as owners they gather the row sums of their tokens from every CTA, form
+//       inv, h and s and send h and inv to every CTA of the cluster. Warp b also owns 32
+//       channels of all four branches and keeps its W_u fragments in registers: for each tile
+//       it waits for h and inv, runs the up projection on the tensor cores (h split into bf16
+//       hi + lo parts), forms σ(a) = ½ + ½·tanh(a/2) (W_u pre-scaled by ½), combines the
+//       branches from the in-place R', stores x, and releases the R buffer for the next TMA.
 //   * mbarriers carry every hand-off (TMA completion, R' ready, R buffer empty, row sums and h
 //     arriving from other CTAs); there is no cluster-wide barrier in the steady state.
 #include <cuda.h>
@@ -138,9 +139,12 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Named barrier among the A warps only.
+// Named barriers among the A warps only and among the B warps only.
 __device__ __forceinline__ void a_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kAThreads) : "memory");
+}
+__device__ __forceinline__ void b_sync() {
+    asm volatile("bar.sync 2, %0;" ::"n"(kBW * 32) : "memory");
 }
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -156,7 +160,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                  : "memory");
 }
 // Bounded wait on phase `parity` (acquire at cluster scope, so data that remote CTAs delivered
-// with complete_tx is visible); records a status bit and returns false if it runs out.
+// with complete_tx is visible); records a status bit and returns false if it runs out. Each
+// try_wait may suspend the warp for up to kSuspendNs, so waiting warps do not take issue slots
+// from the warps that share their scheduler.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     const uint32_t a = smem_u32(bar);
     const long long t0 = clock64();
@@ -164,10 +171,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n"
-            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
             " selp.u32 %0, 1, 0, p;\n}"
             : "=r"(done)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (done) return true;
         if (clock64() - t0 > kWaitLimit) {
@@ -308,7 +315,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                  &mbar[kMbWeights]);
     }
     if (warp < kAW && lane < 2) {
-        for (int k = 0; k < kRStages - 1; ++k) {
+        for (int k = 0; k < kRStages; ++k) {
             if (lane == 0 && warp < 4) issue_r(k, warp);
         }
         for (int k = 0; k < kYStages; ++k) issue_y(k, warp, lane);
@@ -321,7 +328,6 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         mbar_wait(&mbar[kMbWeights], 0);
         const uint4* s_down = reinterpret_cast<const uint4*>(smem);
         float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kAW][kT][rw]
-        float* outrow = reinterpret_cast<float*>(smem + S.off_out);
         for (int64_t k = 0; k < nlocal; ++k) {
             const int64_t t0 = (cid + k * ncl) * kT;
             const int nv = int(N - t0 < kT ? N - t0 : kT);
@@ -331,36 +337,50 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             mbar_wait(&mbar[kMbRFull + int(k % kRStages)], uint32_t((k / kRStages) & 1));
             if (WRITE) mbar_wait(&mbar[kMbYFull + int(k % kYStages)], uint32_t((k / kYStages) & 1));
 
-            // write (eq write) for this warp's branch and 128 channels; R' back in place
+            // write (eq write) for this warp's branch and 128 channels; R' back in place.
+            // All loads first: the in-place stores would otherwise order every later load.
             uint32_t Rp[2][4][4];  // [row g / g+8][chunk][channel pair]
+            uint4 yv[2][4];
+            float sp[2] = {0.f, 0.f};
 #pragma unroll
             for (int row = 0; row < 2; ++row) {
                 const int tok = g + 8 * row, brow = tok * 4 + ib;
-                float sp = 0.f;
-                if (WRITE) sp = *reinterpret_cast<const float*>(yb + kSOff + tok * 16 + ib * 4);
+                if (WRITE) sp[row] = *reinterpret_cast<const float*>(yb + kSOff + tok * 16 + ib * 4);
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4) {
                     const int cb = hh * 2 + (j4 >> 1), cch = ((j4 & 1) << 2) | q4;
-                    char* rp = rb + cb * kRBoxBytes + swz(brow, cch);
-                    const uint4 rv = *reinterpret_cast<const uint4*>(rp);
-                    uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
-                    if (WRITE) {
-                        const uint4 yv = *reinterpret_cast<const uint4*>(
-                            yb + cb * kYBoxBytes + swz(tok, cch));
-                        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+                    const uint4 rv =
+                        *reinterpret_cast<const uint4*>(rb + cb * kRBoxBytes + swz(brow, cch));
+                    Rp[row][j4][0] = rv.x, Rp[row][j4][1] = rv.y, Rp[row][j4][2] = rv.z,
+                    Rp[row][j4][3] = rv.w;
+                    if (WRITE)
+                        yv[row][j4] = *reinterpret_cast<const uint4*>(yb + cb * kYBoxBytes +
+                                                                      swz(tok, cch));
+                }
+            }
+            if (WRITE) {
 #pragma unroll
-                        for (int m = 0; m < 4; ++m)
-                            w[m] = pack_bf2(fmaf(sp, bf_lo(yw[m]), bf_lo(w[m])),
-                                            fmaf(sp, bf_hi(yw[m]), bf_hi(w[m])));
-                        const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4*>(rp) = o;
+                for (int row = 0; row < 2; ++row) {
+                    const int tok = g + 8 * row, brow = tok * 4 + ib;
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int cb = hh * 2 + (j4 >> 1), cch = ((j4 & 1) << 2) | q4;
+                        const uint32_t yw[4] = {yv[row][j4].x, yv[row][j4].y, yv[row][j4].z,
+                                                yv[row][j4].w};
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const uint32_t w = Rp[row][j4][m];
+                            Rp[row][j4][m] = pack_bf2(fmaf(sp[row], bf_lo(yw[m]), bf_lo(w)),
+                                                      fmaf(sp[row], bf_hi(yw[m]), bf_hi(w)));
+                        }
+                        const uint4 o = make_uint4(Rp[row][j4][0], Rp[row][j4][1],
+                                                   Rp[row][j4][2], Rp[row][j4][3]);
+                        *reinterpret_cast<uint4*>(rb + cb * kRBoxBytes + swz(brow, cch)) = o;
                         if (tok < nv)
                             *reinterpret_cast<uint4*>(
                                 R + (size_t(t0 + tok) * 4 + ib) * size_t(D) + size_t(crank) * kDq +
                                 hh * 128 + j4 * 32 + q4 * 8) = o;
                     }
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) Rp[row][j4][m] = w[m];
                 }
             }
             if (WRITE) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -430,85 +450,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             a_sync();  // red and this tile's y buffer are free again
-            // refill: y of tile k+3 into this y buffer; R of tile k+3 into the buffer that
-            // tile k-1 used, once the B warps are done with it
-            if (lane < 2) {
-                issue_y(k + kYStages, a, lane);
-                if (lane == 0 && a < 4 && k + kRStages - 1 < nlocal) {
-                    if (k >= 1)
-                        mbar_wait(&mbar[kMbREmpty + int((k - 1) % kRStages)],
-                                  uint32_t(((k - 1) / kRStages) & 1));
-                    issue_r(k + kRStages - 1, a);
-                }
-            }
-
-            // ---- owner: inv, h (eq gate), s (eq s) for its tokens; send h and inv ----------
-            if (tid == 0) {
-                mbar_expect_tx(&mbar[kMbRecv + p], uint32_t(C * tpc * 4 * rw * 4));
-                mbar_expect_tx(&mbar[kMbBcast + p], uint32_t(kT * nb4 * 4));
-            }
-            mbar_wait(&mbar[kMbRecv + p], uint32_t((k >> 1) & 1));
-            float* recv = recv_ptr(p);              // [C][tpc][4][rw]
-            const int nown = tpc * 4 * rw;          // a multiple of 4
-            for (int v = tid; v < nown; v += kAThreads) {
-                const int grp = v >> 2, qtr = v & 3;
-                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int src = qtr; src < C; src += 4) {
-                    const float4 b =
-                        *reinterpret_cast<const float4*>(recv + src * nown + 4 * grp);
-                    s4.x += b.x, s4.y += b.y, s4.z += b.z, s4.w += b.w;
-                }
-                // nown is a multiple of 4, so the four lanes of a group are active together
-                const unsigned mask = __activemask();
-#pragma unroll
-                for (int o = 1; o < 4; o <<= 1) {
-                    s4.x += __shfl_xor_sync(mask, s4.x, o);
-                    s4.y += __shfl_xor_sync(mask, s4.y, o);
-                    s4.z += __shfl_xor_sync(mask, s4.z, o);
-                    s4.w += __shfl_xor_sync(mask, s4.w, o);
-                }
-                if (qtr == 0) *reinterpret_cast<float4*>(recv + 4 * grp) = s4;
-            }
-            a_sync();
-            for (int v = tid; v < tpc * nb4; v += kAThreads) {
-                const int slot = v / nb4, kk = v - slot * nb4;
-                const int tok = int(crank) * tpc + slot;
-                const float* P = recv + slot * 4 * rw;
-                float out = 0.f;
-                if (kk < nk) {
-                    float inv[4], z = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        inv[i] = rsqrtf(P[i * rw + nk] / float(D) + eps);
-                        z = fmaf(inv[i], P[i * rw + kk], z);
-                    }
-                    z *= 0.25f;
-                    if (kk < r) {
-                        out = z * sigmoid_accurate(z);  // h = SiLU(z)
-                    } else {
-                        if (t0 + tok < N)
-                            s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sigmoid_accurate(z);
-                        out = inv[kk - r];
-                    }
-                }
-                outrow[v] = out;
-            }
-            a_sync();
-            {
-                const uint32_t bc_u32 = smem_u32(bcast_ptr(p));
-                const int ngrp = nb4 / 4;
-                // one thread per (owned token, group of 4 outputs, destination CTA)
-                for (int v = tid; v < tpc * ngrp * C; v += kAThreads) {
-                    const int dst = v % C, rem = v / C;
-                    const int slot = rem / ngrp, g4 = rem - slot * ngrp;
-                    const int tok = int(crank) * tpc + slot;
-                    const float4 o4 =
-                        *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
-                    st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
-                                smem_u32(&mbar[kMbBcast + p]), uint32_t(dst), o4.x, o4.y, o4.z,
-                                o4.w);
-                }
-            }
+            if (lane < 2) issue_y(k + kYStages, a, lane);   // y of tile k+3 into this buffer
         }
     } else {
         // =============================== B warps ===========================================
@@ -528,7 +470,81 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         }
         mbar_wait(&mbar[kMbWeights], 0);
         const float* s_gam = reinterpret_cast<const float*>(smem + S.off_gam);
-        for (int64_t k = 0; k < nlocal; ++k) {
+        float* outrow = reinterpret_cast<float*>(smem + S.off_out);
+        const int bt = tid - kAThreads;              // 0 .. 255
+        const float inv_d = 1.0f / float(D);
+
+        // Owner step for local tile k: row sums of its tokens from every CTA -> inv, h, s.
+        auto owner = [&](int64_t k) {
+            const int64_t t0 = (cid + k * ncl) * kT;
+            const int p = int(k & 1);
+            if (bt == 0) {
+                mbar_expect_tx(&mbar[kMbRecv + p], uint32_t(C * tpc * 4 * rw * 4));
+                mbar_expect_tx(&mbar[kMbBcast + p], uint32_t(kT * nb4 * 4));
+            }
+            mbar_wait(&mbar[kMbRecv + p], uint32_t((k >> 1) & 1));
+            float* recv = recv_ptr(p);              // [C][tpc][4][rw]
+            const int nown = tpc * 4 * rw;          // a multiple of 4
+            for (int v = bt; v < nown; v += kBW * 32) {
+                const int grp = v >> 2, qtr = v & 3;
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int src = qtr; src < C; src += 4) {
+                    const float4 b4 =
+                        *reinterpret_cast<const float4*>(recv + src * nown + 4 * grp);
+                    s4.x += b4.x, s4.y += b4.y, s4.z += b4.z, s4.w += b4.w;
+                }
+                // nown is a multiple of 4, so the four lanes of a group are active together
+                const unsigned mask = __activemask();
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    s4.x += __shfl_xor_sync(mask, s4.x, o);
+                    s4.y += __shfl_xor_sync(mask, s4.y, o);
+                    s4.z += __shfl_xor_sync(mask, s4.z, o);
+                    s4.w += __shfl_xor_sync(mask, s4.w, o);
+                }
+                if (qtr == 0) *reinterpret_cast<float4*>(recv + 4 * grp) = s4;
+            }
+            b_sync();
+            for (int v = bt; v < tpc * nb4; v += kBW * 32) {
+                const int slot = v / nb4, kk = v - slot * nb4;
+                const int tok = int(crank) * tpc + slot;
+                const float* P = recv + slot * 4 * rw;
+                float out = 0.f;
+                if (kk < nk) {
+                    float inv[4], z = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        inv[i] = rsqrtf(fmaf(P[i * rw + nk], inv_d, eps));
+                        z = fmaf(inv[i], P[i * rw + kk], z);
+                    }
+                    z *= 0.25f;
+                    const float sg = __frcp_rn(1.0f + expf(-z));   // σ(z)
+                    if (kk < r) {
+                        out = z * sg;  // h = SiLU(z)
+                    } else {
+                        if (t0 + tok < N) s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sg;
+                        out = inv[kk - r];
+                    }
+                }
+                outrow[v] = out;
+            }
+            b_sync();
+            const uint32_t bc_u32 = smem_u32(bcast_ptr(p));
+            const int ngrp = nb4 / 4;
+            // one thread per (owned token, group of 4 outputs, destination CTA)
+            for (int v = bt; v < tpc * ngrp * C; v += kBW * 32) {
+                const int dst = v % C, rem = v / C;
+                const int slot = rem / ngrp, g4 = rem - slot * ngrp;
+                const int tok = int(crank) * tpc + slot;
+                const float4 o4 = *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
+                st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
+                            smem_u32(&mbar[kMbBcast + p]), uint32_t(dst), o4.x, o4.y, o4.z, o4.w);
+            }
+        };
+
+        // Up projection (eq gate), gates, combine (eq use_gate) and x for local tile k; then the
+        // R buffer is released and refilled with tile k+4.
+        auto combine = [&](int64_t k) {
             const int64_t t0 = (cid + k * ncl) * kT;
             const int p = int(k & 1);
             const char* rb = rbuf(k);
@@ -595,7 +611,19 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                         pack_bf2(0.125f * xacc[row][6], 0.125f * xacc[row][7]));
                 }
             }
+            // refill: once every B warp is done with this buffer, R of tile k+4 goes into it
+            // (lane 0 of B warps 0..3, one box each)
+            if (lane == 0 && b < 4 && k + kRStages < nlocal) {
+                mbar_wait(&mbar[kMbREmpty + int(k % kRStages)], uint32_t((k / kRStages) & 1));
+                issue_r(k + kRStages, b);
+            }
+        };
+
+        for (int64_t k = 0; k < nlocal; ++k) {
+            owner(k);
+            if (k > 0) combine(k - 1);
         }
+        if (nlocal > 0) combine(nlocal - 1);
     }
     cluster_sync();  // no CTA leaves while shared::cluster traffic to it may be in flight
 }
