@@ -50,8 +50,8 @@ constexpr int kColBlocks = kDq / kBoxCh;    // 4 boxes per row slice
 constexpr int kRBoxBytes = kBoxCh * 4 * kT * 2;        // [16 tok][4 br][64 ch] bf16 = 8 KB
 constexpr int kRBufBytes = kColBlocks * kRBoxBytes;     // 32 KB
 constexpr int kYBoxBytes = kBoxCh * kT * 2;             // [16 tok][64 ch] bf16 = 2 KB
-constexpr int kSOff = kColBlocks * kYBoxBytes;          // s_prev rows after the y boxes
-constexpr int kYBufBytes = 9 * 1024;                    // 8 KB of y + 256 B of s_prev, padded
+constexpr int kYBufBytes = kColBlocks * kYBoxBytes;     // 8 KB (1024-aligned: swizzle atoms)
+constexpr int kSBufBytes = kT * 16;                     // s_prev rows of a tile, own small ring
 constexpr int kMaxCluster = 16;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles before a wait gives up (~2 s)
 
@@ -70,12 +70,12 @@ struct FusedShape {
     int nb4;          // broadcast row per token: h (r values) then inv (4), padded to 4 floats
     int down_bytes, up_bytes, gam_bytes, slice_bytes;
     int red_bytes, recv_bytes, bcast_bytes;
-    int off_gam, off_r, off_y, off_red, off_recv, off_bcast, off_out, off_mbar, smem_bytes;
+    int off_gam, off_r, off_y, off_s, off_red, off_recv, off_bcast, off_out, off_mbar, smem_bytes;
 };
 
 // Packed fragment slice of one CTA: down | up | gamma. Shared memory: down | gamma | R ring
-// (1024-aligned) | y ring | red | recv[2] | bcast[2] | out | mbarriers. The up fragments go to
-// the B warps' registers straight from global memory.
+// (1024-aligned) | y ring | s_prev ring | red | recv[2] | bcast[2] | out | mbarriers. The up
+// fragments go to the B warps' registers straight from global memory.
 __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     FusedShape s{};
     s.C = D / kDq;
@@ -90,12 +90,13 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     s.gam_bytes = 4 * kDq * 4;
     s.slice_bytes = s.down_bytes + s.up_bytes + s.gam_bytes;
     s.red_bytes = kAW * kT * s.rw * 4;
-    s.recv_bytes = kT * 4 * s.rw * 4;
+    s.recv_bytes = s.C * ((kT / s.C) * 4 * s.rw + 4) * 4;   // per source: its rows + 4 pad
     s.bcast_bytes = kT * s.nb4 * 4;
     s.off_gam = s.down_bytes;
     s.off_r = round_up(s.off_gam + s.gam_bytes, 1024);
     s.off_y = s.off_r + kRStages * kRBufBytes;
-    s.off_red = s.off_y + kYStages * kYBufBytes;
+    s.off_s = s.off_y + kYStages * kYBufBytes;
+    s.off_red = s.off_s + kYStages * kSBufBytes;
     s.off_recv = s.off_red + round_up(s.red_bytes, 16);
     s.off_bcast = s.off_recv + 2 * round_up(s.recv_bytes, 16);
     s.off_out = s.off_bcast + 2 * round_up(s.bcast_bytes, 16);
@@ -229,13 +230,53 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// d = a·b (accumulator starts at zero)
+__device__ __forceinline__ void mma_bf16_z(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+// Packed fp32 pairs (one instruction for two lanes of fp32 arithmetic).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16 pair (low half first) -> fp32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t u) {
+    return f2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
+    float lo, hi;
+    unf2(v, lo, hi);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+// floor(n / d) for 0 <= n < 512 and 1 <= d <= 64, with m = ceil(2^16 / d): n·m/2^16 exceeds n/d
+// by less than 512/2^16 < 1/64 <= 1/d, so the floor is exact.
+__device__ __forceinline__ int div_small(int n, uint32_t m) { return int((uint32_t(n) * m) >> 16); }
+__host__ __device__ inline uint32_t div_magic(int d) { return (65536u + uint32_t(d) - 1) / uint32_t(d); }
+
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
@@ -267,6 +308,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S.off_mbar);
     auto rbuf = [&](int64_t k) { return smem + S.off_r + int(k % kRStages) * kRBufBytes; };
     auto ybuf = [&](int64_t k) { return smem + S.off_y + int(k % kYStages) * kYBufBytes; };
+    auto sbuf = [&](int64_t k) { return smem + S.off_s + int(k % kYStages) * kSBufBytes; };
     auto recv_ptr = [&](int p) {
         return reinterpret_cast<float*>(smem + S.off_recv + p * round_up(S.recv_bytes, 16));
     };
@@ -305,7 +347,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             tma_load_2d(ybuf(k) + yb * kYBoxBytes, &tm_y, int(crank) * kDq + yb * kBoxCh, t0, bar);
         }
         if (a == 0 && ln == 1)
-            bulk_g2s(ybuf(k) + kSOff, s_prev + size_t(t0) * 4, uint32_t(nv) * 16, bar);
+            bulk_g2s(sbuf(k), s_prev + size_t(t0) * 4, uint32_t(nv) * 16, bar);
     };
 
     if (tid == 0) {
@@ -325,6 +367,12 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     if (warp < kAW) {
         // =============================== A warps ===========================================
         const int a = warp, ib = a & 3, hh = a >> 2;
+        // R row of token g, branch ib, first channel of this thread in this CTA's slice; token
+        // t0 + g of a tile is t0·4·D elements further, token t0 + g + 8 another 32·D
+        __nv_bfloat16* const Rg =
+            R + (size_t(g) * 4 + ib) * size_t(D) + size_t(crank) * kDq + hh * 128 + q4 * 8;
+        // send descriptors: float4 items it = tid, tid + 256 of the tile's 16·rw row-sum items
+        const uint32_t m_rw = div_magic(rw), m_rq = div_magic(rw / 4);
         mbar_wait(&mbar[kMbWeights], 0);
         const uint4* s_down = reinterpret_cast<const uint4*>(smem);
         float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kAW][kT][rw]
@@ -334,6 +382,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             const int p = int(k & 1);
             char* rb = rbuf(k);
             const char* yb = ybuf(k);
+            const char* sb = sbuf(k);
             mbar_wait(&mbar[kMbRFull + int(k % kRStages)], uint32_t((k / kRStages) & 1));
             if (WRITE) mbar_wait(&mbar[kMbYFull + int(k % kYStages)], uint32_t((k / kYStages) & 1));
 
@@ -345,7 +394,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
 #pragma unroll
             for (int row = 0; row < 2; ++row) {
                 const int tok = g + 8 * row, brow = tok * 4 + ib;
-                if (WRITE) sp[row] = *reinterpret_cast<const float*>(yb + kSOff + tok * 16 + ib * 4);
+                if (WRITE) sp[row] = *reinterpret_cast<const float*>(sb + tok * 16 + ib * 4);
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4) {
                     const int cb = hh * 2 + (j4 >> 1), cch = ((j4 & 1) << 2) | q4;
@@ -359,27 +408,25 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             if (WRITE) {
+                __nv_bfloat16* gR = Rg + size_t(t0) * 4 * size_t(D);
 #pragma unroll
                 for (int row = 0; row < 2; ++row) {
                     const int tok = g + 8 * row, brow = tok * 4 + ib;
+                    const uint64_t s2 = f2(sp[row], sp[row]);
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
                         const int cb = hh * 2 + (j4 >> 1), cch = ((j4 & 1) << 2) | q4;
                         const uint32_t yw[4] = {yv[row][j4].x, yv[row][j4].y, yv[row][j4].z,
                                                 yv[row][j4].w};
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint32_t w = Rp[row][j4][m];
-                            Rp[row][j4][m] = pack_bf2(fmaf(sp[row], bf_lo(yw[m]), bf_lo(w)),
-                                                      fmaf(sp[row], bf_hi(yw[m]), bf_hi(w)));
-                        }
+                        for (int m = 0; m < 4; ++m)
+                            Rp[row][j4][m] = f2_to_bf2(
+                                fma2(s2, bf2_to_f2(yw[m]), bf2_to_f2(Rp[row][j4][m])));
                         const uint4 o = make_uint4(Rp[row][j4][0], Rp[row][j4][1],
                                                    Rp[row][j4][2], Rp[row][j4][3]);
                         *reinterpret_cast<uint4*>(rb + cb * kRBoxBytes + swz(brow, cch)) = o;
                         if (tok < nv)
-                            *reinterpret_cast<uint4*>(
-                                R + (size_t(t0 + tok) * 4 + ib) * size_t(D) + size_t(crank) * kDq +
-                                hh * 128 + j4 * 32 + q4 * 8) = o;
+                            *reinterpret_cast<uint4*>(gR + row * 32 * size_t(D) + j4 * 32) = o;
                     }
                 }
             }
@@ -388,25 +435,32 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             if (lane == 0) mbar_arrive(&mbar[kMbRReady + int(k % kRStages)]);
 
             // sums of squares (diagonal of R'·R'ᵀ) and down projections over 128 channels
-            float acc[NTD][4], sq0[4] = {0.f, 0.f, 0.f, 0.f}, sq1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < NTD; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+            float acc[NTD][4], sq0[4], sq1[4];
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     const uint32_t a0 = Rp[0][j4][2 * ks], a1 = Rp[1][j4][2 * ks];
                     const uint32_t a2 = Rp[0][j4][2 * ks + 1], a3 = Rp[1][j4][2 * ks + 1];
-                    mma_bf16(sq0, a0, a1, a2, a3, a0, a2);   // columns: tokens 0..7
-                    mma_bf16(sq1, a0, a1, a2, a3, a1, a3);   // columns: tokens 8..15
+                    if (j4 == 0 && ks == 0) {
+                        mma_bf16_z(sq0, a0, a1, a2, a3, a0, a2);   // columns: tokens 0..7
+                        mma_bf16_z(sq1, a0, a1, a2, a3, a1, a3);   // columns: tokens 8..15
+                    } else {
+                        mma_bf16(sq0, a0, a1, a2, a3, a0, a2);
+                        mma_bf16(sq1, a0, a1, a2, a3, a1, a3);
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < NTD; ++j) {
                     uint4 b = make_uint4(0u, 0u, 0u, 0u);
                     const bool last_half = (j == NTD - 1) && S.half_last;
                     if (!last_half || lane < 16) b = s_down[(a * 4 + j4) * S.upb + j * 32 + lane];
-                    mma_bf16(acc[j], Rp[0][j4][0], Rp[1][j4][0], Rp[0][j4][1], Rp[1][j4][1], b.x,
-                             b.y);
+                    if (j4 == 0)
+                        mma_bf16_z(acc[j], Rp[0][j4][0], Rp[1][j4][0], Rp[0][j4][1], Rp[1][j4][1],
+                                   b.x, b.y);
+                    else
+                        mma_bf16(acc[j], Rp[0][j4][0], Rp[1][j4][0], Rp[0][j4][1], Rp[1][j4][1],
+                                 b.x, b.y);
                     mma_bf16(acc[j], Rp[0][j4][2], Rp[1][j4][2], Rp[0][j4][3], Rp[1][j4][3], b.z,
                              b.w);
                 }
@@ -433,18 +487,20 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             }
             a_sync();
             {
+                // item it: token it / rw, branch (it % rw) / (rw/4), 4 values at o;
                 // value (tok, branch, o) = red[branch][tok][o] + red[branch + 4][tok][o]
-                const int nval = kT * 4 * rw;            // a multiple of 4
+                const int srcstride = tpc * 4 * rw + 4;  // padded per-source rows at the owner
                 const uint32_t recv_u32 = smem_u32(recv_ptr(p));
-                for (int v = 4 * tid; v < nval; v += 4 * kAThreads) {
-                    const int tok = v / (4 * rw), rest = v - tok * 4 * rw;
-                    const int bi = rest / rw, o = rest - bi * rw;
+                for (int it = tid; it < kT * rw; it += kAThreads) {
+                    const int tok = div_small(it, m_rw), rem4 = it - tok * rw;
+                    const int bi = div_small(rem4, m_rq), o = 4 * (rem4 - bi * (rw / 4));
                     const float4 u0 =
                         *reinterpret_cast<const float4*>(red + (bi * kT + tok) * rw + o);
                     const float4 u1 =
                         *reinterpret_cast<const float4*>(red + ((bi + 4) * kT + tok) * rw + o);
                     const int owner = tok / tpc, slot = tok - owner * tpc;
-                    st_async_v4(recv_u32 + uint32_t(((int(crank) * tpc + slot) * 4 * rw + rest) * 4),
+                    st_async_v4(recv_u32 + uint32_t((int(crank) * srcstride +
+                                                     (slot * 4 + bi) * rw + o) * 4),
                                 smem_u32(&mbar[kMbRecv + p]), uint32_t(owner), u0.x + u1.x,
                                 u0.y + u1.y, u0.z + u1.z, u0.w + u1.w);
                 }
@@ -456,6 +512,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         // =============================== B warps ===========================================
         const int b = warp - kAW;
         const int cb = b >> 1, cch = ((b & 1) << 2) | q4;
+        __nv_bfloat16* const xg = x + size_t(g) * D + size_t(crank) * kDq + b * 32 + q4 * 8;
         // W_u fragments (pre-scaled by ½) for this warp's 32 channels: [branch*4 + n-tile]
         uint2 wu[16];
         {
@@ -473,6 +530,9 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         float* outrow = reinterpret_cast<float*>(smem + S.off_out);
         const int bt = tid - kAThreads;              // 0 .. 255
         const float inv_d = 1.0f / float(D);
+        const uint32_t m_nb4 = div_magic(nb4), m_ngrp = div_magic(nb4 / 4);
+        int lc = 0;                                  // log2 C (C is a power of two)
+        while ((1 << lc) < C) ++lc;
 
         // Owner step for local tile k: row sums of its tokens from every CTA -> inv, h, s.
         auto owner = [&](int64_t k) {
@@ -483,14 +543,15 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 mbar_expect_tx(&mbar[kMbBcast + p], uint32_t(kT * nb4 * 4));
             }
             mbar_wait(&mbar[kMbRecv + p], uint32_t((k >> 1) & 1));
-            float* recv = recv_ptr(p);              // [C][tpc][4][rw]
+            float* recv = recv_ptr(p);              // [C][tpc·4·rw + 4 pad]
             const int nown = tpc * 4 * rw;          // a multiple of 4
+            const int srcstride = nown + 4;
             for (int v = bt; v < nown; v += kBW * 32) {
                 const int grp = v >> 2, qtr = v & 3;
                 float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int src = qtr; src < C; src += 4) {
                     const float4 b4 =
-                        *reinterpret_cast<const float4*>(recv + src * nown + 4 * grp);
+                        *reinterpret_cast<const float4*>(recv + src * srcstride + 4 * grp);
                     s4.x += b4.x, s4.y += b4.y, s4.z += b4.z, s4.w += b4.w;
                 }
                 // nown is a multiple of 4, so the four lanes of a group are active together
@@ -506,7 +567,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             }
             b_sync();
             for (int v = bt; v < tpc * nb4; v += kBW * 32) {
-                const int slot = v / nb4, kk = v - slot * nb4;
+                const int slot = div_small(v, m_nb4), kk = v - slot * nb4;
                 const int tok = int(crank) * tpc + slot;
                 const float* P = recv + slot * 4 * rw;
                 float out = 0.f;
@@ -533,8 +594,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             const int ngrp = nb4 / 4;
             // one thread per (owned token, group of 4 outputs, destination CTA)
             for (int v = bt; v < tpc * ngrp * C; v += kBW * 32) {
-                const int dst = v % C, rem = v / C;
-                const int slot = rem / ngrp, g4 = rem - slot * ngrp;
+                const int dst = v & (C - 1), rem = v >> lc;
+                const int slot = div_small(rem, m_ngrp), g4 = rem - slot * ngrp;
                 const int tok = int(crank) * tpc + slot;
                 const float4 o4 = *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
                 st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
@@ -562,11 +623,11 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 ahi[m] = pack_bf2(h0h, h1h);
                 alo[m] = pack_bf2(h0 - h0h, h1 - h1h);
             }
-            float xacc[2][8];
+            uint64_t xacc2[2][4];   // [row][channel pair], packed fp32 pairs
 #pragma unroll
             for (int row = 0; row < 2; ++row)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xacc[row][e] = 0.f;
+                for (int j = 0; j < 4; ++j) xacc2[row][j] = f2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float inv0 = bc[g * nb4 + r + i], inv1 = bc[(g + 8) * nb4 + r + i];
@@ -580,35 +641,33 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 const float4 gB =
                     *reinterpret_cast<const float4*>(s_gam + i * kDq + b * 32 + q4 * 8 + 4);
                 const float gm[8] = {gA.x, gA.y, gA.z, gA.w, gB.x, gB.y, gB.z, gB.w};
+                const uint64_t inv0_2 = f2(inv0, inv0), inv1_2 = f2(inv1, inv1);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_bf16(c, ahi[0], ahi[1], ahi[2], ahi[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
+                    float c[4];
+                    mma_bf16_z(c, ahi[0], ahi[1], ahi[2], ahi[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
                     mma_bf16(c, alo[0], alo[1], alo[2], alo[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
-                    const float a00 = gm[2 * j] * inv0 * bf_lo(q0[j]);
-                    const float a01 = gm[2 * j + 1] * inv0 * bf_hi(q0[j]);
-                    const float a10 = gm[2 * j] * inv1 * bf_lo(q1[j]);
-                    const float a11 = gm[2 * j + 1] * inv1 * bf_hi(q1[j]);
-                    // G·a = ½a + ½·tanh(·)·a; the ½ is applied once at the end
-                    xacc[0][2 * j] += fmaf(tanh_approx(c[0]), a00, a00);
-                    xacc[0][2 * j + 1] += fmaf(tanh_approx(c[1]), a01, a01);
-                    xacc[1][2 * j] += fmaf(tanh_approx(c[2]), a10, a10);
-                    xacc[1][2 * j + 1] += fmaf(tanh_approx(c[3]), a11, a11);
+                    const uint64_t gm2 = f2(gm[2 * j], gm[2 * j + 1]);
+                    const uint64_t u0 = mul2(gm2, bf2_to_f2(q0[j]));   // γ·R' (row g)
+                    const uint64_t u1 = mul2(gm2, bf2_to_f2(q1[j]));   // γ·R' (row g+8)
+                    // G·u = ½u + ½·tanh(·)·u; the ½ is applied once at the end
+                    const uint64_t w0 = fma2(f2(tanh_approx(c[0]), tanh_approx(c[1])), u0, u0);
+                    const uint64_t w1 = fma2(f2(tanh_approx(c[2]), tanh_approx(c[3])), u1, u1);
+                    xacc2[0][j] = fma2(inv0_2, w0, xacc2[0][j]);
+                    xacc2[1][j] = fma2(inv1_2, w1, xacc2[1][j]);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&mbar[kMbREmpty + int(k % kRStages)]);
+            const uint64_t eighth = f2(0.125f, 0.125f);
 #pragma unroll
             for (int row = 0; row < 2; ++row) {
                 const int tok = g + 8 * row;
                 if (t0 + tok < N) {
-                    __nv_bfloat16* dst =
-                        x + size_t(t0 + tok) * D + size_t(crank) * kDq + b * 32 + q4 * 8;
+                    __nv_bfloat16* dst = xg + (size_t(t0) + row * 8) * size_t(D);
                     *reinterpret_cast<uint4*>(dst) = make_uint4(
-                        pack_bf2(0.125f * xacc[row][0], 0.125f * xacc[row][1]),
-                        pack_bf2(0.125f * xacc[row][2], 0.125f * xacc[row][3]),
-                        pack_bf2(0.125f * xacc[row][4], 0.125f * xacc[row][5]),
-                        pack_bf2(0.125f * xacc[row][6], 0.125f * xacc[row][7]));
+                        f2_to_bf2(mul2(eighth, xacc2[row][0])), f2_to_bf2(mul2(eighth, xacc2[row][1])),
+                        f2_to_bf2(mul2(eighth, xacc2[row][2])), f2_to_bf2(mul2(eighth, xacc2[row][3])));
                 }
             }
             // refill: once every B warp is done with this buffer, R of tile k+4 goes into it
