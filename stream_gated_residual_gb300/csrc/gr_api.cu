@@ -70,7 +70,8 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? GR_OK : GR_E_CUDA; }
 
 // Which kernel runs a read (or fused step) for this shape.
 bool use_fused(const gr_shape* s) {
-    return s->state_dtype == GR_BF16 && fused_supported(s->d_model, s->rank);
+    return s->state_dtype == GR_BF16 && fused_supported(s->d_model, s->rank) &&
+           s->n_tokens <= fused_max_tokens();
 }
 
 int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,

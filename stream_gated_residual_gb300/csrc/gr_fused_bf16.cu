@@ -15,15 +15,16 @@
 //   * A thread-block cluster of C = D/256 CTAs splits the channels: CTA q owns channels
 //     [256q, 256q+256) of every branch.
 //   * Tiles of 16 tokens (the mma M dimension) arrive by TMA (128-byte swizzle, zero fill past
-//     N): R into a 4-buffer ring, y and s_prev into a 3-buffer ring.
+//     N): R into a 4-buffer ring, y and s_prev into a 2-buffer ring.
 //   * 16 warps in two roles that run concurrently on different tiles:
 //     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (stored
 //       to HBM and written back in place into the R buffer), the per-branch sums of squares
 //       (diagonal of R'·R'ᵀ on the tensor cores) and the down projections (W_d, W_w with gamma
 //       folded, mma fragments resident in shared memory); sum the two halves; and send each
 //       token's row sums with st.async to the token's owner CTA.
-//     - B warps (8): as owners they gather the row sums of their tokens from every CTA, form
-//       inv, h and s and send h and inv to every CTA of the cluster. Warp b also owns 32
+//     - B warps (8): the CTA's owned token slots of each tile go round the B warps; for each
+//       the warp gathers the token's row sums from every CTA, forms inv, h and s with warp
+//       shuffles only, and sends h and inv to every CTA of the cluster. Warp b also owns 32
 //       channels of all four branches and keeps its W_u fragments in registers: for each tile
 //       it waits for h and inv, runs the up projection on the tensor cores (h split into bf16
 //       hi + lo parts), forms σ(a) = ½ + ½·tanh(a/2) (W_u pre-scaled by ½), combines the
@@ -44,7 +45,8 @@ constexpr int kAW = 8, kBW = 8;             // A warps, B warps
 constexpr int kThreads = (kAW + kBW) * 32;
 constexpr int kAThreads = kAW * 32;
 constexpr int kDq = 256;                    // channels per branch per CTA
-constexpr int kRStages = 4, kYStages = 3;
+constexpr int kRStages = 4, kYStages = 2;
+constexpr int kXStages = 3;                 // slots of the row-sum and h/inv exchange buffers
 constexpr int kBoxCh = 64;                  // channels per TMA box (128 bytes: the swizzle span)
 constexpr int kColBlocks = kDq / kBoxCh;    // 4 boxes per row slice
 constexpr int kRBoxBytes = kBoxCh * 4 * kT * 2;        // [16 tok][4 br][64 ch] bf16 = 8 KB
@@ -53,6 +55,7 @@ constexpr int kYBoxBytes = kBoxCh * kT * 2;             // [16 tok][64 ch] bf16 
 constexpr int kYBufBytes = kColBlocks * kYBoxBytes;     // 8 KB (1024-aligned: swizzle atoms)
 constexpr int kSBufBytes = kT * 16;                     // s_prev rows of a tile, own small ring
 constexpr int kMaxCluster = 16;
+constexpr int64_t kMaxTokens = 0x7fffffff - 64;  // token indices stay in int
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles before a wait gives up (~2 s)
 
 // Bit 0: an mbarrier wait of the fused kernel ran out (the data it waited for never came).
@@ -70,11 +73,11 @@ struct FusedShape {
     int nb4;          // broadcast row per token: h (r values) then inv (4), padded to 4 floats
     int down_bytes, up_bytes, gam_bytes, slice_bytes;
     int red_bytes, recv_bytes, bcast_bytes;
-    int off_gam, off_r, off_y, off_s, off_red, off_recv, off_bcast, off_out, off_mbar, smem_bytes;
+    int off_gam, off_r, off_y, off_s, off_red, off_recv, off_bcast, off_mbar, smem_bytes;
 };
 
 // Packed fragment slice of one CTA: down | up | gamma. Shared memory: down | gamma | R ring
-// (1024-aligned) | y ring | s_prev ring | red | recv[2] | bcast[2] | out | mbarriers. The up
+// (1024-aligned) | y ring | s_prev ring | red | recv[3] | bcast[3] | mbarriers. The up
 // fragments go to the B warps' registers straight from global memory.
 __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     FusedShape s{};
@@ -98,9 +101,8 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     s.off_s = s.off_y + kYStages * kYBufBytes;
     s.off_red = s.off_s + kYStages * kSBufBytes;
     s.off_recv = s.off_red + round_up(s.red_bytes, 16);
-    s.off_bcast = s.off_recv + 2 * round_up(s.recv_bytes, 16);
-    s.off_out = s.off_bcast + 2 * round_up(s.bcast_bytes, 16);
-    s.off_mbar = s.off_out + round_up(s.bcast_bytes, 16);
+    s.off_bcast = s.off_recv + kXStages * round_up(s.recv_bytes, 16);
+    s.off_mbar = s.off_bcast + kXStages * round_up(s.bcast_bytes, 16);
     s.smem_bytes = s.off_mbar + round_up(8 * 24, 16);
     return s;
 }
@@ -111,10 +113,10 @@ constexpr int kMbRReady = kMbRFull + kRStages;     // [4] R' written back (8 A-w
 constexpr int kMbREmpty = kMbRReady + kRStages;    // [4] B warps done with the R buffer (8)
 constexpr int kMbYFull = kMbREmpty + kRStages;     // [3] y and s_prev landed (TMA)
 constexpr int kMbWeights = kMbYFull + kYStages;    // weights landed
-constexpr int kMbRecv = kMbWeights + 1;            // [2] row sums from every CTA (owner)
-constexpr int kMbBcast = kMbRecv + 2;              // [2] h and inv from every owner
-constexpr int kMbCount = kMbBcast + 2;
-static_assert(kMbCount <= 24, "mbarrier area holds 24");
+constexpr int kMbRecv = kMbWeights + 1;            // [3] row sums from every CTA (owner)
+constexpr int kMbBcast = kMbRecv + kXStages;       // [3] h and inv from every owner
+constexpr int kMbCount = kMbBcast + kXStages;
+static_assert(kMbCount * 8 + kRStages * 4 <= 24 * 8, "mbarrier area holds 24 slots");
 
 // ---- PTX wrappers ---------------------------------------------------------------------------
 
@@ -140,12 +142,9 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Named barriers among the A warps only and among the B warps only.
+// Named barrier among the A warps only.
 __device__ __forceinline__ void a_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kAThreads) : "memory");
-}
-__device__ __forceinline__ void b_sync() {
-    asm volatile("bar.sync 2, %0;" ::"n"(kBW * 32) : "memory");
 }
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -214,6 +213,15 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
 }
 // 16 bytes into CTA `rank`'s shared memory at the same offset as `local_addr`, completing
 // 16 transaction bytes on that CTA's mbarrier at the offset of `local_bar`.
+// st.async of 16 bytes to cluster shared memory addresses already mapped to the target CTA.
+__device__ __forceinline__ void st_async_v4_mapped(uint32_t ra, uint32_t rb, float a, float b,
+                                                   float c, float d) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(ra),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(rb)
+        : "memory");
+}
 __device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_bar,
                                             uint32_t rank, float a, float b, float c, float d) {
     const uint32_t ra = map_rank(local_addr, rank), rb = map_rank(local_bar, rank);
@@ -289,7 +297,7 @@ __device__ __forceinline__ int swz(int row, int cch) { return row * 128 + ((cch 
 template <bool WRITE, int NTD>
 __global__ void __launch_bounds__(kThreads, 1)
 gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant__ CUtensorMap tm_y,
-                int64_t N, int D, int r, float eps, __nv_bfloat16* __restrict__ R,
+                int N, int D, int r, float eps, __nv_bfloat16* __restrict__ R,
                 const float* __restrict__ s_prev, const char* __restrict__ frag,
                 __nv_bfloat16* __restrict__ x, float* __restrict__ s_out) {
     extern __shared__ __align__(1024) char smem[];
@@ -299,16 +307,19 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     const uint32_t crank = cluster_ctarank();
     const int C = S.C;
     const int tpc = kT / C;                     // tokens owned per CTA and tile
-    const int64_t ncl = ncluster_x(), cid = cluster_id_x();
-    const int64_t ntiles = (N + kT - 1) / kT;
-    const int64_t nlocal = ntiles > cid ? (ntiles - cid + ncl - 1) / ncl : 0;
+    // token indices fit in int: the host takes this kernel only for N <= kMaxTokens
+    const int ncl = int(ncluster_x()), cid = int(cluster_id_x());
+    const int ntiles = (N + kT - 1) / kT;
+    const int nlocal = ntiles > cid ? (ntiles - cid + ncl - 1) / ncl : 0;
     const int nk = r + 4, rw = S.rw, nb4 = S.nb4;
     const char* slice = frag + size_t(crank) * S.slice_bytes;
 
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S.off_mbar);
-    auto rbuf = [&](int64_t k) { return smem + S.off_r + int(k % kRStages) * kRBufBytes; };
-    auto ybuf = [&](int64_t k) { return smem + S.off_y + int(k % kYStages) * kYBufBytes; };
-    auto sbuf = [&](int64_t k) { return smem + S.off_s + int(k % kYStages) * kSBufBytes; };
+    // per R buffer: count of B warps done with it (the eighth of each round refills it)
+    uint32_t* rdone = reinterpret_cast<uint32_t*>(mbar + kMbCount);
+    auto rbuf = [&](int k) { return smem + S.off_r + int(k % kRStages) * kRBufBytes; };
+    auto ybuf = [&](int k) { return smem + S.off_y + int(k % kYStages) * kYBufBytes; };
+    auto sbuf = [&](int k) { return smem + S.off_s + int(k % kYStages) * kSBufBytes; };
     auto recv_ptr = [&](int p) {
         return reinterpret_cast<float*>(smem + S.off_recv + p * round_up(S.recv_bytes, 16));
     };
@@ -322,12 +333,13 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                                (i >= kMbREmpty && i < kMbREmpty + kRStages);
             mbar_init(&mbar[i], eight ? 8u : 1u);
         }
+        for (int i = 0; i < kRStages; ++i) rdone[i] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
     // TMA of the k-th local tile's R boxes (lane 0 of A warps 0..3, one box each).
-    auto issue_r = [&](int64_t k, int a) {
+    auto issue_r = [&](int k, int a) {
         if (k >= nlocal) return;
         const int t0 = int((cid + k * ncl) * kT);
         uint64_t* bar = &mbar[kMbRFull + int(k % kRStages)];
@@ -336,7 +348,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     };
     // TMA of the k-th local tile's y boxes (lane 0 of A warps 4..7) and s_prev rows (warp 0,
     // lane 1); warp 0 lane 0 arms the barrier.
-    auto issue_y = [&](int64_t k, int a, int ln) {
+    auto issue_y = [&](int k, int a, int ln) {
         if (!WRITE || k >= nlocal) return;
         const int t0 = int((cid + k * ncl) * kT);
         const int nv = int(N - t0 < kT ? N - t0 : kT);
@@ -376,10 +388,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         mbar_wait(&mbar[kMbWeights], 0);
         const uint4* s_down = reinterpret_cast<const uint4*>(smem);
         float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kAW][kT][rw]
-        for (int64_t k = 0; k < nlocal; ++k) {
-            const int64_t t0 = (cid + k * ncl) * kT;
+        for (int k = 0; k < nlocal; ++k) {
+            const int t0 = (cid + k * ncl) * kT;
             const int nv = int(N - t0 < kT ? N - t0 : kT);
-            const int p = int(k & 1);
+            const int p = int(k % kXStages);
             char* rb = rbuf(k);
             const char* yb = ybuf(k);
             const char* sb = sbuf(k);
@@ -465,10 +477,12 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                              b.w);
                 }
             }
-            // before the row sums of tile k leave, tile k-2's h/inv buffer must be consumed
-            if (k >= 2)
-                mbar_wait(&mbar[kMbREmpty + int((k - 2) % kRStages)],
-                          uint32_t(((k - 2) / kRStages) & 1));
+            // Before the row sums of tile k leave, every owner must be done with the exchange
+            // slot of tile k-3 and this CTA's B warps with its h/inv slot: both follow from
+            // the local combine of tile k-3 (it needed h from every owner).
+            if (k >= kXStages)
+                mbar_wait(&mbar[kMbREmpty + int((k - kXStages) % kRStages)],
+                          uint32_t(((k - kXStages) / kRStages) & 1));
             float* r0 = red + (a * kT + g) * rw;
             float* r1 = red + (a * kT + g + 8) * rw;
 #pragma unroll
@@ -506,7 +520,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             a_sync();  // red and this tile's y buffer are free again
-            if (lane < 2) issue_y(k + kYStages, a, lane);   // y of tile k+3 into this buffer
+            if (lane < 2) issue_y(k + kYStages, a, lane);   // y of tile k+2 into this buffer
         }
     } else {
         // =============================== B warps ===========================================
@@ -527,89 +541,98 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         }
         mbar_wait(&mbar[kMbWeights], 0);
         const float* s_gam = reinterpret_cast<const float*>(smem + S.off_gam);
-        float* outrow = reinterpret_cast<float*>(smem + S.off_out);
         const int bt = tid - kAThreads;              // 0 .. 255
         const float inv_d = 1.0f / float(D);
-        const uint32_t m_nb4 = div_magic(nb4), m_ngrp = div_magic(nb4 / 4);
         int lc = 0;                                  // log2 C (C is a power of two)
         while ((1 << lc) < C) ++lc;
 
-        // Owner step for local tile k: row sums of its tokens from every CTA -> inv, h, s.
-        auto owner = [&](int64_t k) {
-            const int64_t t0 = (cid + k * ncl) * kT;
-            const int p = int(k & 1);
-            if (bt == 0) {
-                mbar_expect_tx(&mbar[kMbRecv + p], uint32_t(C * tpc * 4 * rw * 4));
-                mbar_expect_tx(&mbar[kMbBcast + p], uint32_t(kT * nb4 * 4));
-            }
-            mbar_wait(&mbar[kMbRecv + p], uint32_t((k >> 1) & 1));
-            float* recv = recv_ptr(p);              // [C][tpc·4·rw + 4 pad]
-            const int nown = tpc * 4 * rw;          // a multiple of 4
-            const int srcstride = nown + 4;
-            for (int v = bt; v < nown; v += kBW * 32) {
-                const int grp = v >> 2, qtr = v & 3;
-                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int src = qtr; src < C; src += 4) {
-                    const float4 b4 =
-                        *reinterpret_cast<const float4*>(recv + src * srcstride + 4 * grp);
-                    s4.x += b4.x, s4.y += b4.y, s4.z += b4.z, s4.w += b4.w;
+        // Owner step for owned token slot `slot` of local tile k, done by one warp without any
+        // block-level barrier: gather the row sums of that token from every CTA (lane l holds
+        // the float4 group l of the token's 4·rw values), inv_i = 1/sqrt(ssq_i/D + eps) from the
+        // lanes holding the sums of squares, z and u as shuffle sums over the four branch lanes
+        // of each output group, then h (eq gate), s (eq s), and the h/inv row to every CTA.
+        const int rq = rw / 4;                      // float4 groups per branch record
+        auto owner_slot = [&](int k, int slot) {
+            const int t0 = (cid + k * ncl) * kT;
+            const int p = int(k % kXStages);
+            const int tok = int(crank) * tpc + slot;
+            const float* recv = recv_ptr(p);
+            const int srcstride = tpc * 4 * rw + 4;
+            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (lane < 4 * rq) {
+                const float* base = recv + slot * 4 * rw + 4 * lane;
+#pragma unroll 4
+                for (int src = 0; src < C; ++src) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(base + src * srcstride);
+                    v4.x += b4.x, v4.y += b4.y, v4.z += b4.z, v4.w += b4.w;
                 }
-                // nown is a multiple of 4, so the four lanes of a group are active together
-                const unsigned mask = __activemask();
+            }
+            // inv_i: the sum of squares of branch i is value nk of its record, i.e. component
+            // nk & 3 of lane i·rq + nk / 4
+            const int cs = nk & 3;
+            const float mine = cs == 0 ? v4.x : cs == 1 ? v4.y : cs == 2 ? v4.z : v4.w;
+            float inv[4];
 #pragma unroll
-                for (int o = 1; o < 4; o <<= 1) {
-                    s4.x += __shfl_xor_sync(mask, s4.x, o);
-                    s4.y += __shfl_xor_sync(mask, s4.y, o);
-                    s4.z += __shfl_xor_sync(mask, s4.z, o);
-                    s4.w += __shfl_xor_sync(mask, s4.w, o);
-                }
-                if (qtr == 0) *reinterpret_cast<float4*>(recv + 4 * grp) = s4;
-            }
-            b_sync();
-            for (int v = bt; v < tpc * nb4; v += kBW * 32) {
-                const int slot = div_small(v, m_nb4), kk = v - slot * nb4;
-                const int tok = int(crank) * tpc + slot;
-                const float* P = recv + slot * 4 * rw;
-                float out = 0.f;
-                if (kk < nk) {
-                    float inv[4], z = 0.f;
+            for (int i = 0; i < 4; ++i)
+                inv[i] = rsqrtf(fmaf(__shfl_sync(0xffffffffu, mine, i * rq + (nk >> 2)), inv_d, eps));
+            // z/u of outputs 4l .. 4l+3 = ¼ Σ_i inv_i · P[i][o]: scale by the lane's branch
+            // factor, then two shuffle steps leave the branch sum in lanes l < rq
+            const float sc = lane < rq ? inv[0] : lane < 2 * rq ? inv[1] : lane < 3 * rq ? inv[2]
+                           : lane < 4 * rq ? inv[3] : 0.f;
+            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float zz[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        inv[i] = rsqrtf(fmaf(P[i * rw + nk], inv_d, eps));
-                        z = fmaf(inv[i], P[i * rw + kk], z);
-                    }
-                    z *= 0.25f;
-                    const float sg = __frcp_rn(1.0f + expf(-z));   // σ(z)
-                    if (kk < r) {
-                        out = z * sg;  // h = SiLU(z)
-                    } else {
-                        if (t0 + tok < N) s_out[(t0 + tok) * 4 + (kk - r)] = 2.0f * sg;
-                        out = inv[kk - r];
+            for (int e = 0; e < 4; ++e) {
+                float t = sc * vv[e];
+                t += __shfl_down_sync(0xffffffffu, t, rq);
+                t += __shfl_down_sync(0xffffffffu, t, 2 * rq);
+                zz[e] = 0.25f * t;
+            }
+            // lane l < rq: h = SiLU(z) for outputs kk = 4l+e < r; s = 2σ(u) for r <= kk < r+4
+            float hv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (lane < rq) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kk = 4 * lane + e;
+                    if (kk < nk) {
+                        const float sg = __frcp_rn(1.0f + expf(-zz[e]));   // σ(z)
+                        if (kk < r)
+                            hv[e] = zz[e] * sg;
+                        else if (t0 + tok < N)
+                            s_out[size_t(t0 + tok) * 4 + (kk - r)] = 2.0f * sg;
                     }
                 }
-                outrow[v] = out;
             }
-            b_sync();
-            const uint32_t bc_u32 = smem_u32(bcast_ptr(p));
-            const int ngrp = nb4 / 4;
-            // one thread per (owned token, group of 4 outputs, destination CTA)
-            for (int v = bt; v < tpc * ngrp * C; v += kBW * 32) {
-                const int dst = v & (C - 1), rem = v >> lc;
-                const int slot = div_small(rem, m_ngrp), g4 = rem - slot * ngrp;
-                const int tok = int(crank) * tpc + slot;
-                const float4 o4 = *reinterpret_cast<const float4*>(outrow + slot * nb4 + 4 * g4);
-                st_async_v4(bc_u32 + uint32_t((tok * nb4 + 4 * g4) * 4),
-                            smem_u32(&mbar[kMbBcast + p]), uint32_t(dst), o4.x, o4.y, o4.z, o4.w);
+            // Broadcast row of the token: h (r values), inv (4), zero padding to nb4. Lane ->
+            // destination CTA lane % C (C divides 32); each round covers 32 / C float4 groups,
+            // whose values come from the lanes that hold them (component e of group g4 is
+            // output 4·g4 + e, held in hv[e] of lane g4).
+            const uint32_t dst = uint32_t(lane & (C - 1));
+            const uint32_t ra = map_rank(smem_u32(bcast_ptr(p) + tok * nb4), dst);
+            const uint32_t rb = map_rank(smem_u32(&mbar[kMbBcast + p]), dst);
+            const int ngrp = nb4 / 4, per = 32 >> lc;
+            for (int g0 = 0; g0 < ngrp; g0 += per) {
+                const int g4 = g0 + (lane >> lc);
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * g4 + e;
+                    const float hj = __shfl_sync(0xffffffffu, hv[e], g4 & 31);
+                    const int ii = j - r;
+                    const float iv = ii == 0 ? inv[0] : ii == 1 ? inv[1] : ii == 2 ? inv[2] : inv[3];
+                    v[e] = j < r ? hj : (ii < 4 ? iv : 0.f);
+                }
+                if (g4 < ngrp) st_async_v4_mapped(ra + 16u * uint32_t(g4), rb, v[0], v[1], v[2], v[3]);
             }
         };
 
         // Up projection (eq gate), gates, combine (eq use_gate) and x for local tile k; then the
         // R buffer is released and refilled with tile k+4.
-        auto combine = [&](int64_t k) {
-            const int64_t t0 = (cid + k * ncl) * kT;
-            const int p = int(k & 1);
+        auto combine = [&](int k) {
+            const int t0 = (cid + k * ncl) * kT;
+            const int p = int(k % kXStages);
             const char* rb = rbuf(k);
-            mbar_wait(&mbar[kMbBcast + p], uint32_t((k >> 1) & 1));
+            mbar_wait(&mbar[kMbBcast + p], uint32_t((k / kXStages) & 1));
             mbar_wait(&mbar[kMbRReady + int(k % kRStages)], uint32_t((k / kRStages) & 1));
             const float* bc = bcast_ptr(p);
             uint32_t ahi[4], alo[4];
@@ -670,16 +693,32 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                         f2_to_bf2(mul2(eighth, xacc2[row][2])), f2_to_bf2(mul2(eighth, xacc2[row][3])));
                 }
             }
-            // refill: once every B warp is done with this buffer, R of tile k+4 goes into it
-            // (lane 0 of B warps 0..3, one box each)
-            if (lane == 0 && b < 4 && k + kRStages < nlocal) {
-                mbar_wait(&mbar[kMbREmpty + int(k % kRStages)], uint32_t((k / kRStages) & 1));
-                issue_r(k + kRStages, b);
+            // refill: the last B warp done with this buffer loads R of tile k+4 into it (lanes
+            // 0..3, one box each); no other warp waits for it
+            if (k + kRStages < nlocal) {
+                uint32_t last = 0;
+                if (lane == 0) last = (atomicAdd(&rdone[k % kRStages], 1u) & (kBW - 1)) == kBW - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last && lane < 4) {
+                    mbar_wait(&mbar[kMbREmpty + int(k % kRStages)], uint32_t((k / kRStages) & 1));
+                    issue_r(k + kRStages, lane);
+                }
             }
         };
 
-        for (int64_t k = 0; k < nlocal; ++k) {
-            owner(k);
+        for (int k = 0; k < nlocal; ++k) {
+            const int p = int(k % kXStages);
+            if (bt == 0) {
+                mbar_expect_tx(&mbar[kMbRecv + p], uint32_t(C * tpc * 4 * rw * 4));
+                mbar_expect_tx(&mbar[kMbBcast + p], uint32_t(kT * nb4 * 4));
+            }
+            // owned slot j of tile k goes to B warp (k·tpc + j) mod 8, so the owner work
+            // rotates over the warps
+            const int first = (b - k * tpc) & (kBW - 1);
+            if (first < tpc) {
+                mbar_wait(&mbar[kMbRecv + p], uint32_t((k / kXStages) & 1));
+                for (int slot = first; slot < tpc; slot += kBW) owner_slot(k, slot);
+            }
             if (k > 0) combine(k - 1);
         }
         if (nlocal > 0) combine(nlocal - 1);
@@ -839,7 +878,8 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
     const int64_t ntiles = (N + kT - 1) / kT;
     const int64_t ncl = ntiles < maxc ? ntiles : maxc;
     cfg.gridDim = dim3(unsigned(ncl * S.C));
-    return cudaLaunchKernelEx(&cfg, kern, mR, my, N, D, r, eps, static_cast<__nv_bfloat16*>(R),
+    if (N > kMaxTokens) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, kern, mR, my, int(N), D, r, eps, static_cast<__nv_bfloat16*>(R),
                               s_prev, frag, static_cast<__nv_bfloat16*>(x), s_out);
 }
 
@@ -863,6 +903,8 @@ bool fused_supported(int D, int r) {
     if (C < 1 || C > kMaxCluster || (kT % C) != 0) return false;
     return fused_shape(D, r).smem_bytes <= 227 * 1024;
 }
+
+int64_t fused_max_tokens() { return kMaxTokens; }
 
 int fused_status(bool clear) {
     unsigned int v = 0;

@@ -28,8 +28,10 @@ struct Layout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Fused-kernel support and the size of its fragment section (gr_fused_bf16.cu).
+// Fused-kernel support and the size of its fragment section (gr_fused_bf16.cu). The fused
+// kernel also needs n_tokens <= fused_max_tokens().
 bool fused_supported(int D, int r);
+int64_t fused_max_tokens();
 size_t fused_frag_bytes(int D, int r);
 
 inline Layout make_layout(int D, int r, int dtype) {
