@@ -14,8 +14,10 @@
 // Organisation (GB300: 152 SMs, 227 KB shared memory and 64 K registers per SM):
 //   * A thread-block cluster of C = D/256 CTAs splits the channels: CTA q owns channels
 //     [256q, 256q+256) of every branch.
-//   * Tiles of 16 tokens (the mma M dimension) arrive by TMA (128-byte swizzle, zero fill past
-//     N): R into a 4-buffer ring, y and s_prev into a 2-buffer ring.
+//   * Tiles of 16 tokens (the mma M dimension) arrive by TMA (zero fill past N): R in 64-channel
+//     boxes with 128-byte swizzle into a 4-buffer ring, y in 32-channel boxes with 64-byte
+//     swizzle (so the A warps' reads of token rows g and g+1 hit different banks) and s_prev
+//     into a 2-buffer ring.
 //   * 16 warps in two roles that run concurrently on different tiles:
 //     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (stored
 //       to HBM and written back in place into the R buffer), the per-branch sums of squares
@@ -43,6 +45,11 @@ namespace {
 constexpr int kT = 16;                      // tokens per tile (mma M)
 constexpr int kAW = 8, kBW = 8;             // A warps, B warps
 constexpr int kThreads = (kAW + kBW) * 32;
+// Register split: the block launches with 128 per thread (65,536 in all); the A warpgroups give
+// 16 each back and the B warpgroups take them (2·128·112 + 2·128·144 = 65,536).
+constexpr int kLaunchRegs = 128, kARegs = 112, kBRegs = 144;
+static_assert(kAW % 4 == 0 && kBW % 4 == 0, "roles are whole warpgroups");
+static_assert(kAW * kARegs + kBW * kBRegs == (kAW + kBW) * kLaunchRegs, "register split");
 constexpr int kAThreads = kAW * 32;
 constexpr int kDq = 256;                    // channels per branch per CTA
 constexpr int kRStages = 4, kYStages = 2;
@@ -51,8 +58,10 @@ constexpr int kBoxCh = 64;                  // channels per TMA box (128 bytes: 
 constexpr int kColBlocks = kDq / kBoxCh;    // 4 boxes per row slice
 constexpr int kRBoxBytes = kBoxCh * 4 * kT * 2;        // [16 tok][4 br][64 ch] bf16 = 8 KB
 constexpr int kRBufBytes = kColBlocks * kRBoxBytes;     // 32 KB
-constexpr int kYBoxBytes = kBoxCh * kT * 2;             // [16 tok][64 ch] bf16 = 2 KB
-constexpr int kYBufBytes = kColBlocks * kYBoxBytes;     // 8 KB (1024-aligned: swizzle atoms)
+constexpr int kYBoxCh = 32;                             // y boxes: 64-byte rows, 64B swizzle
+constexpr int kYBoxes = kDq / kYBoxCh;                  // 8 boxes per row slice
+constexpr int kYBoxBytes = kYBoxCh * kT * 2;            // [16 tok][32 ch] bf16 = 1 KB
+constexpr int kYBufBytes = kYBoxes * kYBoxBytes;        // 8 KB (1024-aligned: swizzle atoms)
 constexpr int kSBufBytes = kT * 16;                     // s_prev rows of a tile, own small ring
 constexpr int kMaxCluster = 16;
 constexpr int64_t kMaxTokens = 0x7fffffff - 64;  // token indices stay in int
@@ -70,8 +79,11 @@ struct FusedShape {
     int upb;          // down-fragment units (16 B) per (A warp, 32-channel chunk)
     int rw;           // row-sum record per (token, branch): r+4 projections, sum of squares,
                       // padded to a multiple of 4 floats (16-byte records)
-    int nb4;          // broadcast row per token: h (r values) then inv (4), padded to 4 floats
+    int nb4;          // broadcast row per token: inv (4) then h (r values), zero padded to 8 or
+                      // 24 floats (strides that keep the combine's float2/float4 reads free of
+                      // bank conflicts)
     int down_bytes, up_bytes, gam_bytes, slice_bytes;
+    int red_stride;   // partial row sums: [token][A warp][rw] with this token stride (floats)
     int red_bytes, recv_bytes, bcast_bytes;
     int off_gam, off_r, off_y, off_s, off_red, off_recv, off_bcast, off_mbar, smem_bytes;
 };
@@ -87,12 +99,13 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     s.half_last = last_rows <= 4 ? 1 : 0;
     s.upb = (s.ntd - 1) * 32 + (s.half_last ? 16 : 32);
     s.rw = round_up(r + 5, 4);
-    s.nb4 = round_up(r + 4, 4);
+    s.nb4 = r + 4 <= 8 ? 8 : 24;
     s.down_bytes = kAW * 4 * s.upb * 16;
     s.up_bytes = kBW * 32 * 16 * 8;
     s.gam_bytes = 4 * kDq * 4;
     s.slice_bytes = s.down_bytes + s.up_bytes + s.gam_bytes;
-    s.red_bytes = kAW * kT * s.rw * 4;
+    s.red_stride = kAW * s.rw + 8;   // floats per token: ≡ 8 (mod 32) for conflict-free access
+    s.red_bytes = kT * s.red_stride * 4;
     s.recv_bytes = s.C * ((kT / s.C) * 4 * s.rw + 4) * 4;   // per source: its rows + 4 pad
     s.bcast_bytes = kT * s.nb4 * 4;
     s.off_gam = s.down_bytes;
@@ -289,8 +302,10 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
 }
-// Byte offset of the 16-byte chunk `cch` (0..7) of 128-byte row `row` in a swizzled box.
+// Byte offset of the 16-byte chunk `cch` (0..7) of 128-byte row `row` in a 128B-swizzled box.
 __device__ __forceinline__ int swz(int row, int cch) { return row * 128 + ((cch ^ (row & 7)) << 4); }
+// Byte offset of the 16-byte chunk `c` (0..3) of 64-byte row `row` in a 64B-swizzled box.
+__device__ __forceinline__ int swz64(int row, int c) { return row * 64 + ((c ^ ((row >> 1) & 3)) << 4); }
 
 // ---- the kernel -----------------------------------------------------------------------------
 
@@ -353,11 +368,9 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         const int t0 = int((cid + k * ncl) * kT);
         const int nv = int(N - t0 < kT ? N - t0 : kT);
         uint64_t* bar = &mbar[kMbYFull + int(k % kYStages)];
-        if (a == 0 && ln == 0) mbar_expect_tx(bar, uint32_t(kColBlocks * kYBoxBytes + nv * 16));
-        if (ln == 0 && a >= 4) {
-            const int yb = a - 4;
-            tma_load_2d(ybuf(k) + yb * kYBoxBytes, &tm_y, int(crank) * kDq + yb * kBoxCh, t0, bar);
-        }
+        if (a == 0 && ln == 0) mbar_expect_tx(bar, uint32_t(kYBufBytes + nv * 16));
+        if (ln == 0)
+            tma_load_2d(ybuf(k) + a * kYBoxBytes, &tm_y, int(crank) * kDq + a * kYBoxCh, t0, bar);
         if (a == 0 && ln == 1)
             bulk_g2s(sbuf(k), s_prev + size_t(t0) * 4, uint32_t(nv) * 16, bar);
     };
@@ -377,6 +390,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     cluster_sync();  // every CTA of the cluster runs before any shared::cluster access
 
     if (warp < kAW) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kARegs));
         // =============================== A warps ===========================================
         const int a = warp, ib = a & 3, hh = a >> 2;
         // R row of token g, branch ib, first channel of this thread in this CTA's slice; token
@@ -387,7 +401,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         const uint32_t m_rw = div_magic(rw), m_rq = div_magic(rw / 4);
         mbar_wait(&mbar[kMbWeights], 0);
         const uint4* s_down = reinterpret_cast<const uint4*>(smem);
-        float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kAW][kT][rw]
+        float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kT][kAW][rw], padded
         for (int k = 0; k < nlocal; ++k) {
             const int t0 = (cid + k * ncl) * kT;
             const int nv = int(N - t0 < kT ? N - t0 : kT);
@@ -415,8 +429,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                     Rp[row][j4][0] = rv.x, Rp[row][j4][1] = rv.y, Rp[row][j4][2] = rv.z,
                     Rp[row][j4][3] = rv.w;
                     if (WRITE)
-                        yv[row][j4] = *reinterpret_cast<const uint4*>(yb + cb * kYBoxBytes +
-                                                                      swz(tok, cch));
+                        yv[row][j4] = *reinterpret_cast<const uint4*>(
+                            yb + (hh * 4 + j4) * kYBoxBytes + swz64(tok, q4));
                 }
             }
             if (WRITE) {
@@ -483,8 +497,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             if (k >= kXStages)
                 mbar_wait(&mbar[kMbREmpty + int((k - kXStages) % kRStages)],
                           uint32_t(((k - kXStages) / kRStages) & 1));
-            float* r0 = red + (a * kT + g) * rw;
-            float* r1 = red + (a * kT + g + 8) * rw;
+            float* r0 = red + g * S.red_stride + a * rw;
+            float* r1 = red + (g + 8) * S.red_stride + a * rw;
 #pragma unroll
             for (int j = 0; j < NTD; ++j) {
                 const int o = 8 * j + 2 * q4;
@@ -502,16 +516,16 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             a_sync();
             {
                 // item it: token it / rw, branch (it % rw) / (rw/4), 4 values at o;
-                // value (tok, branch, o) = red[branch][tok][o] + red[branch + 4][tok][o]
+                // value (tok, branch, o) = red[tok][branch][o] + red[tok][branch + 4][o]
                 const int srcstride = tpc * 4 * rw + 4;  // padded per-source rows at the owner
                 const uint32_t recv_u32 = smem_u32(recv_ptr(p));
                 for (int it = tid; it < kT * rw; it += kAThreads) {
                     const int tok = div_small(it, m_rw), rem4 = it - tok * rw;
                     const int bi = div_small(rem4, m_rq), o = 4 * (rem4 - bi * (rw / 4));
                     const float4 u0 =
-                        *reinterpret_cast<const float4*>(red + (bi * kT + tok) * rw + o);
+                        *reinterpret_cast<const float4*>(red + tok * S.red_stride + bi * rw + o);
                     const float4 u1 =
-                        *reinterpret_cast<const float4*>(red + ((bi + 4) * kT + tok) * rw + o);
+                        *reinterpret_cast<const float4*>(red + tok * S.red_stride + (bi + 4) * rw + o);
                     const int owner = tok / tpc, slot = tok - owner * tpc;
                     st_async_v4(recv_u32 + uint32_t((int(crank) * srcstride +
                                                      (slot * 4 + bi) * rw + o) * 4),
@@ -523,6 +537,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             if (lane < 2) issue_y(k + kYStages, a, lane);   // y of tile k+2 into this buffer
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBRegs));
         // =============================== B warps ===========================================
         const int b = warp - kAW;
         const int cb = b >> 1, cch = ((b & 1) << 2) | q4;
@@ -588,25 +603,21 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 t += __shfl_down_sync(0xffffffffu, t, 2 * rq);
                 zz[e] = 0.25f * t;
             }
-            // lane l < rq: h = SiLU(z) for outputs kk = 4l+e < r; s = 2σ(u) for r <= kk < r+4
-            float hv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (lane < rq) {
+            // lane l < rq: h = SiLU(z) for outputs kk = 4l+e < r; s = 2σ(u) for r <= kk < r+4.
+            // The four logistic values are independent (no branch between them).
+            float hv[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kk = 4 * lane + e;
-                    if (kk < nk) {
-                        const float sg = __frcp_rn(1.0f + expf(-zz[e]));   // σ(z)
-                        if (kk < r)
-                            hv[e] = zz[e] * sg;
-                        else if (t0 + tok < N)
-                            s_out[size_t(t0 + tok) * 4 + (kk - r)] = 2.0f * sg;
-                    }
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int kk = 4 * lane + e;
+                const float sg = __frcp_rn(1.0f + __expf(-zz[e]));   // σ(z)
+                hv[e] = kk < r ? zz[e] * sg : 0.f;
+                if (lane < rq && kk >= r && kk < nk && t0 + tok < N)
+                    s_out[size_t(t0 + tok) * 4 + (kk - r)] = 2.0f * sg;
             }
-            // Broadcast row of the token: h (r values), inv (4), zero padding to nb4. Lane ->
-            // destination CTA lane % C (C divides 32); each round covers 32 / C float4 groups,
-            // whose values come from the lanes that hold them (component e of group g4 is
-            // output 4·g4 + e, held in hv[e] of lane g4).
+            // Broadcast row of the token: inv (4), h (r values), zeros up to nb4. Lane ->
+            // destination CTA lane % C (C divides 32); each round covers 32 / C float4 groups;
+            // group 0 is inv, and component e of group g4 > 0 is h[4·(g4-1) + e], held in hv[e]
+            // of lane g4 - 1.
             const uint32_t dst = uint32_t(lane & (C - 1));
             const uint32_t ra = map_rank(smem_u32(bcast_ptr(p) + tok * nb4), dst);
             const uint32_t rb = map_rank(smem_u32(&mbar[kMbBcast + p]), dst);
@@ -616,11 +627,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 float v[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int j = 4 * g4 + e;
-                    const float hj = __shfl_sync(0xffffffffu, hv[e], g4 & 31);
-                    const int ii = j - r;
-                    const float iv = ii == 0 ? inv[0] : ii == 1 ? inv[1] : ii == 2 ? inv[2] : inv[3];
-                    v[e] = j < r ? hj : (ii < 4 ? iv : 0.f);
+                    const float hj = __shfl_sync(0xffffffffu, hv[e], (g4 - 1) & 31);
+                    v[e] = g4 == 0 ? inv[e] : (4 * (g4 - 1) + e < r ? hj : 0.f);
                 }
                 if (g4 < ngrp) st_async_v4_mapped(ra + 16u * uint32_t(g4), rb, v[0], v[1], v[2], v[3]);
             }
@@ -639,8 +647,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int tk = g + 8 * (m & 1), kc = 2 * q4 + 8 * (m >> 1);
-                const float h0 = kc < r ? bc[tk * nb4 + kc] : 0.f;
-                const float h1 = kc + 1 < r ? bc[tk * nb4 + kc + 1] : 0.f;
+                // h[kc], h[kc+1] (zero past r: the row is zero padded after h)
+                const float2 hp = kc < r ? *reinterpret_cast<const float2*>(bc + tk * nb4 + 4 + kc)
+                                         : make_float2(0.f, 0.f);
+                const float h0 = hp.x, h1 = hp.y;
                 const float h0h = __bfloat162float(__float2bfloat16_rn(h0));
                 const float h1h = __bfloat162float(__float2bfloat16_rn(h1));
                 ahi[m] = pack_bf2(h0h, h1h);
@@ -651,9 +661,13 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             for (int row = 0; row < 2; ++row)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) xacc2[row][j] = f2(0.f, 0.f);
+            const float4 iv0 = *reinterpret_cast<const float4*>(bc + g * nb4);
+            const float4 iv1 = *reinterpret_cast<const float4*>(bc + (g + 8) * nb4);
+            const float inv0s[4] = {iv0.x, iv0.y, iv0.z, iv0.w};
+            const float inv1s[4] = {iv1.x, iv1.y, iv1.z, iv1.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float inv0 = bc[g * nb4 + r + i], inv1 = bc[(g + 8) * nb4 + r + i];
+                const float inv0 = inv0s[i], inv1 = inv1s[i];
                 const uint4 r0 = *reinterpret_cast<const uint4*>(rb + cb * kRBoxBytes +
                                                                  swz(g * 4 + i, cch));
                 const uint4 r1 = *reinterpret_cast<const uint4*>(rb + cb * kRBoxBytes +
@@ -822,10 +836,10 @@ bool make_map_y(CUtensorMap* m, const void* y, int64_t N, int D) {
     if (!enc) return false;
     const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(N)};
     const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-    const cuuint32_t box[2] = {kBoxCh, kT};
+    const cuuint32_t box[2] = {kYBoxCh, kT};
     const cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(y), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -845,8 +859,12 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
     if (!make_map_R(&mR, R, N, D)) return cudaErrorInvalidValue;
     if (WRITE && !make_map_y(&my, y, N, D)) return cudaErrorInvalidValue;
     auto kern = gr_fused_kernel<WRITE, NTD>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S.smem_bytes);
+    // the register split assumes this launch size; anything else could stall setmaxnreg.inc
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S.smem_bytes);
     if (e != cudaSuccess) return e;
     if (S.C > 8) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
