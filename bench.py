@@ -239,6 +239,30 @@ def run_reference(args, w) -> None:
 
 
 # ---------------------------------------------------------------------------------------------
+# multi-rank host logic (weak scaling: one token shard per rank, no data-path collective)
+
+def shard(w, rank: int):
+    """The workload rank `rank` processes: the same shape on every rank, its own seed."""
+    return w.scaled(seed=w.seed + rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of the ranks' values (the slowest rank sets a job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, n_tokens_per_rank: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the tokens every rank processed over the slowest rank's time."""
+    return world * n_tokens_per_rank * steps / seconds
+
+
+# ---------------------------------------------------------------------------------------------
 # GPU arm
 
 def run_gr(args, w) -> None:
@@ -261,7 +285,7 @@ def run_gr(args, w) -> None:
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
     # each rank owns its own shard of tokens (a different seed), same size on every rank
-    wr = w.scaled(seed=w.seed + rank)
+    wr = shard(w, rank)
 
     def dev_tensor(a):
         if a.dtype == np.uint16:
@@ -307,11 +331,7 @@ def run_gr(args, w) -> None:
         clocks = sampler.stop()
         if world > 1:
             dist.barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         return ms, clocks
 
     ms, clocks = timed()
@@ -319,7 +339,7 @@ def run_gr(args, w) -> None:
         ms, clocks = timed()  # one re-measurement
         clocks["remeasured"] = True
     ms_step = ms / args.steps
-    tokens_per_s = world * w.n_tokens * args.steps / (ms / 1e3)
+    tokens_per_s = job_tokens_per_s(world, w.n_tokens, args.steps, ms / 1e3)
 
     # roofline of the one kernel of the step
     peaks = load_peaks()
@@ -366,15 +386,11 @@ def run_gr(args, w) -> None:
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     es = w.state_bytes_per_elem()
     h2d = w.n_tokens * (4 * w.d_model * es + w.d_model * es + 16)
     d2h = h2d
-    e2e = {"value": world * w.n_tokens * args.e2e_steps / e2e_s, "unit": UNIT,
+    e2e = {"value": job_tokens_per_s(world, w.n_tokens, args.e2e_steps, e2e_s), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "api": "gr_write_then_read_host (pinned host buffers)"}
 
