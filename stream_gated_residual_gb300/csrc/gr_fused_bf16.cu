@@ -19,11 +19,11 @@
 //     swizzle (so the A warps' reads of token rows g and g+1 hit different banks) and s_prev
 //     into a 2-buffer ring.
 //   * 16 warps in two roles that run concurrently on different tiles:
-//     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (stored
-//       to HBM and written back in place into the R buffer), the per-branch sums of squares
-//       (diagonal of R'·R'ᵀ on the tensor cores) and the down projections (W_d, W_w with gamma
-//       folded, mma fragments resident in shared memory); sum the two halves; and send each
-//       token's row sums with st.async to the token's owner CTA.
+//     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (written
+//       back in place into the R buffer, from where a TMA store takes it to HBM), the
+//       per-branch sums of squares (diagonal of R'·R'ᵀ on the tensor cores) and the down
+//       projections (W_d, W_w with gamma folded, mma fragments resident in shared memory); sum
+//       the two halves; and send each token's row sums with st.async to its owner CTA.
 //     - B warps (8): the CTA's owned token slots of each tile go round the B warps; for each
 //       the warp gathers the token's row sums from every CTA, forms inv, h and s with warp
 //       shuffles only, and sends h and inv to every CTA of the cluster. Warp b also owns 32
@@ -211,6 +211,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
+// TMA tensor store of a box from shared memory (clipped to the tensor's extent), bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
                                             uint64_t* bar) {
     asm volatile(
@@ -312,8 +321,7 @@ __device__ __forceinline__ int swz64(int row, int c) { return row * 64 + ((c ^ (
 template <bool WRITE, int NTD>
 __global__ void __launch_bounds__(kThreads, 1)
 gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant__ CUtensorMap tm_y,
-                int N, int D, int r, float eps, __nv_bfloat16* __restrict__ R,
-                const float* __restrict__ s_prev, const char* __restrict__ frag,
+                int N, int D, int r, float eps, const float* __restrict__ s_prev, const char* __restrict__ frag,
                 __nv_bfloat16* __restrict__ x, float* __restrict__ s_out) {
     extern __shared__ __align__(1024) char smem[];
     const FusedShape S = fused_shape(D, r);
@@ -393,18 +401,12 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kARegs));
         // =============================== A warps ===========================================
         const int a = warp, ib = a & 3, hh = a >> 2;
-        // R row of token g, branch ib, first channel of this thread in this CTA's slice; token
-        // t0 + g of a tile is t0·4·D elements further, token t0 + g + 8 another 32·D
-        __nv_bfloat16* const Rg =
-            R + (size_t(g) * 4 + ib) * size_t(D) + size_t(crank) * kDq + hh * 128 + q4 * 8;
         // send descriptors: float4 items it = tid, tid + 256 of the tile's 16·rw row-sum items
         const uint32_t m_rw = div_magic(rw), m_rq = div_magic(rw / 4);
         mbar_wait(&mbar[kMbWeights], 0);
         const uint4* s_down = reinterpret_cast<const uint4*>(smem);
         float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kT][kAW][rw], padded
         for (int k = 0; k < nlocal; ++k) {
-            const int t0 = (cid + k * ncl) * kT;
-            const int nv = int(N - t0 < kT ? N - t0 : kT);
             const int p = int(k % kXStages);
             char* rb = rbuf(k);
             const char* yb = ybuf(k);
@@ -434,7 +436,6 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             if (WRITE) {
-                __nv_bfloat16* gR = Rg + size_t(t0) * 4 * size_t(D);
 #pragma unroll
                 for (int row = 0; row < 2; ++row) {
                     const int tok = g + 8 * row, brow = tok * 4 + ib;
@@ -451,8 +452,6 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                         const uint4 o = make_uint4(Rp[row][j4][0], Rp[row][j4][1],
                                                    Rp[row][j4][2], Rp[row][j4][3]);
                         *reinterpret_cast<uint4*>(rb + cb * kRBoxBytes + swz(brow, cch)) = o;
-                        if (tok < nv)
-                            *reinterpret_cast<uint4*>(gR + row * 32 * size_t(D) + j4 * 32) = o;
                     }
                 }
             }
@@ -642,6 +641,12 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             const char* rb = rbuf(k);
             mbar_wait(&mbar[kMbBcast + p], uint32_t((k / kXStages) & 1));
             mbar_wait(&mbar[kMbRReady + int(k % kRStages)], uint32_t((k / kRStages) & 1));
+            // R' of this tile (written back in place by the A warps) goes to HBM by TMA, one box
+            // per lane 0..3 of B warp 0; the box is clipped to the N tokens
+            if (WRITE && b == 0 && lane < kColBlocks) {
+                tma_store_3d(&tm_R, rb + lane * kRBoxBytes, int(crank) * kDq + lane * kBoxCh, 0, t0);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
             const float* bc = bcast_ptr(p);
             uint32_t ahi[4], alo[4];
 #pragma unroll
@@ -694,6 +699,9 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                     xacc2[1][j] = fma2(inv1_2, w1, xacc2[1][j]);
                 }
             }
+            // the buffer is released only after the TMA store has read it
+            if (WRITE && b == 0 && lane < kColBlocks)
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&mbar[kMbREmpty + int(k % kRStages)]);
             const uint64_t eighth = f2(0.125f, 0.125f);
@@ -736,6 +744,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             if (k > 0) combine(k - 1);
         }
         if (nlocal > 0) combine(nlocal - 1);
+        // the R' stores must be complete before the CTA leaves
+        if (WRITE && b == 0 && lane < kColBlocks) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     cluster_sync();  // no CTA leaves while shared::cluster traffic to it may be in flight
 }
@@ -897,8 +907,8 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
     const int64_t ncl = ntiles < maxc ? ntiles : maxc;
     cfg.gridDim = dim3(unsigned(ncl * S.C));
     if (N > kMaxTokens) return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(&cfg, kern, mR, my, int(N), D, r, eps, static_cast<__nv_bfloat16*>(R),
-                              s_prev, frag, static_cast<__nv_bfloat16*>(x), s_out);
+    return cudaLaunchKernelEx(&cfg, kern, mR, my, int(N), D, r, eps, s_prev, frag,
+                              static_cast<__nv_bfloat16*>(x), s_out);
 }
 
 template <bool WRITE>
