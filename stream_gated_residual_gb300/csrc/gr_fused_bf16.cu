@@ -244,15 +244,6 @@ __device__ __forceinline__ void st_async_v4_mapped(uint32_t ra, uint32_t rb, flo
         "f"(a), "f"(b), "f"(c), "f"(d), "r"(rb)
         : "memory");
 }
-__device__ __forceinline__ void st_async_v4(uint32_t local_addr, uint32_t local_bar,
-                                            uint32_t rank, float a, float b, float c, float d) {
-    const uint32_t ra = map_rank(local_addr, rank), rb = map_rank(local_bar, rank);
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
-        "[%5];" ::"r"(ra),
-        "f"(a), "f"(b), "f"(c), "f"(d), "r"(rb)
-        : "memory");
-}
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
@@ -297,10 +288,6 @@ __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
 }
-// floor(n / d) for 0 <= n < 512 and 1 <= d <= 64, with m = ceil(2^16 / d): n·m/2^16 exceeds n/d
-// by less than 512/2^16 < 1/64 <= 1/d, so the floor is exact.
-__device__ __forceinline__ int div_small(int n, uint32_t m) { return int((uint32_t(n) * m) >> 16); }
-__host__ __device__ inline uint32_t div_magic(int d) { return (65536u + uint32_t(d) - 1) / uint32_t(d); }
 
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
@@ -402,7 +389,23 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         // =============================== A warps ===========================================
         const int a = warp, ib = a & 3, hh = a >> 2;
         // send descriptors: float4 items it = tid, tid + 256 of the tile's 16·rw row-sum items
-        const uint32_t m_rw = div_magic(rw), m_rq = div_magic(rw / 4);
+        // This thread's row-sum items, the same in every tile: float4 items it = tid and
+        // tid + 256 of the tile's 16·rw; item it is token it / rw, branch (it % rw) / (rw/4),
+        // 4 values at o, and its value is red[tok][branch][o] + red[tok][branch + 4][o].
+        int s_red[2], s_off[2], s_own[2];
+        bool s_has[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int it = tid + u * kAThreads;
+            s_has[u] = it < kT * rw;
+            const int tok = it / rw, rem4 = it - tok * rw;
+            const int bi = rem4 / (rw / 4), o = 4 * (rem4 - bi * (rw / 4));
+            const int owner = tok / tpc, slot = tok - owner * tpc;
+            s_red[u] = tok * S.red_stride + bi * rw + o;
+            // byte offset in the owner's receive slot: padded per-source rows of tpc·4·rw + 4
+            s_off[u] = (int(crank) * (tpc * 4 * rw + 4) + slot * 4 * rw + 4 * rem4) * 4;
+            s_own[u] = owner;
+        }
         mbar_wait(&mbar[kMbWeights], 0);
         const uint4* s_down = reinterpret_cast<const uint4*>(smem);
         float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kT][kAW][rw], padded
@@ -514,22 +517,15 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             }
             a_sync();
             {
-                // item it: token it / rw, branch (it % rw) / (rw/4), 4 values at o;
-                // value (tok, branch, o) = red[tok][branch][o] + red[tok][branch + 4][o]
-                const int srcstride = tpc * 4 * rw + 4;  // padded per-source rows at the owner
-                const uint32_t recv_u32 = smem_u32(recv_ptr(p));
-                for (int it = tid; it < kT * rw; it += kAThreads) {
-                    const int tok = div_small(it, m_rw), rem4 = it - tok * rw;
-                    const int bi = div_small(rem4, m_rq), o = 4 * (rem4 - bi * (rw / 4));
-                    const float4 u0 =
-                        *reinterpret_cast<const float4*>(red + tok * S.red_stride + bi * rw + o);
-                    const float4 u1 =
-                        *reinterpret_cast<const float4*>(red + tok * S.red_stride + (bi + 4) * rw + o);
-                    const int owner = tok / tpc, slot = tok - owner * tpc;
-                    st_async_v4(recv_u32 + uint32_t((int(crank) * srcstride +
-                                                     (slot * 4 + bi) * rw + o) * 4),
-                                smem_u32(&mbar[kMbRecv + p]), uint32_t(owner), u0.x + u1.x,
-                                u0.y + u1.y, u0.z + u1.z, u0.w + u1.w);
+                const uint32_t recv_u32 = smem_u32(recv_ptr(p)), bar_u32 = smem_u32(&mbar[kMbRecv + p]);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (!s_has[u]) continue;
+                    const float4 u0 = *reinterpret_cast<const float4*>(red + s_red[u]);
+                    const float4 u1 = *reinterpret_cast<const float4*>(red + s_red[u] + 4 * rw);
+                    st_async_v4_mapped(map_rank(recv_u32 + uint32_t(s_off[u]), uint32_t(s_own[u])),
+                                       map_rank(bar_u32, uint32_t(s_own[u])), u0.x + u1.x,
+                                       u0.y + u1.y, u0.z + u1.z, u0.w + u1.w);
                 }
             }
             a_sync();  // red and this tile's y buffer are free again
