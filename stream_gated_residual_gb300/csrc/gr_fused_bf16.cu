@@ -571,7 +571,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (lane < 4 * rq) {
                 const float* base = recv + slot * 4 * rw + 4 * lane;
-#pragma unroll 4
+#pragma unroll 8
                 for (int src = 0; src < C; ++src) {
                     const float4 b4 = *reinterpret_cast<const float4*>(base + src * srcstride);
                     v4.x += b4.x, v4.y += b4.y, v4.z += b4.z, v4.w += b4.w;
@@ -604,7 +604,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int kk = 4 * lane + e;
-                const float sg = __frcp_rn(1.0f + __expf(-zz[e]));   // σ(z)
+                // σ(z) = 1/(1 + e^-z): the hardware exp2 and reciprocal are a few ulp in fp32
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-zz[e]));
                 hv[e] = kk < r ? zz[e] * sg : 0.f;
                 if (lane < rq && kk >= r && kk < nk && t0 + tok < N)
                     s_out[size_t(t0 + tok) * 4 + (kk - r)] = 2.0f * sg;
