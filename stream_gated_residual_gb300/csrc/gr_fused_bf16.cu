@@ -211,21 +211,22 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
 }
-// TMA tensor store of a box from shared memory (clipped to the tensor's extent), bulk group.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
-                                             int c1, int c2) {
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(bar))
         : "memory");
 }
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
-                                            uint64_t* bar) {
+// TMA tensor store of a box from shared memory (clipped to the tensor's extent), bulk group.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2, int c3) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
         : "memory");
 }
 __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank) {
@@ -348,26 +349,27 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     }
     __syncthreads();
 
-    // TMA of the k-th local tile's R boxes (lane 0 of A warps 0..3, one box each).
-    auto issue_r = [&](int k, int a) {
+    // TMA of the k-th local tile's R slice: one 4-D box {64 ch, 4 br, 16 tok, 4 blocks} = the
+    // CTA's 256 channels as four 64-channel blocks (one thread).
+    auto issue_r = [&](int k) {
         if (k >= nlocal) return;
         const int t0 = int((cid + k * ncl) * kT);
         uint64_t* bar = &mbar[kMbRFull + int(k % kRStages)];
-        if (a == 0) mbar_expect_tx(bar, uint32_t(kRBufBytes));
-        tma_load_3d(rbuf(k) + a * kRBoxBytes, &tm_R, int(crank) * kDq + a * kBoxCh, 0, t0, bar);
+        mbar_expect_tx(bar, uint32_t(kRBufBytes));
+        tma_load_4d(rbuf(k), &tm_R, 0, 0, t0, int(crank) * kColBlocks, bar);
     };
-    // TMA of the k-th local tile's y boxes (lane 0 of A warps 4..7) and s_prev rows (warp 0,
-    // lane 1); warp 0 lane 0 arms the barrier.
-    auto issue_y = [&](int k, int a, int ln) {
+    // TMA of the k-th local tile's y slice: one 3-D box {32 ch, 16 tok, 8 chunks} (lane 0, which
+    // also arms the barrier) and its s_prev rows (lane 1).
+    auto issue_y = [&](int k, int ln) {
         if (!WRITE || k >= nlocal) return;
         const int t0 = int((cid + k * ncl) * kT);
         const int nv = int(N - t0 < kT ? N - t0 : kT);
         uint64_t* bar = &mbar[kMbYFull + int(k % kYStages)];
-        if (a == 0 && ln == 0) mbar_expect_tx(bar, uint32_t(kYBufBytes + nv * 16));
-        if (ln == 0)
-            tma_load_2d(ybuf(k) + a * kYBoxBytes, &tm_y, int(crank) * kDq + a * kYBoxCh, t0, bar);
-        if (a == 0 && ln == 1)
-            bulk_g2s(sbuf(k), s_prev + size_t(t0) * 4, uint32_t(nv) * 16, bar);
+        if (ln == 0) {
+            mbar_expect_tx(bar, uint32_t(kYBufBytes + nv * 16));
+            tma_load_3d(ybuf(k), &tm_y, 0, t0, int(crank) * kYBoxes, bar);
+        }
+        if (ln == 1) bulk_g2s(sbuf(k), s_prev + size_t(t0) * 4, uint32_t(nv) * 16, bar);
     };
 
     if (tid == 0) {
@@ -376,11 +378,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         bulk_g2s(smem + S.off_gam, slice + S.down_bytes + S.up_bytes, uint32_t(S.gam_bytes),
                  &mbar[kMbWeights]);
     }
-    if (warp < kAW && lane < 2) {
-        for (int k = 0; k < kRStages; ++k) {
-            if (lane == 0 && warp < 4) issue_r(k, warp);
-        }
-        for (int k = 0; k < kYStages; ++k) issue_y(k, warp, lane);
+    if (warp == 0 && lane < 2) {
+        if (lane == 0)
+            for (int k = 0; k < kRStages; ++k) issue_r(k);
+        for (int k = 0; k < kYStages; ++k) issue_y(k, lane);
     }
     cluster_sync();  // every CTA of the cluster runs before any shared::cluster access
 
@@ -529,7 +530,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             a_sync();  // red and this tile's y buffer are free again
-            if (lane < 2) issue_y(k + kYStages, a, lane);   // y of tile k+2 into this buffer
+            if (a == 0 && lane < 2) issue_y(k + kYStages, lane);   // y of tile k+2 into this buffer
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBRegs));
@@ -638,10 +639,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             const char* rb = rbuf(k);
             mbar_wait(&mbar[kMbBcast + p], uint32_t((k / kXStages) & 1));
             mbar_wait(&mbar[kMbRReady + int(k % kRStages)], uint32_t((k / kRStages) & 1));
-            // R' of this tile (written back in place by the A warps) goes to HBM by TMA, one box
-            // per lane 0..3 of B warp 0; the box is clipped to the N tokens
-            if (WRITE && b == 0 && lane < kColBlocks) {
-                tma_store_3d(&tm_R, rb + lane * kRBoxBytes, int(crank) * kDq + lane * kBoxCh, 0, t0);
+            // R' of this tile (written back in place by the A warps) goes to HBM by one TMA
+            // store (B warp 0, lane 0); the box is clipped to the N tokens
+            if (WRITE && b == 0 && lane == 0) {
+                tma_store_4d(&tm_R, rb, 0, 0, t0, int(crank) * kColBlocks);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
             const float* bc = bcast_ptr(p);
@@ -697,7 +698,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             // the buffer is released only after the TMA store has read it
-            if (WRITE && b == 0 && lane < kColBlocks)
+            if (WRITE && b == 0 && lane == 0)
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&mbar[kMbREmpty + int(k % kRStages)]);
@@ -712,15 +713,15 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                         f2_to_bf2(mul2(eighth, xacc2[row][2])), f2_to_bf2(mul2(eighth, xacc2[row][3])));
                 }
             }
-            // refill: the last B warp done with this buffer loads R of tile k+4 into it (lanes
-            // 0..3, one box each); no other warp waits for it
+            // refill: the last B warp done with this buffer loads R of tile k+4 into it (lane 0);
+            // no other warp waits for it
             if (k + kRStages < nlocal) {
                 uint32_t last = 0;
                 if (lane == 0) last = (atomicAdd(&rdone[k % kRStages], 1u) & (kBW - 1)) == kBW - 1;
                 last = __shfl_sync(0xffffffffu, last, 0);
-                if (last && lane < 4) {
+                if (last && lane == 0) {
                     mbar_wait(&mbar[kMbREmpty + int(k % kRStages)], uint32_t((k / kRStages) & 1));
-                    issue_r(k + kRStages, lane);
+                    issue_r(k + kRStages);
                 }
             }
         };
@@ -742,7 +743,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         }
         if (nlocal > 0) combine(nlocal - 1);
         // the R' stores must be complete before the CTA leaves
-        if (WRITE && b == 0 && lane < kColBlocks) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (WRITE && b == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     cluster_sync();  // no CTA leaves while shared::cluster traffic to it may be in flight
 }
@@ -823,29 +824,31 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// R as a 3-D tensor {channel, branch, token}; box {64, 4, 16}, 128-byte swizzle.
+// R as a 4-D tensor {channel within a 64-channel block, branch, token, block}; box
+// {64, 4, 16, 4} (one CTA's 256 channels of a tile), 128-byte swizzle on the 128-byte rows.
 bool make_map_R(CUtensorMap* m, const void* R, int64_t N, int D) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {cuuint64_t(D), 4, cuuint64_t(N)};
-    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(D) * 8};
-    const cuuint32_t box[3] = {kBoxCh, 4, kT};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(R), dims, strides, box,
+    const cuuint64_t dims[4] = {cuuint64_t(kBoxCh), 4, cuuint64_t(N), cuuint64_t(D / kBoxCh)};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(D) * 8, cuuint64_t(kBoxCh) * 2};
+    const cuuint32_t box[4] = {kBoxCh, 4, kT, kColBlocks};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(R), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
 
-// y as a 2-D tensor {channel, token}; box {64, 16}, 128-byte swizzle.
+// y as a 3-D tensor {channel within a 32-channel chunk, token, chunk}; box {32, 16, 8} (one
+// CTA's 256 channels of a tile), 64-byte swizzle on the 64-byte rows.
 bool make_map_y(CUtensorMap* m, const void* y, int64_t N, int D) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(N)};
-    const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-    const cuuint32_t box[2] = {kYBoxCh, kT};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(y), dims, strides, box,
+    const cuuint64_t dims[3] = {cuuint64_t(kYBoxCh), cuuint64_t(N), cuuint64_t(D / kYBoxCh)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(kYBoxCh) * 2};
+    const cuuint32_t box[3] = {kYBoxCh, kT, kYBoxes};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(y), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
