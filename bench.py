@@ -380,7 +380,8 @@ def run_gr(args, w) -> None:
     torch.cuda.empty_cache()
     wsb = torch.empty(nws + 256, dtype=torch.uint8, device=dev)
     ws = wsb[(-wsb.data_ptr()) % 256:][:nws]
-    gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)  # warm-up
+    for _ in range(3):  # warm-up (the first transfers from freshly pinned pages are slow)
+        gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()

@@ -141,8 +141,8 @@ int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma
  * n >= 0; pointers 16-byte aligned. */
 int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* stream);
 
-/* Device-side status of the kernels that use bounded waits (the fused kernel waits on its own
- * bulk copies with an iteration limit instead of spinning forever). Synchronises the current
+/* Device-side status of the kernels that use bounded waits (every wait of the fused kernel on
+ * its mbarriers gives up after a time limit instead of spinning forever). Synchronises the current
  * device, then returns GR_OK, GR_E_TIMEOUT if a wait ran out since the last clear (the outputs of
  * that call are not valid), or GR_E_CUDA. `clear` != 0 resets the status. */
 int gr_device_status(int clear);
@@ -153,7 +153,13 @@ int gr_host_workspace_size(const gr_shape* shape, size_t* bytes);
 /* gr_write_then_read on HOST buffers (pinned memory gives asynchronous copies): copies R, y and
  * s_prev into `workspace` (DEVICE, >= gr_host_workspace_size bytes, 256-byte aligned), runs the
  * fused step there, copies R', x and s_next back into R_host, x_host and s_next_host, and
- * synchronises `stream` before returning. Host buffers must not overlap. */
+ * synchronises `stream` before returning. Host buffers must not overlap.
+ * The work is split into up to 16 token chunks (at least 1024 tokens each): each chunk's
+ * host-to-device copies run on an internal stream, its step on `stream`, its device-to-host
+ * copies on a second internal stream (both created once per device), ordered by events, so
+ * copies in both directions overlap the steps. The copies into the workspace start after the
+ * work already queued on `stream`. Calls for the same device are serialised (they share the
+ * internal streams). */
 int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_host,
                             const float* s_prev_host, const gr_params* next, void* x_host,
                             float* s_next_host, void* workspace, size_t workspace_bytes,

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gr_internal.h"
 
 namespace gr {
@@ -34,6 +36,35 @@ int check_device() {
         g_device_ok[d] = (major == 10 && minor == 3) ? 1 : -1;
     }
     return g_device_ok[d] == 1 ? GR_OK : GR_E_DEVICE;
+}
+
+// Per-device objects of the pipelined host entry: a stream for the host-to-device copies, one
+// for the device-to-host copies and two events per chunk, created on first use; the mutex
+// serialises the calls that share them.
+constexpr int kHostChunks = 16;
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t loaded[kHostChunks] = {}, computed[kHostChunks] = {};
+    cudaEvent_t start = nullptr, copied = nullptr;
+};
+HostPipe g_host_pipe[kMaxDevices];
+
+bool host_pipe_init(HostPipe& hp) {
+    if (hp.ready) return true;
+    if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess)
+        return false;
+    for (int i = 0; i < kHostChunks; ++i)
+        if (cudaEventCreateWithFlags(&hp.loaded[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.computed[i], cudaEventDisableTiming) != cudaSuccess)
+            return false;
+    if (cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.copied, cudaEventDisableTiming) != cudaSuccess)
+        return false;
+    hp.ready = true;
+    return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -300,20 +331,58 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
     if (N == 0) return GR_OK;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     char* w = static_cast<char*>(workspace);
-    void* dR = w;
-    void* dy = w + align256(nR);
-    void* dx = w + align256(nR) + align256(ny);
-    float* dsp = reinterpret_cast<float*>(w + align256(nR) + 2 * align256(ny));
-    float* dsn = reinterpret_cast<float*>(w + align256(nR) + 2 * align256(ny) + align256(ns));
-    if (cudaMemcpyAsync(dR, R_host, nR, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-        cudaMemcpyAsync(dy, y_host, ny, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-        cudaMemcpyAsync(dsp, s_prev_host, ns, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    char* dR = w;
+    char* dy = w + align256(nR);
+    char* dx = w + align256(nR) + align256(ny);
+    char* dsp = w + align256(nR) + 2 * align256(ny);
+    char* dsn = w + align256(nR) + 2 * align256(ny) + align256(ns);
+    char* hR = static_cast<char*>(R_host);
+    const char* hy = static_cast<const char*>(y_host);
+    const char* hsp = reinterpret_cast<const char*>(s_prev_host);
+    char* hx = static_cast<char*>(x_host);
+    char* hsn = reinterpret_cast<char*>(s_next_host);
+    // Token chunks of at least 1024 (a multiple of 16): chunk i's host-to-device copies run on
+    // one internal stream, its step on `stream` after them, its device-to-host copies on a second
+    // internal stream after the step, so both copy directions and the steps overlap.
+    const size_t nchunk = N >= 2 * 1024 ? (N / 1024 < kHostChunks ? N / 1024 : kHostChunks) : 1;
+    const size_t per = ((N + nchunk - 1) / nchunk + 15) / 16 * 16;
+    HostPipe& hp = g_host_pipe[current_device()];
+    std::lock_guard<std::mutex> lock(hp.mu);
+    if (!host_pipe_init(hp)) return GR_E_CUDA;
+    // the copies into the workspace wait for the work already queued on `stream`
+    if (cudaEventRecord(hp.start, cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hp.h2d, hp.start, 0) != cudaSuccess)
         return GR_E_CUDA;
-    st = run_step(shape, dR, dy, dsp, next, dx, dsn, cs);
-    if (st) return st;
-    if (cudaMemcpyAsync(R_host, dR, nR, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
-        cudaMemcpyAsync(x_host, dx, ny, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
-        cudaMemcpyAsync(s_next_host, dsn, ns, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    const size_t bR = kBranches * D * es, by = D * es, bs = kBranches * 4;  // bytes per token
+    for (size_t c = 0, t = 0; t < N; ++c, t += per) {
+        const size_t n = N - t < per ? N - t : per;
+        if (cudaMemcpyAsync(dR + t * bR, hR + t * bR, n * bR, cudaMemcpyHostToDevice, hp.h2d) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(dy + t * by, hy + t * by, n * by, cudaMemcpyHostToDevice, hp.h2d) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(dsp + t * bs, hsp + t * bs, n * bs, cudaMemcpyHostToDevice, hp.h2d) !=
+                cudaSuccess ||
+            cudaEventRecord(hp.loaded[c], hp.h2d) != cudaSuccess ||
+            cudaStreamWaitEvent(cs, hp.loaded[c], 0) != cudaSuccess)
+            return GR_E_CUDA;
+        gr_shape sc = *shape;
+        sc.n_tokens = int64_t(n);
+        st = run_step(&sc, dR + t * bR, dy + t * by, reinterpret_cast<const float*>(dsp + t * bs),
+                      next, dx + t * by, reinterpret_cast<float*>(dsn + t * bs), cs);
+        if (st) return st;
+        if (cudaEventRecord(hp.computed[c], cs) != cudaSuccess ||
+            cudaStreamWaitEvent(hp.d2h, hp.computed[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(hR + t * bR, dR + t * bR, n * bR, cudaMemcpyDeviceToHost, hp.d2h) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(hx + t * by, dx + t * by, n * by, cudaMemcpyDeviceToHost, hp.d2h) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(hsn + t * bs, dsn + t * bs, n * bs, cudaMemcpyDeviceToHost,
+                            hp.d2h) != cudaSuccess)
+            return GR_E_CUDA;
+    }
+    // the caller's stream covers the read-back too
+    if (cudaEventRecord(hp.copied, hp.d2h) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, hp.copied, 0) != cudaSuccess)
         return GR_E_CUDA;
     return status_of(cudaStreamSynchronize(cs));
 }

@@ -176,18 +176,23 @@ def test_empty_and_in_place_aliases():
     assert torch.equal(Ra, Rb) and torch.equal(xa, yb) and torch.equal(sa, spb)
 
 
-def test_host_entry_matches_device_entry():
-    w = wl.Workload("host", 256, 1024, 16, "bf16", y_std=0.5, seed=11)
+@pytest.mark.parametrize("N,D,dtype", [(256, 1024, "bf16"), (5000, 512, "bf16"),
+                                       (20000, 256, "bf16"), (3000, 256, "f32")])
+def test_host_entry_matches_device_entry(N, D, dtype):
+    """The host-buffer entry (pipelined over token chunks when N >= 2048, with a ragged last
+    chunk) gives bit-for-bit the device entry's results."""
+    w = wl.Workload("host", N, D, 16, dtype, y_std=0.5, seed=11)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     R, y, sp = wl.make_state(w), wl.make_y(w), wl.make_s_prev(w)
-    P = _pack(wl.make_params(w, 1), "bf16", w.eps)
+    P = _pack(wl.make_params(w, 1), dtype, w.eps)
     Rd = to_torch(R)
     xd, sd = gr.write_then_read(Rd, to_torch(y), torch.from_numpy(sp).cuda(), P)
     Rh = to_torch(R, "cpu").pin_memory()
     yh = to_torch(y, "cpu").pin_memory()
     sph = torch.from_numpy(sp).pin_memory()
-    xh = torch.empty((w.n_tokens, w.d_model), dtype=torch.bfloat16).pin_memory()
+    xh = torch.empty((w.n_tokens, w.d_model), dtype=tdt).pin_memory()
     sh = torch.empty((w.n_tokens, 4), dtype=torch.float32).pin_memory()
-    nws = gr.host_workspace_size(w.n_tokens, w.d_model, torch.bfloat16)
+    nws = gr.host_workspace_size(w.n_tokens, w.d_model, tdt)
     buf = torch.empty(nws + 256, dtype=torch.uint8, device="cuda")
     ws = buf[(-buf.data_ptr()) % 256:][:nws]
     gr.write_then_read_host(Rh, yh, sph, P, xh, sh, ws)
