@@ -165,6 +165,26 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
                             float* s_next_host, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* Size of the fixed device workspace of gr_write_then_read_host_static (32 MiB). */
+#define GR_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/* gr_write_then_read_host without a caller-provided workspace: the same step on HOST buffers,
+ * staged through a fixed device workspace of GR_STATIC_WORKSPACE_BYTES that the library holds
+ * in a file-scope device array. The pages have no counterpart; it is a convenience form of
+ * gr_write_then_read_host for small batches (decode) that allocates nothing: no cudaMalloc,
+ * cudaFree, stream or event creation.
+ *   - Returns GR_E_SIZE, without touching anything, when gr_host_workspace_size(shape) exceeds
+ *     GR_STATIC_WORKSPACE_BYTES (for example N > 682 tokens at D = 4096, bf16).
+ *   - The first call on a device looks the workspace's device address up once
+ *     (cudaGetSymbolAddress); make that first call outside any stream capture.
+ *   - Nothing in the workspace has to start at zero (each call writes all it reads).
+ *   - All calls on a device share the one workspace: calls that overlap in time (on different
+ *     streams or host threads) race on it. Run them one after another.
+ *   - Runs on `stream` (copies in, step, copies out) and synchronises it before returning. */
+int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const void* y_host,
+                                   const float* s_prev_host, const gr_params* next, void* x_host,
+                                   float* s_next_host, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -388,3 +388,70 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
 }
 
 }  // extern "C"
+
+// ---- gr_write_then_read_host_static: the host-buffer step with a fixed device workspace ----
+
+namespace gr {
+namespace {
+
+// The device workspace of gr_write_then_read_host_static: file scope, module lifetime, the same
+// layout gr_write_then_read_host uses in its caller-provided workspace. Nothing in it has to
+// start at zero: every byte a call reads was written earlier in the same call.
+static __device__ __align__(256) unsigned char g_static_ws[GR_STATIC_WORKSPACE_BYTES];
+void* g_static_ws_addr[kMaxDevices];  // device address, looked up once per device
+std::mutex g_static_mu;
+
+}  // namespace
+}  // namespace gr
+
+extern "C" {
+
+int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const void* y_host,
+                                   const float* s_prev_host, const gr_params* next, void* x_host,
+                                   float* s_next_host, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if ((st = validate_params(shape, next))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!R_host || !y_host || !s_prev_host || !x_host || !s_next_host) return GR_E_NULL;
+    size_t need = 0;
+    gr_host_workspace_size(shape, &need);
+    if (need > size_t(GR_STATIC_WORKSPACE_BYTES)) return GR_E_SIZE;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es, ny = N * D * es, ns = N * kBranches * 4;
+    if (overlaps(R_host, nR, y_host, ny) || overlaps(R_host, nR, x_host, ny) ||
+        overlaps(x_host, ny, y_host, ny) || overlaps(s_prev_host, ns, s_next_host, ns) ||
+        overlaps(R_host, nR, s_next_host, ns) || overlaps(x_host, ny, s_next_host, ns))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_ws_addr[dev] &&
+            cudaGetSymbolAddress(&g_static_ws_addr[dev], g_static_ws) != cudaSuccess) {
+            g_static_ws_addr[dev] = nullptr;
+            return GR_E_CUDA;
+        }
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(g_static_ws_addr[dev]);
+    void* dR = w;
+    void* dy = w + align256(nR);
+    void* dx = w + align256(nR) + align256(ny);
+    float* dsp = reinterpret_cast<float*>(w + align256(nR) + 2 * align256(ny));
+    float* dsn = reinterpret_cast<float*>(w + align256(nR) + 2 * align256(ny) + align256(ns));
+    if (cudaMemcpyAsync(dR, R_host, nR, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dy, y_host, ny, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dsp, s_prev_host, ns, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return GR_E_CUDA;
+    st = run_step(shape, dR, dy, dsp, next, dx, dsn, cs);
+    if (st) return st;
+    if (cudaMemcpyAsync(R_host, dR, nR, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaMemcpyAsync(x_host, dx, ny, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaMemcpyAsync(s_next_host, dsn, ns, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return GR_E_CUDA;
+    return status_of(cudaStreamSynchronize(cs));
+}
+
+}  // extern "C"

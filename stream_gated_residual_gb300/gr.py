@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
         "gr_host_workspace_size": ([S, sz], ctypes.c_int),
         "gr_device_status": ([ctypes.c_int], ctypes.c_int),
         "gr_write_then_read_host": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
+        "gr_write_then_read_host_static": ([S, V, V, V, P, V, V, V], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -266,4 +267,20 @@ def write_then_read_host(R: torch.Tensor, y: torch.Tensor, s_prev: torch.Tensor,
     _check(load().gr_write_then_read_host(
         ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev), params.ref(), _ptr(x), _ptr(s_next),
         _ptr(workspace), workspace.numel(), _stream(stream)), "gr_write_then_read_host")
+    return x, s_next
+
+
+def write_then_read_host_static(R: torch.Tensor, y: torch.Tensor, s_prev: torch.Tensor,
+                                params: Params, x: torch.Tensor, s_next: torch.Tensor,
+                                stream=None):
+    """gr_write_then_read_host_static on CPU tensors (pinned for asynchronous copies), staged
+    through the library's fixed device workspace (GR_STATIC_WORKSPACE_BYTES)."""
+    for t, n in ((R, "R"), (y, "y"), (s_prev, "s_prev"), (x, "x"), (s_next, "s_next")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    N, _, D = R.shape
+    shape = make_shape(N, D, params.rank, R.dtype, params.eps)
+    _check(load().gr_write_then_read_host_static(
+        ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev), params.ref(), _ptr(x), _ptr(s_next),
+        _stream(stream)), "gr_write_then_read_host_static")
     return x, s_next

@@ -1,0 +1,83 @@
+"""gr_write_then_read_host_static (the host-buffer step staged through the library's fixed device
+workspace) against gr_write_then_read_host (caller-provided workspace): two fused steps in a
+row, each fed with the previous step's R' and s, give bit-identical results. The file is
+collected last on purpose, so the static entry also runs after every other test has used the
+library in the same process."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from gr_testlib import params_to_torch, to_torch
+from stream_gated_residual_gb300 import build as gbuild
+from stream_gated_residual_gb300 import gr
+from stream_gated_residual_gb300 import workloads as wl
+
+TDT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def _pinned(a):
+    return to_torch(a, "cpu").pin_memory()
+
+
+def _two_steps(entry, w, R0, y0, y1, s0, P):
+    """Two chained host-buffer steps; returns (R, x, s) after each."""
+    tdt = TDT[w.dtype]
+    R = _pinned(R0)
+    s = torch.from_numpy(s0).pin_memory()
+    outs = []
+    for y in (y0, y1):
+        x = torch.empty((w.n_tokens, w.d_model), dtype=tdt).pin_memory()
+        s_next = torch.empty((w.n_tokens, 4), dtype=torch.float32).pin_memory()
+        entry(R, _pinned(y), s, P, x, s_next)
+        outs.append((R.clone(), x.clone(), s_next.clone()))
+        s = s_next
+    return outs
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,D,r,dtype", [(128, 4096, 16, "bf16"), (64, 256, 8, "f32"),
+                                         (333, 1024, 12, "bf16")])
+def test_static_workspace_entry_matches_workspace_entry(N, D, r, dtype):
+    w = wl.Workload("noalloc", N, D, r, dtype, y_std=0.5, seed=23)
+    R0, s0 = wl.make_state(w), wl.make_s_prev(w)
+    y0, y1 = wl.make_y(w, 0), wl.make_y(w, 1)
+    t = params_to_torch(wl.make_params(w, 1))
+    P = gr.pack_params(t["gamma"], t["w_down"], t["w_up"], t["w_write"], TDT[dtype], w.eps)
+    nws = gr.host_workspace_size(N, D, TDT[dtype])
+    buf = torch.empty(nws + 256, dtype=torch.uint8, device="cuda")
+    ws = buf[(-buf.data_ptr()) % 256:][:nws]
+
+    def with_workspace(R, y, s, P, x, sn):
+        gr.write_then_read_host(R, y, s, P, x, sn, ws)
+
+    def static(R, y, s, P, x, sn):
+        gr.write_then_read_host_static(R, y, s, P, x, sn)
+
+    ref = _two_steps(with_workspace, w, R0, y0, y1, s0, P)
+    got = _two_steps(static, w, R0, y0, y1, s0, P)
+    for (Ra, xa, sa), (Rb, xb, sb) in zip(ref, got):
+        assert torch.equal(Ra, Rb) and torch.equal(xa, xb) and torch.equal(sa, sb)
+    assert gr.device_status() == 0
+
+
+def test_static_workspace_entry_rejects_oversize_before_any_cuda_call():
+    """683 tokens at D = 4096 in bf16 need 33,592,832 bytes, more than the 32 MiB workspace:
+    GR_E_SIZE, checked on the host before any copy or launch (no GPU needed)."""
+    gbuild.build()
+    L = gr.load()
+    shape = gr.Shape(683, 4096, 4, 16, gr.GR_BF16, 1e-6)
+    need = ctypes.c_size_t(0)
+    assert L.gr_host_workspace_size(ctypes.byref(shape), ctypes.byref(need)) == 0
+    assert need.value == 33_592_832 > (32 << 20)
+    p = gr.ParamsStruct()
+    p.tag, p.packed = gr.GR_PARAMS_TAG, 0x1000
+    p.d_model, p.n_branch, p.rank, p.state_dtype = 4096, 4, 16, gr.GR_BF16
+    fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(5)]
+    st = L.gr_write_then_read_host_static(ctypes.byref(shape), fake[0], fake[1], fake[2],
+                                          ctypes.byref(p), fake[3], fake[4], None)
+    assert st == -7  # GR_E_SIZE
+    shape.n_tokens = 682
+    assert L.gr_host_workspace_size(ctypes.byref(shape), ctypes.byref(need)) == 0
+    assert need.value <= (32 << 20)
