@@ -416,6 +416,9 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             const char* yb = ybuf(k);
             const char* sb = sbuf(k);
             mbar_wait(&mbar[kMbRFull + int(k % kRStages)], uint32_t((k / kRStages) & 1));
+            // y of tile k+1 into the buffer of tile k-1 (free since that tile's a_sync): issued
+            // once tile k's R has landed, so the y and R loads do not queue up together
+            if (k >= 1 && a == 0 && lane < 2) issue_y(k - 1 + kYStages, lane);
             if (WRITE) mbar_wait(&mbar[kMbYFull + int(k % kYStages)], uint32_t((k / kYStages) & 1));
 
             // write (eq write) for this warp's branch and 128 channels; R' back in place.
@@ -529,8 +532,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                                        u0.y + u1.y, u0.z + u1.z, u0.w + u1.w);
                 }
             }
-            a_sync();  // red and this tile's y buffer are free again
-            if (a == 0 && lane < 2) issue_y(k + kYStages, lane);   // y of tile k+2 into this buffer
+            a_sync();  // red is free again
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBRegs));
