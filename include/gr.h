@@ -147,6 +147,13 @@ int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* 
  * that call are not valid), or GR_E_CUDA. `clear` != 0 resets the status. */
 int gr_device_status(int clear);
 
+/* Self-test of the failure-detection path (the pages have no counterpart): launches one thread
+ * that waits, with the fused kernel's bounded-wait helper, on an mbarrier that nothing arrives
+ * at. After limit_cycles (1 .. 4e9 SM clock cycles; else GR_E_SIZE, nothing launched) the wait
+ * gives up, sets the device status word and the kernel returns, so gr_device_status() reports
+ * GR_E_TIMEOUT until cleared. No fault, trap or hang is involved. Asynchronous on `stream`. */
+int gr_selftest_bounded_wait(int64_t limit_cycles, void* stream);
+
 /* Bytes of device workspace gr_write_then_read_host needs for `shape`. */
 int gr_host_workspace_size(const gr_shape* shape, size_t* bytes);
 

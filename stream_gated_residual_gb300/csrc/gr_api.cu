@@ -295,6 +295,14 @@ int gr_device_status(int clear) {
     return v ? GR_E_TIMEOUT : GR_OK;
 }
 
+int gr_selftest_bounded_wait(int64_t limit_cycles, void* stream) {
+    if (limit_cycles < 1 || limit_cycles > 4000000000LL) return GR_E_SIZE;
+    int st = check_device();
+    if (st) return st;
+    return status_of(launch_wait_selftest(static_cast<long long>(limit_cycles),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 int gr_host_workspace_size(const gr_shape* shape, size_t* bytes) {
     int st = validate_shape(shape);
     if (st) return st;

@@ -177,7 +177,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // try_wait may suspend the warp for up to kSuspendNs, so waiting warps do not take issue slots
 // from the warps that share their scheduler.
 constexpr uint32_t kSuspendNs = 20000;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = kWaitLimit) {
     const uint32_t a = smem_u32(bar);
     const long long t0 = clock64();
     for (;;) {
@@ -190,7 +191,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
             : "r"(a), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (done) return true;
-        if (clock64() - t0 > kWaitLimit) {
+        if (clock64() - t0 > limit) {
             atomicOr(&g_fused_status, 1u);
             return false;
         }
@@ -935,6 +936,24 @@ bool fused_supported(int D, int r) {
 }
 
 int64_t fused_max_tokens() { return kMaxTokens; }
+
+namespace {
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing arrives at, with
+// the fused kernel's wait helper and a short limit; the wait gives up and sets the status word.
+__global__ void wait_selftest_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_wait(&bar, 0u, limit);   // phase 0 never completes
+    }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(limit_cycles);
+    return cudaGetLastError();
+}
 
 int fused_status(bool clear) {
     unsigned int v = 0;

@@ -82,6 +82,9 @@ cudaError_t launch_residual_add(int64_t n, int dtype, const void* y, void* x, cu
 // Status bits recorded by device-side bounded waits (0 = none; -1 = could not be read).
 int fused_status(bool clear);
 
+// One bounded wait that nothing satisfies (gives up after limit_cycles and sets the status).
+cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

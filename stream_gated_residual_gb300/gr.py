@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
         "gr_device_status": ([ctypes.c_int], ctypes.c_int),
         "gr_write_then_read_host": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
         "gr_write_then_read_host_static": ([S, V, V, V, P, V, V, V], ctypes.c_int),
+        "gr_selftest_bounded_wait": ([ctypes.c_int64, V], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -245,6 +246,13 @@ def residual_add_ref(x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Ten
 def device_status(clear: bool = False) -> int:
     """gr_device_status: 0, or the status code of a bounded device-side wait that ran out."""
     return int(load().gr_device_status(1 if clear else 0))
+
+
+def selftest_bounded_wait(limit_cycles: int, stream=None) -> None:
+    """gr_selftest_bounded_wait: one device-side wait that nothing satisfies gives up after
+    limit_cycles and sets the status that device_status() reports."""
+    _check(load().gr_selftest_bounded_wait(int(limit_cycles), _stream(stream)),
+           "gr_selftest_bounded_wait")
 
 
 def host_workspace_size(n_tokens: int, d_model: int, dtype: torch.dtype) -> int:
