@@ -142,6 +142,17 @@ def test_large_skewed_subset():
     check(w, *fused_case(w, n_tokens=1024))
 
 
+def test_large_skewed_full_size_sampled():
+    """The large/skewed workload at its full size (N=65536, D=7168, r=32: a 3.8 GB state) in
+    one call; every output row is finite and in range, and 512 seeded sampled rows (with the
+    first and the last) are compared with the oracle."""
+    w = wl.WORKLOADS["large_skewed"]
+    rng = np.random.default_rng(17)
+    rows = np.unique(np.concatenate([[0, w.n_tokens - 1],
+                                     rng.choice(w.n_tokens, 510, replace=False)]))
+    check(w, *fused_case(w, rows=rows))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_fused_equals_write_then_read_separately(dtype):
     """The fused call reads the stored state, so it equals gr_write followed by gr_read."""
