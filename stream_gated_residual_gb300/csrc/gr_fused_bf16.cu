@@ -46,8 +46,8 @@ constexpr int kT = 16;                      // tokens per tile (mma M)
 constexpr int kAW = 8, kBW = 8;             // A warps, B warps
 constexpr int kThreads = (kAW + kBW) * 32;
 // Register split: the block launches with 128 per thread (65,536 in all); the A warpgroups give
-// 16 each back and the B warpgroups take them (2·128·112 + 2·128·144 = 65,536).
-constexpr int kLaunchRegs = 128, kARegs = 112, kBRegs = 144;
+// 8 each back and the B warpgroups take them (2·128·120 + 2·128·136 = 65,536).
+constexpr int kLaunchRegs = 128, kARegs = 120, kBRegs = 136;
 static_assert(kAW % 4 == 0 && kBW % 4 == 0, "roles are whole warpgroups");
 static_assert(kAW * kARegs + kBW * kBRegs == (kAW + kBW) * kLaunchRegs, "register split");
 constexpr int kAThreads = kAW * 32;
