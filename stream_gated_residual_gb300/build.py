@@ -36,8 +36,8 @@ def sources() -> list[str]:
 
 
 def _deps() -> list[str]:
-    return sources() + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "gr.h"),
-                                                                os.path.abspath(__file__)]
+    headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+    return sources() + headers + [os.path.join(INCLUDE, "gr.h"), os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:
