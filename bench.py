@@ -79,7 +79,8 @@ def load_peaks() -> dict:
 
 def kernel_source_sha(kernel_path: str) -> str:
     from stream_gated_residual_gb300 import build as gbuild
-    name = {"fused_bf16": "gr_fused_bf16.cu", "generic": "gr_generic.cu"}[kernel_path]
+    name = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
+            "generic": "gr_generic.cu"}[kernel_path]
     h = hashlib.sha256()
     for p in (os.path.join(gbuild.CSRC, name), os.path.join(gbuild.CSRC, "gr_internal.h"),
               os.path.join(gbuild.CSRC, "gr_ptx.cuh")):

@@ -94,7 +94,9 @@ int gr_api_version(void);
 const char* gr_status_string(int status);
 
 /* Name of the kernel path a read or fused step takes for `shape` (static string, never NULL):
- * "fused_bf16" (tensor-core kernel), "generic" (one CTA per token), or "invalid". Host only. */
+ * "fused_bf16" (cluster tensor-core kernel: bf16, D in {256, 512, 1024, 2048, 4096}, r <= 16),
+ * "tiled_bf16" (two-pass tensor-core kernel: the other bf16 shapes with D % 64 == 0, r <= 32),
+ * "generic" (one CTA per token), or "invalid". Host only. */
 const char* gr_kernel_path(const gr_shape* shape);
 
 /* Bytes of device memory gr_pack_params needs for `shape` (host only; no CUDA call).

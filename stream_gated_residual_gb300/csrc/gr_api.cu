@@ -105,12 +105,20 @@ bool use_fused(const gr_shape* s) {
            s->n_tokens <= fused_max_tokens();
 }
 
+bool use_tiled(const gr_shape* s) {
+    return s->state_dtype == GR_BF16 && !fused_supported(s->d_model, s->rank) &&
+           tiled_supported(s->d_model, s->rank) && s->n_tokens <= tiled_max_tokens();
+}
+
 int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
              const gr_params* p, void* x, float* s_out, cudaStream_t st) {
     if (s->n_tokens == 0) return GR_OK;
     cudaError_t e;
     if (use_fused(s))
         e = launch_fused_bf16(s->n_tokens, s->d_model, s->rank, s->eps, R, y, s_prev, p->packed,
+                              x, s_out, st);
+    else if (use_tiled(s))
+        e = launch_tiled_bf16(s->n_tokens, s->d_model, s->rank, s->eps, R, y, s_prev, p->packed,
                               x, s_out, st);
     else
         e = launch_generic(s->n_tokens, s->d_model, s->rank, s->state_dtype, s->eps, R, y,
@@ -160,7 +168,7 @@ const char* gr_status_string(int status) {
 
 const char* gr_kernel_path(const gr_shape* shape) {
     if (validate_shape(shape) != GR_OK) return "invalid";
-    return use_fused(shape) ? "fused_bf16" : "generic";
+    return use_fused(shape) ? "fused_bf16" : use_tiled(shape) ? "tiled_bf16" : "generic";
 }
 
 int gr_packed_size(const gr_shape* shape, size_t* bytes) {
@@ -290,9 +298,9 @@ int gr_device_status(int clear) {
     int st = check_device();
     if (st) return st;
     if (cudaDeviceSynchronize() != cudaSuccess) return GR_E_CUDA;
-    const int v = fused_status(clear != 0);
-    if (v < 0) return GR_E_CUDA;
-    return v ? GR_E_TIMEOUT : GR_OK;
+    const int v = fused_status(clear != 0), w = tiled_status(clear != 0);
+    if (v < 0 || w < 0) return GR_E_CUDA;
+    return (v | w) ? GR_E_TIMEOUT : GR_OK;
 }
 
 int gr_selftest_bounded_wait(int64_t limit_cycles, void* stream) {

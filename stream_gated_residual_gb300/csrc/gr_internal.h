@@ -18,9 +18,11 @@ constexpr int kBranches = 4;
 //   wdw     : W    [r+4][4D]                   rows 0..r-1 = W_d, rows r..r+3 = W_w
 //                                              (gamma folded on the bf16 path)
 //   wut     : W    [r][4D]                     W_u transposed
-//   frag    : per-CTA slices for the fused tensor-core kernel (bf16 path, shapes that
-//             fused_supported() accepts): mma fragments of the weights and fp32 gains,
-//             laid out in gr_fused_bf16.cu; 0 bytes otherwise
+//   frag    : bf16 path only: the mma fragments of the weights (and gains) in the layout of the
+//             tensor-core kernel that serves the shape — per-CTA slices for the cluster kernel
+//             (shapes fused_supported() accepts, laid out in gr_fused_bf16.cu), else per-chunk
+//             fragments for the two-pass kernel (tiled_supported(), gr_tiled_bf16.cu); 0 bytes
+//             when neither takes the shape
 struct Layout {
     size_t gamma32, wdw, wut, frag, total;
     size_t frag_bytes;
@@ -34,6 +36,12 @@ bool fused_supported(int D, int r);
 int64_t fused_max_tokens();
 size_t fused_frag_bytes(int D, int r);
 
+// Two-pass tensor-core kernel for the bf16 shapes the cluster kernel does not take
+// (gr_tiled_bf16.cu). It also needs n_tokens <= tiled_max_tokens().
+bool tiled_supported(int D, int r);
+int64_t tiled_max_tokens();
+size_t tiled_frag_bytes(int D, int r);
+
 inline Layout make_layout(int D, int r, int dtype) {
     Layout L{};
     const size_t K = size_t(kBranches) * D;
@@ -45,7 +53,10 @@ inline Layout make_layout(int D, int r, int dtype) {
     off = align256(off + size_t(r + kBranches) * K * w);
     L.wut = off;
     off = align256(off + size_t(r) * K * w);
-    L.frag_bytes = (dtype == GR_BF16 && fused_supported(D, r)) ? fused_frag_bytes(D, r) : 0;
+    L.frag_bytes = dtype != GR_BF16        ? 0
+                   : fused_supported(D, r) ? fused_frag_bytes(D, r)
+                   : tiled_supported(D, r) ? tiled_frag_bytes(D, r)
+                                           : 0;
     L.frag = off;
     off = align256(off + L.frag_bytes);
     L.total = off;
@@ -68,6 +79,11 @@ cudaError_t launch_fused_bf16(int64_t N, int D, int r, float eps, void* R, const
                               const float* s_prev, const void* packed, void* x, float* s_out,
                               cudaStream_t st);
 
+// Two-pass bf16 tensor-core kernel (write then read, or read only when y == nullptr).
+cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
+                              const float* s_prev, const void* packed, void* x, float* s_out,
+                              cudaStream_t st);
+
 // Streaming write R += s_i * y (no read).
 cudaError_t launch_write(int64_t N, int D, int dtype, void* R, const void* y, const float* s,
                          cudaStream_t st);
@@ -79,8 +95,10 @@ cudaError_t launch_fixed_gates(int64_t N, int D, int dtype, float eps, const voi
 // Single-stream x += y.
 cudaError_t launch_residual_add(int64_t n, int dtype, const void* y, void* x, cudaStream_t st);
 
-// Status bits recorded by device-side bounded waits (0 = none; -1 = could not be read).
+// Status bits recorded by device-side bounded waits, one word per kernel unit (0 = none; -1 =
+// could not be read).
 int fused_status(bool clear);
+int tiled_status(bool clear);
 
 // One bounded wait that nothing satisfies (gives up after limit_cycles and sets the status).
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);

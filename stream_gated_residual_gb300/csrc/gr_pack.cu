@@ -45,8 +45,11 @@ __global__ void pack_generic_kernel(int D, int r, const float* __restrict__ gamm
 
 }  // namespace
 
-// Fragment section of the fused kernel (defined in gr_fused_bf16.cu).
+// Fragment sections of the cluster kernel (gr_fused_bf16.cu) and the two-pass kernel
+// (gr_tiled_bf16.cu).
 cudaError_t launch_pack_fused(int D, int r, const float* gamma, const float* wd, const float* wu,
+                              const float* ww, void* frag, cudaStream_t st);
+cudaError_t launch_pack_tiled(int D, int r, const float* gamma, const float* wd, const float* wu,
                               const float* ww, void* frag, cudaStream_t st);
 
 cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float* wd,
@@ -71,7 +74,10 @@ cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (L.frag_bytes) e = launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag, st);
+    if (L.frag_bytes) {
+        e = fused_supported(D, r) ? launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag, st)
+                                  : launch_pack_tiled(D, r, gamma, wd, wu, ww, base + L.frag, st);
+    }
     return e;
 }
 

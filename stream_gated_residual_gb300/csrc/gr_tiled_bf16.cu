@@ -1,0 +1,590 @@
+// Two-pass bf16 GR kernel for the shapes the cluster kernel (gr_fused_bf16.cu) does not take:
+// any D that is a multiple of 64 and 1 <= r <= 32, e.g. D = 7168 with r = 32.
+//
+// What it computes is the same fused step as the cluster kernel, from "【论文解读】 Qwen3.8
+// Flash Next", §二.4: the write R' = R + s_prev·y (eq write), then the read of R': per-branch
+// RMS (eq rms), the low-rank gate (eq gate), the write strengths s = 2σ(u) (eq s) and the gated
+// combine x = (1/n_r)·Σ_i G_i ⊙ R̂_i (eq use_gate).
+//
+// Design. One CTA owns a tile of 32 tokens across all D channels; the CTAs are persistent
+// (one per SM, tiles handed out round-robin). Each tile takes two passes over its channels in
+// 64-channel chunks:
+//   pass 1 (forward over the chunks): TMA-load R [4 branches][32 tokens][64 ch] and y
+//     [32][64]; the write R' = RNE(R + s·y) in registers, stored back in place and sent to HBM by
+//     a per-warp TMA store; per-(token, branch) sums of R'² in registers; the down projection
+//     [W_d; W_w]·R' on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), one
+//     warp per (branch, 16-token m-tile) accumulating over all chunks, the B fragments (γ
+//     folded) streamed from L2 through a weight ring.
+//   owner step (once per tile): inv_i = 1/sqrt(ms_i + eps); z = ¼Σ_i inv_i·P_i, h = SiLU(z)
+//     and u = ¼Σ_i inv_i·Q_i, s = 2σ(u) — through shared memory, no cluster needed.
+//   pass 2 (backward over the chunks, so the R' chunks written last are read first, while
+//     they are still in L2): TMA-load R' again; the up projection W_u·h on the tensor cores
+//     (h as bf16 hi + lo, W_u pre-scaled by ½), σ as ½ + ½·tanh, and the combine; x leaves
+//     through per-warp TMA stores.
+// The price is one more read of R' than the single traversal (about 40% more HBM traffic at
+// D = 7168); in exchange the tile needs no cluster and the weights never have to fit on chip.
+//
+// Roles: warps 0..7 compute, warp 8 (one lane) produces: it fills the state ring (R/R' + y,
+// 20 KB a stage) and the weight ring, and before pass 2 of a tile it waits until the compute
+// warps report pass 1's R' stores complete. Every mbarrier wait is bounded; a wait that runs out
+// sets this unit's status word and a CTA-wide abort flag, after which the CTA's waits return at
+// once and the CTA finishes without blocking (its outputs are then invalid).
+#include <cuda.h>
+#include <string.h>
+
+#include "gr_internal.h"
+#include "gr_ptx.cuh"
+
+namespace gr {
+namespace {
+
+constexpr int kTT = 32;                           // tokens per tile
+constexpr int kCh = 64;                           // channels per chunk
+constexpr int kCW = 8;                            // compute warps
+constexpr int kCThreads = kCW * 32;
+constexpr int kThreadsT = kCThreads + 32;         // + the producer warp
+constexpr int kSStages = 4;                       // state ring depth
+constexpr int kWStages = 4;                       // weight ring depth
+constexpr int kRChunk = kBranches * kTT * kCh * 2;  // 16 KB: R [4][32][64] bf16, 128B-swizzled
+constexpr int kYChunk = kTT * kCh * 2;              // 4 KB: y [32][64] bf16, 128B-swizzled
+constexpr int kStateStage = kRChunk + kYChunk;
+constexpr int kXBuf = 16 * 16 * 2;                // per warp: x [16 tok][16 ch], 32B-swizzled
+constexpr int kMaxTiledRank = 32;
+
+// Compile-time sizes for NTD = ceil((r+4)/8) down-projection n-tiles and KSU = ceil(r/16)
+// up-projection k-steps.
+template <int NTD, int KSU> struct TiledCfg {
+    static constexpr int kNP = 8 * NTD;                        // padded r + 4
+    static constexpr int kHP = 16 * KSU;                       // padded r
+    static constexpr int kDownChunk = kBranches * 4 * NTD * 256;  // [i][ks][nt][lane] uint2
+    static constexpr int kUpFrag = 32 * KSU * 256;             // [cq][i][cg][lane][ks] uint2
+    static constexpr int kUpChunk = kUpFrag + kBranches * kCh * 4;  // + gamma/8 [4][64] fp32
+    static constexpr int kWStage = kDownChunk > kUpChunk ? kDownChunk : kUpChunk;
+    static constexpr int off_state = 0;
+    static constexpr int off_w = off_state + kSStages * kStateStage;
+    static constexpr int off_x = off_w + kWStages * kWStage;
+    static constexpr int off_red = off_x + kCW * 2 * kXBuf;
+    static constexpr int off_h = off_red + kBranches * kTT * kNP * 4;
+    static constexpr int off_inv = off_h + kTT * kHP * 4;
+    static constexpr int off_bar = off_inv + 2 * kBranches * kTT * 4;
+    static constexpr int kBars = 2 * kSStages + 2 * kWStages + 1;
+    static constexpr int off_abort = off_bar + kBars * 8;
+    static constexpr int kSmem = off_abort + 16 + 1024;        // + slack for 1 KB alignment
+};
+
+// Bounded wait that gives up at once after any wait of this CTA has run out.
+__device__ __forceinline__ bool twait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort) {
+    if (*abort) return false;
+    if (mbar_wait(bar, parity)) return true;
+    *abort = 1u;
+    return false;
+}
+
+__device__ __forceinline__ uint32_t lds32(const char* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+__device__ __forceinline__ void sts32(char* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
+// Byte offset of byte `b` (0..31) of row `row` in a 32B-swizzled box of 32-byte rows.
+__device__ __forceinline__ int swz32(int row, int b) {
+    const int off = row * 32 + b;
+    return off ^ ((off >> 3) & 0x10);
+}
+
+template <bool WRITE, int NTD, int KSU>
+__global__ void __launch_bounds__(kThreadsT, 1)
+gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {64, 32, 4, 1}
+                const __grid_constant__ CUtensorMap tm_Rs,  // R' stores, box {64, 16, 1, 1}
+                const __grid_constant__ CUtensorMap tm_y,   // y loads, box {64, 32}
+                const __grid_constant__ CUtensorMap tm_x,   // x stores, box {16, 16}
+                int N, int D, int r, float eps, const float* __restrict__ s_prev,
+                const char* __restrict__ frag, float* __restrict__ s_out) {
+    using C = TiledCfg<NTD, KSU>;
+    extern __shared__ uint8_t smem_raw[];
+    char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                         ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int J = D / kCh;
+    const int ntiles = (N + kTT - 1) / kTT;
+    const char* down_frag = frag;                                   // J chunks of kDownChunk
+    const char* up_frag = frag + size_t(J) * C::kDownChunk;         // J chunks of kUpChunk
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::off_bar);
+    uint64_t* sfull = bars;
+    uint64_t* sempty = bars + kSStages;
+    uint64_t* wfull = bars + 2 * kSStages;
+    uint64_t* wempty = bars + 2 * kSStages + kWStages;
+    uint64_t* t1done = bars + 2 * kSStages + 2 * kWStages;
+    volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(smem + C::off_abort);
+    float* red = reinterpret_cast<float*>(smem + C::off_red);   // [4][32][kNP]
+    float* hbuf = reinterpret_cast<float*>(smem + C::off_h);    // [32][kHP]
+    // [2][4][32] by tile parity: a warp that runs ahead into the next tile's owner step must not
+    // overwrite the values a slower warp has yet to read at the start of this tile's pass 2
+    float* invb_base = reinterpret_cast<float*>(smem + C::off_inv);
+    auto sbuf = [&](uint32_t c) { return smem + C::off_state + int(c % kSStages) * kStateStage; };
+    auto wbuf = [&](uint32_t c) { return smem + C::off_w + int(c % kWStages) * C::kWStage; };
+
+    if (tid == 0) {
+        for (int s = 0; s < kSStages; ++s) {
+            mbar_init(&sfull[s], 1u);
+            mbar_init(&sempty[s], uint32_t(kCW));
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&wfull[s], 1u);
+            mbar_init(&wempty[s], uint32_t(kCW));
+        }
+        mbar_init(t1done, uint32_t(kCW));
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // h columns r .. kHP-1 stay zero (the padded k of the up projection)
+    for (int e = tid; e < kTT * C::kHP; e += kThreadsT) hbuf[e] = 0.f;
+    __syncthreads();
+
+    if (warp == kCW) {
+        // ================================ producer =============================================
+        if (lane != 0) return;
+        uint32_t sc = 0, wc = 0;  // fills issued on each ring
+        uint32_t nt_local = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++nt_local) {
+            const int t0 = tile * kTT;
+            for (int pass = 0; pass < 2; ++pass) {
+                if (pass == 1) {
+                    // pass 2 reads back the R' that pass 1 stored through the async proxy
+                    twait(t1done, nt_local & 1u, abort);
+                    fence_async_global();
+                }
+                for (int jj = 0; jj < J; ++jj) {
+                    const int j = pass == 0 ? jj : J - 1 - jj;
+                    {   // state: R (pass 1) or R' (pass 2) chunk j, plus y chunk j in pass 1
+                        const int st = int(sc % kSStages);
+                        if (sc >= kSStages) twait(&sempty[st], ((sc / kSStages) + 1) & 1u, abort);
+                        char* b = sbuf(sc);
+                        const bool with_y = WRITE && pass == 0;
+                        mbar_expect_tx(&sfull[st], uint32_t(kRChunk + (with_y ? kYChunk : 0)));
+                        tma_load_4d(b, &tm_R, 0, t0, 0, j, &sfull[st]);
+                        if (with_y) tma_load_2d(b + kRChunk, &tm_y, j * kCh, t0, &sfull[st]);
+                        ++sc;
+                    }
+                    {   // weights: down-projection fragments (pass 1) or W_u fragments + γ/8
+                        const int st = int(wc % kWStages);
+                        if (wc >= kWStages) twait(&wempty[st], ((wc / kWStages) + 1) & 1u, abort);
+                        const uint32_t bytes = uint32_t(pass == 0 ? C::kDownChunk : C::kUpChunk);
+                        const char* src = pass == 0 ? down_frag + size_t(j) * C::kDownChunk
+                                                    : up_frag + size_t(j) * C::kUpChunk;
+                        mbar_expect_tx(&wfull[st], bytes);
+                        bulk_g2s(wbuf(wc), src, bytes, &wfull[st]);
+                        ++wc;
+                    }
+                }
+            }
+        }
+        // drain: the last fill of every stage has landed before the CTA may exit
+        for (uint32_t f = sc > kSStages ? sc - kSStages : 0; f < sc; ++f)
+            mbar_wait(&sfull[f % kSStages], (f / kSStages) & 1u);
+        for (uint32_t f = wc > kWStages ? wc - kWStages : 0; f < wc; ++f)
+            mbar_wait(&wfull[f % kWStages], (f / kWStages) & 1u);
+        return;
+    }
+
+    // ================================== compute warps ==========================================
+    const int g = lane >> 2, q = lane & 3;
+    const int ib = warp & 3, mt = warp >> 2;      // pass 1: branch, m-tile
+    const int mt2 = warp & 1, cq = warp >> 1;     // pass 2: m-tile, 16-channel quarter
+    const float inv_d = 1.0f / float(D);
+    char* xb0 = smem + C::off_x + warp * 2 * kXBuf;
+    uint32_t sc = 0, wc = 0, xc = 0, tl = 0;
+
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
+        const int t0 = tile * kTT;
+        float* invb = invb_base + int(tl & 1u) * kBranches * kTT;
+        // ---------------------------------- pass 1 --------------------------------------------
+        uint64_t sp = f2(0.f, 0.f);   // s_prev of tokens g and g+8 of the m-tile, branch ib
+        if (WRITE) {
+            const int ta = t0 + 16 * mt + g, tb = ta + 8;
+            sp = f2(ta < N ? s_prev[size_t(ta) * 4 + ib] : 0.f,
+                    tb < N ? s_prev[size_t(tb) * 4 + ib] : 0.f);
+        }
+        float spa, spb;
+        unf2(sp, spa, spb);
+        const uint64_t sa2 = f2(spa, spa), sb2 = f2(spb, spb);
+        float acc[NTD][4];
+#pragma unroll
+        for (int n = 0; n < NTD; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        uint64_t ssa = f2(0.f, 0.f), ssb = f2(0.f, 0.f);
+        const int rowa = ib * kTT + 16 * mt + g, rowb = rowa + 8;  // rows of the R box
+        const int ya = 16 * mt + g, yb = ya + 8;                     // rows of the y box
+        int prev_st = -1;
+        for (int j = 0; j < J; ++j) {
+            const int st = int(sc % kSStages);
+            twait(&sfull[st], (sc / kSStages) & 1u, abort);
+            twait(&wfull[wc % kWStages], (wc / kWStages) & 1u, abort);
+            char* rb = sbuf(sc);
+            const char* ybuf = rb + kRChunk;
+            const uint2* wd = reinterpret_cast<const uint2*>(wbuf(wc)) + ib * 4 * NTD * 32;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t a[4];
+                const int o[4] = {swz(rowa, 2 * ks) + 4 * q, swz(rowb, 2 * ks) + 4 * q,
+                                  swz(rowa, 2 * ks + 1) + 4 * q, swz(rowb, 2 * ks + 1) + 4 * q};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t v = lds32(rb + o[e]);
+                    if (WRITE) {
+                        const int yo = swz((e & 1) ? yb : ya, 2 * ks + (e >> 1)) + 4 * q;
+                        const uint64_t yy = bf2_to_f2(lds32(ybuf + yo));
+                        v = f2_to_bf2(fma2(yy, (e & 1) ? sb2 : sa2, bf2_to_f2(v)));
+                        sts32(rb + o[e], v);
+                    }
+                    const uint64_t f = bf2_to_f2(v);
+                    if (e & 1) ssb = fma2(f, f, ssb);
+                    else ssa = fma2(f, f, ssa);
+                    a[e] = v;
+                }
+#pragma unroll
+                for (int n = 0; n < NTD; ++n) {
+                    const uint2 b = wd[(ks * NTD + n) * 32 + lane];
+                    mma_bf16(acc[n], a[0], a[1], a[2], a[3], b.x, b.y);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[wc % kWStages]);
+            if (WRITE) {
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    // an m-tile wholly past the last token has nothing to store (empty group)
+                    if (t0 + 16 * mt < N)
+                        tma_store_4d(&tm_Rs, rb + (ib * kTT + 16 * mt) * 128, 0, t0 + 16 * mt, ib,
+                                     j);
+                    bulk_commit();
+                    // the previous chunk's stage is free once its store has read it
+                    bulk_wait_read<1>();
+                    if (prev_st >= 0) mbar_arrive(&sempty[prev_st]);
+                }
+            } else if (lane == 0) {
+                mbar_arrive(&sempty[st]);
+            }
+            prev_st = st;
+            ++sc;
+            ++wc;
+        }
+        if (lane == 0) {
+            if (WRITE) {
+                bulk_wait_all();       // every R' store of the tile has reached global memory
+                fence_async_global();
+                if (prev_st >= 0) mbar_arrive(&sempty[prev_st]);
+            }
+            mbar_arrive(t1done);
+        }
+        // ---------------------------------- owner step ----------------------------------------
+        {
+            float s0, s1, s2, s3;
+            unf2(ssa, s0, s1);
+            unf2(ssb, s2, s3);
+            float qa = s0 + s1, qb = s2 + s3;
+            qa += __shfl_xor_sync(0xffffffffu, qa, 1);
+            qa += __shfl_xor_sync(0xffffffffu, qa, 2);
+            qb += __shfl_xor_sync(0xffffffffu, qb, 1);
+            qb += __shfl_xor_sync(0xffffffffu, qb, 2);
+            const float inva = rsqrtf(qa * inv_d + eps), invb_ = rsqrtf(qb * inv_d + eps);
+            float* ra = red + (ib * kTT + 16 * mt + g) * C::kNP;
+            float* rb_ = ra + 8 * C::kNP;
+#pragma unroll
+            for (int n = 0; n < NTD; ++n) {
+                *reinterpret_cast<float2*>(ra + n * 8 + 2 * q) =
+                    make_float2(acc[n][0] * inva, acc[n][1] * inva);
+                *reinterpret_cast<float2*>(rb_ + n * 8 + 2 * q) =
+                    make_float2(acc[n][2] * invb_, acc[n][3] * invb_);
+            }
+            if (q == 0) {
+                invb[ib * kTT + 16 * mt + g] = inva;
+                invb[ib * kTT + 16 * mt + g + 8] = invb_;
+            }
+        }
+        named_sync(1, kCThreads);
+        {
+            const int nk = r + 4;
+            for (int it = tid; it < kTT * nk; it += kCThreads) {
+                const int tok = it / nk, n = it - tok * nk;
+                const float z = 0.25f * (red[(0 * kTT + tok) * C::kNP + n] +
+                                         red[(1 * kTT + tok) * C::kNP + n] +
+                                         red[(2 * kTT + tok) * C::kNP + n] +
+                                         red[(3 * kTT + tok) * C::kNP + n]);
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
+                if (n < r) hbuf[tok * C::kHP + n] = z * sg;
+                else if (t0 + tok < N) s_out[size_t(t0 + tok) * 4 + (n - r)] = 2.0f * sg;
+            }
+        }
+        named_sync(1, kCThreads);
+        // ---------------------------------- pass 2 --------------------------------------------
+        uint32_t ahi[KSU][4], alo[KSU][4];
+        {
+            const float* ha = hbuf + (16 * mt2 + g) * C::kHP;
+            const float* hb = ha + 8 * C::kHP;
+#pragma unroll
+            for (int ks = 0; ks < KSU; ++ks) {
+                const float2 v[4] = {*reinterpret_cast<const float2*>(ha + ks * 16 + 2 * q),
+                                     *reinterpret_cast<const float2*>(hb + ks * 16 + 2 * q),
+                                     *reinterpret_cast<const float2*>(ha + ks * 16 + 2 * q + 8),
+                                     *reinterpret_cast<const float2*>(hb + ks * 16 + 2 * q + 8)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t hi = pack_bf2(v[e].x, v[e].y);
+                    float hx, hy;
+                    unf2(bf2_to_f2(hi), hx, hy);
+                    ahi[ks][e] = hi;
+                    alo[ks][e] = pack_bf2(v[e].x - hx, v[e].y - hy);
+                }
+            }
+        }
+        float inv2[kBranches][2];
+#pragma unroll
+        for (int i = 0; i < kBranches; ++i) {
+            inv2[i][0] = invb[i * kTT + 16 * mt2 + g];
+            inv2[i][1] = invb[i * kTT + 16 * mt2 + g + 8];
+        }
+        for (int jj = 0; jj < J; ++jj) {
+            const int j = J - 1 - jj;
+            const int st = int(sc % kSStages);
+            twait(&sfull[st], (sc / kSStages) & 1u, abort);
+            twait(&wfull[wc % kWStages], (wc / kWStages) & 1u, abort);
+            const char* rb = sbuf(sc);
+            const char* wb = wbuf(wc);
+            const uint2* wu = reinterpret_cast<const uint2*>(wb) + cq * kBranches * 2 * 32 * KSU;
+            const float* gam = reinterpret_cast<const float*>(wb + C::kUpFrag);  // [4][64], γ/8
+            char* xb = xb0 + int(xc & 1u) * kXBuf;
+            // the x buffer is free once the store issued from it two chunks ago has read it
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int cg = 0; cg < 2; ++cg) {
+                const int ch = cq * 16 + cg * 8 + 2 * q;   // channel pair within the chunk
+                float xa0 = 0.f, xa1 = 0.f, xb0_ = 0.f, xb1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < kBranches; ++i) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ks = 0; ks < KSU; ++ks) {
+                        const uint2 b = wu[((i * 2 + cg) * 32 + lane) * KSU + ks];
+                        mma_bf16(c, ahi[ks][0], ahi[ks][1], ahi[ks][2], ahi[ks][3], b.x, b.y);
+                        mma_bf16(c, alo[ks][0], alo[ks][1], alo[ks][2], alo[ks][3], b.x, b.y);
+                    }
+                    const float2 gm = *reinterpret_cast<const float2*>(gam + i * kCh + ch);
+                    const int row = i * kTT + 16 * mt2 + g;
+                    float ra0, ra1, rb0, rb1;
+                    unf2(bf2_to_f2(lds32(rb + swz(row, ch >> 3) + 4 * q)), ra0, ra1);
+                    unf2(bf2_to_f2(lds32(rb + swz(row + 8, ch >> 3) + 4 * q)), rb0, rb1);
+                    const float wa = inv2[i][0], wb2 = inv2[i][1];
+                    xa0 = fmaf(1.0f + tanh_approx(c[0]), gm.x * wa * ra0, xa0);
+                    xa1 = fmaf(1.0f + tanh_approx(c[1]), gm.y * wa * ra1, xa1);
+                    xb0_ = fmaf(1.0f + tanh_approx(c[2]), gm.x * wb2 * rb0, xb0_);
+                    xb1 = fmaf(1.0f + tanh_approx(c[3]), gm.y * wb2 * rb1, xb1);
+                }
+                sts32(xb + swz32(g, cg * 16 + 4 * q), pack_bf2(xa0, xa1));
+                sts32(xb + swz32(g + 8, cg * 16 + 4 * q), pack_bf2(xb0_, xb1));
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sempty[st]);
+                mbar_arrive(&wempty[wc % kWStages]);
+            }
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                if (t0 + 16 * mt2 < N) tma_store_2d(&tm_x, xb, j * kCh + cq * 16, t0 + 16 * mt2);
+                bulk_commit();
+            }
+            ++sc;
+            ++wc;
+            ++xc;
+        }
+    }
+    if (lane == 0) bulk_wait_all();
+}
+
+// ---- packing ---------------------------------------------------------------------------------
+
+// Fragment section of the tiled kernel: J chunks of down-projection B fragments (γ folded),
+// then J chunks of W_u B fragments (×½) each followed by γ/8 of the chunk's channels.
+template <int NTD, int KSU>
+__global__ void pack_tiled_kernel(int D, int r, const float* __restrict__ gamma,
+                                  const float* __restrict__ wd, const float* __restrict__ wu,
+                                  const float* __restrict__ ww, char* __restrict__ frag) {
+    using C = TiledCfg<NTD, KSU>;
+    const int J = D / kCh;
+    const size_t K = size_t(kBranches) * D;
+    const int n_down = kBranches * 4 * NTD * 32;      // uint2 units per chunk
+    const int n_up = 32 * KSU * 32;                   // uint2 units per chunk
+    const int n_gam = kBranches * kCh;                // floats per chunk
+    const size_t per_chunk = size_t(n_down + n_up + n_gam);
+    const size_t total = per_chunk * J;
+    for (size_t e = blockIdx.x * size_t(blockDim.x) + threadIdx.x; e < total;
+         e += size_t(gridDim.x) * blockDim.x) {
+        const int j = int(e / per_chunk);
+        int u = int(e - size_t(j) * per_chunk);
+        if (u < n_down) {
+            // u = ((i*4 + ks)*NTD + nt)*32 + lane
+            const int lane = u & 31, rest = u >> 5;
+            const int nt = rest % NTD, iks = rest / NTD;
+            const int ks = iks & 3, i = iks >> 2;
+            const int n = nt * 8 + (lane >> 2);
+            const size_t m0 = size_t(i) * D + size_t(j) * kCh + ks * 16 + 2 * (lane & 3);
+            const int koff[4] = {0, 1, 8, 9};
+            __nv_bfloat16* dst =
+                reinterpret_cast<__nv_bfloat16*>(frag + size_t(j) * C::kDownChunk) + size_t(u) * 4;
+            for (int t = 0; t < 4; ++t) {
+                const size_t m = m0 + koff[t];
+                float v = 0.f;
+                if (n < r) v = wd[size_t(n) * K + m] * gamma[m];
+                else if (n < r + 4) v = ww[size_t(n - r) * K + m] * gamma[m];
+                dst[t] = __float2bfloat16_rn(v);
+            }
+        } else if ((u -= n_down) < n_up) {
+            // u = ((((cq*4 + i)*2 + cg)*32 + lane)*KSU + ks
+            const int ks = u % KSU, rest = u / KSU;
+            const int lane = rest & 31, r2 = rest >> 5;
+            const int cg = r2 & 1, i = (r2 >> 1) & 3, cq = r2 >> 3;
+            const size_t m = size_t(i) * D + size_t(j) * kCh + cq * 16 + cg * 8 + (lane >> 2);
+            const int k0 = ks * 16 + 2 * (lane & 3);
+            const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(
+                                     frag + size_t(J) * C::kDownChunk + size_t(j) * C::kUpChunk) +
+                                 size_t(u) * 4;
+            for (int t = 0; t < 4; ++t)
+                dst[t] = __float2bfloat16_rn(kk[t] < r ? 0.5f * wu[m * size_t(r) + kk[t]] : 0.f);
+        } else {
+            u -= n_up;
+            const int i = u / kCh, c = u - i * kCh;
+            float* dst = reinterpret_cast<float*>(frag + size_t(J) * C::kDownChunk +
+                                                  size_t(j) * C::kUpChunk + C::kUpFrag);
+            dst[u] = 0.125f * gamma[size_t(i) * D + size_t(j) * kCh + c];
+        }
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------------------
+
+// R as {channel within a 64-channel chunk, token, branch, chunk}: the box {64, tok_box, br_box, 1}
+// lands as rows (branch, token) of 128 bytes, 128-byte swizzled.
+bool make_map_R(CUtensorMap* m, const void* R, int64_t N, int D, int tok_box, int br_box) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {cuuint64_t(kCh), cuuint64_t(N), 4, cuuint64_t(D / kCh)};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 8, cuuint64_t(D) * 2, cuuint64_t(kCh) * 2};
+    const cuuint32_t box[4] = {cuuint32_t(kCh), cuuint32_t(tok_box), cuuint32_t(br_box), 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(R), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// A [N, D] bf16 matrix (y or x) with box {box_ch, box_tok}.
+bool make_map_nd(CUtensorMap* m, const void* p, int64_t N, int D, int box_ch, int box_tok,
+                 CUtensorMapSwizzle sw) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(N)};
+    const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(box_ch), cuuint32_t(box_tok)};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool WRITE, int NTD, int KSU>
+cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
+                     const float* s_prev, const char* frag, void* x, float* s_out,
+                     cudaStream_t st) {
+    using C = TiledCfg<NTD, KSU>;
+    CUtensorMap mR, mRs, my, mx;
+    memset(&mRs, 0, sizeof(mRs));
+    memset(&my, 0, sizeof(my));
+    if (!make_map_R(&mR, R, N, D, kTT, kBranches)) return cudaErrorInvalidValue;
+    if (WRITE && !make_map_R(&mRs, R, N, D, 16, 1)) return cudaErrorInvalidValue;
+    if (WRITE && !make_map_nd(&my, y, N, D, kCh, kTT, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!make_map_nd(&mx, x, N, D, 16, 16, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
+    auto kern = gr_tiled_kernel<WRITE, NTD, KSU>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (N + kTT - 1) / kTT;
+    const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
+    kern<<<unsigned(grid), kThreadsT, C::kSmem, st>>>(mR, mRs, my, mx, int(N), D, r, eps, s_prev,
+                                                      frag, s_out);
+    return cudaGetLastError();
+}
+
+template <int NTD, int KSU>
+cudaError_t launch_k(int64_t N, int D, int r, float eps, void* R, const void* y,
+                     const float* s_prev, const char* frag, void* x, float* s_out,
+                     cudaStream_t st) {
+    return y ? launch_t<true, NTD, KSU>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st)
+             : launch_t<false, NTD, KSU>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st);
+}
+
+}  // namespace
+
+bool tiled_supported(int D, int r) {
+    return D >= kCh && D % kCh == 0 && r >= 1 && r <= kMaxTiledRank;
+}
+
+int64_t tiled_max_tokens() { return int64_t(0x7fffffff) - kTT; }
+
+// The two instantiations: r <= 12 (NTD 2, KSU 1) is served by NTD 3; r <= 16 by (3, 1); r <= 32
+// by (5, 2). Padded rows and k columns are zero in the packed fragments.
+static void tiled_cfg(int r, int& ntd, int& ksu) {
+    if (r <= 16) { ntd = 3; ksu = 1; }
+    else { ntd = 5; ksu = 2; }
+}
+
+size_t tiled_frag_bytes(int D, int r) {
+    int ntd, ksu;
+    tiled_cfg(r, ntd, ksu);
+    const size_t J = size_t(D / kCh);
+    return ntd == 3 ? J * (TiledCfg<3, 1>::kDownChunk + TiledCfg<3, 1>::kUpChunk)
+                    : J * (TiledCfg<5, 2>::kDownChunk + TiledCfg<5, 2>::kUpChunk);
+}
+
+cudaError_t launch_pack_tiled(int D, int r, const float* gamma, const float* wd, const float* wu,
+                              const float* ww, void* frag, cudaStream_t st) {
+    int ntd, ksu;
+    tiled_cfg(r, ntd, ksu);
+    const size_t total = tiled_frag_bytes(D, r) / 8 + 1;
+    const int threads = 256;
+    const size_t want = (total + threads - 1) / threads;
+    const size_t cap = size_t(sm_count()) * 8;
+    const int blocks = int(want < cap ? want : cap);
+    if (ntd == 3)
+        pack_tiled_kernel<3, 1><<<blocks, threads, 0, st>>>(D, r, gamma, wd, wu, ww,
+                                                            static_cast<char*>(frag));
+    else
+        pack_tiled_kernel<5, 2><<<blocks, threads, 0, st>>>(D, r, gamma, wd, wu, ww,
+                                                            static_cast<char*>(frag));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
+                              const float* s_prev, const void* packed, void* x, float* s_out,
+                              cudaStream_t st) {
+    if (!tiled_supported(D, r) || N < 1 || N > tiled_max_tokens()) return cudaErrorInvalidValue;
+    const Layout L = make_layout(D, r, GR_BF16);
+    const char* frag = static_cast<const char*>(packed) + L.frag;
+    int ntd, ksu;
+    tiled_cfg(r, ntd, ksu);
+    if (ntd == 3) return launch_k<3, 1>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st);
+    return launch_k<5, 2>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st);
+}
+
+int tiled_status(bool clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_status, sizeof(v)) != cudaSuccess) return -1;
+    if (clear && v) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_wait_status, &z, sizeof(z)) != cudaSuccess) return -1;
+    }
+    return int(v);
+}
+
+}  // namespace gr

@@ -123,13 +123,16 @@ def test_calls_validate_before_any_launch(lib):
 @pytest.mark.parametrize("D,r,dtype,path", [
     (4096, 16, gr.GR_BF16, "fused_bf16"), (2048, 16, gr.GR_BF16, "fused_bf16"),
     (256, 8, gr.GR_BF16, "fused_bf16"), (512, 1, gr.GR_BF16, "fused_bf16"),
-    (1024, 12, gr.GR_BF16, "fused_bf16"), (7168, 32, gr.GR_BF16, "generic"),
-    (4096, 32, gr.GR_BF16, "generic"), (4104, 16, gr.GR_BF16, "generic"),
-    (768, 16, gr.GR_BF16, "generic"), (8192, 16, gr.GR_BF16, "generic"),
+    (1024, 12, gr.GR_BF16, "fused_bf16"), (7168, 32, gr.GR_BF16, "tiled_bf16"),
+    (4096, 32, gr.GR_BF16, "tiled_bf16"), (4104, 16, gr.GR_BF16, "generic"),
+    (768, 16, gr.GR_BF16, "tiled_bf16"), (8192, 16, gr.GR_BF16, "tiled_bf16"),
+    (64, 1, gr.GR_BF16, "tiled_bf16"), (4096, 33, gr.GR_BF16, "generic"),
     (4096, 16, gr.GR_F32, "generic"), (8, 4, gr.GR_BF16, "generic")])
 def test_kernel_path_selection(lib, D, r, dtype, path):
-    """The fused tensor-core kernel takes bf16 shapes whose width splits into 1..16 CTAs of 256
-    channels (a power of two) with rank <= 16; every other valid shape runs the generic kernel."""
+    """The cluster tensor-core kernel takes bf16 shapes whose width splits into 1..16 CTAs of 256
+    channels (a power of two) with rank <= 16; the two-pass tensor-core kernel takes the other
+    bf16 shapes with D a multiple of 64 and rank <= 32; every other valid shape (fp32 states
+    included) runs the generic kernel."""
     sh = _shape(n=100, d=D, r=r, dt=dtype)
     assert lib.gr_kernel_path(ctypes.byref(sh)).decode() == path
     assert lib.gr_kernel_path(ctypes.byref(_shape(d=12))).decode() == "invalid"

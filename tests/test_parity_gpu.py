@@ -297,6 +297,39 @@ def test_fused_read_only(D, r, N):
     assert gr.device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("D,r,N", [(64, 1, 1), (192, 8, 31), (320, 12, 33), (448, 16, 65),
+                                   (768, 20, 100), (1536, 32, 257), (4096, 32, 300),
+                                   (6144, 24, 77), (7168, 32, 1000), (1536, 17, 10000)])
+def test_tiled_kernel_shapes(D, r, N):
+    """The two-pass kernel: D = 64 … 7168 (one to 112 channel chunks), both rank classes (up to
+    16 and up to 32), ragged last tiles (including a single token and a tile whose second
+    16-token half is empty), and more tiles than SMs (N = 10000)."""
+    w = wl.Workload("tiled", N, D, r, "bf16", y_std=0.5, seed=29)
+    assert gr.kernel_path(N, D, r, torch.bfloat16) == "tiled_bf16"
+    check(w, *fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    assert gr.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("D,r,N", [(320, 8, 45), (7168, 32, 100)])
+def test_tiled_read_only(D, r, N):
+    """gr_read on the two-pass kernel: R untouched, x and s against the oracle's read."""
+    w = wl.Workload("read", N, D, r, "bf16", y_std=0.5, seed=31)
+    R = wl.make_state(w)
+    p = wl.make_params(w, 1, weight_mult=5.0)
+    p["gamma"] = wl.make_random_gamma(w, 1)
+    Rt = to_torch(R)
+    assert gr.kernel_path(N, D, r, torch.bfloat16) == "tiled_bf16"
+    x, s = gr.read(Rt, _pack(p, "bf16", w.eps))
+    torch.cuda.synchronize()
+    assert torch.equal(Rt, to_torch(R))
+    pm = bf16_path_params(p)
+    xo, so = oracle.read(wl.to_f64(R), pm["gamma"], pm["w_down"], pm["w_up"], pm["w_write"],
+                         w.eps)
+    tol = MODELED_TOL["bf16"]
+    assert rel_rows(to_f64(x), xo) < tol["x"] and rel_rows(to_f64(s), so) < tol["s"]
+    assert gr.device_status(clear=True) == 0
+
+
 def test_deep_stack_chain():
     """96 chained sublayers (48 layers × token mixer, MLP) at N=8192, D=2048, r=16, bf16, fresh
     seeded y_l and weights per sublayer: gr_read, 95 fused steps, gr_write. Every sublayer's
