@@ -43,6 +43,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="prefill")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-tokens", type=int, default=None,
+                    help="run the workload's shape with this many tokens instead (small cases "
+                         "for profiling; the line then reports no ncu traffic)")
     return ap.parse_args(argv)
 
 
@@ -350,7 +353,7 @@ def run_gr(args, w) -> None:
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "kernel": path, "algorithmic_bytes_per_launch": alg_bytes,
-                "traffic": profiled_traffic(path, w.name)}
+                "traffic": None if args.n_tokens is not None else profiled_traffic(path, w.name)}
 
     # bandwidth reference: single-stream x += y on [N, D]
     xr = torch.zeros((w.n_tokens, w.d_model), dtype=tdt, device=dev)
@@ -431,6 +434,10 @@ def main(argv=None):
     if args.workload not in wl.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; one of {sorted(wl.WORKLOADS)}")
     w = wl.WORKLOADS[args.workload]
+    if args.n_tokens is not None:
+        if args.n_tokens < 1:
+            raise SystemExit("--n-tokens must be >= 1")
+        w = w.scaled(n_tokens=args.n_tokens)
     if args.impl == "reference":
         run_reference(args, w)
     else:

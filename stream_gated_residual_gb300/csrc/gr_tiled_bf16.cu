@@ -11,24 +11,28 @@
 // 64-channel chunks:
 //   pass 1 (forward over the chunks): TMA-load R [4 branches][32 tokens][64 ch] and y
 //     [32][64]; the write R' = RNE(R + s·y) in registers, stored back in place and sent to HBM by
-//     a per-warp TMA store; per-(token, branch) sums of R'² in registers; the down projection
-//     [W_d; W_w]·R' on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), one
-//     warp per (branch, 16-token m-tile) accumulating over all chunks, the B fragments (γ
-//     folded) streamed from L2 through a weight ring.
+//     a TMA store per (branch, 16-token m-tile); per-(token, branch) sums of R'² in registers;
+//     the down projection [W_d; W_w]·R' on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+//     accumulate). Warp (branch, m-tile, k-half) takes two of the chunk's four 16-channel
+//     k-steps and accumulates over all chunks; the B fragments (γ folded) stream from L2
+//     through a weight ring.
 //   owner step (once per tile): inv_i = 1/sqrt(ms_i + eps); z = ¼Σ_i inv_i·P_i, h = SiLU(z)
 //     and u = ¼Σ_i inv_i·Q_i, s = 2σ(u) — through shared memory, no cluster needed.
 //   pass 2 (backward over the chunks, so the R' chunks written last are read first, while
-//     they are still in L2): TMA-load R' again; the up projection W_u·h on the tensor cores
-//     (h as bf16 hi + lo, W_u pre-scaled by ½), σ as ½ + ½·tanh, and the combine; x leaves
-//     through per-warp TMA stores.
+//     some are still in L2): TMA-load R' again; the up projection W_u·h on the tensor cores
+//     (h as bf16 hi + lo, W_u pre-scaled by ½), σ as ½ + ½·tanh, and the combine. Warp
+//     (m-tile, 8-channel group) covers the four branches of its channels; x leaves through a
+//     per-warp TMA store.
 // The price is one more read of R' than the single traversal (about 40% more HBM traffic at
 // D = 7168); in exchange the tile needs no cluster and the weights never have to fit on chip.
 //
-// Roles: warps 0..7 compute, warp 8 (one lane) produces: it fills the state ring (R/R' + y,
+// Roles: warps 0..15 compute, warp 16 (one lane) produces: it fills the state ring (R/R' + y,
 // 20 KB a stage) and the weight ring, and before pass 2 of a tile it waits until the compute
-// warps report pass 1's R' stores complete. Every mbarrier wait is bounded; a wait that runs out
-// sets this unit's status word and a CTA-wide abort flag, after which the CTA's waits return at
-// once and the CTA finishes without blocking (its outputs are then invalid).
+// warps report pass 1's R' stores complete. Sixteen compute warps (rather than eight) are there
+// for latency hiding: each step of a chunk is a short dependent chain of shared-memory loads,
+// conversions and mma. Every mbarrier wait is bounded; a wait that runs out sets this unit's
+// status word and a CTA-wide abort flag, after which the CTA's waits return at once and the CTA
+// finishes without blocking (its outputs are then invalid).
 #include <cuda.h>
 #include <string.h>
 
@@ -40,15 +44,15 @@ namespace {
 
 constexpr int kTT = 32;                           // tokens per tile
 constexpr int kCh = 64;                           // channels per chunk
-constexpr int kCW = 8;                            // compute warps
+constexpr int kCW = 16;                           // compute warps
 constexpr int kCThreads = kCW * 32;
 constexpr int kThreadsT = kCThreads + 32;         // + the producer warp
-constexpr int kSStages = 4;                       // state ring depth
-constexpr int kWStages = 4;                       // weight ring depth
+constexpr int kSStages = 5;                       // state ring depth
+constexpr int kWStages = 3;                       // weight ring depth
 constexpr int kRChunk = kBranches * kTT * kCh * 2;  // 16 KB: R [4][32][64] bf16, 128B-swizzled
 constexpr int kYChunk = kTT * kCh * 2;              // 4 KB: y [32][64] bf16, 128B-swizzled
 constexpr int kStateStage = kRChunk + kYChunk;
-constexpr int kXBuf = 16 * 16 * 2;                // per warp: x [16 tok][16 ch], 32B-swizzled
+constexpr int kXBuf = 16 * 8 * 2;                 // per warp: x [16 tok][8 ch], unswizzled
 constexpr int kMaxTiledRank = 32;
 
 // Compile-time sizes for NTD = ceil((r+4)/8) down-projection n-tiles and KSU = ceil(r/16)
@@ -57,45 +61,63 @@ template <int NTD, int KSU> struct TiledCfg {
     static constexpr int kNP = 8 * NTD;                        // padded r + 4
     static constexpr int kHP = 16 * KSU;                       // padded r
     static constexpr int kDownChunk = kBranches * 4 * NTD * 256;  // [i][ks][nt][lane] uint2
-    static constexpr int kUpFrag = 32 * KSU * 256;             // [cq][i][cg][lane][ks] uint2
+    static constexpr int kUpFrag = 32 * KSU * 256;             // [co][i][lane][ks] uint2
     static constexpr int kUpChunk = kUpFrag + kBranches * kCh * 4;  // + gamma/8 [4][64] fp32
     static constexpr int kWStage = kDownChunk > kUpChunk ? kDownChunk : kUpChunk;
     static constexpr int off_state = 0;
     static constexpr int off_w = off_state + kSStages * kStateStage;
     static constexpr int off_x = off_w + kWStages * kWStage;
     static constexpr int off_red = off_x + kCW * 2 * kXBuf;
-    static constexpr int off_h = off_red + kBranches * kTT * kNP * 4;
+    static constexpr int off_ssq = off_red + 2 * kBranches * kTT * kNP * 4;
+    static constexpr int off_h = off_ssq + 2 * kBranches * kTT * 4;
     static constexpr int off_inv = off_h + kTT * kHP * 4;
-    static constexpr int off_bar = off_inv + 2 * kBranches * kTT * 4;
+    static constexpr int off_bar = off_inv + kBranches * kTT * 4;
     static constexpr int kBars = 2 * kSStages + 2 * kWStages + 1;
     static constexpr int off_abort = off_bar + kBars * 8;
     static constexpr int kSmem = off_abort + 16 + 1024;        // + slack for 1 KB alignment
 };
 
-// Bounded wait that gives up at once after any wait of this CTA has run out.
+// Bounded wait: one non-blocking test first (the common case: the data is there), then the
+// bounded wait, which gives up at once after any wait of this CTA has run out.
 __device__ __forceinline__ bool twait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
     if (*abort) return false;
     if (mbar_wait(bar, parity)) return true;
     *abort = 1u;
     return false;
 }
 
+// Position in a ring of S stages: the stage index and the parity of the round through the ring.
+template <int S> struct RingPos {
+    int st = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next() {
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ uint32_t lds32(const char* p) {
     return *reinterpret_cast<const uint32_t*>(p);
 }
 __device__ __forceinline__ void sts32(char* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
-// Byte offset of byte `b` (0..31) of row `row` in a 32B-swizzled box of 32-byte rows.
-__device__ __forceinline__ int swz32(int row, int b) {
-    const int off = row * 32 + b;
-    return off ^ ((off >> 3) & 0x10);
-}
 
 template <bool WRITE, int NTD, int KSU>
 __global__ void __launch_bounds__(kThreadsT, 1)
 gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {64, 32, 4, 1}
                 const __grid_constant__ CUtensorMap tm_Rs,  // R' stores, box {64, 16, 1, 1}
                 const __grid_constant__ CUtensorMap tm_y,   // y loads, box {64, 32}
-                const __grid_constant__ CUtensorMap tm_x,   // x stores, box {16, 16}
+                const __grid_constant__ CUtensorMap tm_x,   // x stores, box {8, 16}
                 int N, int D, int r, float eps, const float* __restrict__ s_prev,
                 const char* __restrict__ frag, float* __restrict__ s_out) {
     using C = TiledCfg<NTD, KSU>;
@@ -115,13 +137,12 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
     uint64_t* wempty = bars + 2 * kSStages + kWStages;
     uint64_t* t1done = bars + 2 * kSStages + 2 * kWStages;
     volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(smem + C::off_abort);
-    float* red = reinterpret_cast<float*>(smem + C::off_red);   // [4][32][kNP]
+    float* red = reinterpret_cast<float*>(smem + C::off_red);   // [k-half][4][32][kNP]
+    float* ssqb = reinterpret_cast<float*>(smem + C::off_ssq);  // [k-half][4][32]
     float* hbuf = reinterpret_cast<float*>(smem + C::off_h);    // [32][kHP]
-    // [2][4][32] by tile parity: a warp that runs ahead into the next tile's owner step must not
-    // overwrite the values a slower warp has yet to read at the start of this tile's pass 2
-    float* invb_base = reinterpret_cast<float*>(smem + C::off_inv);
-    auto sbuf = [&](uint32_t c) { return smem + C::off_state + int(c % kSStages) * kStateStage; };
-    auto wbuf = [&](uint32_t c) { return smem + C::off_w + int(c % kWStages) * C::kWStage; };
+    float* invb = reinterpret_cast<float*>(smem + C::off_inv);  // [4][32]
+    auto sbuf = [&](int st) { return smem + C::off_state + st * kStateStage; };
+    auto wbuf = [&](int st) { return smem + C::off_w + st * C::kWStage; };
 
     if (tid == 0) {
         for (int s = 0; s < kSStages; ++s) {
@@ -132,7 +153,7 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             mbar_init(&wfull[s], 1u);
             mbar_init(&wempty[s], uint32_t(kCW));
         }
-        mbar_init(t1done, uint32_t(kCW));
+        mbar_init(t1done, uint32_t(kCW / 2));
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -143,7 +164,9 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
     if (warp == kCW) {
         // ================================ producer =============================================
         if (lane != 0) return;
-        uint32_t sc = 0, wc = 0;  // fills issued on each ring
+        RingPos<kSStages> sp;   // next fill of each ring; a stage is refilled once the compute
+        RingPos<kWStages> wp;   // warps released the previous round's fill (after the first round)
+        bool s_wrapped = false, w_wrapped = false;
         uint32_t nt_local = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++nt_local) {
             const int t0 = tile * kTT;
@@ -156,56 +179,61 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 for (int jj = 0; jj < J; ++jj) {
                     const int j = pass == 0 ? jj : J - 1 - jj;
                     {   // state: R (pass 1) or R' (pass 2) chunk j, plus y chunk j in pass 1
-                        const int st = int(sc % kSStages);
-                        if (sc >= kSStages) twait(&sempty[st], ((sc / kSStages) + 1) & 1u, abort);
-                        char* b = sbuf(sc);
+                        const int st = sp.st;
+                        if (s_wrapped) twait(&sempty[st], sp.ph ^ 1u, abort);
+                        char* b = sbuf(st);
                         const bool with_y = WRITE && pass == 0;
                         mbar_expect_tx(&sfull[st], uint32_t(kRChunk + (with_y ? kYChunk : 0)));
                         tma_load_4d(b, &tm_R, 0, t0, 0, j, &sfull[st]);
                         if (with_y) tma_load_2d(b + kRChunk, &tm_y, j * kCh, t0, &sfull[st]);
-                        ++sc;
+                        sp.next();
+                        s_wrapped |= sp.st == 0;
                     }
                     {   // weights: down-projection fragments (pass 1) or W_u fragments + γ/8
-                        const int st = int(wc % kWStages);
-                        if (wc >= kWStages) twait(&wempty[st], ((wc / kWStages) + 1) & 1u, abort);
+                        const int st = wp.st;
+                        if (w_wrapped) twait(&wempty[st], wp.ph ^ 1u, abort);
                         const uint32_t bytes = uint32_t(pass == 0 ? C::kDownChunk : C::kUpChunk);
                         const char* src = pass == 0 ? down_frag + size_t(j) * C::kDownChunk
                                                     : up_frag + size_t(j) * C::kUpChunk;
                         mbar_expect_tx(&wfull[st], bytes);
-                        bulk_g2s(wbuf(wc), src, bytes, &wfull[st]);
-                        ++wc;
+                        bulk_g2s(wbuf(st), src, bytes, &wfull[st]);
+                        wp.next();
+                        w_wrapped |= wp.st == 0;
                     }
                 }
             }
         }
-        // drain: the last fill of every stage has landed before the CTA may exit
-        for (uint32_t f = sc > kSStages ? sc - kSStages : 0; f < sc; ++f)
-            mbar_wait(&sfull[f % kSStages], (f / kSStages) & 1u);
-        for (uint32_t f = wc > kWStages ? wc - kWStages : 0; f < wc; ++f)
-            mbar_wait(&wfull[f % kWStages], (f / kWStages) & 1u);
+        // drain: the last fill of every stage has landed before the CTA may exit (stage s was
+        // last filled in the current round if s < the next fill's index, else in the previous)
+        for (int s = 0; s < kSStages; ++s)
+            if (s < sp.st || s_wrapped) mbar_wait(&sfull[s], s < sp.st ? sp.ph : sp.ph ^ 1u);
+        for (int s = 0; s < kWStages; ++s)
+            if (s < wp.st || w_wrapped) mbar_wait(&wfull[s], s < wp.st ? wp.ph : wp.ph ^ 1u);
         return;
     }
 
     // ================================== compute warps ==========================================
     const int g = lane >> 2, q = lane & 3;
-    const int ib = warp & 3, mt = warp >> 2;      // pass 1: branch, m-tile
-    const int mt2 = warp & 1, cq = warp >> 1;     // pass 2: m-tile, 16-channel quarter
+    // pass 1: branch ib, m-tile mt, k-half kh (k-steps 2kh and 2kh+1 of every chunk); the two
+    // k-halves of one (branch, m-tile) meet at named barrier 2 + pair before its R' store
+    const int ib = warp & 3, mt = (warp >> 2) & 1, kh = warp >> 3, pair = warp & 7;
+    // pass 2: m-tile mt2, 8-channel group co of the chunk
+    const int mt2 = warp & 1, co = warp >> 1;
     const float inv_d = 1.0f / float(D);
     char* xb0 = smem + C::off_x + warp * 2 * kXBuf;
-    uint32_t sc = 0, wc = 0, xc = 0, tl = 0;
+    RingPos<kSStages> sr;   // next chunk to consume on each ring
+    RingPos<kWStages> wr;
+    uint32_t xc = 0;
 
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int t0 = tile * kTT;
-        float* invb = invb_base + int(tl & 1u) * kBranches * kTT;
         // ---------------------------------- pass 1 --------------------------------------------
-        uint64_t sp = f2(0.f, 0.f);   // s_prev of tokens g and g+8 of the m-tile, branch ib
+        float spa = 0.f, spb = 0.f;   // s_prev of tokens g and g+8 of the m-tile, branch ib
         if (WRITE) {
             const int ta = t0 + 16 * mt + g, tb = ta + 8;
-            sp = f2(ta < N ? s_prev[size_t(ta) * 4 + ib] : 0.f,
-                    tb < N ? s_prev[size_t(tb) * 4 + ib] : 0.f);
+            if (ta < N) spa = s_prev[size_t(ta) * 4 + ib];
+            if (tb < N) spb = s_prev[size_t(tb) * 4 + ib];
         }
-        float spa, spb;
-        unf2(sp, spa, spb);
         const uint64_t sa2 = f2(spa, spa), sb2 = f2(spb, spb);
         float acc[NTD][4];
 #pragma unroll
@@ -215,14 +243,15 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
         const int ya = 16 * mt + g, yb = ya + 8;                     // rows of the y box
         int prev_st = -1;
         for (int j = 0; j < J; ++j) {
-            const int st = int(sc % kSStages);
-            twait(&sfull[st], (sc / kSStages) & 1u, abort);
-            twait(&wfull[wc % kWStages], (wc / kWStages) & 1u, abort);
-            char* rb = sbuf(sc);
+            const int st = sr.st;
+            twait(&sfull[st], sr.ph, abort);
+            twait(&wfull[wr.st], wr.ph, abort);
+            char* rb = sbuf(st);
             const char* ybuf = rb + kRChunk;
-            const uint2* wd = reinterpret_cast<const uint2*>(wbuf(wc)) + ib * 4 * NTD * 32;
+            const uint2* wd = reinterpret_cast<const uint2*>(wbuf(wr.st)) + ib * 4 * NTD * 32;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            for (int kk = 0; kk < 2; ++kk) {
+                const int ks = 2 * kh + kk;
                 uint32_t a[4];
                 const int o[4] = {swz(rowa, 2 * ks) + 4 * q, swz(rowb, 2 * ks) + 4 * q,
                                   swz(rowa, 2 * ks + 1) + 4 * q, swz(rowb, 2 * ks + 1) + 4 * q};
@@ -247,11 +276,14 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty[wc % kWStages]);
+            if (lane == 0) mbar_arrive(&wempty[wr.st]);
             if (WRITE) {
+                // both k-halves of this (branch, m-tile) have written R' back before its store
                 fence_async_shared();
-                __syncwarp();
-                if (lane == 0) {
+                named_sync(2 + pair, 64);
+                if (kh == 1) {
+                    if (lane == 0) mbar_arrive(&sempty[st]);
+                } else if (lane == 0) {
                     // an m-tile wholly past the last token has nothing to store (empty group)
                     if (t0 + 16 * mt < N)
                         tma_store_4d(&tm_Rs, rb + (ib * kTT + 16 * mt) * 128, 0, t0 + 16 * mt, ib,
@@ -265,10 +297,10 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 mbar_arrive(&sempty[st]);
             }
             prev_st = st;
-            ++sc;
-            ++wc;
+            sr.next();
+            wr.next();
         }
-        if (lane == 0) {
+        if (lane == 0 && kh == 0) {
             if (WRITE) {
                 bulk_wait_all();       // every R' store of the tile has reached global memory
                 fence_async_global();
@@ -286,19 +318,17 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             qa += __shfl_xor_sync(0xffffffffu, qa, 2);
             qb += __shfl_xor_sync(0xffffffffu, qb, 1);
             qb += __shfl_xor_sync(0xffffffffu, qb, 2);
-            const float inva = rsqrtf(qa * inv_d + eps), invb_ = rsqrtf(qb * inv_d + eps);
-            float* ra = red + (ib * kTT + 16 * mt + g) * C::kNP;
+            const int ra_row = ib * kTT + 16 * mt + g;
+            float* ra = red + (kh * kBranches * kTT + ra_row) * C::kNP;
             float* rb_ = ra + 8 * C::kNP;
 #pragma unroll
             for (int n = 0; n < NTD; ++n) {
-                *reinterpret_cast<float2*>(ra + n * 8 + 2 * q) =
-                    make_float2(acc[n][0] * inva, acc[n][1] * inva);
-                *reinterpret_cast<float2*>(rb_ + n * 8 + 2 * q) =
-                    make_float2(acc[n][2] * invb_, acc[n][3] * invb_);
+                *reinterpret_cast<float2*>(ra + n * 8 + 2 * q) = make_float2(acc[n][0], acc[n][1]);
+                *reinterpret_cast<float2*>(rb_ + n * 8 + 2 * q) = make_float2(acc[n][2], acc[n][3]);
             }
             if (q == 0) {
-                invb[ib * kTT + 16 * mt + g] = inva;
-                invb[ib * kTT + 16 * mt + g + 8] = invb_;
+                ssqb[kh * kBranches * kTT + ra_row] = qa;
+                ssqb[kh * kBranches * kTT + ra_row + 8] = qb;
             }
         }
         named_sync(1, kCThreads);
@@ -306,10 +336,17 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             const int nk = r + 4;
             for (int it = tid; it < kTT * nk; it += kCThreads) {
                 const int tok = it / nk, n = it - tok * nk;
-                const float z = 0.25f * (red[(0 * kTT + tok) * C::kNP + n] +
-                                         red[(1 * kTT + tok) * C::kNP + n] +
-                                         red[(2 * kTT + tok) * C::kNP + n] +
-                                         red[(3 * kTT + tok) * C::kNP + n]);
+                float z = 0.f;
+#pragma unroll
+                for (int i = 0; i < kBranches; ++i) {
+                    const int row = i * kTT + tok;
+                    const float inv =
+                        rsqrtf((ssqb[row] + ssqb[kBranches * kTT + row]) * inv_d + eps);
+                    z = fmaf(inv, red[row * C::kNP + n] + red[(kBranches * kTT + row) * C::kNP + n],
+                             z);
+                    if (n == 0) invb[row] = inv;
+                }
+                z *= 0.25f;
                 const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
                 if (n < r) hbuf[tok * C::kHP + n] = z * sg;
                 else if (t0 + tok < N) s_out[size_t(t0 + tok) * 4 + (n - r)] = 2.0f * sg;
@@ -343,59 +380,71 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             inv2[i][0] = invb[i * kTT + 16 * mt2 + g];
             inv2[i][1] = invb[i * kTT + 16 * mt2 + g + 8];
         }
+        const int ch = co * 8 + 2 * q;   // this thread's channel pair within the chunk
         for (int jj = 0; jj < J; ++jj) {
             const int j = J - 1 - jj;
-            const int st = int(sc % kSStages);
-            twait(&sfull[st], (sc / kSStages) & 1u, abort);
-            twait(&wfull[wc % kWStages], (wc / kWStages) & 1u, abort);
-            const char* rb = sbuf(sc);
-            const char* wb = wbuf(wc);
-            const uint2* wu = reinterpret_cast<const uint2*>(wb) + cq * kBranches * 2 * 32 * KSU;
+            const int st = sr.st;
+            twait(&sfull[st], sr.ph, abort);
+            twait(&wfull[wr.st], wr.ph, abort);
+            const char* rb = sbuf(st);
+            const char* wb = wbuf(wr.st);
+            const uint2* wu = reinterpret_cast<const uint2*>(wb) + co * kBranches * 32 * KSU;
             const float* gam = reinterpret_cast<const float*>(wb + C::kUpFrag);  // [4][64], γ/8
             char* xb = xb0 + int(xc & 1u) * kXBuf;
             // the x buffer is free once the store issued from it two chunks ago has read it
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
+            // all of the chunk's mma first (hi and lo parts in separate accumulators, so no
+            // chain is longer than KSU), then the combine in packed fp32 pairs
+            float chi[kBranches][4], clo[kBranches][4];
 #pragma unroll
-            for (int cg = 0; cg < 2; ++cg) {
-                const int ch = cq * 16 + cg * 8 + 2 * q;   // channel pair within the chunk
-                float xa0 = 0.f, xa1 = 0.f, xb0_ = 0.f, xb1 = 0.f;
+            for (int i = 0; i < kBranches; ++i) {
+                const uint2 b = wu[(i * 32 + lane) * KSU];
+                mma_bf16_z(chi[i], ahi[0][0], ahi[0][1], ahi[0][2], ahi[0][3], b.x, b.y);
+                mma_bf16_z(clo[i], alo[0][0], alo[0][1], alo[0][2], alo[0][3], b.x, b.y);
+            }
+#pragma unroll
+            for (int ks = 1; ks < KSU; ++ks)
 #pragma unroll
                 for (int i = 0; i < kBranches; ++i) {
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int ks = 0; ks < KSU; ++ks) {
-                        const uint2 b = wu[((i * 2 + cg) * 32 + lane) * KSU + ks];
-                        mma_bf16(c, ahi[ks][0], ahi[ks][1], ahi[ks][2], ahi[ks][3], b.x, b.y);
-                        mma_bf16(c, alo[ks][0], alo[ks][1], alo[ks][2], alo[ks][3], b.x, b.y);
-                    }
-                    const float2 gm = *reinterpret_cast<const float2*>(gam + i * kCh + ch);
-                    const int row = i * kTT + 16 * mt2 + g;
-                    float ra0, ra1, rb0, rb1;
-                    unf2(bf2_to_f2(lds32(rb + swz(row, ch >> 3) + 4 * q)), ra0, ra1);
-                    unf2(bf2_to_f2(lds32(rb + swz(row + 8, ch >> 3) + 4 * q)), rb0, rb1);
-                    const float wa = inv2[i][0], wb2 = inv2[i][1];
-                    xa0 = fmaf(1.0f + tanh_approx(c[0]), gm.x * wa * ra0, xa0);
-                    xa1 = fmaf(1.0f + tanh_approx(c[1]), gm.y * wa * ra1, xa1);
-                    xb0_ = fmaf(1.0f + tanh_approx(c[2]), gm.x * wb2 * rb0, xb0_);
-                    xb1 = fmaf(1.0f + tanh_approx(c[3]), gm.y * wb2 * rb1, xb1);
+                    const uint2 b = wu[(i * 32 + lane) * KSU + ks];
+                    mma_bf16(chi[i], ahi[ks][0], ahi[ks][1], ahi[ks][2], ahi[ks][3], b.x, b.y);
+                    mma_bf16(clo[i], alo[ks][0], alo[ks][1], alo[ks][2], alo[ks][3], b.x, b.y);
                 }
-                sts32(xb + swz32(g, cg * 16 + 4 * q), pack_bf2(xa0, xa1));
-                sts32(xb + swz32(g + 8, cg * 16 + 4 * q), pack_bf2(xb0_, xb1));
+            uint64_t xa = f2(0.f, 0.f), xbv = f2(0.f, 0.f);
+            const uint64_t one2 = f2(1.0f, 1.0f);
+#pragma unroll
+            for (int i = 0; i < kBranches; ++i) {
+                const float2 gm = *reinterpret_cast<const float2*>(gam + i * kCh + ch);
+                const uint64_t g2 = f2(gm.x, gm.y);
+                const int row = i * kTT + 16 * mt2 + g;
+                const uint64_t ra = mul2(bf2_to_f2(lds32(rb + swz(row, co) + 4 * q)),
+                                         mul2(g2, f2(inv2[i][0], inv2[i][0])));
+                const uint64_t rbv = mul2(bf2_to_f2(lds32(rb + swz(row + 8, co) + 4 * q)),
+                                          mul2(g2, f2(inv2[i][1], inv2[i][1])));
+                float a0, a1, b0, b1;
+                unf2(add2(f2(chi[i][0], chi[i][1]), f2(clo[i][0], clo[i][1])), a0, a1);
+                unf2(add2(f2(chi[i][2], chi[i][3]), f2(clo[i][2], clo[i][3])), b0, b1);
+                const uint64_t ta = add2(f2(tanh_approx(a0), tanh_approx(a1)), one2);
+                const uint64_t tb = add2(f2(tanh_approx(b0), tanh_approx(b1)), one2);
+                xa = fma2(ta, ra, xa);
+                xbv = fma2(tb, rbv, xbv);
             }
+            sts32(xb + g * 16 + 4 * q, f2_to_bf2(xa));
+            sts32(xb + (g + 8) * 16 + 4 * q, f2_to_bf2(xbv));
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sempty[st]);
-                mbar_arrive(&wempty[wc % kWStages]);
+                mbar_arrive(&wempty[wr.st]);
             }
             fence_async_shared();
             __syncwarp();
             if (lane == 0) {
-                if (t0 + 16 * mt2 < N) tma_store_2d(&tm_x, xb, j * kCh + cq * 16, t0 + 16 * mt2);
+                if (t0 + 16 * mt2 < N) tma_store_2d(&tm_x, xb, j * kCh + co * 8, t0 + 16 * mt2);
                 bulk_commit();
             }
-            ++sc;
-            ++wc;
+            sr.next();
+            wr.next();
             ++xc;
         }
     }
@@ -440,11 +489,11 @@ __global__ void pack_tiled_kernel(int D, int r, const float* __restrict__ gamma,
                 dst[t] = __float2bfloat16_rn(v);
             }
         } else if ((u -= n_down) < n_up) {
-            // u = ((((cq*4 + i)*2 + cg)*32 + lane)*KSU + ks
+            // u = ((co*4 + i)*32 + lane)*KSU + ks
             const int ks = u % KSU, rest = u / KSU;
             const int lane = rest & 31, r2 = rest >> 5;
-            const int cg = r2 & 1, i = (r2 >> 1) & 3, cq = r2 >> 3;
-            const size_t m = size_t(i) * D + size_t(j) * kCh + cq * 16 + cg * 8 + (lane >> 2);
+            const int i = r2 & 3, co = r2 >> 2;
+            const size_t m = size_t(i) * D + size_t(j) * kCh + co * 8 + (lane >> 2);
             const int k0 = ks * 16 + 2 * (lane & 3);
             const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(
@@ -505,7 +554,7 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
     if (WRITE && !make_map_R(&mRs, R, N, D, 16, 1)) return cudaErrorInvalidValue;
     if (WRITE && !make_map_nd(&my, y, N, D, kCh, kTT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!make_map_nd(&mx, x, N, D, 16, 16, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
+    if (!make_map_nd(&mx, x, N, D, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
     auto kern = gr_tiled_kernel<WRITE, NTD, KSU>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
