@@ -47,12 +47,13 @@ constexpr int kCh = 64;                           // channels per chunk
 constexpr int kCW = 16;                           // compute warps
 constexpr int kCThreads = kCW * 32;
 constexpr int kThreadsT = kCThreads + 32;         // + the producer warp
-constexpr int kSStages = 5;                       // state ring depth
+constexpr int kSStages = 7;                       // state ring depth
 constexpr int kWStages = 3;                       // weight ring depth
 constexpr int kRChunk = kBranches * kTT * kCh * 2;  // 16 KB: R [4][32][64] bf16, 128B-swizzled
 constexpr int kYChunk = kTT * kCh * 2;              // 4 KB: y [32][64] bf16, 128B-swizzled
 constexpr int kStateStage = kRChunk + kYChunk;
 constexpr int kXBuf = 16 * 8 * 2;                 // per warp: x [16 tok][8 ch], unswizzled
+constexpr int kXBufs = 4;                         // x buffers per warp (stores in flight)
 constexpr int kMaxTiledRank = 32;
 
 // Compile-time sizes for NTD = ceil((r+4)/8) down-projection n-tiles and KSU = ceil(r/16)
@@ -67,8 +68,12 @@ template <int NTD, int KSU> struct TiledCfg {
     static constexpr int off_state = 0;
     static constexpr int off_w = off_state + kSStages * kStateStage;
     static constexpr int off_x = off_w + kWStages * kWStage;
-    static constexpr int off_red = off_x + kCW * 2 * kXBuf;
-    static constexpr int off_ssq = off_red + 2 * kBranches * kTT * kNP * 4;
+    // the owner step's partial sums [k-half][4][32][kNP] live in the state ring: between the
+    // end of a tile's pass 1 and the owner step's completion no state fill is in flight or issued
+    static constexpr int off_red = off_state;
+    static constexpr int kRedBytes = 2 * kBranches * kTT * kNP * 4;
+    static_assert(kRedBytes <= kSStages * kStateStage, "partial sums must fit in the state ring");
+    static constexpr int off_ssq = off_x + kCW * kXBufs * kXBuf;
     static constexpr int off_h = off_ssq + 2 * kBranches * kTT * 4;
     static constexpr int off_inv = off_h + kTT * kHP * 4;
     static constexpr int off_bar = off_inv + kBranches * kTT * 4;
@@ -153,7 +158,7 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             mbar_init(&wfull[s], 1u);
             mbar_init(&wempty[s], uint32_t(kCW));
         }
-        mbar_init(t1done, uint32_t(kCW / 2));
+        mbar_init(t1done, 1u);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -172,7 +177,8 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             const int t0 = tile * kTT;
             for (int pass = 0; pass < 2; ++pass) {
                 if (pass == 1) {
-                    // pass 2 reads back the R' that pass 1 stored through the async proxy
+                    // pass 2 reads back the R' that pass 1 stored through the async proxy, and
+                    // its fills reuse the ring the owner step borrowed for its partial sums
                     twait(t1done, nt_local & 1u, abort);
                     fence_async_global();
                 }
@@ -220,7 +226,7 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
     // pass 2: m-tile mt2, 8-channel group co of the chunk
     const int mt2 = warp & 1, co = warp >> 1;
     const float inv_d = 1.0f / float(D);
-    char* xb0 = smem + C::off_x + warp * 2 * kXBuf;
+    char* xb0 = smem + C::off_x + warp * kXBufs * kXBuf;
     RingPos<kSStages> sr;   // next chunk to consume on each ring
     RingPos<kWStages> wr;
     uint32_t xc = 0;
@@ -300,15 +306,15 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             sr.next();
             wr.next();
         }
-        if (lane == 0 && kh == 0) {
-            if (WRITE) {
-                bulk_wait_all();       // every R' store of the tile has reached global memory
-                fence_async_global();
-                if (prev_st >= 0) mbar_arrive(&sempty[prev_st]);
-            }
-            mbar_arrive(t1done);
+        if (WRITE && lane == 0 && kh == 0) {
+            bulk_wait_all();           // every R' store of the tile has reached global memory
+            fence_async_global();
+            if (prev_st >= 0) mbar_arrive(&sempty[prev_st]);
         }
         // ---------------------------------- owner step ----------------------------------------
+        // every warp is done with pass 1's stages and every store has read them: the partial
+        // sums may now overwrite the ring
+        named_sync(1, kCThreads);
         {
             float s0, s1, s2, s3;
             unf2(ssa, s0, s1);
@@ -353,6 +359,8 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             }
         }
         named_sync(1, kCThreads);
+        // the partial sums are consumed: the producer may start pass 2's fills
+        if (tid == 0) mbar_arrive(t1done);
         // ---------------------------------- pass 2 --------------------------------------------
         uint32_t ahi[KSU][4], alo[KSU][4];
         {
@@ -390,9 +398,9 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             const char* wb = wbuf(wr.st);
             const uint2* wu = reinterpret_cast<const uint2*>(wb) + co * kBranches * 32 * KSU;
             const float* gam = reinterpret_cast<const float*>(wb + C::kUpFrag);  // [4][64], γ/8
-            char* xb = xb0 + int(xc & 1u) * kXBuf;
-            // the x buffer is free once the store issued from it two chunks ago has read it
-            if (lane == 0) bulk_wait_read<1>();
+            char* xb = xb0 + int(xc % kXBufs) * kXBuf;
+            // the x buffer is free once the store issued from it kXBufs chunks ago has read it
+            if (lane == 0) bulk_wait_read<kXBufs - 1>();
             __syncwarp();
             // all of the chunk's mma first (hi and lo parts in separate accumulators, so no
             // chain is longer than KSU), then the combine in packed fp32 pairs
