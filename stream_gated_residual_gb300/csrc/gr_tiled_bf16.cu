@@ -20,7 +20,10 @@
 //     and u = ¼Σ_i inv_i·Q_i, s = 2σ(u) — through shared memory, no cluster needed.
 //   pass 2 (backward over the chunks, so the R' chunks written last are read first, while
 //     some are still in L2): TMA-load R' again; the up projection W_u·h on the tensor cores
-//     (h as bf16 hi + lo, W_u pre-scaled by ½), σ as ½ + ½·tanh, and the combine. Warp
+//     in fp16 (½·W_u packed as fp16; each token's h row scaled by an exact power of two that
+//     keeps it below 2^15, undone on the fp32 accumulator), σ as ½ + ½·tanh, and the combine.
+//     fp16 carries 11 significant bits for both operands, so one mma per k-step does what the
+//     cluster kernel does with bf16 hi + lo parts of h (and rounds W_u more finely). Warp
 //     (m-tile, 8-channel group) covers the four branches of its channels; x leaves through a
 //     per-warp TMA store.
 // The price is one more read of R' than the single traversal (about 40% more HBM traffic at
@@ -62,7 +65,7 @@ template <int NTD, int KSU> struct TiledCfg {
     static constexpr int kNP = 8 * NTD;                        // padded r + 4
     static constexpr int kHP = 16 * KSU;                       // padded r
     static constexpr int kDownChunk = kBranches * 4 * NTD * 256;  // [i][ks][nt][lane] uint2
-    static constexpr int kUpFrag = 32 * KSU * 256;             // [co][i][lane][ks] uint2
+    static constexpr int kUpFrag = 32 * KSU * 256;             // [co][i][lane][ks] uint2 (fp16)
     static constexpr int kUpChunk = kUpFrag + kBranches * kCh * 4;  // + gamma/8 [4][64] fp32
     static constexpr int kWStage = kDownChunk > kUpChunk ? kDownChunk : kUpChunk;
     static constexpr int off_state = 0;
@@ -362,25 +365,43 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
         // the partial sums are consumed: the producer may start pass 2's fills
         if (tid == 0) mbar_arrive(t1done);
         // ---------------------------------- pass 2 --------------------------------------------
-        uint32_t ahi[KSU][4], alo[KSU][4];
+        uint32_t ah[KSU][4];     // fp16 A fragments of the scaled h
+        uint64_t unscale_a, unscale_b;   // 2^e of tokens g and g+8, as fp32 pairs
         {
             const float* ha = hbuf + (16 * mt2 + g) * C::kHP;
             const float* hb = ha + 8 * C::kHP;
+            float2 v[KSU][4];
+            float ma = 0.f, mb = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KSU; ++ks) {
-                const float2 v[4] = {*reinterpret_cast<const float2*>(ha + ks * 16 + 2 * q),
-                                     *reinterpret_cast<const float2*>(hb + ks * 16 + 2 * q),
-                                     *reinterpret_cast<const float2*>(ha + ks * 16 + 2 * q + 8),
-                                     *reinterpret_cast<const float2*>(hb + ks * 16 + 2 * q + 8)};
+                v[ks][0] = *reinterpret_cast<const float2*>(ha + ks * 16 + 2 * q);
+                v[ks][1] = *reinterpret_cast<const float2*>(hb + ks * 16 + 2 * q);
+                v[ks][2] = *reinterpret_cast<const float2*>(ha + ks * 16 + 2 * q + 8);
+                v[ks][3] = *reinterpret_cast<const float2*>(hb + ks * 16 + 2 * q + 8);
+                ma = fmaxf(ma, fmaxf(fmaxf(fabsf(v[ks][0].x), fabsf(v[ks][0].y)),
+                                     fmaxf(fabsf(v[ks][2].x), fabsf(v[ks][2].y))));
+                mb = fmaxf(mb, fmaxf(fmaxf(fabsf(v[ks][1].x), fabsf(v[ks][1].y)),
+                                     fmaxf(fabsf(v[ks][3].x), fabsf(v[ks][3].y))));
+            }
+            // the four lanes of a quad hold the whole row of a token
+            ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+            ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            // e = max(0, exponent(max) - 14): the scaled row stays below 2^15 (fp16 max 65504)
+            const int ea = min(max(((__float_as_int(ma) >> 23) & 0xff) - 127 - 14, 0), 126);
+            const int eb = min(max(((__float_as_int(mb) >> 23) & 0xff) - 127 - 14, 0), 126);
+            const float sa = __int_as_float((127 - ea) << 23), sb = __int_as_float((127 - eb) << 23);
+            const float ua = __int_as_float((127 + ea) << 23), ub = __int_as_float((127 + eb) << 23);
+            unscale_a = f2(ua, ua);
+            unscale_b = f2(ub, ub);
+#pragma unroll
+            for (int ks = 0; ks < KSU; ++ks)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t hi = pack_bf2(v[e].x, v[e].y);
-                    float hx, hy;
-                    unf2(bf2_to_f2(hi), hx, hy);
-                    ahi[ks][e] = hi;
-                    alo[ks][e] = pack_bf2(v[e].x - hx, v[e].y - hy);
+                    const float sc = (e & 1) ? sb : sa;
+                    ah[ks][e] = pack_h2(v[ks][e].x * sc, v[ks][e].y * sc);
                 }
-            }
         }
         float inv2[kBranches][2];
 #pragma unroll
@@ -402,22 +423,19 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             // the x buffer is free once the store issued from it kXBufs chunks ago has read it
             if (lane == 0) bulk_wait_read<kXBufs - 1>();
             __syncwarp();
-            // all of the chunk's mma first (hi and lo parts in separate accumulators, so no
-            // chain is longer than KSU), then the combine in packed fp32 pairs
-            float chi[kBranches][4], clo[kBranches][4];
+            // all of the chunk's mma first, then the combine in packed fp32 pairs
+            float cg4[kBranches][4];
 #pragma unroll
             for (int i = 0; i < kBranches; ++i) {
                 const uint2 b = wu[(i * 32 + lane) * KSU];
-                mma_bf16_z(chi[i], ahi[0][0], ahi[0][1], ahi[0][2], ahi[0][3], b.x, b.y);
-                mma_bf16_z(clo[i], alo[0][0], alo[0][1], alo[0][2], alo[0][3], b.x, b.y);
+                mma_f16_z(cg4[i], ah[0][0], ah[0][1], ah[0][2], ah[0][3], b.x, b.y);
             }
 #pragma unroll
             for (int ks = 1; ks < KSU; ++ks)
 #pragma unroll
                 for (int i = 0; i < kBranches; ++i) {
                     const uint2 b = wu[(i * 32 + lane) * KSU + ks];
-                    mma_bf16(chi[i], ahi[ks][0], ahi[ks][1], ahi[ks][2], ahi[ks][3], b.x, b.y);
-                    mma_bf16(clo[i], alo[ks][0], alo[ks][1], alo[ks][2], alo[ks][3], b.x, b.y);
+                    mma_f16(cg4[i], ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3], b.x, b.y);
                 }
             uint64_t xa = f2(0.f, 0.f), xbv = f2(0.f, 0.f);
             const uint64_t one2 = f2(1.0f, 1.0f);
@@ -431,8 +449,8 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 const uint64_t rbv = mul2(bf2_to_f2(lds32(rb + swz(row + 8, co) + 4 * q)),
                                           mul2(g2, f2(inv2[i][1], inv2[i][1])));
                 float a0, a1, b0, b1;
-                unf2(add2(f2(chi[i][0], chi[i][1]), f2(clo[i][0], clo[i][1])), a0, a1);
-                unf2(add2(f2(chi[i][2], chi[i][3]), f2(clo[i][2], clo[i][3])), b0, b1);
+                unf2(mul2(f2(cg4[i][0], cg4[i][1]), unscale_a), a0, a1);
+                unf2(mul2(f2(cg4[i][2], cg4[i][3]), unscale_b), b0, b1);
                 const uint64_t ta = add2(f2(tanh_approx(a0), tanh_approx(a1)), one2);
                 const uint64_t tb = add2(f2(tanh_approx(b0), tanh_approx(b1)), one2);
                 xa = fma2(ta, ra, xa);
@@ -461,8 +479,9 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
 
 // ---- packing ---------------------------------------------------------------------------------
 
-// Fragment section of the tiled kernel: J chunks of down-projection B fragments (γ folded),
-// then J chunks of W_u B fragments (×½) each followed by γ/8 of the chunk's channels.
+// Fragment section of the tiled kernel: J chunks of down-projection B fragments (bf16, γ
+// folded), then J chunks of W_u B fragments (fp16, ×½, clamped to ±65504) each followed by γ/8
+// of the chunk's channels.
 template <int NTD, int KSU>
 __global__ void pack_tiled_kernel(int D, int r, const float* __restrict__ gamma,
                                   const float* __restrict__ wd, const float* __restrict__ wu,
@@ -504,11 +523,13 @@ __global__ void pack_tiled_kernel(int D, int r, const float* __restrict__ gamma,
             const size_t m = size_t(i) * D + size_t(j) * kCh + co * 8 + (lane >> 2);
             const int k0 = ks * 16 + 2 * (lane & 3);
             const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(
-                                     frag + size_t(J) * C::kDownChunk + size_t(j) * C::kUpChunk) +
-                                 size_t(u) * 4;
-            for (int t = 0; t < 4; ++t)
-                dst[t] = __float2bfloat16_rn(kk[t] < r ? 0.5f * wu[m * size_t(r) + kk[t]] : 0.f);
+            __half* dst = reinterpret_cast<__half*>(frag + size_t(J) * C::kDownChunk +
+                                                    size_t(j) * C::kUpChunk) +
+                          size_t(u) * 4;
+            for (int t = 0; t < 4; ++t) {
+                const float v = kk[t] < r ? 0.5f * wu[m * size_t(r) + kk[t]] : 0.f;
+                dst[t] = __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
+            }
         } else {
             u -= n_up;
             const int i = u / kCh, c = u - i * kCh;

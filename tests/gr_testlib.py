@@ -45,11 +45,13 @@ def max_abs(a, b) -> float:
     return float(np.max(np.abs(a - b))) if a.size else 0.0
 
 
-def bf16_path_params(p: dict) -> dict:
+def bf16_path_params(p: dict, w_up: str = "bf16") -> dict:
     """The parameters the bf16 path computes with, written as oracle inputs: W_d and W_w with
     gamma folded in and rounded to bf16 (fp32 product, nearest even), divided back by gamma in
-    fp64 so that the oracle's W·(γ ⊙ R) reproduces the folded weight; W_u rounded to bf16.
-    Computed here from the fp32 inputs, never read back from the GPU."""
+    fp64 so that the oracle's W·(γ ⊙ R) reproduces the folded weight; W_u rounded to bf16
+    (w_up="bf16", the cluster kernel) or, as ½·W_u, to fp16 (w_up="f16", the two-pass kernel,
+    which packs ½·W_u as fp16 clamped to ±65504). Computed here from the fp32 inputs, never
+    read back from the GPU."""
     K = p["w_down"].shape[1]
     g = np.asarray(p["gamma"], dtype=np.float32).reshape(-1)
     assert g.size == K and np.all(g != 0)
@@ -58,9 +60,21 @@ def bf16_path_params(p: dict) -> dict:
         Wf = wl.round_to_bf16((np.asarray(W, dtype=np.float32) * g[None, :]).astype(np.float32))
         return Wf.astype(np.float64) / g.astype(np.float64)[None, :]
 
+    wu32 = np.asarray(p["w_up"], dtype=np.float32)
+    if w_up == "bf16":
+        wu = wl.round_to_bf16(wu32).astype(np.float64)
+    elif w_up == "f16":
+        half = np.clip(np.float32(0.5) * wu32, -65504.0, 65504.0).astype(np.float16)
+        wu = 2.0 * half.astype(np.float64)
+    else:
+        raise ValueError(w_up)
     return {"gamma": np.asarray(p["gamma"], dtype=np.float64), "w_down": fold(p["w_down"]),
-            "w_up": wl.round_to_bf16(np.asarray(p["w_up"], dtype=np.float32)).astype(np.float64),
-            "w_write": fold(p["w_write"])}
+            "w_up": wu, "w_write": fold(p["w_write"])}
+
+
+def path_params(p: dict, kernel_path: str) -> dict:
+    """bf16_path_params for the kernel that serves a shape (gr.kernel_path's name)."""
+    return bf16_path_params(p, "f16" if kernel_path == "tiled_bf16" else "bf16")
 
 
 def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:
@@ -73,4 +87,4 @@ def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:
 
 
 __all__ = ["TOL", "TORCH_DTYPE", "to_torch", "to_f64", "params_to_torch", "rel_rows", "max_abs",
-           "sample_rows", "bf16_path_params", "wl"]
+           "sample_rows", "bf16_path_params", "path_params", "wl"]

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from gr_testlib import TOL, TORCH_DTYPE, bf16_path_params, max_abs, params_to_torch, \
-    rel_rows, to_f64, to_torch
+    path_params, rel_rows, to_f64, to_torch
 from stream_gated_residual_gb300 import gr
 from stream_gated_residual_gb300 import workloads as wl
 
@@ -52,7 +52,10 @@ def fused_case(w: wl.Workload, n_tokens=None, weight_mult=1.0, random_gamma=Fals
     p = wl.make_params(w, 1, weight_mult)
     if random_gamma:
         p["gamma"] = wl.make_random_gamma(w, 1)
-    pm = bf16_path_params(p) if w.dtype == "bf16" else p
+    if w.dtype == "bf16":
+        pm = path_params(p, gr.kernel_path(N, w.d_model, w.rank, torch.bfloat16))
+    else:
+        pm = p
     Rt, yt, st = to_torch(R), to_torch(y), torch.from_numpy(s_prev).cuda()
     P = _pack(p, w.dtype, w.eps)
     x, s = gr.write_then_read(Rt, yt, st, P)
@@ -322,7 +325,7 @@ def test_tiled_read_only(D, r, N):
     x, s = gr.read(Rt, _pack(p, "bf16", w.eps))
     torch.cuda.synchronize()
     assert torch.equal(Rt, to_torch(R))
-    pm = bf16_path_params(p)
+    pm = bf16_path_params(p, "f16")
     xo, so = oracle.read(wl.to_f64(R), pm["gamma"], pm["w_down"], pm["w_up"], pm["w_write"],
                          w.eps)
     tol = MODELED_TOL["bf16"]
