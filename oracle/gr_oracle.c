@@ -245,6 +245,125 @@ int gro_round_significand(int64_t n, int bits, double *v)
     return 0;
 }
 
+/* ---- FP8 state (OCP e4m3 "e4m3fn" codes, one power-of-two scale per 32-channel block) ----
+ * The pages name FP8 storage of the widened state ("【论文解读】 Qwen3.8 Flash Next", §二.7)
+ * without a format; the repository's SPEC file, section "FP8 state", fixes the one used here.
+ * An e4m3 code is sign | 4 exponent bits (bias 7) | 3 fraction bits; exponent field 0 holds
+ * the subnormals m/8 · 2^-6; 0x7F and 0xFF are NaN; there are no infinities. */
+
+/* Value of one e4m3 code. */
+static double fp8_decode(uint8_t code)
+{
+    const int sign = code >> 7, E = (code >> 3) & 15, m = code & 7;
+    if (E == 15 && m == 7)
+        return NAN;
+    const double mag = E == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, E - 10);
+    return sign ? -mag : mag;
+}
+
+/* Nearest e4m3 code to w (ties to even), for |w| <= 448 (larger magnitudes saturate to 448). */
+static uint8_t fp8_encode(double w)
+{
+    if (isnan(w))
+        return 0x7F;
+    const uint8_t sign = signbit(w) ? 0x80 : 0;
+    double a = fabs(w);
+    if (a >= 448.0)
+        return sign | 0x7E;               /* 448 = 2^8 · 1.75: exponent field 15, fraction 6 */
+    if (a < ldexp(1.0, -6)) {             /* subnormal: a multiple of 2^-9 */
+        const double m = nearbyint(ldexp(a, 9)); /* 0 .. 8; 8 is the smallest normal, 2^-6 */
+        return sign | (uint8_t)m;
+    }
+    int E;
+    frexp(a, &E);                         /* a = f·2^E, 0.5 <= f < 1: binary exponent E-1 */
+    E -= 1;                               /* a in [2^E, 2^(E+1)) */
+    double m = nearbyint(ldexp(a, 3 - E)); /* 8 .. 16 */
+    if (m == 16.0) {
+        m = 8.0;
+        E += 1;
+    }
+    if (E + 7 > 15 || (E + 7 == 15 && m > 14.0))
+        return sign | 0x7E;               /* rounding went past 448 */
+    return sign | (uint8_t)(((E + 7) << 3) | ((int)m - 8));
+}
+
+/* Scale exponent of a block whose largest magnitude is a: the smallest e with a <= 448·2^e,
+ * clamped to [-127, 127] (a = 0 gives -127). */
+static int fp8_block_exponent(double a)
+{
+    if (!(a > 0.0))
+        return -127;
+    int E;
+    const double f = frexp(a, &E);        /* a = f·2^E, f in [0.5, 1): significand 2f */
+    int e = (E - 1) - 8;                  /* 448·2^e = 1.75·2^(e+8) */
+    if (2.0 * f > 1.75)
+        e += 1;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+/* Encode rows of D values (D a multiple of 32) into e4m3 codes [rows][D] and biased block
+ * exponents [rows][D/32] (scale 2^(b-127)). The inputs are exact fp32 values (the stored
+ * write result), so dividing by the power-of-two scale is exact. */
+int gro_fp8_encode(int64_t rows, int D, const double *v, uint8_t *codes, uint8_t *scales)
+{
+    if (rows < 0 || D < 32 || D % 32 || !v || !codes || !scales)
+        return -1;
+    const int nblk = D / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < rows; ++t) {
+        for (int k = 0; k < nblk; ++k) {
+            const double *vb = v + (size_t)t * D + (size_t)k * 32;
+            double a = 0.0;
+            for (int c = 0; c < 32; ++c)
+                if (fabs(vb[c]) > a)
+                    a = fabs(vb[c]);
+            const int e = fp8_block_exponent(a);
+            scales[(size_t)t * nblk + k] = (uint8_t)(e + 127);
+            for (int c = 0; c < 32; ++c)
+                codes[(size_t)t * D + (size_t)k * 32 + c] = fp8_encode(ldexp(vb[c], -e));
+        }
+    }
+    return 0;
+}
+
+/* Decode codes [rows][D] with block exponents [rows][D/32] into values. */
+int gro_fp8_decode(int64_t rows, int D, const uint8_t *codes, const uint8_t *scales, double *v)
+{
+    if (rows < 0 || D < 32 || D % 32 || !v || !codes || !scales)
+        return -1;
+    const int nblk = D / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < rows; ++t)
+        for (int c = 0; c < D; ++c)
+            v[(size_t)t * D + c] = ldexp(fp8_decode(codes[(size_t)t * D + c]),
+                                         (int)scales[(size_t)t * nblk + c / 32] - 127);
+    return 0;
+}
+
+/* The value of each single code 0..255 (for checks against other e4m3 implementations). */
+int gro_fp8_code_values(double *out)
+{
+    if (!out)
+        return -1;
+    for (int c = 0; c < 256; ++c)
+        out[c] = fp8_decode((uint8_t)c);
+    return 0;
+}
+
+/* Nearest e4m3 code of each value (|w| <= 448; ties to even), no block scale. */
+int gro_fp8_round_codes(int64_t n, const double *w, uint8_t *codes)
+{
+    if (n < 0 || !w || !codes)
+        return -1;
+    for (int64_t e = 0; e < n; ++e)
+        codes[e] = fp8_encode(w[e]);
+    return 0;
+}
+
 /* Single-stream residual add x += y (the bandwidth reference path), n elements. */
 int gro_residual_add(int64_t n, const double *y, double *x)
 {

@@ -40,8 +40,14 @@ def _load(path: str) -> ctypes.CDLL:
     L.gro_num_threads.argtypes = []
     L.gro_set_num_threads.argtypes = [i32]
     L.gro_set_num_threads.restype = None
+    U = ctypes.POINTER(ctypes.c_uint8)
+    L.gro_fp8_encode.argtypes = [i64, i32, P, U, U]
+    L.gro_fp8_decode.argtypes = [i64, i32, U, U, P]
+    L.gro_fp8_code_values.argtypes = [P]
+    L.gro_fp8_round_codes.argtypes = [i64, P, U]
     for f in ("gro_read", "gro_write", "gro_write_then_read", "gro_read_fixed_gates",
-              "gro_residual_add", "gro_num_threads", "gro_round_significand"):
+              "gro_residual_add", "gro_num_threads", "gro_round_significand", "gro_fp8_encode",
+              "gro_fp8_decode", "gro_fp8_code_values", "gro_fp8_round_codes"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -76,6 +82,11 @@ def _p(a: np.ndarray | None):
     if a is None:
         return None
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _pu8(a: np.ndarray):
+    assert a.dtype == np.uint8 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
 
 
 def _check(st: int, what: str) -> None:
@@ -155,6 +166,59 @@ def write_then_read(R, y, s_prev, params: dict, eps: float = 1e-6, store: str | 
                                      _p(gamma), _p(Wd), _p(Wu), _p(Ww), _p(R_out), _p(x), _p(s)),
            "write_then_read")
     return R_out, x, s
+
+
+# ---- FP8 state: e4m3 codes with one power-of-two scale per 32-channel block -----------------
+
+def fp8_encode(V):
+    """Encode a state [..., D] (D a multiple of 32; exact fp32 values) into e4m3 codes
+    (uint8, same shape) and biased block exponents (uint8, [..., D/32]; scale 2^(b-127))."""
+    V = _f64(V)
+    D = V.shape[-1]
+    rows = V.size // D if D else 0
+    codes = np.empty(V.shape, dtype=np.uint8)
+    scales = np.empty(V.shape[:-1] + (D // 32,), dtype=np.uint8)
+    _check(lib().gro_fp8_encode(rows, D, _p(V), _pu8(codes), _pu8(scales)), "fp8_encode")
+    return codes, scales
+
+
+def fp8_decode(codes, scales):
+    """Values of an FP8 state (codes [..., D], block exponents [..., D/32]) as float64."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    D = codes.shape[-1]
+    assert scales.shape == codes.shape[:-1] + (D // 32,)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _check(lib().gro_fp8_decode(codes.size // D if D else 0, D, _pu8(codes), _pu8(scales),
+                                _p(out)), "fp8_decode")
+    return out
+
+
+def fp8_code_values():
+    """The value of every e4m3 code 0..255 (NaN for 0x7F and 0xFF)."""
+    out = np.empty(256)
+    _check(lib().gro_fp8_code_values(_p(out)), "fp8_code_values")
+    return out
+
+
+def fp8_round_codes(w):
+    """Nearest e4m3 code of each value (no block scale; |w| <= 448, ties to even)."""
+    w = _f64(w)
+    codes = np.empty(w.shape, dtype=np.uint8)
+    _check(lib().gro_fp8_round_codes(w.size, _p(w), _pu8(codes)), "fp8_round_codes")
+    return codes
+
+
+def write_then_read_fp8(codes, scales, y, s_prev, params: dict, eps: float = 1e-6):
+    """Fused step on an FP8 state, modelling the storage: the write decodes R, forms R + s·y
+    with one fp32 rounding (as a fused multiply-add does), encodes the result block by block,
+    and the read sees the decoded stored values. Returns (codes', scales', x, s_next)."""
+    R = fp8_decode(codes, scales)
+    W = round_to_storage(write(R, y, s_prev), "f32")
+    c2, b2 = fp8_encode(W)
+    p = params
+    x, s = read(fp8_decode(c2, b2), p["gamma"], p["w_down"], p["w_up"], p["w_write"], eps)
+    return c2, b2, x, s
 
 
 def read_fixed_gates(R, gamma, G, eps: float = 1e-6):

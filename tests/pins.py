@@ -294,8 +294,110 @@ def pin_residual_add():
     assert np.array_equal(oracle.residual_add(a, b), a + b)
 
 
+# ---- FP8 state (SPEC R21: e4m3 codes, one power-of-two scale per 32-channel block) ----------
+
+def _torch_e4m3_values():
+    """Value of every e4m3 code by torch's float8_e4m3fn (a library conversion)."""
+    import torch
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_fp8_codes_match_torch():
+    """Every code decodes as torch's float8_e4m3fn does; rounding to the nearest code (ties to
+    even) agrees with torch's conversion on random values, subnormals and every exact tie."""
+    import torch
+    t = _torch_e4m3_values()
+    v = oracle.fp8_code_values()
+    assert np.array_equal(np.isnan(v), np.isnan(t))
+    assert np.array_equal(v[~np.isnan(v)], t[~np.isnan(t)])
+    vals = np.unique(t[~np.isnan(t)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(131)
+    w = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-0.03, 0.03, 20000),
+                        mids, -mids, vals]).astype(np.float32).astype(np.float64)
+    ct = torch.from_numpy(w).float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.fp8_round_codes(w), ct)
+
+
+def pin_fp8_block_scale():
+    """The block exponent is the smallest e with amax <= 448·2^e (closed-form cases and the
+    two defining inequalities on random blocks); an all-zero block gets the smallest scale."""
+    cases = {448.0: 0, 449.0: 1, 1.0: -8, 1.75: -8, 1.7500001: -7, 0.875: -9, 2.0 ** -100: -108,
+             3.0e38: 120}
+    for amax, e in cases.items():
+        V = np.zeros((1, 32))
+        V[0, 5] = -amax
+        _, b = oracle.fp8_encode(V)
+        assert int(b[0, 0]) - 127 == e, (amax, int(b[0, 0]) - 127, e)
+    _, b = oracle.fp8_encode(np.zeros((1, 64)))
+    assert np.all(b == 0)
+    rng = np.random.default_rng(137)
+    V = (rng.standard_normal((64, 4, 256)) * np.exp(rng.uniform(-20, 20, (64, 4, 1)))
+         ).astype(np.float32).astype(np.float64)
+    _, b = oracle.fp8_encode(V)
+    amax = np.abs(V).reshape(64, 4, 8, 32).max(-1)
+    e = b.astype(np.float64) - 127
+    assert np.all(amax <= 448 * 2.0 ** e) and np.all(amax > 448 * 2.0 ** (e - 1))
+
+
+def pin_fp8_roundtrip():
+    """Decoding an encoded block errs by at most half a code step: 2^-4 relative for values in
+    the normal range of the scaled codes, 2^-10·scale absolute below it; encoding what a
+    decode produced gives back the same values (the stored values are fixed points; the codes
+    may differ where rounding brought a block's maximum down to 448·2^(e-1), which the smaller
+    scale then represents exactly)."""
+    rng = np.random.default_rng(139)
+    V = (rng.standard_normal((32, 4, 512)) * np.exp(rng.uniform(-8, 8, (32, 4, 16, 1)))
+         .repeat(32, axis=-1).reshape(32, 4, 512)).astype(np.float32).astype(np.float64)
+    c, b = oracle.fp8_encode(V)
+    W = oracle.fp8_decode(c, b)
+    scale = (2.0 ** (b.astype(np.float64) - 127)).repeat(32, axis=-1)
+    err = np.abs(W - V)
+    normal = np.abs(V) >= scale * 2.0 ** -6
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(V[normal]))
+    assert np.all(err[~normal] <= 2.0 ** -10 * scale[~normal])
+    c2, b2 = oracle.fp8_encode(W)
+    assert np.array_equal(oracle.fp8_decode(c2, b2), W)
+
+
+def pin_fp8_blocks_independent():
+    """A block's codes and scale depend on its own 32 channels only (blocks start at multiples
+    of 32): scaling one block by 2^10 changes that block's scale by 10 and nothing else."""
+    rng = np.random.default_rng(149)
+    V = rng.standard_normal((3, 4, 128)).astype(np.float32).astype(np.float64)
+    c, b = oracle.fp8_encode(V)
+    V2 = V.copy()
+    V2[1, 2, 64:96] *= 1024.0
+    c2, b2 = oracle.fp8_encode(V2)
+    mask = np.zeros(V.shape, bool)
+    mask[1, 2, 64:96] = True
+    assert np.array_equal(c2[~mask], c[~mask]) and np.array_equal(c2[mask], c[mask])
+    bm = np.zeros(b.shape, bool)
+    bm[1, 2, 2] = True
+    assert np.array_equal(b2[~bm], b[~bm]) and int(b2[1, 2, 2]) == int(b[1, 2, 2]) + 10
+
+
+def pin_fp8_write_then_read_error():
+    """The FP8 fused step against the plain definition (fp64, no storage rounding) stays within
+    SPEC R22's bounds: R' within 2^-4, x and s within 2^-3 (per-row relative L2)."""
+    rng = np.random.default_rng(151)
+    n, nb, D, r = 16, 4, 128, 8
+    R0 = rng.standard_normal((n, nb, D)).astype(np.float32)
+    c, b = oracle.fp8_encode(R0)
+    R = oracle.fp8_decode(c, b)
+    y = rng.standard_normal((n, D)).astype(np.float32) * 0.5
+    sp = rng.uniform(0, 2, (n, nb))
+    p = _params(rng, nb, D, r)
+    c2, b2, x, s = oracle.write_then_read_fp8(c, b, y, sp, p)
+    Rp, xp, sp2 = oracle.write_then_read(R, y, sp, p)
+    assert _rel(oracle.fp8_decode(c2, b2).reshape(n * nb, D), Rp.reshape(n * nb, D)) <= 2.0 ** -4
+    assert _rel(x, xp) <= 2.0 ** -3 and _rel(s, sp2) <= 2.0 ** -3
+
+
 ALL_PINS = [pin_dense_bruteforce, pin_zero_down_projection, pin_zero_up_projection,
             pin_zero_write_projection, pin_gatednorm_single_branch, pin_replicated_branches,
             pin_prenorm_reduction, pin_two_branch_toy, pin_two_branch_learned_gate,
             pin_chain_closed_form, pin_decomposition, pin_branch_permutation,
-            pin_branch_scale_invariance, pin_ranges_and_saturation, pin_residual_add]
+            pin_branch_scale_invariance, pin_ranges_and_saturation, pin_residual_add,
+            pin_fp8_codes_match_torch, pin_fp8_block_scale, pin_fp8_roundtrip,
+            pin_fp8_blocks_independent, pin_fp8_write_then_read_error]

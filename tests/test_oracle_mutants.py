@@ -35,6 +35,15 @@ MUTANTS = {
                             "x[(size_t)t * D + c] = acc;"),
     "gamma_wrong_branch": ("Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];",
                            "Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[c];"),
+    "fp8_scale_may_clip": ("    if (2.0 * f > 1.75)\n        e += 1;\n", ""),
+    "fp8_truncating_rounding": ("double m = nearbyint(ldexp(a, 3 - E));",
+                                "double m = floor(ldexp(a, 3 - E));"),
+    "fp8_exponent_bias": ("ldexp(8.0 + m, E - 10)", "ldexp(8.0 + m, E - 9)"),
+    "fp8_subnormal_step": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "fp8_scale_bias": ("scales[(size_t)t * nblk + k] = (uint8_t)(e + 127);",
+                       "scales[(size_t)t * nblk + k] = (uint8_t)(e + 128);"),
+    "fp8_amax_over_16": ("            for (int c = 0; c < 32; ++c)\n                if (fabs(vb[c]) > a)",
+                         "            for (int c = 0; c < 16; ++c)\n                if (fabs(vb[c]) > a)"),
 }
 
 
