@@ -64,8 +64,9 @@ enum {
     GR_E_TIMEOUT = -12     /* a kernel's bounded device-side wait ran out (see gr_device_status) */
 };
 
-/* Storage dtype of R, y and x. */
-typedef enum { GR_F32 = 0, GR_BF16 = 1 } gr_dtype;
+/* Storage dtype of R, y and x. GR_FP8 is the FP8 branch state (see the FP8 section below): R is
+ * e4m3 codes plus block exponents, y and x are bf16. */
+typedef enum { GR_F32 = 0, GR_BF16 = 1, GR_FP8 = 2 } gr_dtype;
 
 /* Problem shape. n_branch must be 4; d_model a multiple of 8 in [8, GR_MAX_D]; 1 <= rank <= 64. */
 typedef struct gr_shape {
@@ -96,7 +97,8 @@ const char* gr_status_string(int status);
 /* Name of the kernel path a read or fused step takes for `shape` (static string, never NULL):
  * "fused_bf16" (cluster tensor-core kernel: bf16, D in {256, 512, 1024, 2048, 4096}, r <= 16),
  * "tiled_bf16" (two-pass tensor-core kernel: the other bf16 shapes with D % 64 == 0, r <= 32),
- * "generic" (one CTA per token), or "invalid". Host only. */
+ * "tiled_fp8" (the two-pass kernel on an FP8 state), "generic" (one CTA per token), or
+ * "invalid". Host only. */
 const char* gr_kernel_path(const gr_shape* shape);
 
 /* Bytes of device memory gr_pack_params needs for `shape` (host only; no CUDA call).
@@ -193,6 +195,48 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
 int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const void* y_host,
                                    const float* s_prev_host, const gr_params* next, void* x_host,
                                    float* s_next_host, void* stream);
+
+/* ---- FP8 branch state ------------------------------------------------------------------------
+ * "【论文解读】 Qwen3.8 Flash Next", §二.7 stores the widened state in FP8 and fixes no format.
+ * This library's FP8 state is two DEVICE arrays:
+ *   codes  [N][4][D]     uint8, OCP FP8 E4M3 ("e4m3fn": bias 7, 3 fraction bits, largest
+ *                        finite 448, no infinities; 0x7F/0xFF are NaN)
+ *   scales [N][4][D/32]  uint8 biased exponents b: channels 32k..32k+31 of row (t, i) have the
+ *                        scale 2^(b - 127)
+ * Element (t, i, c) is decode(codes[t][i][c]) · 2^(scales[t][i][c/32] - 127). A block of 32 values
+ * v is encoded with the smallest e such that max|v| <= 448·2^e (e clamped to [-127, 127]; an
+ * all-zero block gets e = -127) and codes v/2^e rounded to the nearest e4m3 value, ties to even.
+ * The FP8 write decodes R, forms R + s·y as one fp32 fused multiply-add and encodes the result;
+ * the read uses the decoded stored values. y and x are bf16, s fp32; params are packed with
+ * state_dtype GR_FP8 (bf16 weights, as on the bf16 path).
+ * Shapes: state_dtype GR_FP8, d_model a multiple of 128 in [128, 8192], rank 1..32 for the read
+ * calls (encode, decode and write take any multiple of 32 up to GR_MAX_D). codes, scales, y, x
+ * and s must be 16-byte aligned. Inputs with NaN or infinite values have no FP8 encoding; their
+ * blocks come out undefined. */
+
+/* Encode a state R [N][4][D] given in `in_dtype` (GR_BF16 or GR_F32) into codes and scales. */
+int gr_fp8_encode(const gr_shape* shape, const void* R, int32_t in_dtype, uint8_t* codes,
+                  uint8_t* scales, void* stream);
+
+/* Decode codes and scales into R [N][4][D] in `out_dtype` (GR_BF16: rounded to nearest even;
+ * GR_F32: exact). */
+int gr_fp8_decode(const gr_shape* shape, const uint8_t* codes, const uint8_t* scales, void* R,
+                  int32_t out_dtype, void* stream);
+
+/* gr_read on an FP8 state: x [N][D] bf16 and s [N][4] fp32. codes and scales are only read. */
+int gr_read_fp8(const gr_shape* shape, const uint8_t* codes, const uint8_t* scales,
+                const gr_params* params, void* x, float* s, void* stream);
+
+/* gr_write on an FP8 state, in place: R[t][i][:] += s[t][i] · y[t][:] (y bf16), re-encoded. */
+int gr_write_fp8(const gr_shape* shape, uint8_t* codes, uint8_t* scales, const void* y,
+                 const float* s, void* stream);
+
+/* gr_write_then_read on an FP8 state: the write in place (codes and scales), then the read of
+ * the stored state with `next` into x (bf16) and s_next. The aliasing rules are those of
+ * gr_write_then_read, with codes and scales in the place of R. */
+int gr_write_then_read_fp8(const gr_shape* shape, uint8_t* codes, uint8_t* scales,
+                           const void* y, const float* s_prev, const gr_params* next, void* x,
+                           float* s_next, void* stream);
 
 #ifdef __cplusplus
 }

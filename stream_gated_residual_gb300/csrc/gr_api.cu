@@ -75,12 +75,18 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return na && nb && a0 < b0 + nb && b0 < a0 + na;
 }
 
-int validate_shape(const gr_shape* s) {
+// Shape checks of the bf16/fp32 calls; fp8_ok also admits GR_FP8 (the calls that only pack or
+// describe parameters), whose width must be a multiple of 32.
+int validate_shape(const gr_shape* s, bool fp8_ok = false) {
     if (!s) return GR_E_NULL;
     if (s->n_tokens < 0 || s->n_branch != kBranches || s->d_model < 8 || s->d_model % 8 != 0 ||
         s->d_model > GR_MAX_D)
         return GR_E_SHAPE;
-    if (s->state_dtype != GR_F32 && s->state_dtype != GR_BF16) return GR_E_DTYPE;
+    if (s->state_dtype == GR_FP8 && fp8_ok) {
+        if (s->d_model % 32 != 0) return GR_E_SHAPE;
+    } else if (s->state_dtype != GR_F32 && s->state_dtype != GR_BF16) {
+        return GR_E_DTYPE;
+    }
     if (s->rank < 1 || s->rank > GR_MAX_RANK) return GR_E_RANK;
     if (!(s->eps >= 0.0f) || !isfinite(s->eps)) return GR_E_EPS;
     return GR_OK;
@@ -92,6 +98,21 @@ int validate_params(const gr_shape* s, const gr_params* p) {
     if (p->d_model != s->d_model || p->n_branch != s->n_branch || p->rank != s->rank ||
         p->state_dtype != s->state_dtype)
         return GR_E_PARAMS;
+    return GR_OK;
+}
+
+// Shape checks of the FP8-state calls: state_dtype GR_FP8, D a multiple of 32; the calls that
+// read through the two-pass kernel (tensor_core) also need D % 128 == 0, D <= 8192, r <= 32.
+int validate_fp8(const gr_shape* s, bool tensor_core) {
+    if (!s) return GR_E_NULL;
+    if (s->state_dtype != GR_FP8) return GR_E_DTYPE;
+    int st = validate_shape(s, true);
+    if (st) return st;
+    if (tensor_core) {
+        if (!tiled_fp8_supported(s->d_model, 1)) return GR_E_SHAPE;
+        if (!tiled_fp8_supported(s->d_model, s->rank)) return GR_E_RANK;
+        if (s->n_tokens > tiled_max_tokens()) return GR_E_SHAPE;
+    }
     return GR_OK;
 }
 
@@ -167,12 +188,14 @@ const char* gr_status_string(int status) {
 }
 
 const char* gr_kernel_path(const gr_shape* shape) {
+    if (shape && shape->state_dtype == GR_FP8)
+        return validate_fp8(shape, true) == GR_OK ? "tiled_fp8" : "invalid";
     if (validate_shape(shape) != GR_OK) return "invalid";
     return use_fused(shape) ? "fused_bf16" : use_tiled(shape) ? "tiled_bf16" : "generic";
 }
 
 int gr_packed_size(const gr_shape* shape, size_t* bytes) {
-    int st = validate_shape(shape);
+    int st = validate_shape(shape, true);
     if (st) return st;
     if (!bytes) return GR_E_NULL;
     *bytes = make_layout(shape->d_model, shape->rank, shape->state_dtype).total;
@@ -182,7 +205,7 @@ int gr_packed_size(const gr_shape* shape, size_t* bytes) {
 int gr_pack_params(const gr_shape* shape, const float* gamma, const float* w_down,
                    const float* w_up, const float* w_write, void* packed, size_t packed_bytes,
                    gr_params* out, void* stream) {
-    int st = validate_shape(shape);
+    int st = validate_shape(shape, true);
     if (st) return st;
     if (!gamma || !w_down || !w_up || !w_write || !packed || !out) return GR_E_NULL;
     if (!aligned16(gamma) || !aligned16(w_down) || !aligned16(w_up) || !aligned16(w_write) ||
@@ -292,6 +315,111 @@ int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* 
     int st = check_device();
     if (st) return st;
     return status_of(launch_residual_add(n, dtype, y, x, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- FP8 branch state ------------------------------------------------------------------------
+
+int gr_fp8_encode(const gr_shape* shape, const void* R, int32_t in_dtype, uint8_t* codes,
+                  uint8_t* scales, void* stream) {
+    int st = validate_fp8(shape, false);
+    if (st) return st;
+    if (in_dtype != GR_BF16 && in_dtype != GR_F32) return GR_E_DTYPE;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!R || !codes || !scales) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(codes) || !aligned16(scales)) return GR_E_ALIGN;
+    const size_t n = size_t(shape->n_tokens) * kBranches * size_t(shape->d_model);
+    if (overlaps(R, n * elem_size(in_dtype), codes, n) ||
+        overlaps(R, n * elem_size(in_dtype), scales, n / 32) || overlaps(codes, n, scales, n / 32))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_fp8_encode(shape->n_tokens * kBranches, shape->d_model, in_dtype, R,
+                                       codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_fp8_decode(const gr_shape* shape, const uint8_t* codes, const uint8_t* scales, void* R,
+                  int32_t out_dtype, void* stream) {
+    int st = validate_fp8(shape, false);
+    if (st) return st;
+    if (out_dtype != GR_BF16 && out_dtype != GR_F32) return GR_E_DTYPE;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!R || !codes || !scales) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(codes) || !aligned16(scales)) return GR_E_ALIGN;
+    const size_t n = size_t(shape->n_tokens) * kBranches * size_t(shape->d_model);
+    if (overlaps(R, n * elem_size(out_dtype), codes, n) ||
+        overlaps(R, n * elem_size(out_dtype), scales, n / 32))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_fp8_decode(shape->n_tokens * kBranches, shape->d_model, out_dtype,
+                                       codes, scales, R, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_read_fp8(const gr_shape* shape, const uint8_t* codes, const uint8_t* scales,
+                const gr_params* params, void* x, float* s, void* stream) {
+    int st = validate_fp8(shape, true);
+    if (st) return st;
+    if ((st = validate_params(shape, params))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!codes || !scales || !x || !s) return GR_E_NULL;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(s))
+        return GR_E_ALIGN;
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nc = N * kBranches * D, nb = nc / 32, nx = N * D * 2, ns = N * kBranches * 4;
+    if (overlaps(x, nx, codes, nc) || overlaps(x, nx, scales, nb) || overlaps(s, ns, codes, nc) ||
+        overlaps(s, ns, scales, nb) || overlaps(x, nx, s, ns))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_tiled_fp8(shape->n_tokens, shape->d_model, shape->rank, shape->eps,
+                                      const_cast<uint8_t*>(codes), const_cast<uint8_t*>(scales),
+                                      nullptr, nullptr, params->packed, x, s,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int gr_write_fp8(const gr_shape* shape, uint8_t* codes, uint8_t* scales, const void* y,
+                 const float* s, void* stream) {
+    int st = validate_fp8(shape, false);
+    if (st) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!codes || !scales || !y || !s) return GR_E_NULL;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(y) || !aligned16(s))
+        return GR_E_ALIGN;
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nc = N * kBranches * D, nb = nc / 32, ny = N * D * 2, ns = N * kBranches * 4;
+    if (overlaps(codes, nc, scales, nb) || overlaps(codes, nc, y, ny) ||
+        overlaps(codes, nc, s, ns) || overlaps(scales, nb, y, ny) || overlaps(scales, nb, s, ns))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_fp8_write(shape->n_tokens, shape->d_model, codes, scales, y, s,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int gr_write_then_read_fp8(const gr_shape* shape, uint8_t* codes, uint8_t* scales,
+                           const void* y, const float* s_prev, const gr_params* next, void* x,
+                           float* s_next, void* stream) {
+    int st = validate_fp8(shape, true);
+    if (st) return st;
+    if ((st = validate_params(shape, next))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!codes || !scales || !y || !s_prev || !x || !s_next) return GR_E_NULL;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(y) || !aligned16(s_prev) ||
+        !aligned16(x) || !aligned16(s_next))
+        return GR_E_ALIGN;
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nc = N * kBranches * D, nb = nc / 32, ny = N * D * 2, ns = N * kBranches * 4;
+    const void* state[2] = {codes, scales};
+    const size_t sz[2] = {nc, nb};
+    if (overlaps(codes, nc, scales, nb)) return GR_E_ALIAS;
+    for (int k = 0; k < 2; ++k)
+        if (overlaps(state[k], sz[k], y, ny) || overlaps(state[k], sz[k], s_prev, ns) ||
+            overlaps(state[k], sz[k], x, ny) || overlaps(state[k], sz[k], s_next, ns))
+            return GR_E_ALIAS;
+    if (overlaps(x, ny, s_next, ns) || overlaps(x, ny, s_prev, ns) ||
+        overlaps(s_next, ns, y, ny) || (x != y && overlaps(x, ny, y, ny)) ||
+        (s_next != s_prev && overlaps(s_next, ns, s_prev, ns)))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_tiled_fp8(shape->n_tokens, shape->d_model, shape->rank, shape->eps,
+                                      codes, scales, y, s_prev, next->packed, x, s_next,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 int gr_device_status(int clear) {

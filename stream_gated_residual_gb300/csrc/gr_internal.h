@@ -41,11 +41,13 @@ size_t fused_frag_bytes(int D, int r);
 bool tiled_supported(int D, int r);
 int64_t tiled_max_tokens();
 size_t tiled_frag_bytes(int D, int r);
+// The two-pass kernel on an FP8 state also needs D % 128 == 0 and D <= 8192.
+bool tiled_fp8_supported(int D, int r);
 
 inline Layout make_layout(int D, int r, int dtype) {
     Layout L{};
     const size_t K = size_t(kBranches) * D;
-    const size_t w = dtype == GR_BF16 ? 2 : 4;
+    const size_t w = dtype == GR_F32 ? 4 : 2;   // the FP8 path computes with bf16 weights
     size_t off = 0;
     L.gamma32 = off;
     off = align256(off + K * 4);
@@ -53,10 +55,10 @@ inline Layout make_layout(int D, int r, int dtype) {
     off = align256(off + size_t(r + kBranches) * K * w);
     L.wut = off;
     off = align256(off + size_t(r) * K * w);
-    L.frag_bytes = dtype != GR_BF16        ? 0
-                   : fused_supported(D, r) ? fused_frag_bytes(D, r)
-                   : tiled_supported(D, r) ? tiled_frag_bytes(D, r)
-                                           : 0;
+    L.frag_bytes = dtype == GR_F32                            ? 0
+                   : dtype == GR_BF16 && fused_supported(D, r) ? fused_frag_bytes(D, r)
+                   : tiled_supported(D, r)                     ? tiled_frag_bytes(D, r)
+                                                               : 0;
     L.frag = off;
     off = align256(off + L.frag_bytes);
     L.total = off;
@@ -83,6 +85,20 @@ cudaError_t launch_fused_bf16(int64_t N, int D, int r, float eps, void* R, const
 cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
                               const float* s_prev, const void* packed, void* x, float* s_out,
                               cudaStream_t st);
+
+// The two-pass kernel on an FP8 state (codes [N][4][D], block exponents [N][4][D/32]); y and x
+// bf16; read only when y == nullptr.
+cudaError_t launch_tiled_fp8(int64_t N, int D, int r, float eps, uint8_t* codes,
+                             uint8_t* scales, const void* y, const float* s_prev,
+                             const void* packed, void* x, float* s_out, cudaStream_t st);
+
+// FP8 state conversions and the streaming FP8 write (gr_fp8.cu); rows = N·4 for the state.
+cudaError_t launch_fp8_encode(int64_t rows, int D, int in_dtype, const void* in, uint8_t* codes,
+                              uint8_t* scales, cudaStream_t st);
+cudaError_t launch_fp8_decode(int64_t rows, int D, int out_dtype, const uint8_t* codes,
+                              const uint8_t* scales, void* out, cudaStream_t st);
+cudaError_t launch_fp8_write(int64_t N, int D, uint8_t* codes, uint8_t* scales, const void* y,
+                             const float* s, cudaStream_t st);
 
 // Streaming write R += s_i * y (no read).
 cudaError_t launch_write(int64_t N, int D, int dtype, void* R, const void* y, const float* s,

@@ -63,7 +63,7 @@ cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float
     const size_t cap = size_t(sm_count()) * 8;
     const int blocks = int(want < cap ? want : cap);
     float* g32 = reinterpret_cast<float*>(base + L.gamma32);
-    if (dtype == GR_BF16) {
+    if (dtype != GR_F32) {   // bf16 weights, gamma folded (the bf16 and FP8 paths)
         pack_generic_kernel<__nv_bfloat16, true><<<blocks, threads, 0, st>>>(
             D, r, gamma, wd, wu, ww, g32, reinterpret_cast<__nv_bfloat16*>(base + L.wdw),
             reinterpret_cast<__nv_bfloat16*>(base + L.wut));
@@ -75,8 +75,9 @@ cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (L.frag_bytes) {
-        e = fused_supported(D, r) ? launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag, st)
-                                  : launch_pack_tiled(D, r, gamma, wd, wu, ww, base + L.frag, st);
+        e = dtype == GR_BF16 && fused_supported(D, r)
+                ? launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag, st)
+                : launch_pack_tiled(D, r, gamma, wd, wu, ww, base + L.frag, st);
     }
     return e;
 }

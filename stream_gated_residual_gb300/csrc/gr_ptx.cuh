@@ -230,6 +230,32 @@ __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// ---- FP8 (e4m3) state: codes with one power-of-two scale per 32-channel block ----
+// Two fp32 values -> an e4m3 pair (lo in the low byte), round to nearest even, saturating.
+__device__ __forceinline__ uint16_t f2_to_e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// An e4m3 pair -> two fp32 values (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t v) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+// 2^e as fp32 for -127 <= e <= 127 (2^-127 is the one subnormal).
+__device__ __forceinline__ float pow2f(int e) {
+    return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(0x00400000);
+}
+// Block exponent for a block whose largest magnitude is a (finite, >= 0): the smallest e with
+// a <= 448·2^e, clamped to [-127, 127]; 448 = 1.75·2^8, so e = exponent(a) - 8, plus one when
+// the significand of a exceeds 1.75 (fraction bits above 0x600000).
+__device__ __forceinline__ int fp8_block_exp(float a) {
+    const int bits = __float_as_int(a);
+    const int e = ((bits >> 23) & 0xff) - 127 - 8 + ((bits & 0x7fffff) > 0x600000 ? 1 : 0);
+    return min(max(e, -127), 127);
+}
+
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -52,16 +52,20 @@ constexpr int kCThreads = kCW * 32;
 constexpr int kThreadsT = kCThreads + 32;         // + the producer warp
 constexpr int kSStages = 7;                       // state ring depth
 constexpr int kWStages = 3;                       // weight ring depth
-constexpr int kRChunk = kBranches * kTT * kCh * 2;  // 16 KB: R [4][32][64] bf16, 128B-swizzled
 constexpr int kYChunk = kTT * kCh * 2;              // 4 KB: y [32][64] bf16, 128B-swizzled
-constexpr int kStateStage = kRChunk + kYChunk;
 constexpr int kXBuf = 16 * 8 * 2;                 // per warp: x [16 tok][8 ch], unswizzled
 constexpr int kXBufs = 4;                         // x buffers per warp (stores in flight)
 constexpr int kMaxTiledRank = 32;
+constexpr int kMaxFp8D = 8192;                    // the tile's block exponents: 4·D bytes on chip
 
 // Compile-time sizes for NTD = ceil((r+4)/8) down-projection n-tiles and KSU = ceil(r/16)
-// up-projection k-steps.
-template <int NTD, int KSU> struct TiledCfg {
+// up-projection k-steps, for a bf16 state or an FP8 state (e4m3 codes; the tile's block
+// exponents [32 tok][4][D/32] then sit at the end of shared memory, 4·D bytes).
+template <int NTD, int KSU, bool FP8> struct TiledCfg {
+    // R chunk [4][32][64]: bf16 with 128-byte rows (128B swizzle) or e4m3 codes with 64-byte
+    // rows (64B swizzle)
+    static constexpr int kRChunk = kBranches * kTT * kCh * (FP8 ? 1 : 2);
+    static constexpr int kStateStage = kRChunk + kYChunk;
     static constexpr int kNP = 8 * NTD;                        // padded r + 4
     static constexpr int kHP = 16 * KSU;                       // padded r
     static constexpr int kDownChunk = kBranches * 4 * NTD * 256;  // [i][ks][nt][lane] uint2
@@ -82,7 +86,11 @@ template <int NTD, int KSU> struct TiledCfg {
     static constexpr int off_bar = off_inv + kBranches * kTT * 4;
     static constexpr int kBars = 2 * kSStages + 2 * kWStages + 1;
     static constexpr int off_abort = off_bar + kBars * 8;
-    static constexpr int kSmem = off_abort + 16 + 1024;        // + slack for 1 KB alignment
+    // 16-byte vector copies move the block exponents in and out: keep the buffer aligned
+    static constexpr int off_scl = (off_abort + 16 + 127) / 128 * 128;
+    static_assert(off_scl % 16 == 0, "exponent buffer must be 16-byte aligned");
+    // + 4·D bytes of block exponents on the FP8 path, + slack for the 1 KB alignment
+    static int smem_bytes(int D) { return off_scl + (FP8 ? 4 * D : 0) + 1024; }
 };
 
 // Bounded wait: one non-blocking test first (the common case: the data is there), then the
@@ -119,16 +127,23 @@ __device__ __forceinline__ uint32_t lds32(const char* p) {
     return *reinterpret_cast<const uint32_t*>(p);
 }
 __device__ __forceinline__ void sts32(char* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
+__device__ __forceinline__ uint16_t lds16(const char* p) {
+    return *reinterpret_cast<const uint16_t*>(p);
+}
+__device__ __forceinline__ void sts16(char* p, uint16_t v) { *reinterpret_cast<uint16_t*>(p) = v; }
 
-template <bool WRITE, int NTD, int KSU>
+template <bool WRITE, int NTD, int KSU, bool FP8>
 __global__ void __launch_bounds__(kThreadsT, 1)
 gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {64, 32, 4, 1}
                 const __grid_constant__ CUtensorMap tm_Rs,  // R' stores, box {64, 16, 1, 1}
                 const __grid_constant__ CUtensorMap tm_y,   // y loads, box {64, 32}
                 const __grid_constant__ CUtensorMap tm_x,   // x stores, box {8, 16}
                 int N, int D, int r, float eps, const float* __restrict__ s_prev,
-                const char* __restrict__ frag, float* __restrict__ s_out) {
-    using C = TiledCfg<NTD, KSU>;
+                const char* __restrict__ frag, float* __restrict__ s_out,
+                uint8_t* __restrict__ scales) {              // FP8: block exponents [N][4][D/32]
+    using C = TiledCfg<NTD, KSU, FP8>;
+    constexpr int kRChunk = C::kRChunk;
+    constexpr int kStateStage = C::kStateStage;
     extern __shared__ uint8_t smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~uintptr_t(1023));
@@ -149,6 +164,8 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
     float* ssqb = reinterpret_cast<float*>(smem + C::off_ssq);  // [k-half][4][32]
     float* hbuf = reinterpret_cast<float*>(smem + C::off_h);    // [32][kHP]
     float* invb = reinterpret_cast<float*>(smem + C::off_inv);  // [4][32]
+    uint8_t* scl = reinterpret_cast<uint8_t*>(smem + C::off_scl);  // FP8: [32 tok][4][D/32]
+    const int nblk = D / 32;
     auto sbuf = [&](int st) { return smem + C::off_state + st * kStateStage; };
     auto wbuf = [&](int st) { return smem + C::off_w + st * C::kWStage; };
 
@@ -236,6 +253,17 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
 
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int t0 = tile * kTT;
+        if constexpr (FP8) {
+            // The tile's block exponents, [32 tok][4][D/32], contiguous in HBM: plain 16-byte
+            // loads (D % 128 == 0 keeps every row block 16-byte aligned). The first barrier
+            // waits until no warp still reads the previous tile's exponents in its pass 2.
+            named_sync(1, kCThreads);
+            const int nv = min(kTT, N - t0);
+            const int nvec = int(size_t(nv) * size_t(D) / 128);
+            const uint4* src = reinterpret_cast<const uint4*>(scales + size_t(t0) * (D / 8));
+            for (int e = tid; e < nvec; e += kCThreads) reinterpret_cast<uint4*>(scl)[e] = src[e];
+            named_sync(1, kCThreads);
+        }
         // ---------------------------------- pass 1 --------------------------------------------
         float spa = 0.f, spb = 0.f;   // s_prev of tokens g and g+8 of the m-tile, branch ib
         if (WRITE) {
@@ -258,30 +286,116 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             char* rb = sbuf(st);
             const char* ybuf = rb + kRChunk;
             const uint2* wd = reinterpret_cast<const uint2*>(wbuf(wr.st)) + ib * 4 * NTD * 32;
+            if constexpr (!FP8) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int ks = 2 * kh + kk;
-                uint32_t a[4];
-                const int o[4] = {swz(rowa, 2 * ks) + 4 * q, swz(rowb, 2 * ks) + 4 * q,
-                                  swz(rowa, 2 * ks + 1) + 4 * q, swz(rowb, 2 * ks + 1) + 4 * q};
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int ks = 2 * kh + kk;
+                    uint32_t a[4];
+                    const int o[4] = {swz(rowa, 2 * ks) + 4 * q, swz(rowb, 2 * ks) + 4 * q,
+                                      swz(rowa, 2 * ks + 1) + 4 * q, swz(rowb, 2 * ks + 1) + 4 * q};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint32_t v = lds32(rb + o[e]);
-                    if (WRITE) {
-                        const int yo = swz((e & 1) ? yb : ya, 2 * ks + (e >> 1)) + 4 * q;
-                        const uint64_t yy = bf2_to_f2(lds32(ybuf + yo));
-                        v = f2_to_bf2(fma2(yy, (e & 1) ? sb2 : sa2, bf2_to_f2(v)));
-                        sts32(rb + o[e], v);
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t v = lds32(rb + o[e]);
+                        if (WRITE) {
+                            const int yo = swz((e & 1) ? yb : ya, 2 * ks + (e >> 1)) + 4 * q;
+                            const uint64_t yy = bf2_to_f2(lds32(ybuf + yo));
+                            v = f2_to_bf2(fma2(yy, (e & 1) ? sb2 : sa2, bf2_to_f2(v)));
+                            sts32(rb + o[e], v);
+                        }
+                        const uint64_t f = bf2_to_f2(v);
+                        if (e & 1) ssb = fma2(f, f, ssb);
+                        else ssa = fma2(f, f, ssa);
+                        a[e] = v;
                     }
-                    const uint64_t f = bf2_to_f2(v);
-                    if (e & 1) ssb = fma2(f, f, ssb);
-                    else ssa = fma2(f, f, ssa);
-                    a[e] = v;
+#pragma unroll
+                    for (int n = 0; n < NTD; ++n) {
+                        const uint2 b = wd[(ks * NTD + n) * 32 + lane];
+                        mma_bf16(acc[n], a[0], a[1], a[2], a[3], b.x, b.y);
+                    }
+                }
+            } else {
+                // FP8: this warp's two k-steps are exactly one 32-channel block (2j + kh) of its
+                // rows; the four lanes of a quad hold the block. Decode R with the old exponent,
+                // write in fp32, pick the new exponent from the block maximum, encode in place.
+                uint8_t* ea_p = scl + ((16 * mt + g) * kBranches + ib) * nblk + 2 * j + kh;
+                uint8_t* eb_p = ea_p + 8 * kBranches * nblk;
+                const float da = pow2f(int(*ea_p) - 127), db = pow2f(int(*eb_p) - 127);
+                float2 v[2][4];
+                // byte offset of the code pair (row a or b, channels 2q, 2q+1 (+8)) in the box
+                auto code_off = [&](int kk, int e) {
+                    return swz64((e & 1) ? rowb : rowa, 2 * kh + kk) + 2 * q + 8 * (e >> 1);
+                };
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int ks = 2 * kh + kk;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 w = e4m3x2_to_f2(lds16(rb + code_off(kk, e)));
+                        const float d = (e & 1) ? db : da;
+                        w.x *= d;
+                        w.y *= d;
+                        if (WRITE) {
+                            const int yo = swz((e & 1) ? yb : ya, 2 * ks + (e >> 1)) + 4 * q;
+                            float yx, yy;
+                            unf2(bf2_to_f2(lds32(ybuf + yo)), yx, yy);
+                            const float sv = (e & 1) ? spb : spa;
+                            w.x = fmaf(sv, yx, w.x);
+                            w.y = fmaf(sv, yy, w.y);
+                        }
+                        v[kk][e] = w;
+                    }
+                }
+                if (WRITE) {
+                    float ma = 0.f, mb = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float m = fmaxf(fabsf(v[kk][e].x), fabsf(v[kk][e].y));
+                            if (e & 1) mb = fmaxf(mb, m);
+                            else ma = fmaxf(ma, m);
+                        }
+                    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+                    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+                    const int na = fp8_block_exp(ma), nb = fp8_block_exp(mb);
+                    const float ia = pow2f(-na), ib_ = pow2f(-nb);
+                    const float ua = pow2f(na), ub = pow2f(nb);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float i_ = (e & 1) ? ib_ : ia, u_ = (e & 1) ? ub : ua;
+                            const uint16_t code = f2_to_e4m3x2(v[kk][e].x * i_, v[kk][e].y * i_);
+                            sts16(rb + code_off(kk, e), code);
+                            float2 w = e4m3x2_to_f2(code);   // the stored value, for the read
+                            w.x *= u_;
+                            w.y *= u_;
+                            v[kk][e] = w;
+                        }
+                    // every lane of the quad has read the old exponent (it fed the maximum)
+                    if (q == 0) {
+                        *ea_p = uint8_t(na + 127);
+                        *eb_p = uint8_t(nb + 127);
+                    }
                 }
 #pragma unroll
-                for (int n = 0; n < NTD; ++n) {
-                    const uint2 b = wd[(ks * NTD + n) * 32 + lane];
-                    mma_bf16(acc[n], a[0], a[1], a[2], a[3], b.x, b.y);
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int ks = 2 * kh + kk;
+                    uint32_t a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint64_t f = f2(v[kk][e].x, v[kk][e].y);
+                        if (e & 1) ssb = fma2(f, f, ssb);
+                        else ssa = fma2(f, f, ssa);
+                        a[e] = pack_bf2(v[kk][e].x, v[kk][e].y);   // exact: 4 significant bits
+                    }
+#pragma unroll
+                    for (int n = 0; n < NTD; ++n) {
+                        const uint2 b = wd[(ks * NTD + n) * 32 + lane];
+                        mma_bf16(acc[n], a[0], a[1], a[2], a[3], b.x, b.y);
+                    }
                 }
             }
             __syncwarp();
@@ -295,8 +409,8 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 } else if (lane == 0) {
                     // an m-tile wholly past the last token has nothing to store (empty group)
                     if (t0 + 16 * mt < N)
-                        tma_store_4d(&tm_Rs, rb + (ib * kTT + 16 * mt) * 128, 0, t0 + 16 * mt, ib,
-                                     j);
+                        tma_store_4d(&tm_Rs, rb + (ib * kTT + 16 * mt) * kCh * (FP8 ? 1 : 2), 0,
+                                     t0 + 16 * mt, ib, j);
                     bulk_commit();
                     // the previous chunk's stage is free once its store has read it
                     bulk_wait_read<1>();
@@ -318,6 +432,13 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
         // every warp is done with pass 1's stages and every store has read them: the partial
         // sums may now overwrite the ring
         named_sync(1, kCThreads);
+        if constexpr (FP8 && WRITE) {
+            // the tile's new block exponents go back to HBM (pass 2 reads them from here)
+            const int nv = min(kTT, N - t0);
+            const int nvec = int(size_t(nv) * size_t(D) / 128);
+            uint4* dst = reinterpret_cast<uint4*>(scales + size_t(t0) * (D / 8));
+            for (int e = tid; e < nvec; e += kCThreads) dst[e] = reinterpret_cast<uint4*>(scl)[e];
+        }
         {
             float s0, s1, s2, s3;
             unf2(ssa, s0, s1);
@@ -444,10 +565,23 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 const float2 gm = *reinterpret_cast<const float2*>(gam + i * kCh + ch);
                 const uint64_t g2 = f2(gm.x, gm.y);
                 const int row = i * kTT + 16 * mt2 + g;
-                const uint64_t ra = mul2(bf2_to_f2(lds32(rb + swz(row, co) + 4 * q)),
-                                         mul2(g2, f2(inv2[i][0], inv2[i][0])));
-                const uint64_t rbv = mul2(bf2_to_f2(lds32(rb + swz(row + 8, co) + 4 * q)),
-                                          mul2(g2, f2(inv2[i][1], inv2[i][1])));
+                uint64_t rpa, rpb;   // R' of tokens g and g+8 at this thread's channel pair
+                if constexpr (!FP8) {
+                    rpa = bf2_to_f2(lds32(rb + swz(row, co) + 4 * q));
+                    rpb = bf2_to_f2(lds32(rb + swz(row + 8, co) + 4 * q));
+                } else {
+                    const int off = (co & 1) * 8 + 2 * q;
+                    const uint8_t* ep =
+                        scl + ((16 * mt2 + g) * kBranches + i) * nblk + 2 * j + (co >> 2);
+                    const float da = pow2f(int(ep[0]) - 127);
+                    const float db = pow2f(int(ep[8 * kBranches * nblk]) - 127);
+                    const float2 wa = e4m3x2_to_f2(lds16(rb + swz64(row, co >> 1) + off));
+                    const float2 wb = e4m3x2_to_f2(lds16(rb + swz64(row + 8, co >> 1) + off));
+                    rpa = f2(wa.x * da, wa.y * da);
+                    rpb = f2(wb.x * db, wb.y * db);
+                }
+                const uint64_t ra = mul2(rpa, mul2(g2, f2(inv2[i][0], inv2[i][0])));
+                const uint64_t rbv = mul2(rpb, mul2(g2, f2(inv2[i][1], inv2[i][1])));
                 float a0, a1, b0, b1;
                 unf2(mul2(f2(cg4[i][0], cg4[i][1]), unscale_a), a0, a1);
                 unf2(mul2(f2(cg4[i][2], cg4[i][3]), unscale_b), b0, b1);
@@ -486,7 +620,7 @@ template <int NTD, int KSU>
 __global__ void pack_tiled_kernel(int D, int r, const float* __restrict__ gamma,
                                   const float* __restrict__ wd, const float* __restrict__ wu,
                                   const float* __restrict__ ww, char* __restrict__ frag) {
-    using C = TiledCfg<NTD, KSU>;
+    using C = TiledCfg<NTD, KSU, false>;   // the fragment layout is the same for both states
     const int J = D / kCh;
     const size_t K = size_t(kBranches) * D;
     const int n_down = kBranches * 4 * NTD * 32;      // uint2 units per chunk
@@ -543,16 +677,21 @@ __global__ void pack_tiled_kernel(int D, int r, const float* __restrict__ gamma,
 // ---- host side ---------------------------------------------------------------------------------
 
 // R as {channel within a 64-channel chunk, token, branch, chunk}: the box {64, tok_box, br_box, 1}
-// lands as rows (branch, token) of 128 bytes, 128-byte swizzled.
-bool make_map_R(CUtensorMap* m, const void* R, int64_t N, int D, int tok_box, int br_box) {
+// lands as rows (branch, token) of 64 elements: 128 bytes of bf16 (128-byte swizzle) or 64 bytes
+// of e4m3 codes (64-byte swizzle).
+bool make_map_R(CUtensorMap* m, const void* R, int64_t N, int D, int tok_box, int br_box,
+                bool fp8) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    const cuuint64_t es_b = fp8 ? 1 : 2;
     const cuuint64_t dims[4] = {cuuint64_t(kCh), cuuint64_t(N), 4, cuuint64_t(D / kCh)};
-    const cuuint64_t strides[3] = {cuuint64_t(D) * 8, cuuint64_t(D) * 2, cuuint64_t(kCh) * 2};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 4 * es_b, cuuint64_t(D) * es_b,
+                                   cuuint64_t(kCh) * es_b};
     const cuuint32_t box[4] = {cuuint32_t(kCh), cuuint32_t(tok_box), cuuint32_t(br_box), 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(R), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void*>(R), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -571,35 +710,38 @@ bool make_map_nd(CUtensorMap* m, const void* p, int64_t N, int D, int box_ch, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool WRITE, int NTD, int KSU>
-cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
+template <bool WRITE, int NTD, int KSU, bool FP8>
+cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, uint8_t* scales, const void* y,
                      const float* s_prev, const char* frag, void* x, float* s_out,
                      cudaStream_t st) {
-    using C = TiledCfg<NTD, KSU>;
+    using C = TiledCfg<NTD, KSU, FP8>;
     CUtensorMap mR, mRs, my, mx;
     memset(&mRs, 0, sizeof(mRs));
     memset(&my, 0, sizeof(my));
-    if (!make_map_R(&mR, R, N, D, kTT, kBranches)) return cudaErrorInvalidValue;
-    if (WRITE && !make_map_R(&mRs, R, N, D, 16, 1)) return cudaErrorInvalidValue;
+    if (!make_map_R(&mR, R, N, D, kTT, kBranches, FP8)) return cudaErrorInvalidValue;
+    if (WRITE && !make_map_R(&mRs, R, N, D, 16, 1, FP8)) return cudaErrorInvalidValue;
     if (WRITE && !make_map_nd(&my, y, N, D, kCh, kTT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (!make_map_nd(&mx, x, N, D, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
-    auto kern = gr_tiled_kernel<WRITE, NTD, KSU>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    auto kern = gr_tiled_kernel<WRITE, NTD, KSU, FP8>;
+    const int smem = C::smem_bytes(D);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (N + kTT - 1) / kTT;
     const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
-    kern<<<unsigned(grid), kThreadsT, C::kSmem, st>>>(mR, mRs, my, mx, int(N), D, r, eps, s_prev,
-                                                      frag, s_out);
+    kern<<<unsigned(grid), kThreadsT, smem, st>>>(mR, mRs, my, mx, int(N), D, r, eps, s_prev,
+                                                  frag, s_out, scales);
     return cudaGetLastError();
 }
 
-template <int NTD, int KSU>
-cudaError_t launch_k(int64_t N, int D, int r, float eps, void* R, const void* y,
+template <int NTD, int KSU, bool FP8>
+cudaError_t launch_k(int64_t N, int D, int r, float eps, void* R, uint8_t* scales, const void* y,
                      const float* s_prev, const char* frag, void* x, float* s_out,
                      cudaStream_t st) {
-    return y ? launch_t<true, NTD, KSU>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st)
-             : launch_t<false, NTD, KSU>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st);
+    return y ? launch_t<true, NTD, KSU, FP8>(N, D, r, eps, R, scales, y, s_prev, frag, x, s_out,
+                                             st)
+             : launch_t<false, NTD, KSU, FP8>(N, D, r, eps, R, scales, y, s_prev, frag, x, s_out,
+                                              st);
 }
 
 }  // namespace
@@ -621,8 +763,9 @@ size_t tiled_frag_bytes(int D, int r) {
     int ntd, ksu;
     tiled_cfg(r, ntd, ksu);
     const size_t J = size_t(D / kCh);
-    return ntd == 3 ? J * (TiledCfg<3, 1>::kDownChunk + TiledCfg<3, 1>::kUpChunk)
-                    : J * (TiledCfg<5, 2>::kDownChunk + TiledCfg<5, 2>::kUpChunk);
+    using C3 = TiledCfg<3, 1, false>;
+    using C5 = TiledCfg<5, 2, false>;
+    return ntd == 3 ? J * (C3::kDownChunk + C3::kUpChunk) : J * (C5::kDownChunk + C5::kUpChunk);
 }
 
 cudaError_t launch_pack_tiled(int D, int r, const float* gamma, const float* wd, const float* wu,
@@ -651,8 +794,27 @@ cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const
     const char* frag = static_cast<const char*>(packed) + L.frag;
     int ntd, ksu;
     tiled_cfg(r, ntd, ksu);
-    if (ntd == 3) return launch_k<3, 1>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st);
-    return launch_k<5, 2>(N, D, r, eps, R, y, s_prev, frag, x, s_out, st);
+    if (ntd == 3)
+        return launch_k<3, 1, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st);
+    return launch_k<5, 2, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st);
+}
+
+bool tiled_fp8_supported(int D, int r) {
+    return tiled_supported(D, r) && D % 128 == 0 && D <= kMaxFp8D;
+}
+
+cudaError_t launch_tiled_fp8(int64_t N, int D, int r, float eps, uint8_t* codes,
+                             uint8_t* scales, const void* y, const float* s_prev,
+                             const void* packed, void* x, float* s_out, cudaStream_t st) {
+    if (!tiled_fp8_supported(D, r) || N < 1 || N > tiled_max_tokens())
+        return cudaErrorInvalidValue;
+    const Layout L = make_layout(D, r, GR_FP8);
+    const char* frag = static_cast<const char*>(packed) + L.frag;
+    int ntd, ksu;
+    tiled_cfg(r, ntd, ksu);
+    if (ntd == 3)
+        return launch_k<3, 1, true>(N, D, r, eps, codes, scales, y, s_prev, frag, x, s_out, st);
+    return launch_k<5, 2, true>(N, D, r, eps, codes, scales, y, s_prev, frag, x, s_out, st);
 }
 
 int tiled_status(bool clear) {

@@ -15,10 +15,14 @@ import torch
 
 from . import build as _build
 
-GR_F32, GR_BF16 = 0, 1
+GR_F32, GR_BF16, GR_FP8 = 0, 1, 2
 GR_PARAMS_TAG = 0x47523330304B5031
 
 _DTYPES = {torch.float32: GR_F32, torch.bfloat16: GR_BF16}
+# The FP8 branch state is named by torch's e4m3 dtype in shapes and parameter packing; the state
+# itself is a pair of uint8 tensors (codes [N,4,D], block exponents [N,4,D/32]).
+FP8 = torch.float8_e4m3fn
+_SHAPE_DTYPES = {**_DTYPES, FP8: GR_FP8}
 
 
 class GRError(RuntimeError):
@@ -73,6 +77,11 @@ def load() -> ctypes.CDLL:
         "gr_write_then_read_host": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
         "gr_write_then_read_host_static": ([S, V, V, V, P, V, V, V], ctypes.c_int),
         "gr_selftest_bounded_wait": ([ctypes.c_int64, V], ctypes.c_int),
+        "gr_fp8_encode": ([S, V, ctypes.c_int32, V, V, V], ctypes.c_int),
+        "gr_fp8_decode": ([S, V, V, V, ctypes.c_int32, V], ctypes.c_int),
+        "gr_read_fp8": ([S, V, V, P, V, V, V], ctypes.c_int),
+        "gr_write_fp8": ([S, V, V, V, V, V], ctypes.c_int),
+        "gr_write_then_read_fp8": ([S, V, V, V, V, P, V, V, V], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -87,7 +96,8 @@ def status_string(status: int) -> str:
 
 
 def kernel_path(n_tokens: int, d_model: int, rank: int, dtype: torch.dtype) -> str:
-    """Which kernel a read or fused step of this shape runs ("fused_bf16" or "generic")."""
+    """Which kernel a read or fused step of this shape runs ("fused_bf16", "tiled_bf16",
+    "tiled_fp8" for dtype FP8, or "generic")."""
     return load().gr_kernel_path(ctypes.byref(make_shape(n_tokens, d_model, rank, dtype))).decode()
 
 
@@ -115,9 +125,9 @@ def _dev(t: torch.Tensor, name: str) -> None:
 
 def make_shape(n_tokens: int, d_model: int, rank: int, dtype: torch.dtype,
                eps: float = 1e-6) -> Shape:
-    if dtype not in _DTYPES:
-        raise ValueError(f"state dtype must be float32 or bfloat16, got {dtype}")
-    return Shape(int(n_tokens), int(d_model), 4, int(rank), _DTYPES[dtype], float(eps))
+    if dtype not in _SHAPE_DTYPES:
+        raise ValueError(f"state dtype must be float32, bfloat16 or FP8, got {dtype}")
+    return Shape(int(n_tokens), int(d_model), 4, int(rank), _SHAPE_DTYPES[dtype], float(eps))
 
 
 class Params:
@@ -292,3 +302,94 @@ def write_then_read_host_static(R: torch.Tensor, y: torch.Tensor, s_prev: torch.
         ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev), params.ref(), _ptr(x), _ptr(s_next),
         _stream(stream)), "gr_write_then_read_host_static")
     return x, s_next
+
+
+# ---- FP8 branch state (e4m3 codes, one power-of-two exponent per 32-channel block) ------------
+
+def _fp8_state(codes: torch.Tensor, scales: torch.Tensor):
+    _dev(codes, "codes")
+    _dev(scales, "scales")
+    if codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
+        raise ValueError("codes and scales must be uint8")
+    if codes.dim() != 3 or codes.shape[1] != 4 or codes.shape[2] % 32:
+        raise ValueError("codes must have shape [N, 4, D] with D a multiple of 32")
+    N, _, D = codes.shape
+    if tuple(scales.shape) != (N, 4, D // 32):
+        raise ValueError("scales must have shape [N, 4, D/32]")
+    return N, D
+
+
+def fp8_encode(R: torch.Tensor, codes: torch.Tensor | None = None,
+               scales: torch.Tensor | None = None, stream=None):
+    """gr_fp8_encode: a bf16 or fp32 state R [N,4,D] -> (codes [N,4,D], scales [N,4,D/32])."""
+    _dev(R, "R")
+    if R.dtype not in _DTYPES or R.dim() != 3 or R.shape[1] != 4:
+        raise ValueError("R must be a float32 or bfloat16 tensor of shape [N, 4, D]")
+    N, _, D = R.shape
+    codes = torch.empty((N, 4, D), dtype=torch.uint8, device=R.device) if codes is None else codes
+    scales = torch.empty((N, 4, D // 32), dtype=torch.uint8, device=R.device) if scales is None \
+        else scales
+    _fp8_state(codes, scales)
+    shape = make_shape(N, D, 1, FP8)
+    _check(load().gr_fp8_encode(ctypes.byref(shape), _ptr(R), _DTYPES[R.dtype], _ptr(codes),
+                                _ptr(scales), _stream(stream)), "gr_fp8_encode")
+    return codes, scales
+
+
+def fp8_decode(codes: torch.Tensor, scales: torch.Tensor, dtype: torch.dtype = torch.float32,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gr_fp8_decode: (codes, scales) -> the state's values [N,4,D] in float32 or bfloat16."""
+    N, D = _fp8_state(codes, scales)
+    if dtype not in _DTYPES:
+        raise ValueError("dtype must be float32 or bfloat16")
+    out = torch.empty((N, 4, D), dtype=dtype, device=codes.device) if out is None else out
+    _dev(out, "out")
+    shape = make_shape(N, D, 1, FP8)
+    _check(load().gr_fp8_decode(ctypes.byref(shape), _ptr(codes), _ptr(scales), _ptr(out),
+                                _DTYPES[dtype], _stream(stream)), "gr_fp8_decode")
+    return out
+
+
+def read_fp8(codes: torch.Tensor, scales: torch.Tensor, params: Params,
+             x: torch.Tensor | None = None, s: torch.Tensor | None = None, stream=None):
+    """gr_read_fp8: FP8 state -> (x [N,D] bf16, s [N,4] fp32)."""
+    N, D = _fp8_state(codes, scales)
+    shape = make_shape(N, D, params.rank, FP8, params.eps)
+    x = torch.empty((N, D), dtype=torch.bfloat16, device=codes.device) if x is None else x
+    s = torch.empty((N, 4), dtype=torch.float32, device=codes.device) if s is None else s
+    _dev(x, "x")
+    _dev(s, "s")
+    _check(load().gr_read_fp8(ctypes.byref(shape), _ptr(codes), _ptr(scales), params.ref(),
+                              _ptr(x), _ptr(s), _stream(stream)), "gr_read_fp8")
+    return x, s
+
+
+def write_fp8(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor, s: torch.Tensor,
+              stream=None):
+    """gr_write_fp8: R += s_i y on the FP8 state (y bf16 [N,D]), in place."""
+    N, D = _fp8_state(codes, scales)
+    _dev(y, "y")
+    _dev(s, "s")
+    shape = make_shape(N, D, 1, FP8)
+    _check(load().gr_write_fp8(ctypes.byref(shape), _ptr(codes), _ptr(scales), _ptr(y), _ptr(s),
+                               _stream(stream)), "gr_write_fp8")
+    return codes, scales
+
+
+def write_then_read_fp8(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor,
+                        s_prev: torch.Tensor, params: Params, x: torch.Tensor | None = None,
+                        s_next: torch.Tensor | None = None, stream=None):
+    """gr_write_then_read_fp8: the write in place on the FP8 state, then the read with
+    `params` -> (x [N,D] bf16, s_next [N,4] fp32)."""
+    N, D = _fp8_state(codes, scales)
+    shape = make_shape(N, D, params.rank, FP8, params.eps)
+    x = torch.empty((N, D), dtype=torch.bfloat16, device=codes.device) if x is None else x
+    s_next = torch.empty((N, 4), dtype=torch.float32, device=codes.device) if s_next is None \
+        else s_next
+    for t, n in ((y, "y"), (s_prev, "s_prev"), (x, "x"), (s_next, "s_next")):
+        _dev(t, n)
+    _check(load().gr_write_then_read_fp8(ctypes.byref(shape), _ptr(codes), _ptr(scales), _ptr(y),
+                                         _ptr(s_prev), params.ref(), _ptr(x), _ptr(s_next),
+                                         _stream(stream)), "gr_write_then_read_fp8")
+    return x, s_next
+

@@ -7,7 +7,10 @@ Storage conventions of the returned arrays:
   * state-dtype arrays (R, y, x) are numpy ``uint16`` bf16 bit patterns for ``dtype == "bf16"``
     and ``float32`` for ``dtype == "f32"``; ``to_f64`` converts either exactly to float64;
   * parameters (gamma, W_d, W_u, W_w) and write strengths s are ``float32``. On bf16 workloads
-    the weights are rounded to bf16-representable values, so packing them to bf16 is exact.
+    the weights are rounded to bf16-representable values, so packing them to bf16 is exact;
+  * on FP8-state workloads (``dtype == "fp8"``) the state's values come as ``float32`` (the
+    consumer encodes them into the FP8 state format), y is bf16 and the weights are
+    bf16-representable, as on the bf16 path.
 
 Shapes follow the library: R ``[N, 4, D]``, y ``[N, D]``, s ``[N, 4]``, gamma ``[4, D]``,
 W_d ``[r, 4D]``, W_u ``[4D, r]``, W_w ``[4, 4D]``.
@@ -33,7 +36,7 @@ class Workload:
     n_tokens: int
     d_model: int
     rank: int
-    dtype: str  # "f32" or "bf16"
+    dtype: str  # "f32", "bf16" or "fp8" (FP8 branch state; y and x bf16)
     y_std: float
     y_kind: str = "normal"  # "normal" or "t3" (Student-t with 3 degrees of freedom)
     branch_scales: tuple = (1.0, 1.0, 1.0, 1.0)
@@ -52,7 +55,17 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
     def state_bytes_per_elem(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        return {"f32": 4, "bf16": 2, "fp8": 1}[self.dtype]
+
+    @property
+    def state_storage(self) -> str:
+        """Storage of make_state's arrays: the FP8 state's source values come as fp32."""
+        return "f32" if self.dtype == "fp8" else self.dtype
+
+    @property
+    def io_storage(self) -> str:
+        """Storage of y and x: bf16 on the FP8 path."""
+        return "bf16" if self.dtype == "fp8" else self.dtype
 
 
 WORKLOADS = {
@@ -64,6 +77,8 @@ WORKLOADS = {
     "prefill": Workload("prefill", 16384, 4096, 16, "bf16", y_std=0.5),
     # 48 layers x (token mixer, MLP) = 96 chained sublayers
     "deep_stack": Workload("deep_stack", 8192, 2048, 16, "bf16", y_std=0.1, n_sublayers=96),
+    # prefill with the FP8 branch state (e4m3 codes + per-32-channel exponents; y, x bf16)
+    "prefill_fp8": Workload("prefill_fp8", 16384, 4096, 16, "fp8", y_std=0.5),
     # skewed branch scales, 1% outlier channels x50, heavy-tailed y
     "large_skewed": Workload("large_skewed", 65536, 7168, 32, "bf16", y_std=0.5, y_kind="t3",
                              branch_scales=(0.1, 1.0, 10.0, 100.0), outlier_frac=0.01,
@@ -167,7 +182,7 @@ def make_state(w: Workload, n_tokens: int | None = None) -> np.ndarray:
             R[:, :, ch] *= np.float32(w.outlier_mult)
         return R
 
-    return _draw_rows(w, _K_STATE, 0, n, (N_BRANCH, w.d_model), fill, w.dtype)
+    return _draw_rows(w, _K_STATE, 0, n, (N_BRANCH, w.d_model), fill, w.state_storage)
 
 
 def make_y(w: Workload, layer: int = 0, n_tokens: int | None = None) -> np.ndarray:
@@ -181,7 +196,7 @@ def make_y(w: Workload, layer: int = 0, n_tokens: int | None = None) -> np.ndarr
             return rng.standard_normal((rows, w.d_model), dtype=np.float32) * np.float32(w.y_std)
         return (w.y_std * rng.standard_t(3, size=(rows, w.d_model))).astype(np.float32)
 
-    return _draw_rows(w, _K_Y, layer, n, (w.d_model,), fill, w.dtype)
+    return _draw_rows(w, _K_Y, layer, n, (w.d_model,), fill, w.io_storage)
 
 
 def make_params(w: Workload, layer: int = 0, weight_mult: float = 1.0) -> dict:
@@ -194,7 +209,7 @@ def make_params(w: Workload, layer: int = 0, weight_mult: float = 1.0) -> dict:
     Wd = (std * rng.standard_normal((w.rank, K))).astype(np.float32)
     Wu = (std * rng.standard_normal((K, w.rank))).astype(np.float32)
     Ww = (std * rng.standard_normal((N_BRANCH, K))).astype(np.float32)
-    if w.dtype == "bf16":
+    if w.dtype in ("bf16", "fp8"):
         Wd, Wu, Ww = round_to_bf16(Wd), round_to_bf16(Wu), round_to_bf16(Ww)
     gamma = np.ones((N_BRANCH, w.d_model), dtype=np.float32)
     return {"gamma": gamma, "w_down": Wd, "w_up": Wu, "w_write": Ww}

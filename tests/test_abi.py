@@ -136,3 +136,64 @@ def test_kernel_path_selection(lib, D, r, dtype, path):
     sh = _shape(n=100, d=D, r=r, dt=dtype)
     assert lib.gr_kernel_path(ctypes.byref(sh)).decode() == path
     assert lib.gr_kernel_path(ctypes.byref(_shape(d=12))).decode() == "invalid"
+
+
+def test_fp8_calls_validate_before_any_launch(lib):
+    """The FP8-state entries: dtype, width, rank, NULL, alignment and aliasing are checked on
+    the host first; valid arguments get as far as the device check (no GPU here)."""
+    E = header_constant
+    null = ctypes.c_void_p(None)
+    P = gr.ParamsStruct()
+    P.tag, P.packed = gr.GR_PARAMS_TAG, 0x1000
+    P.d_model, P.n_branch, P.rank, P.state_dtype = 4096, 4, 16, gr.GR_FP8
+    sh = _shape(n=64, d=4096, r=16, dt=gr.GR_FP8)
+    pr = ctypes.byref(P)
+    # encode / decode
+    assert lib.gr_fp8_encode(ctypes.byref(_shape(d=4096, dt=gr.GR_BF16)), FAKE, gr.GR_BF16,
+                             FAKE2, FAKE3, null) == E("GR_E_DTYPE")
+    assert lib.gr_fp8_encode(sh, FAKE, 7, FAKE2, FAKE3, null) == E("GR_E_DTYPE")
+    assert lib.gr_fp8_encode(ctypes.byref(_shape(d=48, dt=gr.GR_FP8)), FAKE, gr.GR_BF16, FAKE2,
+                             FAKE3, null) == E("GR_E_SHAPE")
+    assert lib.gr_fp8_encode(ctypes.byref(_shape(n=0, d=4096, dt=gr.GR_FP8)), null, gr.GR_BF16,
+                             null, null, null) == 0
+    assert lib.gr_fp8_encode(sh, null, gr.GR_BF16, FAKE2, FAKE3, null) == E("GR_E_NULL")
+    assert lib.gr_fp8_encode(sh, ctypes.c_void_p(0x10008), gr.GR_BF16, FAKE2, FAKE3,
+                             null) == E("GR_E_ALIGN")
+    assert lib.gr_fp8_encode(sh, FAKE, gr.GR_BF16, FAKE2, ctypes.c_void_p(0x20000000 + 4096),
+                             null) == E("GR_E_ALIAS")
+    assert lib.gr_fp8_encode(sh, FAKE, gr.GR_BF16, FAKE2, FAKE3, null) == E("GR_E_DEVICE")
+    assert lib.gr_fp8_decode(sh, FAKE2, FAKE3, FAKE, 3, null) == E("GR_E_DTYPE")
+    assert lib.gr_fp8_decode(sh, FAKE2, FAKE3, FAKE, gr.GR_F32, null) == E("GR_E_DEVICE")
+    # the read calls need the two-pass kernel's shapes
+    for d, code in ((160, "GR_E_SHAPE"), (8320, "GR_E_SHAPE"), (4096, "GR_E_DEVICE")):
+        P.d_model = d
+        s2 = _shape(n=64, d=d, r=16, dt=gr.GR_FP8)
+        assert lib.gr_read_fp8(ctypes.byref(s2), FAKE2, FAKE3, pr, FAKE4, FAKE5,
+                               null) == E(code), d
+    P.rank = 33
+    assert lib.gr_read_fp8(ctypes.byref(_shape(n=64, d=4096, r=33, dt=gr.GR_FP8)), FAKE2, FAKE3,
+                           pr, FAKE4, FAKE5, null) == E("GR_E_RANK")
+    P.rank, P.state_dtype = 16, gr.GR_BF16
+    assert lib.gr_read_fp8(sh, FAKE2, FAKE3, pr, FAKE4, FAKE5, null) == E("GR_E_PARAMS")
+    P.state_dtype = gr.GR_FP8
+    # x overlapping the codes is refused; x == y (F's in/out buffer) is allowed
+    assert lib.gr_write_then_read_fp8(sh, FAKE2, FAKE3, FAKE, FAKE5, pr, FAKE2, FAKE4,
+                                      null) == E("GR_E_ALIAS")
+    assert lib.gr_write_then_read_fp8(sh, FAKE2, FAKE3, FAKE, FAKE5, pr, FAKE, FAKE4,
+                                      null) == E("GR_E_DEVICE")
+    assert lib.gr_write_fp8(sh, FAKE2, FAKE2, FAKE, FAKE5, null) == E("GR_E_ALIAS")
+    assert lib.gr_write_fp8(sh, FAKE2, FAKE3, FAKE, FAKE5, null) == E("GR_E_DEVICE")
+    # the bf16/fp32 entries do not take an FP8 shape
+    assert lib.gr_read(sh, FAKE, pr, FAKE2, FAKE3, null) == E("GR_E_DTYPE")
+    assert lib.gr_write(sh, FAKE, FAKE2, FAKE3, null) == E("GR_E_DTYPE")
+
+
+def test_fp8_kernel_path_and_packing(lib):
+    def path(d, r):
+        return lib.gr_kernel_path(ctypes.byref(_shape(n=100, d=d, r=r, dt=gr.GR_FP8))).decode()
+    assert path(4096, 16) == "tiled_fp8" and path(7168, 32) == "tiled_fp8"
+    assert path(128, 1) == "tiled_fp8" and path(8192, 8) == "tiled_fp8"
+    assert path(160, 8) == "invalid" and path(8320, 8) == "invalid" and path(4096, 33) == "invalid"
+    n = ctypes.c_size_t(0)
+    assert lib.gr_packed_size(ctypes.byref(_shape(d=4096, r=16, dt=gr.GR_FP8)),
+                              ctypes.byref(n)) == 0 and n.value > 0
