@@ -57,14 +57,19 @@ def parse_args(argv=None):
 
 def bytes_per_token(w) -> int:
     """Algorithmic HBM bytes of one token in the fused step: R read and written (4·D each),
-    y read, x written (D each), s_prev read and s_next written (4 fp32 each)."""
+    y read, x written (D each), s_prev read and s_next written (4 fp32 each). On the FP8 state
+    R is 4·D one-byte codes plus 4·D/32 one-byte block exponents, and y and x are bf16."""
+    D = w.d_model
+    if w.dtype == "fp8":
+        return 2 * (4 * D + 4 * D // 32) + 2 * D * 2 + 2 * 4 * 4
     b = w.state_bytes_per_elem()
-    return 2 * 4 * w.d_model * b + 2 * w.d_model * b + 2 * 4 * 4
+    return 2 * 4 * D * b + 2 * D * b + 2 * 4 * 4
 
 
 def weight_bytes(w) -> int:
-    """Parameter bytes a fused launch reads once: W_d, W_w, W_u in the state dtype, gamma fp32."""
-    b = w.state_bytes_per_elem()
+    """Parameter bytes a fused launch reads once: W_d, W_w, W_u (fp32 on the fp32 path, bf16
+    otherwise), gamma fp32."""
+    b = 4 if w.dtype == "f32" else 2
     K = 4 * w.d_model
     return (2 * w.rank + 4) * K * b + K * 4
 
@@ -86,7 +91,7 @@ def load_peaks() -> dict:
 def kernel_source_sha(kernel_path: str) -> str:
     from stream_gated_residual_gb300 import build as gbuild
     name = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
-            "generic": "gr_generic.cu"}[kernel_path]
+            "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu"}[kernel_path]
     h = hashlib.sha256()
     for p in (os.path.join(gbuild.CSRC, name), os.path.join(gbuild.CSRC, "gr_internal.h"),
               os.path.join(gbuild.CSRC, "gr_ptx.cuh")):
@@ -178,10 +183,13 @@ class OracleInputs:
     """The workload's inputs in fp64 for the first n tokens (generated once)."""
 
     def __init__(self, w, n_tokens: int):
+        import oracle
         from stream_gated_residual_gb300 import workloads as wl
         self.w = w
         self.n = n_tokens
         self.R = wl.to_f64(wl.make_state(w, n_tokens))
+        if w.dtype == "fp8":   # the FP8 state of the same values (the oracle's own encoding)
+            self.codes, self.scales = oracle.fp8_encode(self.R)
         self.y = wl.to_f64(wl.make_y(w, 0, n_tokens))
         self.sp = wl.make_s_prev(w, n_tokens)
         self.p = wl.make_params(w, 1)
@@ -190,7 +198,11 @@ class OracleInputs:
         """Seconds of one fused oracle step on tokens a..b-1."""
         import oracle
         t0 = time.perf_counter()
-        oracle.write_then_read(self.R[a:b], self.y[a:b], self.sp[a:b], self.p, self.w.eps)
+        if self.w.dtype == "fp8":
+            oracle.write_then_read_fp8(self.codes[a:b], self.scales[a:b], self.y[a:b],
+                                       self.sp[a:b], self.p, self.w.eps)
+        else:
+            oracle.write_then_read(self.R[a:b], self.y[a:b], self.sp[a:b], self.p, self.w.eps)
         return time.perf_counter() - t0
 
 
@@ -290,7 +302,9 @@ def run_gr(args, w) -> None:
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     gr.load()
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    fp8 = w.dtype == "fp8"
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16   # y and x
+    sdt = gr.FP8 if fp8 else tdt                                  # the state, for shapes
 
     # each rank owns its own shard of tokens (a different seed), same size on every rank
     wr = shard(w, rank)
@@ -302,19 +316,33 @@ def run_gr(args, w) -> None:
 
     R_h, y_h, sp_h = wl.make_state(wr), wl.make_y(wr), wl.make_s_prev(wr)
     p = wl.make_params(wr, 1)
-    R, y = dev_tensor(R_h), dev_tensor(y_h)
+    y = dev_tensor(y_h)
+    if fp8:   # the FP8 state, encoded by the library from the workload's fp32 values
+        src = dev_tensor(R_h)
+        codes, scales = gr.fp8_encode(src)
+        del src
+        state = (codes, scales)
+    else:
+        R = dev_tensor(R_h)
+        state = (R,)
     s_a = torch.from_numpy(sp_h).to(dev)
     s_b = torch.empty_like(s_a)
     x = torch.empty((w.n_tokens, w.d_model), dtype=tdt, device=dev)
     pt = {k: torch.from_numpy(v).to(dev) for k, v in p.items()}
-    P = gr.pack_params(pt["gamma"], pt["w_down"], pt["w_up"], pt["w_write"], tdt, w.eps)
-    path = gr.kernel_path(w.n_tokens, w.d_model, w.rank, tdt)
+    P = gr.pack_params(pt["gamma"], pt["w_down"], pt["w_up"], pt["w_write"], sdt, w.eps)
+    path = gr.kernel_path(w.n_tokens, w.d_model, w.rank, sdt)
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 1
 
+    def fused(sp, sn, st):
+        if fp8:
+            gr.write_then_read_fp8(codes, scales, y, sp, P, x=x, s_next=sn, stream=st)
+        else:
+            gr.write_then_read(R, y, sp, P, x=x, s_next=sn, stream=st)
+
     def step(i):
         sp, sn = (s_a, s_b) if i % 2 == 0 else (s_b, s_a)
-        gr.write_then_read(R, y, sp, P, x=x, s_next=sn, stream=stream)
+        fused(sp, sn, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -325,12 +353,13 @@ def run_gr(args, w) -> None:
     # Inputs at least twice the L2 stream from HBM by themselves; smaller ones (decode) get the
     # L2 flushed before every step, outside that step's timed window.
     l2_bytes = int(getattr(props, "L2_cache_size", 0) or (128 << 20))
-    in_bytes = sum(t.numel() * t.element_size() for t in (R, y, x, s_a, s_b))
+    in_bytes = sum(t.numel() * t.element_size() for t in (*state, y, x, s_a, s_b))
     flush = in_bytes < 2 * l2_bytes
     fbuf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
     l2_note = (f"L2 flushed before every step ({2 * l2_bytes >> 20} MiB written; inputs "
                f"{in_bytes >> 20} MiB), per-step event windows" if flush else
-               f"inputs larger than L2 (state {R_h.nbytes >> 20} MiB), no flush")
+               f"inputs larger than L2 (state "
+               f"{sum(t.numel() * t.element_size() for t in state) >> 20} MiB), no flush")
 
     # The timed steps replay CUDA graphs of the same launches (no host work per step: the small
     # workloads are otherwise bound by the host's launch path). With the flush, one graph per
@@ -344,7 +373,7 @@ def run_gr(args, w) -> None:
                 cs = torch.cuda.current_stream(dev)
                 for i in rng_:
                     sp, sn = (s_a, s_b) if i % 2 == 0 else (s_b, s_a)
-                    gr.write_then_read(R, y, sp, P, x=x, s_next=sn, stream=cs)
+                    fused(sp, sn, cs)
             g_.replay()   # one untimed replay
             graphs.append(g_)
         torch.cuda.synchronize(dev)
@@ -419,34 +448,13 @@ def run_gr(args, w) -> None:
     ref_gbs = 3 * xr.numel() * xr.element_size() / (e0.elapsed_time(e1) / nref / 1e3) / 1e9
     del xr, yr
 
-    # end to end through the host-buffer C entry: H2D of R, y, s_prev; D2H of R', x, s_next
-    Rh = torch.from_numpy(R_h.view(np.int16) if R_h.dtype == np.uint16 else R_h)
-    yh = torch.from_numpy(y_h.view(np.int16) if y_h.dtype == np.uint16 else y_h)
-    if tdt == torch.bfloat16:
-        Rh, yh = Rh.view(torch.bfloat16), yh.view(torch.bfloat16)
-    Rh, yh = Rh.pin_memory(), yh.pin_memory()
-    sph = torch.from_numpy(sp_h).pin_memory()
-    xh = torch.empty((w.n_tokens, w.d_model), dtype=tdt).pin_memory()
-    snh = torch.empty((w.n_tokens, 4), dtype=torch.float32).pin_memory()
-    nws = gr.host_workspace_size(w.n_tokens, w.d_model, tdt)
-    del R, y, x, s_a, s_b
+    if fp8:
+        e2e = e2e_fp8(args, w, world, dev, stream, codes, scales, y, s_a, x, s_b, fused)
+    else:
+        e2e = e2e_host_entry(args, w, world, dev, stream, tdt, R_h, y_h, sp_h, P)
+        del R
+    del state, y, x, s_a, s_b
     torch.cuda.empty_cache()
-    wsb = torch.empty(nws + 256, dtype=torch.uint8, device=dev)
-    ws = wsb[(-wsb.data_ptr()) % 256:][:nws]
-    for _ in range(3):  # warm-up (the first transfers from freshly pinned pages are slow)
-        gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
-    if world > 1:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-    es = w.state_bytes_per_elem()
-    h2d = w.n_tokens * (4 * w.d_model * es + w.d_model * es + 16)
-    d2h = h2d
-    e2e = {"value": job_tokens_per_s(world, w.n_tokens, args.e2e_steps, e2e_s), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "api": "gr_write_then_read_host (pinned host buffers)"}
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -475,6 +483,72 @@ def run_gr(args, w) -> None:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def e2e_host_entry(args, w, world, dev, stream, tdt, R_h, y_h, sp_h, P) -> dict:
+    """End to end through the host-buffer C entry: H2D of R, y, s_prev; D2H of R', x, s_next."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from stream_gated_residual_gb300 import gr
+    Rh = torch.from_numpy(R_h.view(np.int16) if R_h.dtype == np.uint16 else R_h)
+    yh = torch.from_numpy(y_h.view(np.int16) if y_h.dtype == np.uint16 else y_h)
+    if tdt == torch.bfloat16:
+        Rh, yh = Rh.view(torch.bfloat16), yh.view(torch.bfloat16)
+    Rh, yh = Rh.pin_memory(), yh.pin_memory()
+    sph = torch.from_numpy(sp_h).pin_memory()
+    xh = torch.empty((w.n_tokens, w.d_model), dtype=tdt).pin_memory()
+    snh = torch.empty((w.n_tokens, 4), dtype=torch.float32).pin_memory()
+    nws = gr.host_workspace_size(w.n_tokens, w.d_model, tdt)
+    wsb = torch.empty(nws + 256, dtype=torch.uint8, device=dev)
+    ws = wsb[(-wsb.data_ptr()) % 256:][:nws]
+    for _ in range(3):  # warm-up (the first transfers from freshly pinned pages are slow)
+        gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        gr.write_then_read_host(Rh, yh, sph, P, xh, snh, ws, stream=stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    es = w.state_bytes_per_elem()
+    h2d = w.n_tokens * (4 * w.d_model * es + w.d_model * es + 16)
+    d2h = h2d
+    return {"value": job_tokens_per_s(world, w.n_tokens, args.e2e_steps, e2e_s), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "gr_write_then_read_host (pinned host buffers)"}
+
+
+def e2e_fp8(args, w, world, dev, stream, codes, scales, y, s_prev, x, s_next, fused) -> dict:
+    """End to end on the FP8 state: per step, pinned host copies of the codes, exponents, y and
+    s_prev go to the device, gr_write_then_read_fp8 runs, and the written codes and exponents,
+    x and s_next come back (torch copies on the same stream, not pipelined)."""
+    import torch
+    import torch.distributed as dist
+    host = [t.cpu().pin_memory() for t in (codes, scales, y, s_prev)]
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (codes, scales, x, s_next)]
+
+    def one():
+        for h, d in zip(host, (codes, scales, y, s_prev)):
+            d.copy_(h, non_blocking=True)
+        fused(s_prev, s_next, stream)
+        for h, d in zip(outs, (codes, scales, x, s_next)):
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (codes, scales, y, s_prev))
+    d2h = sum(t.numel() * t.element_size() for t in (codes, scales, x, s_next))
+    return {"value": job_tokens_per_s(world, w.n_tokens, args.e2e_steps, e2e_s), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "gr_write_then_read_fp8 with pinned-host torch copies on the same stream"}
 
 
 def main(argv=None):
