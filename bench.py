@@ -90,11 +90,15 @@ def load_peaks() -> dict:
 
 def kernel_source_sha(kernel_path: str) -> str:
     from stream_gated_residual_gb300 import build as gbuild
-    name = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
-            "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu"}[kernel_path]
+    files = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
+             "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu"}
+    # a split path ("fused_bf16+tiled_bf16") hashes both kernels' sources and the dispatch
+    names = [files[k] for k in kernel_path.split("+")]
+    if len(names) > 1:
+        names.append("gr_api.cu")
     h = hashlib.sha256()
-    for p in (os.path.join(gbuild.CSRC, name), os.path.join(gbuild.CSRC, "gr_internal.h"),
-              os.path.join(gbuild.CSRC, "gr_ptx.cuh")):
+    for p in [os.path.join(gbuild.CSRC, n) for n in names] + [
+            os.path.join(gbuild.CSRC, "gr_internal.h"), os.path.join(gbuild.CSRC, "gr_ptx.cuh")]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -332,7 +336,7 @@ def run_gr(args, w) -> None:
     P = gr.pack_params(pt["gamma"], pt["w_down"], pt["w_up"], pt["w_write"], sdt, w.eps)
     path = gr.kernel_path(w.n_tokens, w.d_model, w.rank, sdt)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1
+    launches_per_step = len(path.split("+"))   # "fused_bf16+tiled_bf16": two kernels a step
 
     def fused(sp, sn, st):
         if fp8:

@@ -96,6 +96,9 @@ const char* gr_status_string(int status);
 
 /* Name of the kernel path a read or fused step takes for `shape` (static string, never NULL):
  * "fused_bf16" (cluster tensor-core kernel: bf16, D in {256, 512, 1024, 2048, 4096}, r <= 16),
+ * "fused_bf16+tiled_bf16" (the same shapes when n_tokens is large enough that a share of the
+ * tokens also runs on the two-pass kernel, concurrently, on the SMs the clusters leave idle;
+ * this form needs the device, so without one the plain "fused_bf16" is reported),
  * "tiled_bf16" (two-pass tensor-core kernel: the other bf16 shapes with D % 64 == 0, r <= 32),
  * "tiled_fp8" (the two-pass kernel on an FP8 state), "generic" (one CTA per token), or
  * "invalid". Host only. */
@@ -129,7 +132,12 @@ int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void
  *   x, s_next  = read of the written (stored) R with `next`       (eq rms … eq s)
  * y and x may be the same buffer (F's input/output buffer), and s_prev and s_next may be the
  * same buffer: each token's y and s_prev are read before its x and s_next are written. Apart
- * from those two exact matches, x and s_next must not overlap R, y, s_prev or each other. */
+ * from those two exact matches, x and s_next must not overlap R, y, s_prev or each other.
+ * On the "fused_bf16+tiled_bf16" path (here and in gr_read) the trailing share of the tokens
+ * runs on an internal per-device stream that first waits for the work already queued on
+ * `stream`, and `stream` then waits for it, so the call stays ordered on `stream`; that stream
+ * and two events are created on the first such call (CUDA graph capture of the call captures
+ * the fork and the join). */
 int gr_write_then_read(const gr_shape* shape, void* R, const void* y, const float* s_prev,
                        const gr_params* next, void* x, float* s_next, void* stream);
 

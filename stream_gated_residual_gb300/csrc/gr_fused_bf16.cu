@@ -28,8 +28,9 @@
 //       the warp gathers the token's row sums from every CTA, forms inv, h and s with warp
 //       shuffles only, and sends h and inv to every CTA of the cluster. Warp b also owns 32
 //       channels of all four branches and keeps its W_u fragments in registers: for each tile
-//       it waits for h and inv, runs the up projection on the tensor cores (h split into bf16
-//       hi + lo parts), forms σ(a) = ½ + ½·tanh(a/2) (W_u pre-scaled by ½), combines the
+//       it waits for h and inv, runs the up projection on the tensor cores in fp16 (½·W_u
+//       packed as fp16; each token's h row scaled by an exact power of two that keeps it below
+//       2^15, undone on the accumulator), forms σ(a) = ½ + ½·tanh(a/2), combines the
 //       branches from the in-place R', stores x, and releases the R buffer for the next TMA.
 //   * mbarriers carry every hand-off (TMA completion, R' ready, R buffer empty, row sums and h
 //     arriving from other CTAs); there is no cluster-wide barrier in the steady state.
@@ -475,18 +476,35 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
             const float* bc = bcast_ptr(p);
-            uint32_t ahi[4], alo[4];
+            // h as fp16 A fragments (11 significant bits, as the packed ½·W_u), each token's row
+            // scaled by an exact power of two that keeps it below 2^15; the scale is undone on
+            // the fp32 accumulator
+            uint32_t ah[4];
+            float2 hv2[4];
+            float ma = 0.f, mb = 0.f;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int tk = g + 8 * (m & 1), kc = 2 * q4 + 8 * (m >> 1);
                 // h[kc], h[kc+1] (zero past r: the row is zero padded after h)
-                const float2 hp = kc < r ? *reinterpret_cast<const float2*>(bc + tk * nb4 + 4 + kc)
-                                         : make_float2(0.f, 0.f);
-                const float h0 = hp.x, h1 = hp.y;
-                const float h0h = __bfloat162float(__float2bfloat16_rn(h0));
-                const float h1h = __bfloat162float(__float2bfloat16_rn(h1));
-                ahi[m] = pack_bf2(h0h, h1h);
-                alo[m] = pack_bf2(h0 - h0h, h1 - h1h);
+                hv2[m] = kc < r ? *reinterpret_cast<const float2*>(bc + tk * nb4 + 4 + kc)
+                                : make_float2(0.f, 0.f);
+                const float mm = fmaxf(fabsf(hv2[m].x), fabsf(hv2[m].y));
+                if (m & 1) mb = fmaxf(mb, mm);
+                else ma = fmaxf(ma, mm);
+            }
+            // the four lanes of a quad hold the whole row of a token
+            ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+            ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+            const int ea = min(max(((__float_as_int(ma) >> 23) & 0xff) - 127 - 14, 0), 126);
+            const int eb = min(max(((__float_as_int(mb) >> 23) & 0xff) - 127 - 14, 0), 126);
+            const float sa = __int_as_float((127 - ea) << 23), sb = __int_as_float((127 - eb) << 23);
+            const float ua = __int_as_float((127 + ea) << 23), ub = __int_as_float((127 + eb) << 23);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float sc = (m & 1) ? sb : sa;
+                ah[m] = pack_h2(hv2[m].x * sc, hv2[m].y * sc);
             }
             uint64_t xacc2[2][4];   // [row][channel pair], packed fp32 pairs
 #pragma unroll
@@ -514,8 +532,11 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float c[4];
-                    mma_bf16_z(c, ahi[0], ahi[1], ahi[2], ahi[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
-                    mma_bf16(c, alo[0], alo[1], alo[2], alo[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
+                    mma_f16_z(c, ah[0], ah[1], ah[2], ah[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
+                    c[0] *= ua;
+                    c[1] *= ua;
+                    c[2] *= ub;
+                    c[3] *= ub;
                     const uint64_t gm2 = f2(gm[2 * j], gm[2 * j + 1]);
                     const uint64_t u0 = mul2(gm2, bf2_to_f2(q0[j]));   // γ·R' (row g)
                     const uint64_t u1 = mul2(gm2, bf2_to_f2(q1[j]));   // γ·R' (row g+8)
@@ -620,10 +641,11 @@ __global__ void pack_fused_kernel(int D, int r, const float* __restrict__ gamma,
             const int gg = lane >> 2, qq = lane & 3;
             const int m = i * D + q * kDq + bw * 32 + 8 * (gg >> 1) + 2 * j + (gg & 1);
             const int kk[4] = {2 * qq, 2 * qq + 1, 2 * qq + 8, 2 * qq + 9};
-            __nv_bfloat16* dst =
-                reinterpret_cast<__nv_bfloat16*>(slice + S.down_bytes + size_t(u) * 8);
-            for (int t = 0; t < 4; ++t)
-                dst[t] = __float2bfloat16_rn(kk[t] < r ? 0.5f * wu[size_t(m) * r + kk[t]] : 0.f);
+            __half* dst = reinterpret_cast<__half*>(slice + S.down_bytes + size_t(u) * 8);
+            for (int t = 0; t < 4; ++t) {
+                const float v = kk[t] < r ? 0.5f * wu[size_t(m) * r + kk[t]] : 0.f;
+                dst[t] = __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
+            }
         } else {
             u -= n_up;
             const int i = u / kDq, cl = u - i * kDq;
@@ -670,15 +692,12 @@ struct ClusterCache {
 };
 ClusterCache g_cluster_cache[64];
 
+// Kernel attributes and the launch configuration (all but grid and stream) of one
+// instantiation, and the number of its clusters that can be resident at once (queried once per
+// device and cached).
 template <bool WRITE, int NTD>
-cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
-                     const float* s_prev, const char* frag, void* x, float* s_out,
-                     cudaStream_t st) {
-    const FusedShape S = fused_shape(D, r);
-    CUtensorMap mR, my;
-    memset(&my, 0, sizeof(my));
-    if (!make_map_R(&mR, R, N, D)) return cudaErrorInvalidValue;
-    if (WRITE && !make_map_y(&my, y, N, D)) return cudaErrorInvalidValue;
+cudaError_t prepare_t(const FusedShape& S, cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr,
+                      int& max_clusters) {
     auto kern = gr_fused_kernel<WRITE, NTD>;
     // the register split assumes this launch size; anything else could stall setmaxnreg.inc
     cudaFuncAttributes fa;
@@ -691,8 +710,7 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cfg = cudaLaunchConfig_t{};
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(S.C);
     attr[0].val.clusterDim.y = 1;
@@ -701,7 +719,6 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = size_t(S.smem_bytes);
-    cfg.stream = st;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     int lc = 0;
@@ -714,12 +731,48 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
         if (n < 1) return cudaErrorInvalidConfiguration;
         maxc = n;
     }
+    max_clusters = maxc;
+    return cudaSuccess;
+}
+
+template <bool WRITE, int NTD>
+cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, const void* y,
+                     const float* s_prev, const char* frag, void* x, float* s_out,
+                     cudaStream_t st) {
+    const FusedShape S = fused_shape(D, r);
+    CUtensorMap mR, my;
+    memset(&my, 0, sizeof(my));
+    if (!make_map_R(&mR, R, N, D)) return cudaErrorInvalidValue;
+    if (WRITE && !make_map_y(&my, y, N, D)) return cudaErrorInvalidValue;
+    auto kern = gr_fused_kernel<WRITE, NTD>;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    int maxc = 0;
+    cudaError_t e = prepare_t<WRITE, NTD>(S, cfg, attr, maxc);
+    if (e != cudaSuccess) return e;
+    cfg.stream = st;
     const int64_t ntiles = (N + kT - 1) / kT;
     const int64_t ncl = ntiles < maxc ? ntiles : maxc;
     cfg.gridDim = dim3(unsigned(ncl * S.C));
     if (N > kMaxTokens) return cudaErrorInvalidValue;
     return cudaLaunchKernelEx(&cfg, kern, mR, my, int(N), D, r, eps, s_prev, frag,
                               static_cast<__nv_bfloat16*>(x), s_out);
+}
+
+template <bool WRITE>
+int max_ctas_w(int D, int r) {
+    const FusedShape S = fused_shape(D, r);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    int maxc = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (S.ntd) {
+        case 1: e = prepare_t<WRITE, 1>(S, cfg, attr, maxc); break;
+        case 2: e = prepare_t<WRITE, 2>(S, cfg, attr, maxc); break;
+        case 3: e = prepare_t<WRITE, 3>(S, cfg, attr, maxc); break;
+        default: break;
+    }
+    return e == cudaSuccess ? maxc * S.C : 0;
 }
 
 template <bool WRITE>
@@ -744,6 +797,11 @@ bool fused_supported(int D, int r) {
 }
 
 int64_t fused_max_tokens() { return kMaxTokens; }
+
+int fused_resident_ctas(int D, int r, bool write) {
+    if (!fused_supported(D, r)) return 0;
+    return write ? max_ctas_w<true>(D, r) : max_ctas_w<false>(D, r);
+}
 
 namespace {
 // Self-test of the bounded waits: one thread waits on an mbarrier that nothing arrives at, with

@@ -26,6 +26,9 @@ constexpr int kBranches = 4;
 struct Layout {
     size_t gamma32, wdw, wut, frag, total;
     size_t frag_bytes;
+    // bf16 shapes of the cluster kernel also carry the two-pass kernel's fragments, which the
+    // two-pass kernel uses for the tokens it takes on the SMs the clusters leave idle
+    size_t frag2, frag2_bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -34,6 +37,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // kernel also needs n_tokens <= fused_max_tokens().
 bool fused_supported(int D, int r);
 int64_t fused_max_tokens();
+// CTAs of the cluster kernel that can be resident at once on the current device (clusters ×
+// cluster size; 0 if it cannot be queried).
+int fused_resident_ctas(int D, int r, bool write);
 size_t fused_frag_bytes(int D, int r);
 
 // Two-pass tensor-core kernel for the bf16 shapes the cluster kernel does not take
@@ -61,6 +67,11 @@ inline Layout make_layout(int D, int r, int dtype) {
                                                                : 0;
     L.frag = off;
     off = align256(off + L.frag_bytes);
+    L.frag2_bytes = (dtype == GR_BF16 && fused_supported(D, r) && tiled_supported(D, r))
+                        ? tiled_frag_bytes(D, r)
+                        : 0;
+    L.frag2 = off;
+    off = align256(off + L.frag2_bytes);
     L.total = off;
     return L;
 }
@@ -82,9 +93,11 @@ cudaError_t launch_fused_bf16(int64_t N, int D, int r, float eps, void* R, const
                               cudaStream_t st);
 
 // Two-pass bf16 tensor-core kernel (write then read, or read only when y == nullptr).
+// max_ctas > 0 caps the grid (the SMs left to it); the fragments come from the section the
+// packed buffer has for the two-pass kernel (frag, or frag2 on a cluster-kernel shape).
 cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
                               const float* s_prev, const void* packed, void* x, float* s_out,
-                              cudaStream_t st);
+                              cudaStream_t st, int max_ctas = 0);
 
 // The two-pass kernel on an FP8 state (codes [N][4][D], block exponents [N][4][D/32]); y and x
 // bf16; read only when y == nullptr.

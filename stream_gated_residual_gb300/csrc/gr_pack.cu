@@ -74,6 +74,10 @@ cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (L.frag2_bytes) {
+        e = launch_pack_tiled(D, r, gamma, wd, wu, ww, base + L.frag2, st);
+        if (e != cudaSuccess) return e;
+    }
     if (L.frag_bytes) {
         e = dtype == GR_BF16 && fused_supported(D, r)
                 ? launch_pack_fused(D, r, gamma, wd, wu, ww, base + L.frag, st)

@@ -22,8 +22,8 @@
 //     some are still in L2): TMA-load R' again; the up projection W_u·h on the tensor cores
 //     in fp16 (½·W_u packed as fp16; each token's h row scaled by an exact power of two that
 //     keeps it below 2^15, undone on the fp32 accumulator), σ as ½ + ½·tanh, and the combine.
-//     fp16 carries 11 significant bits for both operands, so one mma per k-step does what the
-//     cluster kernel does with bf16 hi + lo parts of h (and rounds W_u more finely). Warp
+//     fp16 carries 11 significant bits for both operands, so one mma per k-step suffices
+//     (the cluster kernel does the same). Warp
 //     (m-tile, 8-channel group) covers the four branches of its channels; x leaves through a
 //     per-warp TMA store.
 // The price is one more read of R' than the single traversal (about 40% more HBM traffic at
@@ -713,7 +713,7 @@ bool make_map_nd(CUtensorMap* m, const void* p, int64_t N, int D, int box_ch, in
 template <bool WRITE, int NTD, int KSU, bool FP8>
 cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, uint8_t* scales, const void* y,
                      const float* s_prev, const char* frag, void* x, float* s_out,
-                     cudaStream_t st) {
+                     cudaStream_t st, int max_ctas) {
     using C = TiledCfg<NTD, KSU, FP8>;
     CUtensorMap mR, mRs, my, mx;
     memset(&mRs, 0, sizeof(mRs));
@@ -728,7 +728,8 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, uint8_t* scale
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (N + kTT - 1) / kTT;
-    const int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
+    int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
     kern<<<unsigned(grid), kThreadsT, smem, st>>>(mR, mRs, my, mx, int(N), D, r, eps, s_prev,
                                                   frag, s_out, scales);
     return cudaGetLastError();
@@ -737,11 +738,11 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, uint8_t* scale
 template <int NTD, int KSU, bool FP8>
 cudaError_t launch_k(int64_t N, int D, int r, float eps, void* R, uint8_t* scales, const void* y,
                      const float* s_prev, const char* frag, void* x, float* s_out,
-                     cudaStream_t st) {
+                     cudaStream_t st, int max_ctas = 0) {
     return y ? launch_t<true, NTD, KSU, FP8>(N, D, r, eps, R, scales, y, s_prev, frag, x, s_out,
-                                             st)
+                                             st, max_ctas)
              : launch_t<false, NTD, KSU, FP8>(N, D, r, eps, R, scales, y, s_prev, frag, x, s_out,
-                                              st);
+                                              st, max_ctas);
 }
 
 }  // namespace
@@ -788,15 +789,17 @@ cudaError_t launch_pack_tiled(int D, int r, const float* gamma, const float* wd,
 
 cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
                               const float* s_prev, const void* packed, void* x, float* s_out,
-                              cudaStream_t st) {
+                              cudaStream_t st, int max_ctas) {
     if (!tiled_supported(D, r) || N < 1 || N > tiled_max_tokens()) return cudaErrorInvalidValue;
     const Layout L = make_layout(D, r, GR_BF16);
-    const char* frag = static_cast<const char*>(packed) + L.frag;
+    const char* frag = static_cast<const char*>(packed) + (L.frag2_bytes ? L.frag2 : L.frag);
     int ntd, ksu;
     tiled_cfg(r, ntd, ksu);
     if (ntd == 3)
-        return launch_k<3, 1, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st);
-    return launch_k<5, 2, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st);
+        return launch_k<3, 1, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st,
+                                     max_ctas);
+    return launch_k<5, 2, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st,
+                                 max_ctas);
 }
 
 bool tiled_fp8_supported(int D, int r) {

@@ -52,8 +52,8 @@ def bf16_path_params(p: dict, w_up: str = "bf16") -> dict:
     """The parameters the bf16 path computes with, written as oracle inputs: W_d and W_w with
     gamma folded in and rounded to bf16 (fp32 product, nearest even), divided back by gamma in
     fp64 so that the oracle's W·(γ ⊙ R) reproduces the folded weight; W_u rounded to bf16
-    (w_up="bf16", the cluster kernel) or, as ½·W_u, to fp16 (w_up="f16", the two-pass kernel,
-    which packs ½·W_u as fp16 clamped to ±65504). Computed here from the fp32 inputs, never
+    (w_up="bf16", the generic kernel) or, as ½·W_u, to fp16 (w_up="f16", the two tensor-core
+    kernels, which pack ½·W_u as fp16 clamped to ±65504). Computed here from the fp32 inputs, never
     read back from the GPU."""
     K = p["w_down"].shape[1]
     g = np.asarray(p["gamma"], dtype=np.float32).reshape(-1)
@@ -76,8 +76,9 @@ def bf16_path_params(p: dict, w_up: str = "bf16") -> dict:
 
 
 def path_params(p: dict, kernel_path: str) -> dict:
-    """bf16_path_params for the kernel that serves a shape (gr.kernel_path's name)."""
-    return bf16_path_params(p, "f16" if kernel_path == "tiled_bf16" else "bf16")
+    """bf16_path_params for the kernel that serves a shape (gr.kernel_path's name): both
+    tensor-core kernels run the up projection in fp16, the generic kernel keeps bf16 W_u."""
+    return bf16_path_params(p, "bf16" if kernel_path == "generic" else "f16")
 
 
 def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:

@@ -292,7 +292,7 @@ def test_fused_read_only(D, r, N):
     x, s = gr.read(Rt, _pack(p, "bf16", w.eps))
     torch.cuda.synchronize()
     assert torch.equal(Rt, to_torch(R))
-    pm = bf16_path_params(p)
+    pm = bf16_path_params(p, "f16")
     xo, so = oracle.read(wl.to_f64(R), pm["gamma"], pm["w_down"], pm["w_up"], pm["w_write"],
                          w.eps)
     tol = MODELED_TOL["bf16"]
@@ -330,6 +330,35 @@ def test_tiled_read_only(D, r, N):
                          w.eps)
     tol = MODELED_TOL["bf16"]
     assert rel_rows(to_f64(x), xo) < tol["x"] and rel_rows(to_f64(s), so) < tol["s"]
+    assert gr.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("N,write", [(8192, True), (16384, False)])
+def test_split_cluster_and_two_pass(N, write):
+    """A large step on a cluster-kernel shape (D = 4096, r = 16) also runs a share of its tokens
+    on the two-pass kernel, on the SMs the clusters leave idle and on a second stream: every row
+    (both shares and the boundary between them) against the oracle, for the fused step and for
+    the read alone, with sharp gates and random gains."""
+    D, r = 4096, 16
+    assert gr.kernel_path(N, D, r, torch.bfloat16) == "fused_bf16+tiled_bf16"
+    w = wl.Workload("split", N, D, r, "bf16", y_std=0.5, seed=37)
+    if write:
+        check(w, *fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    else:
+        R = wl.make_state(w)
+        p = wl.make_params(w, 1, weight_mult=5.0)
+        p["gamma"] = wl.make_random_gamma(w, 1)
+        Rt = to_torch(R)
+        x, s = gr.read(Rt, _pack(p, "bf16", w.eps))
+        torch.cuda.synchronize()
+        assert torch.equal(Rt, to_torch(R))
+        pm = path_params(p, "fused_bf16+tiled_bf16")
+        rows = np.arange(0, N, 7)
+        xo, so = oracle.read(wl.to_f64(R[rows]), pm["gamma"], pm["w_down"], pm["w_up"],
+                             pm["w_write"], w.eps)
+        sel = torch.from_numpy(rows).cuda()
+        tol = MODELED_TOL["bf16"]
+        assert rel_rows(to_f64(x[sel]), xo) < tol["x"] and rel_rows(to_f64(s[sel]), so) < tol["s"]
     assert gr.device_status(clear=True) == 0
 
 
