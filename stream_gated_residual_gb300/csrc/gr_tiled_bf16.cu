@@ -90,7 +90,15 @@ template <int NTD, int KSU, bool FP8> struct TiledCfg {
     static constexpr int off_scl = (off_abort + 16 + 127) / 128 * 128;
     static_assert(off_scl % 16 == 0, "exponent buffer must be 16-byte aligned");
     // + 4·D bytes of block exponents on the FP8 path, + slack for the 1 KB alignment
-    static int smem_bytes(int D) { return off_scl + (FP8 ? 4 * D : 0) + 1024; }
+    static int smem_bytes(int D) {
+        return off_scl + (FP8 ? kBranches * kTT * scl_stride(D) : 0) + 1024;
+    }
+    // Row stride of the on-chip exponents [32 tok][4 br] rows of D/32 bytes: padded to 4 mod 8
+    // bytes so that the rows 4g + i a warp reads together (g = 0..7) fall on 8 different banks.
+    static __host__ __device__ int scl_stride(int D) {
+        const int nblk = D / 32;   // a multiple of 4 (D % 128 == 0)
+        return nblk % 8 == 0 ? nblk + 4 : nblk;
+    }
 };
 
 // Bounded wait: one non-blocking test first (the common case: the data is there), then the
@@ -166,6 +174,7 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
     float* invb = reinterpret_cast<float*>(smem + C::off_inv);  // [4][32]
     uint8_t* scl = reinterpret_cast<uint8_t*>(smem + C::off_scl);  // FP8: [32 tok][4][D/32]
     const int nblk = D / 32;
+    const int sst = C::scl_stride(D);   // bytes between the exponent rows on chip
     auto sbuf = [&](int st) { return smem + C::off_state + st * kStateStage; };
     auto wbuf = [&](int st) { return smem + C::off_w + st * C::kWStage; };
 
@@ -254,14 +263,19 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int t0 = tile * kTT;
         if constexpr (FP8) {
-            // The tile's block exponents, [32 tok][4][D/32], contiguous in HBM: plain 16-byte
-            // loads (D % 128 == 0 keeps every row block 16-byte aligned). The first barrier
-            // waits until no warp still reads the previous tile's exponents in its pass 2.
+            // The tile's block exponents, [32 tok][4][D/32], contiguous in HBM, into padded rows
+            // on chip with 4-byte loads (D % 128 == 0: every row is a whole number of words).
+            // The first barrier waits until no warp still reads the previous tile's exponents
+            // in its pass 2.
             named_sync(1, kCThreads);
             const int nv = min(kTT, N - t0);
-            const int nvec = int(size_t(nv) * size_t(D) / 128);
-            const uint4* src = reinterpret_cast<const uint4*>(scales + size_t(t0) * (D / 8));
-            for (int e = tid; e < nvec; e += kCThreads) reinterpret_cast<uint4*>(scl)[e] = src[e];
+            const int wpr = nblk / 4;   // words per row
+            const int nw = nv * kBranches * wpr;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(scales + size_t(t0) * (D / 8));
+            for (int e = tid; e < nw; e += kCThreads) {
+                const int row = e / wpr, w = e - row * wpr;
+                *reinterpret_cast<uint32_t*>(scl + row * sst + 4 * w) = src[e];
+            }
             named_sync(1, kCThreads);
         }
         // ---------------------------------- pass 1 --------------------------------------------
@@ -317,8 +331,8 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 // FP8: this warp's two k-steps are exactly one 32-channel block (2j + kh) of its
                 // rows; the four lanes of a quad hold the block. Decode R with the old exponent,
                 // write in fp32, pick the new exponent from the block maximum, encode in place.
-                uint8_t* ea_p = scl + ((16 * mt + g) * kBranches + ib) * nblk + 2 * j + kh;
-                uint8_t* eb_p = ea_p + 8 * kBranches * nblk;
+                uint8_t* ea_p = scl + ((16 * mt + g) * kBranches + ib) * sst + 2 * j + kh;
+                uint8_t* eb_p = ea_p + 8 * kBranches * sst;
                 const float da = pow2f(int(*ea_p) - 127), db = pow2f(int(*eb_p) - 127);
                 float2 v[2][4];
                 // byte offset of the code pair (row a or b, channels 2q, 2q+1 (+8)) in the box
@@ -435,9 +449,13 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
         if constexpr (FP8 && WRITE) {
             // the tile's new block exponents go back to HBM (pass 2 reads them from here)
             const int nv = min(kTT, N - t0);
-            const int nvec = int(size_t(nv) * size_t(D) / 128);
-            uint4* dst = reinterpret_cast<uint4*>(scales + size_t(t0) * (D / 8));
-            for (int e = tid; e < nvec; e += kCThreads) dst[e] = reinterpret_cast<uint4*>(scl)[e];
+            const int wpr = nblk / 4;
+            const int nw = nv * kBranches * wpr;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(scales + size_t(t0) * (D / 8));
+            for (int e = tid; e < nw; e += kCThreads) {
+                const int row = e / wpr, w = e - row * wpr;
+                dst[e] = *reinterpret_cast<const uint32_t*>(scl + row * sst + 4 * w);
+            }
         }
         {
             float s0, s1, s2, s3;
@@ -572,9 +590,9 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 } else {
                     const int off = (co & 1) * 8 + 2 * q;
                     const uint8_t* ep =
-                        scl + ((16 * mt2 + g) * kBranches + i) * nblk + 2 * j + (co >> 2);
+                        scl + ((16 * mt2 + g) * kBranches + i) * sst + 2 * j + (co >> 2);
                     const float da = pow2f(int(ep[0]) - 127);
-                    const float db = pow2f(int(ep[8 * kBranches * nblk]) - 127);
+                    const float db = pow2f(int(ep[8 * kBranches * sst]) - 127);
                     const float2 wa = e4m3x2_to_f2(lds16(rb + swz64(row, co >> 1) + off));
                     const float2 wb = e4m3x2_to_f2(lds16(rb + swz64(row + 8, co >> 1) + off));
                     rpa = f2(wa.x * da, wa.y * da);
