@@ -154,6 +154,177 @@ int gro_read(int64_t n, int nb, int D, int r, double eps, const double *R, const
     return failed ? -2 : 0;
 }
 
+/* ---- backward (the chain rule through eq rms … eq s and eq write) ----------------------------
+ * Gradients of a scalar loss L given dL/dx [n][D] and dL/ds [n][nb] (the read's outputs).
+ * Per token, with a = W_d vec R̂ / n_r, u = W_w vec R̂ / n_r, g = W_u h (the read's own
+ * intermediates, recomputed in fp64):
+ *   dG_i[c]  = dx[c] · R̂_i[c] / n_r                dR̂_i[c] += dx[c] · G_i[c] / n_r
+ *   dg       = dG ⊙ G ⊙ (1 − G)                     (σ' = σ(1 − σ))
+ *   dh       = W_uᵀ dg,        dW_u += dg ⊗ h
+ *   dz       = dh ⊙ SiLU'(z),  SiLU'(z) = σ(z)(1 + z(1 − σ(z)))
+ *   du       = ds ⊙ 2σ(u)(1 − σ(u))
+ *   dvec R̂ += (W_dᵀ dz + W_wᵀ du) / n_r,  dW_d += dz ⊗ vec R̂ / n_r,  dW_w += du ⊗ vec R̂ / n_r
+ *   dγ_i[c] += dR̂_i[c] · R_i[c] · inv_i
+ *   with p_i[c] = dR̂_i[c] γ_i[c]:  dR_i[c] = inv_i p_i[c] − inv_i³ R_i[c] Σ_c' p_i[c'] R_i[c'] / D
+ * (the last line differentiates R̂_i = γ_i R_i (mean R_i² + eps)^-1/2). The weight gradients
+ * are sums over the n tokens (outputs overwritten). */
+int gro_read_backward(int64_t n, int nb, int D, int r, double eps, const double *R,
+                      const double *gamma, const double *Wd, const double *Wu, const double *Ww,
+                      const double *dx, const double *ds, double *dR, double *dgamma,
+                      double *dWd, double *dWu, double *dWw)
+{
+    if (bad_dims(n, nb, D, r) || !R || !gamma || !Wd || !Wu || !Ww || !dx || !ds || !dR ||
+        !dgamma || !dWd || !dWu || !dWw)
+        return -1;
+    const size_t K = (size_t)nb * D;
+    const double inv_nb = 1.0 / (double)nb;
+    memset(dgamma, 0, K * sizeof(double));
+    memset(dWd, 0, (size_t)r * K * sizeof(double));
+    memset(dWu, 0, K * (size_t)r * sizeof(double));
+    memset(dWw, 0, (size_t)nb * K * sizeof(double));
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *Rh = malloc(K * sizeof(double)), *inv = malloc((size_t)nb * sizeof(double));
+        double *z = malloc((size_t)r * sizeof(double)), *h = malloc((size_t)r * sizeof(double));
+        double *u = malloc((size_t)nb * sizeof(double)), *G = malloc(K * sizeof(double));
+        double *dRh = malloc(K * sizeof(double)), *dg = malloc(K * sizeof(double));
+        double *dz = malloc((size_t)r * sizeof(double)), *du = malloc((size_t)nb * sizeof(double));
+        /* per-thread partial sums of the parameter gradients */
+        double *pg = calloc(K, sizeof(double)), *pWd = calloc((size_t)r * K, sizeof(double));
+        double *pWu = calloc(K * (size_t)r, sizeof(double));
+        double *pWw = calloc((size_t)nb * K, sizeof(double));
+        if (!Rh || !inv || !z || !h || !u || !G || !dRh || !dg || !dz || !du || !pg || !pWd ||
+            !pWu || !pWw) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < n; ++t) {
+                const double *Rt = R + (size_t)t * K;
+                const double *dxt = dx + (size_t)t * D, *dst = ds + (size_t)t * nb;
+                group_rmsnorm(nb, D, eps, Rt, gamma, Rh, inv);
+                for (int k = 0; k < r; ++k) {          /* z, h */
+                    double acc = 0.0;
+                    for (size_t j = 0; j < K; ++j)
+                        acc += Wd[(size_t)k * K + j] * Rh[j];
+                    z[k] = inv_nb * acc;
+                    h[k] = silu(z[k]);
+                }
+                for (size_t j = 0; j < K; ++j) {       /* G */
+                    double acc = 0.0;
+                    for (int k = 0; k < r; ++k)
+                        acc += Wu[j * (size_t)r + k] * h[k];
+                    G[j] = sigmoid(acc);
+                }
+                for (int i = 0; i < nb; ++i) {          /* u */
+                    double acc = 0.0;
+                    for (size_t j = 0; j < K; ++j)
+                        acc += Ww[(size_t)i * K + j] * Rh[j];
+                    u[i] = inv_nb * acc;
+                }
+                /* eq use_gate: x[c] = (1/n_r) Σ_i G_i[c] R̂_i[c] */
+                for (int i = 0; i < nb; ++i)
+                    for (int c = 0; c < D; ++c) {
+                        const size_t j = (size_t)i * D + c;
+                        const double dG = inv_nb * dxt[c] * Rh[j];
+                        dRh[j] = inv_nb * dxt[c] * G[j];
+                        dg[j] = dG * G[j] * (1.0 - G[j]);
+                    }
+                /* eq gate: g = W_u h, h = SiLU(z) */
+                for (int k = 0; k < r; ++k) {
+                    double acc = 0.0;
+                    for (size_t j = 0; j < K; ++j)
+                        acc += Wu[j * (size_t)r + k] * dg[j];
+                    const double sg = sigmoid(z[k]);
+                    dz[k] = acc * sg * (1.0 + z[k] * (1.0 - sg));
+                }
+                for (size_t j = 0; j < K; ++j)
+                    for (int k = 0; k < r; ++k)
+                        pWu[j * (size_t)r + k] += dg[j] * h[k];
+                /* eq s: s = 2σ(u) */
+                for (int i = 0; i < nb; ++i) {
+                    const double sg = sigmoid(u[i]);
+                    du[i] = dst[i] * 2.0 * sg * (1.0 - sg);
+                }
+                /* z = W_d vec R̂ / n_r and u = W_w vec R̂ / n_r */
+                for (size_t j = 0; j < K; ++j) {
+                    double acc = 0.0;
+                    for (int k = 0; k < r; ++k)
+                        acc += Wd[(size_t)k * K + j] * dz[k];
+                    for (int i = 0; i < nb; ++i)
+                        acc += Ww[(size_t)i * K + j] * du[i];
+                    dRh[j] += inv_nb * acc;
+                }
+                for (int k = 0; k < r; ++k)
+                    for (size_t j = 0; j < K; ++j)
+                        pWd[(size_t)k * K + j] += inv_nb * dz[k] * Rh[j];
+                for (int i = 0; i < nb; ++i)
+                    for (size_t j = 0; j < K; ++j)
+                        pWw[(size_t)i * K + j] += inv_nb * du[i] * Rh[j];
+                /* eq rms: R̂_i = γ_i R_i inv_i */
+                for (int i = 0; i < nb; ++i) {
+                    const double *Ri = Rt + (size_t)i * D;
+                    double pr = 0.0;
+                    for (int c = 0; c < D; ++c) {
+                        const size_t j = (size_t)i * D + c;
+                        pg[j] += dRh[j] * Ri[c] * inv[i];
+                        pr += dRh[j] * gamma[j] * Ri[c];
+                    }
+                    const double i3 = inv[i] * inv[i] * inv[i];
+                    for (int c = 0; c < D; ++c) {
+                        const size_t j = (size_t)i * D + c;
+                        dR[(size_t)t * K + j] =
+                            inv[i] * dRh[j] * gamma[j] - i3 * Ri[c] * pr / (double)D;
+                    }
+                }
+            }
+#pragma omp critical
+            {
+                for (size_t j = 0; j < K; ++j)
+                    dgamma[j] += pg[j];
+                for (size_t j = 0; j < (size_t)r * K; ++j) {
+                    dWd[j] += pWd[j];
+                    dWu[j] += pWu[j];
+                }
+                for (size_t j = 0; j < (size_t)nb * K; ++j)
+                    dWw[j] += pWw[j];
+            }
+        }
+        free(Rh); free(inv); free(z); free(h); free(u); free(G); free(dRh); free(dg); free(dz);
+        free(du); free(pg); free(pWd); free(pWu); free(pWw);
+    }
+    return failed ? -2 : 0;
+}
+
+/* Backward of eq write R' = R + s_i y: dR = dR', ds_i = Σ_c dR'_i[c] y[c], dy = Σ_i s_i dR'_i.
+ * dR may equal dRp. */
+int gro_write_backward(int64_t n, int nb, int D, const double *dRp, const double *y,
+                       const double *s, double *dR, double *dy, double *ds)
+{
+    if (n < 0 || nb < 1 || D < 1 || !dRp || !y || !s || !dR || !dy || !ds)
+        return -1;
+    const size_t K = (size_t)nb * D;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        for (int c = 0; c < D; ++c) {
+            double acc = 0.0;
+            for (int i = 0; i < nb; ++i)
+                acc += s[(size_t)t * nb + i] * dRp[(size_t)t * K + (size_t)i * D + c];
+            dy[(size_t)t * D + c] = acc;
+        }
+        for (int i = 0; i < nb; ++i) {
+            double acc = 0.0;
+            for (int c = 0; c < D; ++c)
+                acc += dRp[(size_t)t * K + (size_t)i * D + c] * y[(size_t)t * D + c];
+            ds[(size_t)t * nb + i] = acc;
+        }
+        for (size_t j = 0; j < K; ++j)
+            dR[(size_t)t * K + j] = dRp[(size_t)t * K + j];
+    }
+    return 0;
+}
+
 /* gr_write: eq write, R'_i = R_i + s_i y, for n tokens. R_out may equal R. */
 int gro_write(int64_t n, int nb, int D, const double *R, const double *y, const double *s,
               double *R_out)

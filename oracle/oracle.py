@@ -41,12 +41,15 @@ def _load(path: str) -> ctypes.CDLL:
     L.gro_set_num_threads.argtypes = [i32]
     L.gro_set_num_threads.restype = None
     U = ctypes.POINTER(ctypes.c_uint8)
+    L.gro_read_backward.argtypes = [i64, i32, i32, i32, f64] + [P] * 12
+    L.gro_write_backward.argtypes = [i64, i32, i32, P, P, P, P, P, P]
     L.gro_fp8_encode.argtypes = [i64, i32, P, U, U]
     L.gro_fp8_decode.argtypes = [i64, i32, U, U, P]
     L.gro_fp8_code_values.argtypes = [P]
     L.gro_fp8_round_codes.argtypes = [i64, P, U]
     for f in ("gro_read", "gro_write", "gro_write_then_read", "gro_read_fixed_gates",
               "gro_residual_add", "gro_num_threads", "gro_round_significand", "gro_fp8_encode",
+              "gro_read_backward", "gro_write_backward",
               "gro_fp8_decode", "gro_fp8_code_values", "gro_fp8_round_codes"):
         getattr(L, f).restype = ctypes.c_int
     return L
@@ -166,6 +169,37 @@ def write_then_read(R, y, s_prev, params: dict, eps: float = 1e-6, store: str | 
                                      _p(gamma), _p(Wd), _p(Wu), _p(Ww), _p(R_out), _p(x), _p(s)),
            "write_then_read")
     return R_out, x, s
+
+
+# ---- backward ---------------------------------------------------------------------------------
+
+def read_backward(R, params: dict, dx, ds, eps: float = 1e-6):
+    """Gradients of the read given dL/dx [n, D] and dL/ds [n, nb]: returns dR [n, nb, D] and a
+    dict of parameter gradients (gamma, w_down, w_up, w_write), summed over the tokens."""
+    R = _f64(R)
+    n, nb, D = R.shape
+    gamma, Wd, Wu, Ww = (_f64(params[k]) for k in ("gamma", "w_down", "w_up", "w_write"))
+    r = Wd.shape[0]
+    dx, ds = _f64(dx), _f64(ds)
+    assert dx.shape == (n, D) and ds.shape == (n, nb)
+    dR = np.empty_like(R)
+    out = {"gamma": np.empty((nb, D)), "w_down": np.empty((r, nb * D)),
+           "w_up": np.empty((nb * D, r)), "w_write": np.empty((nb, nb * D))}
+    _check(lib().gro_read_backward(n, nb, D, r, float(eps), _p(R), _p(gamma), _p(Wd), _p(Wu),
+                                   _p(Ww), _p(dx), _p(ds), _p(dR), _p(out["gamma"]),
+                                   _p(out["w_down"]), _p(out["w_up"]), _p(out["w_write"])),
+           "read_backward")
+    return dR, out
+
+
+def write_backward(dRp, y, s):
+    """Gradients of the write R' = R + s_i y given dL/dR': returns (dR, dy, ds)."""
+    dRp, y, s = _f64(dRp), _f64(y), _f64(s)
+    n, nb, D = dRp.shape
+    dR, dy, ds = np.empty_like(dRp), np.empty((n, D)), np.empty((n, nb))
+    _check(lib().gro_write_backward(n, nb, D, _p(dRp), _p(y), _p(s), _p(dR), _p(dy), _p(ds)),
+           "write_backward")
+    return dR, dy, ds
 
 
 # ---- FP8 state: e4m3 codes with one power-of-two scale per 32-channel block -----------------

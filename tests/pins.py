@@ -294,6 +294,82 @@ def pin_residual_add():
     assert np.array_equal(oracle.residual_add(a, b), a + b)
 
 
+# ---- backward (NEXT-3) --------------------------------------------------------------------------
+
+def _fd_grad(f, A, h=1e-6):
+    """Central finite differences of the scalar f() with respect to every entry of A."""
+    G = np.zeros_like(A)
+    for idx in np.ndindex(A.shape):
+        o = A[idx]
+        A[idx] = o + h
+        a = f()
+        A[idx] = o - h
+        b = f()
+        A[idx] = o
+        G[idx] = (a - b) / (2 * h)
+    return G
+
+
+def pin_backward_finite_differences():
+    """The read's gradients (state and all four parameters) equal central finite differences
+    of L = Σ dx·x + Σ ds·s, for n_r = 4 and n_r = 2, eps > 0, random gains."""
+    for nb, D, r, seed in ((4, 8, 3, 157), (2, 6, 2, 163)):
+        rng = np.random.default_rng(seed)
+        n, eps = 3, 1e-3
+        R = rng.standard_normal((n, nb, D))
+        p = _params(rng, nb, D, r, std=0.5)
+        dx, ds = rng.standard_normal((n, D)), rng.standard_normal((n, nb))
+
+        def L():
+            x, s = _read(R, p, eps)
+            return float((dx * x).sum() + (ds * s).sum())
+
+        dR, g = oracle.read_backward(R, p, dx, ds, eps)
+        assert _rel(_fd_grad(L, R), dR) < 1e-6
+        for k in ("gamma", "w_down", "w_up", "w_write"):
+            assert _rel(_fd_grad(L, p[k]), g[k]) < 1e-6, k
+
+
+def pin_backward_torch_autograd():
+    """The same gradients from torch's autograd (a library's reverse mode) through the read
+    written in torch ops, on a few tokens."""
+    import torch
+    rng = np.random.default_rng(167)
+    n, nb, D, r, eps = 5, 4, 16, 4, 1e-5
+    R = rng.standard_normal((n, nb, D))
+    p = _params(rng, nb, D, r, std=0.3)
+    dx, ds = rng.standard_normal((n, D)), rng.standard_normal((n, nb))
+    Rt = torch.tensor(R, requires_grad=True)
+    pt = {k: torch.tensor(v, requires_grad=True) for k, v in p.items()}
+    inv = torch.rsqrt((Rt * Rt).mean(-1, keepdim=True) + eps)
+    Rh = Rt * inv * pt["gamma"]
+    v = Rh.reshape(n, nb * D)
+    z = v @ pt["w_down"].T / nb
+    G = torch.sigmoid((z * torch.sigmoid(z)) @ pt["w_up"].T).reshape(n, nb, D)
+    x = (G * Rh).sum(1) / nb
+    s = 2 * torch.sigmoid(v @ pt["w_write"].T / nb)
+    ((torch.tensor(dx) * x).sum() + (torch.tensor(ds) * s).sum()).backward()
+    dR, g = oracle.read_backward(R, p, dx, ds, eps)
+    assert _rel(dR, Rt.grad.numpy()) < 1e-12
+    for k in g:
+        assert _rel(g[k], pt[k].grad.numpy()) < 1e-12, k
+
+
+def pin_write_backward():
+    """eq write is linear: its gradients equal finite differences exactly enough, and dR = dR'."""
+    rng = np.random.default_rng(173)
+    n, nb, D = 3, 4, 5
+    R, y, s = rng.standard_normal((n, nb, D)), rng.standard_normal((n, D)), rng.uniform(0, 2, (n, nb))
+    dRp = rng.standard_normal((n, nb, D))
+
+    def L():
+        return float((dRp * oracle.write(R, y, s)).sum())
+
+    dR, dy, dsv = oracle.write_backward(dRp, y, s)
+    assert np.array_equal(dR, dRp)
+    assert _rel(_fd_grad(L, y), dy) < 1e-8 and _rel(_fd_grad(L, s), dsv) < 1e-8
+
+
 # ---- FP8 state (SPEC R21: e4m3 codes, one power-of-two scale per 32-channel block) ----------
 
 def _torch_e4m3_values():
@@ -400,4 +476,5 @@ ALL_PINS = [pin_dense_bruteforce, pin_zero_down_projection, pin_zero_up_projecti
             pin_chain_closed_form, pin_decomposition, pin_branch_permutation,
             pin_branch_scale_invariance, pin_ranges_and_saturation, pin_residual_add,
             pin_fp8_codes_match_torch, pin_fp8_block_scale, pin_fp8_roundtrip,
-            pin_fp8_blocks_independent, pin_fp8_write_then_read_error]
+            pin_fp8_blocks_independent, pin_fp8_write_then_read_error,
+            pin_backward_finite_differences, pin_backward_torch_autograd, pin_write_backward]

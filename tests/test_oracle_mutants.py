@@ -35,6 +35,15 @@ MUTANTS = {
                             "x[(size_t)t * D + c] = acc;"),
     "gamma_wrong_branch": ("Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[(size_t)i * D + c];",
                            "Rh[(size_t)i * D + c] = Ri[c] * inv[i] * gamma[c];"),
+    "bwd_drop_norm_term": ("inv[i] * dRh[j] * gamma[j] - i3 * Ri[c] * pr / (double)D;",
+                           "inv[i] * dRh[j] * gamma[j];"),
+    "bwd_silu_derivative": ("dz[k] = acc * sg * (1.0 + z[k] * (1.0 - sg));",
+                            "dz[k] = acc * sg;"),
+    "bwd_drop_sigmoid_derivative": ("dg[j] = dG * G[j] * (1.0 - G[j]);", "dg[j] = dG;"),
+    "bwd_drop_1/n_r_in_dvec": ("dRh[j] += inv_nb * acc;", "dRh[j] += acc;"),
+    "bwd_dgamma_without_inv": ("pg[j] += dRh[j] * Ri[c] * inv[i];", "pg[j] += dRh[j] * Ri[c];"),
+    "bwd_write_ds_wrong_branch": ("acc += dRp[(size_t)t * K + (size_t)i * D + c] * y[(size_t)t * D + c];",
+                                  "acc += dRp[(size_t)t * K + c] * y[(size_t)t * D + c];"),
     "fp8_scale_may_clip": ("    if (2.0 * f > 1.75)\n        e += 1;\n", ""),
     "fp8_truncating_rounding": ("double m = nearbyint(ldexp(a, 3 - E));",
                                 "double m = floor(ldexp(a, 3 - E));"),
