@@ -204,6 +204,37 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
                                    const float* s_prev_host, const gr_params* next, void* x_host,
                                    float* s_next_host, void* stream);
 
+/* ---- backward (training) ------------------------------------------------------------------------
+ * The gradients of the read and the write by the chain rule through eq rms, eq gate, eq use_gate,
+ * eq s and eq write ("【论文解读】 Qwen3.8 Flash Next", §二.4), in fp32 on CUDA cores. States (R,
+ * y) in shape->state_dtype (GR_BF16 or GR_F32), parameters and every gradient fp32, all DEVICE
+ * pointers, 16-byte aligned. */
+
+/* Bytes of device workspace gr_read_backward needs: 3·N·4·D·4 bytes of per-token factors of
+ * the parameter gradients plus N·(2r+5)·4, each part rounded up to 256 bytes. */
+int gr_read_backward_workspace_size(const gr_shape* shape, size_t* bytes);
+
+/* Backward of the read of R [N][4][D] with the fp32 parameters gamma [4][D], W_d [r][4D],
+ * W_u [4D][r], W_w [4][4D] (unpacked), given dL/dx [N][D] and dL/ds [N][4]:
+ *   dR [N][4][D]   dL/dR (overwritten)
+ *   dgamma, dw_down, dw_up, dw_write   the parameter gradients summed over the N tokens, in the
+ *                                      parameters' shapes (overwritten)
+ * `workspace` (>= gr_read_backward_workspace_size bytes, 256-byte aligned) holds per-token
+ * factors between the two kernels. Outputs must not overlap the inputs, the workspace or each
+ * other. Asynchronous on `stream`; the parameter gradients are reduced with fp32 atomics, so their
+ * last bits may differ from run to run. */
+int gr_read_backward(const gr_shape* shape, const void* R, const float* gamma,
+                     const float* w_down, const float* w_up, const float* w_write,
+                     const float* dx, const float* ds, float* dR, float* dgamma, float* dw_down,
+                     float* dw_up, float* dw_write, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Backward of the write R' = R + s_i·y given dL/dR' [N][4][D]: dR = dL/dR' (dR may be the same
+ * buffer as dR_next), dy [N][D] = Σ_i s_i dL/dR'_i, ds [N][4] with ds_i = Σ_c dL/dR'_i[c] y[c].
+ * y in the state dtype; s and every gradient fp32. */
+int gr_write_backward(const gr_shape* shape, const float* dR_next, const void* y, const float* s,
+                      float* dR, float* dy, float* ds, void* stream);
+
 /* ---- FP8 branch state ------------------------------------------------------------------------
  * "【论文解读】 Qwen3.8 Flash Next", §二.7 stores the widened state in FP8 and fixes no format.
  * This library's FP8 state is two DEVICE arrays:

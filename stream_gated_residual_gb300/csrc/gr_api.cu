@@ -411,6 +411,81 @@ int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* 
     return status_of(launch_residual_add(n, dtype, y, x, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- backward ---------------------------------------------------------------------------------
+
+int gr_read_backward_workspace_size(const gr_shape* shape, size_t* bytes) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (!bytes) return GR_E_NULL;
+    *bytes = read_backward_workspace(shape->n_tokens, shape->d_model, shape->rank);
+    return GR_OK;
+}
+
+int gr_read_backward(const gr_shape* shape, const void* R, const float* gamma,
+                     const float* w_down, const float* w_up, const float* w_write,
+                     const float* dx, const float* ds, float* dR, float* dgamma, float* dw_down,
+                     float* dw_up, float* dw_write, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    const void* in[8] = {R, gamma, w_down, w_up, w_write, dx, ds, workspace};
+    const void* out[5] = {dR, dgamma, dw_down, dw_up, dw_write};
+    for (const void* p : in)
+        if (!p) return GR_E_NULL;
+    for (const void* p : out)
+        if (!p) return GR_E_NULL;
+    for (const void* p : in)
+        if (!aligned16(p)) return GR_E_ALIGN;
+    for (const void* p : out)
+        if (!aligned16(p)) return GR_E_ALIGN;
+    if (!aligned256(workspace)) return GR_E_ALIGN;
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model), r = size_t(shape->rank);
+    const size_t K = kBranches * D;
+    const size_t need = read_backward_workspace(shape->n_tokens, shape->d_model, shape->rank);
+    if (workspace_bytes < need) return GR_E_SIZE;
+    const size_t in_n[8] = {N * K * elem_size(shape->state_dtype), K * 4, r * K * 4, r * K * 4,
+                            kBranches * K * 4, N * D * 4, N * kBranches * 4, need};
+    const size_t out_n[5] = {N * K * 4, K * 4, r * K * 4, r * K * 4, kBranches * K * 4};
+    for (int a = 0; a < 5; ++a) {
+        for (int b = 0; b < 8; ++b)
+            if (overlaps(out[a], out_n[a], in[b], in_n[b])) return GR_E_ALIAS;
+        for (int b = a + 1; b < 5; ++b)
+            if (overlaps(out[a], out_n[a], out[b], out_n[b])) return GR_E_ALIAS;
+    }
+    for (int b = 0; b < 7; ++b)
+        if (overlaps(workspace, need, in[b], in_n[b])) return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_read_backward(shape->n_tokens, shape->d_model, shape->rank,
+                                          shape->eps, shape->state_dtype, R, gamma, w_down, w_up,
+                                          w_write, dx, ds, dR, dgamma, dw_down, dw_up, dw_write,
+                                          workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_write_backward(const gr_shape* shape, const float* dR_next, const void* y, const float* s,
+                      float* dR, float* dy, float* ds, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!dR_next || !y || !s || !dR || !dy || !ds) return GR_E_NULL;
+    if (!aligned16(dR_next) || !aligned16(y) || !aligned16(s) || !aligned16(dR) ||
+        !aligned16(dy) || !aligned16(ds))
+        return GR_E_ALIGN;
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * 4, ny = N * D * elem_size(shape->state_dtype);
+    const size_t nd = N * D * 4, ns = N * kBranches * 4;
+    if ((dR != dR_next && overlaps(dR, nR, dR_next, nR)) || overlaps(dR, nR, y, ny) ||
+        overlaps(dR, nR, s, ns) || overlaps(dy, nd, dR_next, nR) || overlaps(dy, nd, y, ny) ||
+        overlaps(dy, nd, s, ns) || overlaps(dy, nd, dR, nR) || overlaps(ds, ns, dR_next, nR) ||
+        overlaps(ds, ns, y, ny) || overlaps(ds, ns, s, ns) || overlaps(ds, ns, dR, nR) ||
+        overlaps(ds, ns, dy, nd))
+        return GR_E_ALIAS;
+    if ((st = check_device())) return st;
+    return status_of(launch_write_backward(shape->n_tokens, shape->d_model, shape->state_dtype,
+                                           dR_next, y, s, dR, dy, ds,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 // ---- FP8 branch state ------------------------------------------------------------------------
 
 int gr_fp8_encode(const gr_shape* shape, const void* R, int32_t in_dtype, uint8_t* codes,

@@ -113,6 +113,17 @@ cudaError_t launch_fp8_decode(int64_t rows, int D, int out_dtype, const uint8_t*
 cudaError_t launch_fp8_write(int64_t N, int D, uint8_t* codes, uint8_t* scales, const void* y,
                              const float* s, cudaStream_t st);
 
+// Backward of the read and of the write (gr_backward.cu).
+size_t read_backward_workspace(int64_t N, int D, int r);
+cudaError_t launch_read_backward(int64_t N, int D, int r, float eps, int dtype, const void* R,
+                                 const float* gamma, const float* Wd, const float* Wu,
+                                 const float* Ww, const float* dx, const float* ds, float* dR,
+                                 float* dgamma, float* dWd, float* dWu, float* dWw,
+                                 void* workspace, cudaStream_t st);
+cudaError_t launch_write_backward(int64_t N, int D, int dtype, const float* dRp, const void* y,
+                                  const float* s, float* dR, float* dy, float* ds,
+                                  cudaStream_t st);
+
 // Streaming write R += s_i * y (no read).
 cudaError_t launch_write(int64_t N, int D, int dtype, void* R, const void* y, const float* s,
                          cudaStream_t st);

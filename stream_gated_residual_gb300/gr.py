@@ -77,6 +77,9 @@ def load() -> ctypes.CDLL:
         "gr_write_then_read_host": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
         "gr_write_then_read_host_static": ([S, V, V, V, P, V, V, V], ctypes.c_int),
         "gr_selftest_bounded_wait": ([ctypes.c_int64, V], ctypes.c_int),
+        "gr_read_backward_workspace_size": ([S, sz], ctypes.c_int),
+        "gr_read_backward": ([S] + [V] * 13 + [ctypes.c_size_t, V], ctypes.c_int),
+        "gr_write_backward": ([S, V, V, V, V, V, V, V], ctypes.c_int),
         "gr_fp8_encode": ([S, V, ctypes.c_int32, V, V, V], ctypes.c_int),
         "gr_fp8_decode": ([S, V, V, V, ctypes.c_int32, V], ctypes.c_int),
         "gr_read_fp8": ([S, V, V, P, V, V, V], ctypes.c_int),
@@ -302,6 +305,56 @@ def write_then_read_host_static(R: torch.Tensor, y: torch.Tensor, s_prev: torch.
         ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev), params.ref(), _ptr(x), _ptr(s_next),
         _stream(stream)), "gr_write_then_read_host_static")
     return x, s_next
+
+
+# ---- backward (training) ------------------------------------------------------------------------
+
+def read_backward(R: torch.Tensor, gamma: torch.Tensor, w_down: torch.Tensor, w_up: torch.Tensor,
+                  w_write: torch.Tensor, dx: torch.Tensor, ds: torch.Tensor, eps: float = 1e-6,
+                  workspace: torch.Tensor | None = None, stream=None):
+    """gr_read_backward: dL/dR [N,4,D] fp32 and the parameter gradients (dict like the
+    parameters: gamma, w_down, w_up, w_write; fp32) given dL/dx [N,D] and dL/ds [N,4] (fp32).
+    The parameters are the fp32 tensors (not the packed buffer)."""
+    _dev(R, "R")
+    N, _, D = R.shape
+    r = w_down.shape[0]
+    shape = make_shape(N, D, r, R.dtype, eps)
+    for t, n in ((gamma, "gamma"), (w_down, "w_down"), (w_up, "w_up"), (w_write, "w_write"),
+                 (dx, "dx"), (ds, "ds")):
+        _dev(t, n)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{n} must be float32")
+    need = ctypes.c_size_t(0)
+    _check(load().gr_read_backward_workspace_size(ctypes.byref(shape), ctypes.byref(need)),
+           "gr_read_backward_workspace_size")
+    if workspace is None:
+        buf = torch.empty(need.value + 256, dtype=torch.uint8, device=R.device)
+        workspace = buf[(-buf.data_ptr()) % 256:][:need.value]
+    dev = R.device
+    dR = torch.empty((N, 4, D), dtype=torch.float32, device=dev)
+    g = {"gamma": torch.empty_like(gamma), "w_down": torch.empty_like(w_down),
+         "w_up": torch.empty_like(w_up), "w_write": torch.empty_like(w_write)}
+    _check(load().gr_read_backward(
+        ctypes.byref(shape), _ptr(R), _ptr(gamma), _ptr(w_down), _ptr(w_up), _ptr(w_write),
+        _ptr(dx), _ptr(ds), _ptr(dR), _ptr(g["gamma"]), _ptr(g["w_down"]), _ptr(g["w_up"]),
+        _ptr(g["w_write"]), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "gr_read_backward")
+    return dR, g
+
+
+def write_backward(dR_next: torch.Tensor, y: torch.Tensor, s: torch.Tensor, stream=None):
+    """gr_write_backward: (dR, dy, ds) from dL/dR' [N,4,D] fp32, y [N,D] (state dtype), s [N,4]."""
+    for t, n in ((dR_next, "dR_next"), (y, "y"), (s, "s")):
+        _dev(t, n)
+    N, _, D = dR_next.shape
+    shape = make_shape(N, D, 1, y.dtype)
+    dR = torch.empty_like(dR_next)
+    dy = torch.empty((N, D), dtype=torch.float32, device=dR_next.device)
+    ds = torch.empty((N, 4), dtype=torch.float32, device=dR_next.device)
+    _check(load().gr_write_backward(ctypes.byref(shape), _ptr(dR_next), _ptr(y), _ptr(s),
+                                    _ptr(dR), _ptr(dy), _ptr(ds), _stream(stream)),
+           "gr_write_backward")
+    return dR, dy, ds
 
 
 # ---- FP8 branch state (e4m3 codes, one power-of-two exponent per 32-channel block) ------------

@@ -197,3 +197,31 @@ def test_fp8_kernel_path_and_packing(lib):
     n = ctypes.c_size_t(0)
     assert lib.gr_packed_size(ctypes.byref(_shape(d=4096, r=16, dt=gr.GR_FP8)),
                               ctypes.byref(n)) == 0 and n.value > 0
+
+
+def test_backward_calls_validate_before_any_launch(lib):
+    E = header_constant
+    null = ctypes.c_void_p(None)
+    sh = _shape(n=64, d=256, r=16, dt=gr.GR_BF16)
+    need = ctypes.c_size_t(0)
+    assert lib.gr_read_backward_workspace_size(ctypes.byref(sh), ctypes.byref(need)) == 0
+    assert need.value >= 3 * 64 * 4 * 256 * 4
+    # R, gamma, W_d, W_u, W_w, dx, ds, then dR, dgamma, dW_d, dW_u, dW_w
+    ptrs = [ctypes.c_void_p(0x100000 * (k + 1)) for k in range(12)]
+    ws = ctypes.c_void_p(0x7000000000)
+    args = lambda p, w=ws, nb=need.value: (ctypes.byref(sh), *p, w, nb, null)
+    assert lib.gr_read_backward(*args(ptrs)) == E("GR_E_DEVICE")
+    assert lib.gr_read_backward(*args(ptrs, nb=need.value - 1)) == E("GR_E_SIZE")
+    assert lib.gr_read_backward(*args(ptrs[:3] + [null] + ptrs[4:])) == E("GR_E_NULL")
+    assert lib.gr_read_backward(*args(ptrs, w=ctypes.c_void_p(0x7000000010))) == E("GR_E_ALIGN")
+    aliased = ptrs[:7] + [ptrs[0]] + ptrs[8:]          # dR on top of R
+    assert lib.gr_read_backward(*args(aliased)) == E("GR_E_ALIAS")
+    fp8 = _shape(n=64, d=256, r=16, dt=gr.GR_FP8)
+    assert lib.gr_read_backward(ctypes.byref(fp8), *ptrs, ws, need.value, null) == E("GR_E_DTYPE")
+    assert lib.gr_read_backward(ctypes.byref(_shape(n=0, d=256, r=16)), *[null] * 12, null, 0,
+                                null) == 0
+    # write backward: dR may be dR_next itself; dy on top of dR_next is refused
+    assert lib.gr_write_backward(ctypes.byref(sh), FAKE, FAKE2, FAKE3, FAKE, FAKE4, FAKE5,
+                                 null) == E("GR_E_DEVICE")
+    assert lib.gr_write_backward(ctypes.byref(sh), FAKE, FAKE2, FAKE3, FAKE4, FAKE, FAKE5,
+                                 null) == E("GR_E_ALIAS")
