@@ -46,6 +46,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every timed step from the host instead of replaying a CUDA graph "
                          "of them")
+    ap.add_argument("--backward", action="store_true",
+                    help="time one sublayer's GR backward (gr_read_backward, then "
+                         "gr_write_backward in place) instead of the fused forward step")
     ap.add_argument("--n-tokens", type=int, default=None,
                     help="run the workload's shape with this many tokens instead (small cases "
                          "for profiling; the line then reports no ncu traffic)")
@@ -489,6 +492,106 @@ def run_gr(args, w) -> None:
         dist.destroy_process_group()
 
 
+def backward_flops_per_token(w) -> int:
+    """Arithmetic of one token's GR backward (FMA = 2 FLOP), per element of vec R̂ (4·D): the
+    forward projections recomputed (z, u: r+4; g: r), W_uᵀ dg (r), W_dᵀ dz + W_wᵀ du (r+4), the
+    parameter-gradient products (dW_u: r, dW_d and dW_w: r+4, dγ: 1), and about 12 more for the
+    element-wise chain (σ, dG, dR̂, the RMSNorm backward); then the write's backward (4 per
+    element)."""
+    r, K = w.rank, 4 * w.d_model
+    return 2 * K * ((r + 4) + r + r + (r + 4) + r + (r + 4) + 1) + 12 * K + 4 * K
+
+
+def run_backward(args, w) -> None:
+    """gr_read_backward then gr_write_backward (in place on the same dR) on the workload, K
+    timed steps after W warm-up steps, one GPU (a replica per rank under torchrun)."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from stream_gated_residual_gb300 import gr
+    from stream_gated_residual_gb300 import workloads as wl
+    if w.dtype == "fp8":
+        raise SystemExit("the backward takes bf16 or fp32 states")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    gr.load()
+    wr = shard(w, rank)
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+    def dev_tensor(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    R, y = dev_tensor(wl.make_state(wr)), dev_tensor(wl.make_y(wr))
+    s = torch.from_numpy(wl.make_s_prev(wr)).to(dev)
+    p = {k: torch.from_numpy(v).to(dev) for k, v in wl.make_params(wr, 1).items()}
+    rng = np.random.default_rng(wr.seed + 1000)
+    dx = torch.from_numpy(rng.standard_normal((w.n_tokens, w.d_model), dtype=np.float32)).to(dev)
+    ds = torch.from_numpy(rng.standard_normal((w.n_tokens, 4), dtype=np.float32)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dR, _ = gr.read_backward(R, p["gamma"], p["w_down"], p["w_up"], p["w_write"], dx, ds,
+                                 w.eps, workspace=ws, stream=stream)
+        gr.write_backward(dR, y, s, stream=stream)
+
+    import ctypes
+    need = ctypes.c_size_t(0)
+    shape = gr.make_shape(w.n_tokens, w.d_model, w.rank, tdt, w.eps)
+    gr.load().gr_read_backward_workspace_size(ctypes.byref(shape), ctypes.byref(need))
+    wsb = torch.empty(need.value + 256, dtype=torch.uint8, device=dev)
+    ws = wsb[(-wsb.data_ptr()) % 256:][:need.value]
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    props = torch.cuda.get_device_properties(dev)
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(str(getattr(props, "uuid", "") or ""))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms_step = ms / args.steps
+    # fp32 CUDA-core peak: SMs × 128 fp32 lanes × 2 FLOP × the SM clock seen under load
+    mhz = clocks.get("sm_mhz") or 2070.0
+    peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+    flops = w.n_tokens * backward_flops_per_token(w)
+    achieved = flops / (ms_step / 1e3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": "GR read+write backward tokens/s (one sublayer)",
+            "value": job_tokens_per_s(world, w.n_tokens, args.steps, ms / 1e3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded numpy PCG64; no dataset)",
+            "config": {"workload": workload_desc(w), "n_tokens_per_gpu": w.n_tokens,
+                       "d_model": w.d_model, "rank": w.rank, "state_dtype": w.dtype,
+                       "pass": "backward (gr_read_backward + gr_write_backward)"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": "SMs x 128 fp32 lanes x 2 x sampled SM clock"},
+            "gpu_launches": 6 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def e2e_host_entry(args, w, world, dev, stream, tdt, R_h, y_h, sp_h, P) -> dict:
     """End to end through the host-buffer C entry: H2D of R, y, s_prev; D2H of R', x, s_next."""
     import numpy as np
@@ -567,6 +670,8 @@ def main(argv=None):
         w = w.scaled(n_tokens=args.n_tokens)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.backward:
+        run_backward(args, w)
     else:
         run_gr(args, w)
 

@@ -211,7 +211,8 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
  * pointers, 16-byte aligned. */
 
 /* Bytes of device workspace gr_read_backward needs: 3·N·4·D·4 bytes of per-token factors of
- * the parameter gradients plus N·(2r+5)·4, each part rounded up to 256 bytes. */
+ * the parameter gradients, N·(2r+5)·4 more, and r·4·D·4 for W_u transposed, each part rounded
+ * up to 256 bytes. */
 int gr_read_backward_workspace_size(const gr_shape* shape, size_t* bytes);
 
 /* Backward of the read of R [N][4][D] with the fp32 parameters gamma [4][D], W_d [r][4D],

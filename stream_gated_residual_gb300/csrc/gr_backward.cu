@@ -49,138 +49,220 @@ __device__ __forceinline__ void block_sum(const float (&v)[M], int m, float* red
     __syncthreads();
 }
 
-// RM: the largest rank of the instantiation (16, 32 or 64).
-template <typename T, int RM>
-__global__ void __launch_bounds__(kThreads)
+// Sums of M per-thread values over a block of NW warps; the totals land in out[0..M).
+template <int M, int NW>
+__device__ __forceinline__ void block_sum_w(const float (&v)[M], float* red, float* out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int k = 0; k < M; ++k) {
+        float a = v[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) red[warp * M + k] = a;
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < M; k += NW * 32) {
+        float a = 0.f;
+        for (int w = 0; w < NW; ++w) a += red[w * M + k];
+        out[k] = a;
+    }
+    __syncthreads();
+}
+
+// Threads of the per-token kernel: 512, or 256 at rank 64 (whose accumulators need more than
+// the 128 registers a thread of a 512-thread block can have).
+template <int RM>
+__host__ __device__ constexpr int bwd_threads() { return RM > 32 ? 256 : 512; }
+
+// RM: the largest rank of the instantiation (16, 32 or 64); TB: tokens per CTA at a time. Every
+// weight element a thread loads serves the TB tokens (the weights stream from L2 once per TB
+// tokens); the TB state rows sit in shared memory in the state's own type.
+template <typename T, int RM, int TB>
+__global__ void __launch_bounds__(bwd_threads<RM>())
 read_backward_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
                      const float* __restrict__ gamma, const float* __restrict__ Wd,
-                     const float* __restrict__ Wu, const float* __restrict__ Ww,
+                     const float* __restrict__ WuT, const float* __restrict__ Ww,
                      const float* __restrict__ dx, const float* __restrict__ ds,
                      float* __restrict__ dR, float* __restrict__ DG, float* __restrict__ V,
                      float* __restrict__ P, float* __restrict__ S) {
+    // WuT is W_u transposed, [r][4D]: for each k the block's threads read consecutive channels
     constexpr int M = RM + kBranches;
+    constexpr int kBwdThreads = bwd_threads<RM>();
+    constexpr int kBwdWarps = kBwdThreads / 32;
     extern __shared__ float smem[];
     const int K = kBranches * D;
-    const int ss = 2 * r + kBranches + 1;     // row stride of S
-    float* Rs = smem;                         // [4D] the state row
-    float* red = Rs + K;                      // [kWarps][M]
-    float* tot = red + kWarps * M;            // [M]
-    float* q = tot + M;                       // [M] z at 0..r-1, u at RM..RM+3; then dz, du
-    float* inv = q + M;                       // [4]
+    const int ss = 2 * r + kBranches + 1;                   // row stride of S
+    T* Rs = reinterpret_cast<T*>(smem);                     // [TB][4D] the state rows
+    float* fl = smem + (size_t(TB) * K * sizeof(T) + 15) / 16 * 4;
+    float* red = fl;                                        // [warps][TB·M]
+    float* tot = red + kBwdWarps * TB * M;                  // [TB·M]
+    float* q = tot + TB * M;                                // [TB][M] z|u, then dz|du
+    float* hs = q + TB * M;                                 // [TB][RM] h
+    float* inv = hs + TB * RM;                              // [TB][4]
     const int tid = threadIdx.x;
+    const int64_t ntiles = (N + TB - 1) / TB;
 
-    for (int64_t t = blockIdx.x; t < N; t += gridDim.x) {
-        __syncthreads();   // the previous token is done with the shared arrays
-        const T* Rt = R + t * K;
-        float sq[kBranches] = {0.f, 0.f, 0.f, 0.f};
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t t0 = tile * TB;
+        const int nt = int(N - t0 < TB ? N - t0 : TB);
+        __syncthreads();   // the previous tile is done with the shared arrays
+        float sq[TB * kBranches];
 #pragma unroll
-        for (int i = 0; i < kBranches; ++i)
-            for (int c = tid; c < D; c += kThreads) {
-                const float v = to_f32(Rt[i * D + c]);
-                Rs[i * D + c] = v;
-                sq[i] = fmaf(v, v, sq[i]);
-            }
-        block_sum<kBranches>(sq, kBranches, red, tot);
-        if (tid < kBranches) inv[tid] = rsqrtf(tot[tid] / float(D) + eps);
+        for (int k = 0; k < TB * kBranches; ++k) sq[k] = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < TB; ++tt)
+#pragma unroll
+            for (int i = 0; i < kBranches; ++i)
+                for (int c = tid; c < D; c += kBwdThreads) {
+                    const T v = tt < nt ? R[(t0 + tt) * K + i * D + c] : from_f32<T>(0.f);
+                    Rs[tt * K + i * D + c] = v;
+                    const float f = to_f32(v);
+                    sq[tt * kBranches + i] = fmaf(f, f, sq[tt * kBranches + i]);
+                }
+        block_sum_w<TB * kBranches, kBwdWarps>(sq, red, tot);
+        if (tid < TB * kBranches) inv[tid] = rsqrtf(tot[tid] / float(D) + eps);
         __syncthreads();
-        // z = W_d vec R̂ / 4 and u = W_w vec R̂ / 4 (indices 0..r-1 and RM..RM+3; the slots
-        // between stay zero, so that every index is a compile-time constant)
-        float az[M];
+        // z = W_d vec R̂ / 4 (slots 0..r-1) and u = W_w vec R̂ / 4 (slots RM..RM+3) per token
+        {
+            float az[TB * M];
 #pragma unroll
-        for (int k = 0; k < M; ++k) az[k] = 0.f;
+            for (int k = 0; k < TB * M; ++k) az[k] = 0.f;
 #pragma unroll
-        for (int i = 0; i < kBranches; ++i)
-            for (int c = tid; c < D; c += kThreads) {
-                const int e = i * D + c;
-                const float rh = gamma[e] * Rs[e] * inv[i];
+            for (int i = 0; i < kBranches; ++i)
+                for (int c = tid; c < D; c += kBwdThreads) {
+                    const int e = i * D + c;
+                    const float ge = gamma[e];
+                    float wd[RM], ww[kBranches];
 #pragma unroll
-                for (int k = 0; k < RM; ++k)
-                    if (k < r) az[k] = fmaf(Wd[size_t(k) * K + e], rh, az[k]);
+                    for (int k = 0; k < RM; ++k) wd[k] = k < r ? Wd[size_t(k) * K + e] : 0.f;
 #pragma unroll
-                for (int j = 0; j < kBranches; ++j)
-                    az[RM + j] = fmaf(Ww[size_t(j) * K + e], rh, az[RM + j]);
-            }
-        block_sum<M>(az, M, red, q);
-        // q = [z, u] (scaled below); h = SiLU(z)
-        float h[RM];
+                    for (int j = 0; j < kBranches; ++j) ww[j] = Ww[size_t(j) * K + e];
 #pragma unroll
-        for (int k = 0; k < RM; ++k) {
-            const float z = k < r ? 0.25f * q[k] : 0.f;
-            h[k] = z * sigm(z);
+                    for (int tt = 0; tt < TB; ++tt) {
+                        const float rh = ge * to_f32(Rs[tt * K + e]) * inv[tt * kBranches + i];
+#pragma unroll
+                        for (int k = 0; k < RM; ++k)
+                            az[tt * M + k] = fmaf(wd[k], rh, az[tt * M + k]);
+#pragma unroll
+                        for (int j = 0; j < kBranches; ++j)
+                            az[tt * M + RM + j] = fmaf(ww[j], rh, az[tt * M + RM + j]);
+                    }
+                }
+            block_sum_w<TB * M, kBwdWarps>(az, red, q);
         }
-        // dg and the partial sums of dh = W_uᵀ dg
-        float adh[RM];
-#pragma unroll
-        for (int k = 0; k < RM; ++k) adh[k] = 0.f;
-#pragma unroll
-        for (int i = 0; i < kBranches; ++i)
-            for (int c = tid; c < D; c += kThreads) {
-                const int e = i * D + c;
-                const float* wu = Wu + size_t(e) * r;
-                float g = 0.f;
-#pragma unroll
-                for (int k = 0; k < RM; ++k)
-                    if (k < r) g = fmaf(wu[k], h[k], g);
-                const float G = sigm(g);
-                const float rh = gamma[e] * Rs[e] * inv[i];
-                const float dG = 0.25f * dx[t * D + c] * rh;
-                const float dg = dG * G * (1.0f - G);
-                DG[t * K + e] = dg;
-#pragma unroll
-                for (int k = 0; k < RM; ++k)
-                    if (k < r) adh[k] = fmaf(wu[k], dg, adh[k]);
-            }
-        __syncthreads();   // every thread has read q before it is overwritten
-        block_sum<RM>(adh, r, red, tot);
-        // dz = dh ⊙ SiLU'(z), du = ds ⊙ 2σ'(u); q becomes [dz, .., du] (without the 1/4), and
-        // the token's row of S is [h | dz/4 | du/4 | 1]
-        if (tid < r) {
-            const float z = 0.25f * q[tid];
-            const float sg = sigm(z);
-            S[t * ss + tid] = z * sg;
-            q[tid] = tot[tid] * sg * (1.0f + z * (1.0f - sg));
-            S[t * ss + r + tid] = 0.25f * q[tid];
-        } else if (tid >= RM && tid < RM + kBranches) {
-            const int j = tid - RM;
-            const float sg = sigm(0.25f * q[tid]);
-            q[tid] = ds[t * kBranches + j] * 2.0f * sg * (1.0f - sg);
-            S[t * ss + 2 * r + j] = 0.25f * q[tid];
+        for (int e2 = tid; e2 < TB * RM; e2 += kBwdThreads) {
+            const int tt = e2 / RM, k = e2 - tt * RM;
+            const float z = k < r ? 0.25f * q[tt * M + k] : 0.f;
+            hs[e2] = z * sigm(z);
         }
-        if (tid == 0) S[t * ss + 2 * r + kBranches] = 1.0f;
+        __syncthreads();
+        // dg (streamed out) and the partial sums of dh = W_uᵀ dg
+        {
+            float adh[TB * RM];
+#pragma unroll
+            for (int k = 0; k < TB * RM; ++k) adh[k] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kBranches; ++i)
+                for (int c = tid; c < D; c += kBwdThreads) {
+                    const int e = i * D + c;
+                    const float ge = gamma[e];
+                    float wu[RM];
+#pragma unroll
+                    for (int k = 0; k < RM; ++k) wu[k] = k < r ? WuT[size_t(k) * K + e] : 0.f;
+#pragma unroll
+                    for (int tt = 0; tt < TB; ++tt) {
+                        float g = 0.f;
+#pragma unroll
+                        for (int k = 0; k < RM; ++k) g = fmaf(wu[k], hs[tt * RM + k], g);
+                        const float G = sigm(g);
+                        const float rh = ge * to_f32(Rs[tt * K + e]) * inv[tt * kBranches + i];
+                        const float dxc = tt < nt ? dx[(t0 + tt) * D + c] : 0.f;
+                        const float dg = 0.25f * dxc * rh * G * (1.0f - G);
+                        if (tt < nt) __stcs(&DG[(t0 + tt) * K + e], dg);   // keep weights in L2
+#pragma unroll
+                        for (int k = 0; k < RM; ++k)
+                            adh[tt * RM + k] = fmaf(wu[k], dg, adh[tt * RM + k]);
+                    }
+                }
+            block_sum_w<TB * RM, kBwdWarps>(adh, red, tot);
+        }
+        // dz = dh ⊙ SiLU'(z), du = ds ⊙ 2σ'(u) into q (without the 1/4); the token's row of S
+        // is [h | dz/4 | du/4 | 1]
+        for (int e2 = tid; e2 < TB * M; e2 += kBwdThreads) {
+            const int tt = e2 / M, k = e2 - tt * M;
+            if (tt >= nt) continue;
+            float* Srow = S + (t0 + tt) * ss;
+            if (k < r) {
+                const float z = 0.25f * q[e2];
+                const float sg = sigm(z);
+                Srow[k] = z * sg;
+                q[e2] = tot[tt * RM + k] * sg * (1.0f + z * (1.0f - sg));
+                Srow[r + k] = 0.25f * q[e2];
+            } else if (k >= RM) {
+                const int j = k - RM;
+                const float sg = sigm(0.25f * q[e2]);
+                q[e2] = ds[(t0 + tt) * kBranches + j] * 2.0f * sg * (1.0f - sg);
+                Srow[2 * r + j] = 0.25f * q[e2];
+                if (j == 0) Srow[2 * r + kBranches] = 1.0f;
+            }
+        }
         __syncthreads();
         // dR̂, the token's factors for dγ and the weight gradients, and γ ⊙ dR̂ into dR
-        float apr[kBranches] = {0.f, 0.f, 0.f, 0.f};
+        {
+            float apr[TB * kBranches];
 #pragma unroll
-        for (int i = 0; i < kBranches; ++i)
-            for (int c = tid; c < D; c += kThreads) {
-                const int e = i * D + c;
-                const float* wu = Wu + size_t(e) * r;
-                float g = 0.f;
+            for (int k = 0; k < TB * kBranches; ++k) apr[k] = 0.f;
 #pragma unroll
-                for (int k = 0; k < RM; ++k)
-                    if (k < r) g = fmaf(wu[k], h[k], g);
-                const float G = sigm(g);
-                float back = 0.f;   // W_dᵀ dz + W_wᵀ du at e
+            for (int i = 0; i < kBranches; ++i)
+                for (int c = tid; c < D; c += kBwdThreads) {
+                    const int e = i * D + c;
+                    const float ge = gamma[e];
+                    float wu[RM], wd[RM], ww[kBranches];
 #pragma unroll
-                for (int k = 0; k < RM; ++k)
-                    if (k < r) back = fmaf(Wd[size_t(k) * K + e], q[k], back);
+                    for (int k = 0; k < RM; ++k) {
+                        wu[k] = k < r ? WuT[size_t(k) * K + e] : 0.f;
+                        wd[k] = k < r ? Wd[size_t(k) * K + e] : 0.f;
+                    }
 #pragma unroll
-                for (int j = 0; j < kBranches; ++j) back = fmaf(Ww[size_t(j) * K + e], q[RM + j], back);
-                const float dRh = 0.25f * (dx[t * D + c] * G + back);
-                const float ri = Rs[e] * inv[i];
-                V[t * K + e] = gamma[e] * ri;
-                P[t * K + e] = dRh * ri;
-                const float a = dRh * gamma[e];
-                dR[t * K + e] = a;
-                apr[i] = fmaf(a, Rs[e], apr[i]);
-            }
-        block_sum<kBranches>(apr, kBranches, red, tot);
+                    for (int j = 0; j < kBranches; ++j) ww[j] = Ww[size_t(j) * K + e];
 #pragma unroll
-        for (int i = 0; i < kBranches; ++i) {
-            const float iv = inv[i], i3 = iv * iv * iv * tot[i] / float(D);
-            for (int c = tid; c < D; c += kThreads) {
-                const int e = i * D + c;
-                dR[t * K + e] = iv * dR[t * K + e] - i3 * Rs[e];
+                    for (int tt = 0; tt < TB; ++tt) {
+                        float g = 0.f, back = 0.f;   // W_u h and (W_dᵀ dz + W_wᵀ du) at e
+#pragma unroll
+                        for (int k = 0; k < RM; ++k) {
+                            g = fmaf(wu[k], hs[tt * RM + k], g);
+                            back = fmaf(wd[k], q[tt * M + k], back);
+                        }
+#pragma unroll
+                        for (int j = 0; j < kBranches; ++j)
+                            back = fmaf(ww[j], q[tt * M + RM + j], back);
+                        const float G = sigm(g);
+                        const float dxc = tt < nt ? dx[(t0 + tt) * D + c] : 0.f;
+                        const float dRh = 0.25f * (dxc * G + back);
+                        const float rv = to_f32(Rs[tt * K + e]);
+                        const float ri = rv * inv[tt * kBranches + i];
+                        const float a = dRh * ge;
+                        if (tt < nt) {
+                            __stcs(&V[(t0 + tt) * K + e], ge * ri);
+                            __stcs(&P[(t0 + tt) * K + e], dRh * ri);
+                            dR[(t0 + tt) * K + e] = a;
+                        }
+                        apr[tt * kBranches + i] = fmaf(a, rv, apr[tt * kBranches + i]);
+                    }
+                }
+            block_sum_w<TB * kBranches, kBwdWarps>(apr, red, tot);
+        }
+#pragma unroll
+        for (int tt = 0; tt < TB; ++tt) {
+            if (tt >= nt) break;
+#pragma unroll
+            for (int i = 0; i < kBranches; ++i) {
+                const float iv = inv[tt * kBranches + i];
+                const float i3 = iv * iv * iv * tot[tt * kBranches + i] / float(D);
+                for (int c = tid; c < D; c += kBwdThreads) {
+                    const size_t e = size_t(t0 + tt) * K + i * D + c;
+                    __stcs(&dR[e], iv * dR[e] - i3 * to_f32(Rs[tt * K + i * D + c]));
+                }
             }
         }
     }
@@ -209,6 +291,7 @@ token_sum_kernel(int64_t N, int K, int M, const float* __restrict__ S, int s_str
         }
         __syncthreads();
         if (j < K) {
+#pragma unroll 4
             for (int tt = 0; tt < nt; ++tt) {
                 const float b = B[(t0 + tt) * K + j];
 #pragma unroll
@@ -227,6 +310,16 @@ token_sum_kernel(int64_t N, int K, int M, const float* __restrict__ S, int s_str
                 else atomicAdd(&out1[size_t(m - m0) * K + j], acc[m]);
             }
         }
+    }
+}
+
+// W_u [K][r] -> its transpose [r][K].
+__global__ void transpose_kernel(int K, int r, const float* __restrict__ Wu,
+                                 float* __restrict__ WuT) {
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < int64_t(K) * r;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int k = int(e / K), j = int(e - int64_t(k) * K);
+        WuT[e] = Wu[size_t(j) * r + k];
     }
 }
 
@@ -265,32 +358,63 @@ int grid_tokens(int64_t N) {
     return int(N < cap ? N : cap);
 }
 
-template <typename T, int RM>
-cudaError_t launch_rb(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
-                      const float* Wd, const float* Wu, const float* Ww, const float* dx,
-                      const float* ds, float* dR, float* DG, float* V, float* P, float* S,
-                      cudaStream_t st) {
+template <typename T, int RM, int TB>
+cudaError_t launch_rb_t(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
+                        const float* Wd, const float* WuT, const float* Ww, const float* dx,
+                        const float* ds, float* dR, float* DG, float* V, float* P, float* S,
+                        cudaStream_t st) {
     constexpr int M = RM + kBranches;
-    const size_t smem = (size_t(kBranches) * D + kWarps * M + 2 * M + kBranches) * sizeof(float);
-    auto kern = read_backward_kernel<T, RM>;
+    constexpr int kBwdThreads = bwd_threads<RM>();
+    const size_t K = size_t(kBranches) * D;
+    const size_t smem =
+        (size_t(TB) * K * sizeof(T) + 15) / 16 * 16 +
+        (size_t(kBwdThreads / 32) * TB * M + 2 * TB * M + TB * RM + TB * kBranches) * 4;
+    auto kern = read_backward_kernel<T, RM, TB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid_tokens(N), kThreads, smem, st>>>(N, D, r, eps, static_cast<const T*>(R), gamma,
-                                                  Wd, Wu, Ww, dx, ds, dR, DG, V, P, S);
+    int per_sm = 0;   // a persistent grid: as many CTAs as stay resident
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int64_t ntiles = (N + TB - 1) / TB;
+    const int64_t cap = int64_t(sm_count()) * per_sm;
+    kern<<<unsigned(ntiles < cap ? ntiles : cap), kBwdThreads, smem, st>>>(
+        N, D, r, eps, static_cast<const T*>(R), gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P, S);
     return cudaGetLastError();
+}
+
+// The most tokens per CTA that the registers (TB·(RM+4) accumulators) and shared memory
+// (TB state rows, up to about 200 KB) allow: 4, 2 or 1.
+template <typename T, int RM>
+cudaError_t launch_rb(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
+                      const float* Wd, const float* WuT, const float* Ww, const float* dx,
+                      const float* ds, float* dR, float* DG, float* V, float* P, float* S,
+                      cudaStream_t st) {
+    const size_t row = size_t(kBranches) * D * sizeof(T);
+    const int tb_reg = RM <= 16 ? 4 : RM <= 32 ? 2 : 1;
+    const int tb_smem = row * 4 <= 200 * 1024 ? 4 : row * 2 <= 200 * 1024 ? 2 : 1;
+    const int tb = tb_reg < tb_smem ? tb_reg : tb_smem;
+    if (tb >= 4 && RM <= 16)
+        return launch_rb_t<T, RM, (RM <= 16 ? 4 : 1)>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds,
+                                                      dR, DG, V, P, S, st);
+    if (tb >= 2 && RM <= 32)
+        return launch_rb_t<T, RM, (RM <= 32 ? 2 : 1)>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds,
+                                                      dR, DG, V, P, S, st);
+    return launch_rb_t<T, RM, 1>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P, S,
+                                 st);
 }
 
 template <int MM>
 cudaError_t launch_sum(int64_t N, int K, int M, const float* S, int s_stride, int soff,
                        const float* B, float* out0, float* out1, int m0, bool transposed,
                        cudaStream_t st) {
+    // 128 tokens per CTA: thousands of CTAs keep enough loads of the long factor in flight
+    // (a few CTAs walking thousands of tokens each were latency-bound); the cost is one atomic
+    // per output element and CTA row
     const int gx = (K + kThreads - 1) / kThreads;
-    int gy = (2 * sm_count() + gx - 1) / gx;
-    const int64_t max_gy = (N + 31) / 32;
-    if (gy > max_gy) gy = int(max_gy);
-    if (gy < 1) gy = 1;
-    const int64_t per = ((N + gy - 1) / gy + 31) / 32 * 32;
+    const int64_t per = 128;
+    const int gy = int((N + per - 1) / per);
     token_sum_kernel<MM><<<dim3(gx, gy), kThreads, 0, st>>>(N, K, M, S, s_stride, soff, B, out0,
                                                             out1, m0, transposed, per);
     return cudaGetLastError();
@@ -300,7 +424,8 @@ cudaError_t launch_sum(int64_t N, int K, int M, const float* S, int s_stride, in
 
 size_t read_backward_workspace(int64_t N, int D, int r) {
     const size_t K = size_t(kBranches) * D;
-    return 3 * align256(size_t(N) * K * 4) + align256(size_t(N) * (2 * r + kBranches + 1) * 4);
+    return 3 * align256(size_t(N) * K * 4) + align256(size_t(N) * (2 * r + kBranches + 1) * 4) +
+           align256(size_t(r) * K * 4);
 }
 
 cudaError_t launch_read_backward(int64_t N, int D, int r, float eps, int dtype, const void* R,
@@ -314,6 +439,8 @@ cudaError_t launch_read_backward(int64_t N, int D, int r, float eps, int dtype, 
     float* V = reinterpret_cast<float*>(ws + align256(size_t(N) * K * 4));
     float* P = reinterpret_cast<float*>(ws + 2 * align256(size_t(N) * K * 4));
     float* S = reinterpret_cast<float*>(ws + 3 * align256(size_t(N) * K * 4));
+    float* WuT = reinterpret_cast<float*>(ws + 3 * align256(size_t(N) * K * 4) +
+                                          align256(size_t(N) * (2 * r + kBranches + 1) * 4));
     const int ss = 2 * r + kBranches + 1;
     cudaError_t e;
     if ((e = cudaMemsetAsync(dgamma, 0, K * 4, st)) != cudaSuccess ||
@@ -322,22 +449,24 @@ cudaError_t launch_read_backward(int64_t N, int D, int r, float eps, int dtype, 
         (e = cudaMemsetAsync(dWw, 0, size_t(kBranches) * K * 4, st)) != cudaSuccess)
         return e;
     if (N == 0) return cudaSuccess;
+    transpose_kernel<<<sm_count() * 4, kThreads, 0, st>>>(int(K), r, Wu, WuT);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool bf = dtype == GR_BF16;
     if (r <= 16)
-        e = bf ? launch_rb<__nv_bfloat16, 16>(N, D, r, eps, R, gamma, Wd, Wu, Ww, dx, ds, dR, DG,
-                                              V, P, S, st)
-               : launch_rb<float, 16>(N, D, r, eps, R, gamma, Wd, Wu, Ww, dx, ds, dR, DG, V, P, S,
-                                      st);
+        e = bf ? launch_rb<__nv_bfloat16, 16>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR,
+                                              DG, V, P, S, st)
+               : launch_rb<float, 16>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P,
+                                      S, st);
     else if (r <= 32)
-        e = bf ? launch_rb<__nv_bfloat16, 32>(N, D, r, eps, R, gamma, Wd, Wu, Ww, dx, ds, dR, DG,
-                                              V, P, S, st)
-               : launch_rb<float, 32>(N, D, r, eps, R, gamma, Wd, Wu, Ww, dx, ds, dR, DG, V, P, S,
-                                      st);
+        e = bf ? launch_rb<__nv_bfloat16, 32>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR,
+                                              DG, V, P, S, st)
+               : launch_rb<float, 32>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P,
+                                      S, st);
     else
-        e = bf ? launch_rb<__nv_bfloat16, 64>(N, D, r, eps, R, gamma, Wd, Wu, Ww, dx, ds, dR, DG,
-                                              V, P, S, st)
-               : launch_rb<float, 64>(N, D, r, eps, R, gamma, Wd, Wu, Ww, dx, ds, dR, DG, V, P, S,
-                                      st);
+        e = bf ? launch_rb<__nv_bfloat16, 64>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR,
+                                              DG, V, P, S, st)
+               : launch_rb<float, 64>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P,
+                                      S, st);
     if (e != cudaSuccess) return e;
     const int Kk = int(K);
     // dW_u[j][k] = Σ_t dg[t][j] h[t][k]
