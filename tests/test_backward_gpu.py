@@ -37,7 +37,9 @@ def rel_rows_floor(a, b, floor_frac=1e-3):
 @pytest.mark.parametrize("N,D,r,dtype", [(1, 64, 1, "f32"), (5, 64, 4, "f32"),
                                          (37, 256, 16, "bf16"), (100, 1032, 32, "f32"),
                                          (64, 4096, 16, "bf16"), (17, 520, 64, "f32"),
-                                         (300, 2048, 20, "bf16")])
+                                         (300, 2048, 20, "bf16"), (33, 512, 24, "bf16"),
+                                         (9, 4096, 8, "f32"), (3, 12288, 40, "f32"),
+                                         (7, 12288, 16, "bf16")])
 def test_read_backward_matches_oracle(N, D, r, dtype):
     w = wl.Workload("bwd", N, D, r, dtype, y_std=0.5, seed=41)
     R = wl.make_state(w)
