@@ -92,16 +92,17 @@ def load_peaks() -> dict:
 
 
 def kernel_source_sha(kernel_path: str) -> str:
+    """Hash of the sources that decide a kernel path's device traffic: the kernels' .cu files and
+    the PTX wrappers they share; a split path ("fused_bf16+tiled_bf16") adds the split dispatch
+    (gr_split.cu), which decides how many tokens each kernel gets."""
     from stream_gated_residual_gb300 import build as gbuild
     files = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
              "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu"}
-    # a split path ("fused_bf16+tiled_bf16") hashes both kernels' sources and the dispatch
     names = [files[k] for k in kernel_path.split("+")]
     if len(names) > 1:
-        names.append("gr_api.cu")
+        names.append("gr_split.cu")
     h = hashlib.sha256()
-    for p in [os.path.join(gbuild.CSRC, n) for n in names] + [
-            os.path.join(gbuild.CSRC, "gr_internal.h"), os.path.join(gbuild.CSRC, "gr_ptx.cuh")]:
+    for p in [os.path.join(gbuild.CSRC, n) for n in names + ["gr_ptx.cuh"]]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -126,67 +126,6 @@ bool use_fused(const gr_shape* s) {
            s->n_tokens <= fused_max_tokens();
 }
 
-// Concurrent split of a large cluster-kernel step. The cluster kernel fills only the SMs its
-// resident clusters take (7 clusters of 16 = 112 of 152 SMs at D = 4096); the two-pass kernel
-// takes a share of the tokens on the rest, on an internal stream forked from the caller's stream
-// and joined back to it.
-// The share is k whole rounds of 32-token tiles on the free SMs, with k chosen to minimise the
-// later of the two finish times. Time model, in units of the cluster kernel's period per
-// 16-token tile and cluster (about 2.2 µs, nearly independent of D since each CTA always owns
-// 256 channels): a two-pass tile of 32 tokens takes kTiledTilePerChannel · D of them (about
-// 115 µs at D = 4096). At the prefill shape this gives 2560 of 16384 tokens to 40 SMs, the best
-// split measured there.
-constexpr double kTiledTilePerChannel = 0.0122;
-
-struct SplitPipe {
-    std::mutex mu;
-    bool ready = false;
-    cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-SplitPipe g_split[kMaxDevices];
-
-bool split_pipe_init(SplitPipe& sp) {
-    if (sp.ready) return true;
-    if (cudaStreamCreateWithFlags(&sp.aux, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&sp.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&sp.join, cudaEventDisableTiming) != cudaSuccess)
-        return false;
-    sp.ready = true;
-    return true;
-}
-
-// Tokens of a cluster-kernel step that go to the two-pass kernel (a multiple of 32), and the
-// SMs it gets; 0 when the step is not split.
-int64_t split_tokens(const gr_shape* s, bool write, int* free_sms) {
-    if (s->state_dtype != GR_BF16 || !fused_supported(s->d_model, s->rank) ||
-        !tiled_supported(s->d_model, s->rank))
-        return 0;
-    const double rho = kTiledTilePerChannel * s->d_model;   // one two-pass round
-    // cheap bound first (no device query): one two-pass round must fit in the cluster kernel's
-    // time even with a single cluster of 16 per 16 SMs' worth of the device
-    if (double(s->n_tokens) < 16.0 * 4.0 * rho) return 0;
-    const int fused_ctas = fused_resident_ctas(s->d_model, s->rank, write);
-    const int clusters = fused_ctas / (s->d_model / 256);
-    const int free = sm_count() - fused_ctas;
-    if (fused_ctas <= 0 || clusters <= 0 || free < 1) return 0;
-    const double N = double(s->n_tokens);
-    double best = N / (16.0 * clusters);   // no split
-    int64_t best_n2 = 0;
-    for (int k = 1; k * rho < best; ++k) {
-        const int64_t n2 = int64_t(32) * k * free;
-        if (n2 >= s->n_tokens) break;
-        const double t_f = (N - double(n2)) / (16.0 * clusters);
-        const double t = t_f > k * rho ? t_f : k * rho;
-        if (t < best) {
-            best = t;
-            best_n2 = n2;
-        }
-    }
-    if (best_n2 > 0 && free_sms) *free_sms = free;
-    return best_n2;
-}
-
 bool use_tiled(const gr_shape* s) {
     return s->state_dtype == GR_BF16 && !fused_supported(s->d_model, s->rank) &&
            tiled_supported(s->d_model, s->rank) && s->n_tokens <= tiled_max_tokens();
@@ -197,36 +136,12 @@ int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
     if (s->n_tokens == 0) return GR_OK;
     cudaError_t e;
     int free_sms = 0;
-    const int64_t n2 = use_fused(s) ? split_tokens(s, y != nullptr, &free_sms) : 0;
-    if (n2 > 0) {
-        // tokens [0, n1) on the cluster kernel (caller's stream), [n1, N) on the two-pass kernel
-        // (internal stream), which waits for the work already on the caller's stream and which
-        // the caller's stream waits for afterwards
-        const int d = current_device();
-        if (d < 0) return GR_E_DEVICE;
-        SplitPipe& sp = g_split[d];
-        std::lock_guard<std::mutex> lock(sp.mu);
-        if (!split_pipe_init(sp)) return GR_E_CUDA;
-        const int64_t n1 = s->n_tokens - n2;
-        const size_t D = size_t(s->d_model);
-        char* R2 = static_cast<char*>(R) + size_t(n1) * kBranches * D * 2;
-        const char* y2 = y ? static_cast<const char*>(y) + size_t(n1) * D * 2 : nullptr;
-        const float* sp2 = s_prev ? s_prev + size_t(n1) * kBranches : nullptr;
-        char* x2 = static_cast<char*>(x) + size_t(n1) * D * 2;
-        float* so2 = s_out + size_t(n1) * kBranches;
-        if (cudaEventRecord(sp.fork, st) != cudaSuccess ||
-            cudaStreamWaitEvent(sp.aux, sp.fork, 0) != cudaSuccess)
-            return GR_E_CUDA;
-        e = launch_fused_bf16(n1, s->d_model, s->rank, s->eps, R, y, s_prev, p->packed, x, s_out,
-                              st);
-        if (e == cudaSuccess)
-            e = launch_tiled_bf16(n2, s->d_model, s->rank, s->eps, R2, y2, sp2, p->packed, x2, so2,
-                                  sp.aux, free_sms);
-        if (e == cudaSuccess && (cudaEventRecord(sp.join, sp.aux) != cudaSuccess ||
-                                 cudaStreamWaitEvent(st, sp.join, 0) != cudaSuccess))
-            return GR_E_CUDA;
-        return status_of(e);
-    }
+    const int64_t n2 =
+        use_fused(s) ? split_tokens(s->n_tokens, s->d_model, s->rank, y != nullptr, &free_sms)
+                     : 0;
+    if (n2 > 0)
+        return status_of(launch_split_bf16(s->n_tokens, n2, free_sms, s->d_model, s->rank,
+                                           s->eps, R, y, s_prev, p->packed, x, s_out, st));
     if (use_fused(s))
         e = launch_fused_bf16(s->n_tokens, s->d_model, s->rank, s->eps, R, y, s_prev, p->packed,
                               x, s_out, st);
@@ -284,7 +199,9 @@ const char* gr_kernel_path(const gr_shape* shape) {
         return validate_fp8(shape, true) == GR_OK ? "tiled_fp8" : "invalid";
     if (validate_shape(shape) != GR_OK) return "invalid";
     if (use_fused(shape))
-        return split_tokens(shape, true, nullptr) > 0 ? "fused_bf16+tiled_bf16" : "fused_bf16";
+        return split_tokens(shape->n_tokens, shape->d_model, shape->rank, true, nullptr) > 0
+                   ? "fused_bf16+tiled_bf16"
+                   : "fused_bf16";
     return use_tiled(shape) ? "tiled_bf16" : "generic";
 }
 

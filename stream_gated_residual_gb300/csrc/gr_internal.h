@@ -47,6 +47,15 @@ size_t fused_frag_bytes(int D, int r);
 bool tiled_supported(int D, int r);
 int64_t tiled_max_tokens();
 size_t tiled_frag_bytes(int D, int r);
+// Concurrent split of a bf16 cluster-kernel shape (gr_split.cu): the tokens of the step that go
+// to the two-pass kernel (a multiple of 32; 0 = no split) and the SMs it gets (*free_sms).
+int64_t split_tokens(int64_t N, int D, int r, bool write, int* free_sms);
+// Tokens [0, N − n2) on the cluster kernel on st, [N − n2, N) on the two-pass kernel on an
+// internal stream forked from st and joined back to it.
+cudaError_t launch_split_bf16(int64_t N, int64_t n2, int free_sms, int D, int r, float eps,
+                              void* R, const void* y, const float* s_prev, const void* packed,
+                              void* x, float* s_out, cudaStream_t st);
+
 // The two-pass kernel on an FP8 state also needs D % 128 == 0 and D <= 8192.
 bool tiled_fp8_supported(int D, int r);
 
