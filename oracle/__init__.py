@@ -8,12 +8,12 @@ product path (the CUDA library and its Python binding) never does, and the two s
 The functions here take numpy arrays of any float dtype, convert them exactly to float64, and
 return float64 arrays.
 """
-from .oracle import (build, chain, fp8_code_values, fp8_decode, fp8_encode, fp8_round_codes,
+from .oracle import (build, chain, decompose, fp8_code_values, fp8_decode, fp8_encode, fp8_round_codes,
                      lib, num_threads, read, read_backward, read_fixed_gates, residual_add,
                      round_to_storage, set_num_threads, use_library, write, write_backward,
                      write_then_read, write_then_read_fp8)
 
-__all__ = ["build", "chain", "fp8_code_values", "fp8_decode", "fp8_encode", "fp8_round_codes",
+__all__ = ["build", "chain", "decompose", "fp8_code_values", "fp8_decode", "fp8_encode", "fp8_round_codes",
            "lib", "num_threads", "read", "read_backward", "read_fixed_gates", "residual_add",
            "round_to_storage", "write_backward",
            "set_num_threads", "use_library", "write", "write_then_read", "write_then_read_fp8"]

@@ -325,6 +325,94 @@ int gro_write_backward(int64_t n, int nb, int D, const double *dRp, const double
     return 0;
 }
 
+/* ---- contribution decomposition (eq auv and π, §二.6) -----------------------------------------
+ * GR never mixes branches, so each branch of the state block v reads is the initial state plus
+ * the writes of the blocks before it, and the read splits exactly into per-writer terms. Reader v
+ * reads R (= R^(v)) with its parameters; writers u = 0..U-1 wrote y^(u) with strengths s^(u).
+ * Per token, with G the read's gates and inv_i = 1/rms(R_i):
+ *   a_{u→v,i}[c] = (1/n_r) G_i[c] γ_i[c] inv_i s_i^(u) y^(u)[c]     (branch i's share)
+ *   a_{u→v}[c]   = Σ_i a_{u→v,i}[c]                                    (eq auv)
+ *   norm[u]      = ‖a_{u→v}‖₂ over the D channels,  bnorm[u][i] = ‖a_{u→v,i}‖₂
+ *   pi[u]        = norm[u] / Σ_u' norm[u']  (0 when that sum is 0)
+ *   a_{0→v}[c]   = (1/n_r) Σ_i G_i[c] γ_i[c] inv_i R0_i[c],  a0_norm = ‖a_{0→v}‖₂  (R0 given)
+ * Layouts: Y [U][n][D], S [U][n][nb], R0 [n][nb][D] (or NULL); outputs norm [n][U],
+ * bnorm [n][U][nb], pi [n][U], a0_norm [n] (with R0); optional vectors A [n][U][D], A0 [n][D]. */
+int gro_decompose(int64_t n, int nb, int D, int r, double eps, const double *R,
+                  const double *gamma, const double *Wd, const double *Wu, const double *Ww,
+                  int U, const double *Y, const double *S, const double *R0, double *norm,
+                  double *bnorm, double *pi, double *a0_norm, double *A, double *A0)
+{
+    if (bad_dims(n, nb, D, r) || U < 0 || !R || !gamma || !Wd || !Wu || !Ww || !norm ||
+        !bnorm || !pi || (U > 0 && (!Y || !S)) || (R0 && !a0_norm))
+        return -1;
+    const size_t K = (size_t)nb * D;
+    const double inv_nb = 1.0 / (double)nb;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *Rh = malloc(K * sizeof(double));
+        double *G = malloc(K * sizeof(double));
+        double *h = malloc((size_t)r * sizeof(double));
+        double *inv = malloc((size_t)nb * sizeof(double));
+        double *xs = malloc(((size_t)D + nb) * sizeof(double));
+        double *bq = malloc((size_t)nb * sizeof(double));
+        if (!Rh || !G || !h || !inv || !xs || !bq) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < n; ++t) {
+                const double *Rt = R + (size_t)t * K;
+                group_rmsnorm(nb, D, eps, Rt, gamma, Rh, inv);
+                read_from_normalised(nb, D, r, Rh, Wd, Wu, Ww, h, G, xs, xs + D, NULL);
+                double total = 0.0;
+                for (int u = 0; u < U; ++u) {
+                    const double *yu = Y + ((size_t)u * n + t) * D;
+                    const double *su = S + ((size_t)u * n + t) * nb;
+                    double sq = 0.0;
+                    for (int i = 0; i < nb; ++i)
+                        bq[i] = 0.0;
+                    for (int c = 0; c < D; ++c) {
+                        double a = 0.0;
+                        for (int i = 0; i < nb; ++i) {
+                            const size_t j = (size_t)i * D + c;
+                            const double ai = inv_nb * G[j] * gamma[j] * inv[i] * su[i] * yu[c];
+                            bq[i] += ai * ai;
+                            a += ai;
+                        }
+                        sq += a * a;
+                        if (A)
+                            A[((size_t)t * U + u) * D + c] = a;
+                    }
+                    norm[(size_t)t * U + u] = sqrt(sq);
+                    for (int i = 0; i < nb; ++i)
+                        bnorm[((size_t)t * U + u) * nb + i] = sqrt(bq[i]);
+                    total += sqrt(sq);
+                }
+                for (int u = 0; u < U; ++u)
+                    pi[(size_t)t * U + u] = total > 0.0 ? norm[(size_t)t * U + u] / total : 0.0;
+                if (R0) {
+                    const double *R0t = R0 + (size_t)t * K;
+                    double sq = 0.0;
+                    for (int c = 0; c < D; ++c) {
+                        double a = 0.0;
+                        for (int i = 0; i < nb; ++i) {
+                            const size_t j = (size_t)i * D + c;
+                            a += inv_nb * G[j] * gamma[j] * inv[i] * R0t[j];
+                        }
+                        sq += a * a;
+                        if (A0)
+                            A0[(size_t)t * D + c] = a;
+                    }
+                    a0_norm[t] = sqrt(sq);
+                }
+            }
+        }
+        free(Rh); free(G); free(h); free(inv); free(xs); free(bq);
+    }
+    return failed ? -2 : 0;
+}
+
 /* gr_write: eq write, R'_i = R_i + s_i y, for n tokens. R_out may equal R. */
 int gro_write(int64_t n, int nb, int D, const double *R, const double *y, const double *s,
               double *R_out)

@@ -47,9 +47,11 @@ def _load(path: str) -> ctypes.CDLL:
     L.gro_fp8_decode.argtypes = [i64, i32, U, U, P]
     L.gro_fp8_code_values.argtypes = [P]
     L.gro_fp8_round_codes.argtypes = [i64, P, U]
+    L.gro_decompose.argtypes = [i64, i32, i32, i32, f64, P, P, P, P, P, i32, P, P, P, P, P, P,
+                                P, P, P]
     for f in ("gro_read", "gro_write", "gro_write_then_read", "gro_read_fixed_gates",
               "gro_residual_add", "gro_num_threads", "gro_round_significand", "gro_fp8_encode",
-              "gro_read_backward", "gro_write_backward",
+              "gro_read_backward", "gro_write_backward", "gro_decompose",
               "gro_fp8_decode", "gro_fp8_code_values", "gro_fp8_round_codes"):
         getattr(L, f).restype = ctypes.c_int
     return L
@@ -200,6 +202,39 @@ def write_backward(dRp, y, s):
     _check(lib().gro_write_backward(n, nb, D, _p(dRp), _p(y), _p(s), _p(dR), _p(dy), _p(ds)),
            "write_backward")
     return dR, dy, ds
+
+
+# ---- contribution decomposition ---------------------------------------------------------------
+
+def decompose(R, params: dict, ys, ss, eps: float = 1e-6, R0=None, vectors: bool = False):
+    """eq auv at reader v: R [n, nb, D] the state the reader reads, ``params`` its parameters,
+    ys [U, n, D] and ss [U, n, nb] the writers' outputs and write strengths, R0 [n, nb, D] the
+    initial state (optional). Returns a dict with norm [n, U] (‖a_{u→v}‖ per token), bnorm
+    [n, U, nb] (per branch), pi [n, U], and with R0 a0_norm [n]; with ``vectors`` also A
+    [n, U, D] (the vectors a_{u→v}) and, with R0, A0 [n, D]."""
+    R = _f64(R)
+    n, nb, D = R.shape
+    gamma, Wd, Wu, Ww = (_f64(params[k]) for k in ("gamma", "w_down", "w_up", "w_write"))
+    r = Wd.shape[0]
+    ys = _f64(ys).reshape(-1, n, D)
+    ss = _f64(ss).reshape(-1, n, nb)
+    U = ys.shape[0]
+    assert ss.shape[0] == U
+    R0 = None if R0 is None else _f64(R0)
+    assert R0 is None or R0.shape == R.shape
+    out = {"norm": np.empty((n, U)), "bnorm": np.empty((n, U, nb)), "pi": np.empty((n, U))}
+    if R0 is not None:
+        out["a0_norm"] = np.empty(n)
+    if vectors:
+        out["A"] = np.empty((n, U, D))
+        if R0 is not None:
+            out["A0"] = np.empty((n, D))
+    _check(lib().gro_decompose(n, nb, D, r, float(eps), _p(R), _p(gamma), _p(Wd), _p(Wu),
+                               _p(Ww), U, _p(ys) if U else None, _p(ss) if U else None,
+                               _p(R0), _p(out["norm"]), _p(out["bnorm"]), _p(out["pi"]),
+                               _p(out.get("a0_norm")), _p(out.get("A")), _p(out.get("A0"))),
+           "decompose")
+    return out
 
 
 # ---- FP8 state: e4m3 codes with one power-of-two scale per 32-channel block -----------------

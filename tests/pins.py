@@ -470,6 +470,87 @@ def pin_fp8_write_then_read_error():
     assert _rel(x, xp) <= 2.0 ** -3 and _rel(s, sp2) <= 2.0 ** -3
 
 
+def pin_decompose_exact_split():
+    """eq rcv + eq auv (Digest §二.6): on an fp64 chain the reader's input splits exactly into
+    the initial state's share and the writers' shares, a_{0→v} + Σ_u a_{u→v} = x^(v), so the
+    fractions π sum to 1 for every token; the norms are those of the returned vectors."""
+    rng = np.random.default_rng(113)
+    n, nb, D, r, L, eps = 3, 4, 24, 4, 6, 1e-6
+    R0 = rng.standard_normal((n, nb, D))
+    ys = [0.7 * rng.standard_normal((n, D)) for _ in range(L)]
+    ps = [_params(rng, nb, D, r, std=0.4) for _ in range(L)]
+    states, xs, ss = oracle.chain(R0, ys, ps, eps)
+    for v in (1, L - 1):
+        o = oracle.decompose(states[v], ps[v], np.stack(ys[:v]), np.stack(ss[:v]), eps, R0=R0,
+                             vectors=True)
+        assert _rel(o["A0"] + o["A"].sum(axis=1), xs[v]) < 1e-13
+        assert np.allclose(o["pi"].sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert np.allclose(o["norm"], np.linalg.norm(o["A"], axis=2), rtol=1e-14, atol=0)
+        assert np.allclose(o["a0_norm"], np.linalg.norm(o["A0"], axis=1), rtol=1e-14, atol=0)
+
+
+def pin_decompose_closed_form():
+    """With W_u = 0 every gate is exactly σ(0) = ½, and with a gain g_i constant over each branch
+    a_{u→v,i} = (1/8) g_i s_i^(u) y^(u) / rms(R_i): every norm in closed form from the inputs
+    (rms taken here with numpy from its definition, eps = 1e-3, signed s and gains)."""
+    rng = np.random.default_rng(114)
+    n, nb, D, r, U, eps = 5, 4, 16, 3, 7, 1e-3
+    R = rng.standard_normal((n, nb, D)) * np.array([0.5, 1.0, 2.0, 4.0])[None, :, None]
+    R0 = rng.standard_normal((n, nb, D))
+    g = np.array([1.5, -0.7, 0.9, 2.0])
+    p = _params(rng, nb, D, r, std=0.5)
+    p["gamma"] = np.repeat(g[:, None], D, axis=1)
+    p["w_up"] = np.zeros((nb * D, r))
+    ys = rng.standard_normal((U, n, D))
+    ss = rng.uniform(-2.0, 2.0, (U, n, nb))
+    o = oracle.decompose(R, p, ys, ss, eps, R0=R0)
+    inv = 1.0 / np.sqrt(np.mean(R * R, axis=2) + eps)                  # [n, nb]
+    ynorm = np.linalg.norm(ys, axis=2).T                               # [n, U]
+    coef = g[None, :] * inv                                            # [n, nb]
+    bn = np.abs(coef[:, None, :] * ss.transpose(1, 0, 2)) * ynorm[:, :, None] / 8.0
+    tot = np.abs((coef[:, None, :] * ss.transpose(1, 0, 2)).sum(axis=2)) * ynorm / 8.0
+    a0 = np.linalg.norm((coef[:, :, None] * R0).sum(axis=1), axis=1) / 8.0
+    assert np.allclose(o["bnorm"], bn, rtol=1e-13, atol=0)
+    assert np.allclose(o["norm"], tot, rtol=1e-13, atol=0)
+    assert np.allclose(o["pi"], tot / tot.sum(axis=1, keepdims=True), rtol=1e-13, atol=0)
+    assert np.allclose(o["a0_norm"], a0, rtol=1e-13, atol=0)
+
+
+def pin_decompose_branch_permutation():
+    """Branches are exchangeable (Digest §二.6): permuting the branches of the state, the
+    parameters, the write strengths and the initial state permutes the per-branch norms and
+    leaves the per-writer norms, π and the initial state's share unchanged."""
+    rng = np.random.default_rng(115)
+    n, nb, D, r, U = 3, 4, 12, 3, 5
+    R, R0 = rng.standard_normal((n, nb, D)), rng.standard_normal((n, nb, D))
+    p = _params(rng, nb, D, r, std=0.5)
+    ys, ss = rng.standard_normal((U, n, D)), rng.uniform(0, 2, (U, n, nb))
+    perm = np.array([2, 0, 3, 1])
+    blocks = np.concatenate([np.arange(i * D, (i + 1) * D) for i in perm])
+    q = {"gamma": p["gamma"][perm], "w_down": p["w_down"][:, blocks],
+         "w_up": p["w_up"][blocks, :], "w_write": p["w_write"][perm][:, blocks]}
+    o = oracle.decompose(R, p, ys, ss, R0=R0)
+    o2 = oracle.decompose(R[:, perm], q, ys, ss[:, :, perm], R0=R0[:, perm])
+    assert _rel(o2["norm"], o["norm"]) < 1e-13 and _rel(o2["pi"], o["pi"]) < 1e-13
+    assert _rel(o2["bnorm"], o["bnorm"][:, :, perm]) < 1e-13
+    assert _rel(o2["a0_norm"], o["a0_norm"]) < 1e-13
+
+
+def pin_decompose_degenerate():
+    """No writers: empty outputs; writers that wrote zeros: zero norms and π = 0; one writer:
+    π = 1."""
+    rng = np.random.default_rng(116)
+    n, nb, D, r = 2, 4, 8, 2
+    R = rng.standard_normal((n, nb, D))
+    p = _params(rng, nb, D, r)
+    o = oracle.decompose(R, p, np.zeros((0, n, D)), np.zeros((0, n, nb)))
+    assert o["norm"].shape == (n, 0) and o["pi"].shape == (n, 0)
+    o = oracle.decompose(R, p, np.zeros((3, n, D)), np.ones((3, n, nb)))
+    assert np.all(o["norm"] == 0) and np.all(o["pi"] == 0) and np.all(o["bnorm"] == 0)
+    o = oracle.decompose(R, p, rng.standard_normal((1, n, D)), np.ones((1, n, nb)))
+    assert np.all(o["pi"] == 1.0)
+
+
 ALL_PINS = [pin_dense_bruteforce, pin_zero_down_projection, pin_zero_up_projection,
             pin_zero_write_projection, pin_gatednorm_single_branch, pin_replicated_branches,
             pin_prenorm_reduction, pin_two_branch_toy, pin_two_branch_learned_gate,
@@ -477,4 +558,6 @@ ALL_PINS = [pin_dense_bruteforce, pin_zero_down_projection, pin_zero_up_projecti
             pin_branch_scale_invariance, pin_ranges_and_saturation, pin_residual_add,
             pin_fp8_codes_match_torch, pin_fp8_block_scale, pin_fp8_roundtrip,
             pin_fp8_blocks_independent, pin_fp8_write_then_read_error,
-            pin_backward_finite_differences, pin_backward_torch_autograd, pin_write_backward]
+            pin_backward_finite_differences, pin_backward_torch_autograd, pin_write_backward,
+            pin_decompose_exact_split, pin_decompose_closed_form, pin_decompose_branch_permutation,
+            pin_decompose_degenerate]

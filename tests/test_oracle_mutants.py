@@ -53,6 +53,20 @@ MUTANTS = {
                        "scales[(size_t)t * nblk + k] = (uint8_t)(e + 128);"),
     "fp8_amax_over_16": ("            for (int c = 0; c < 32; ++c)\n                if (fabs(vb[c]) > a)",
                          "            for (int c = 0; c < 16; ++c)\n                if (fabs(vb[c]) > a)"),
+    "dec_drop_1/n_r": ("const double ai = inv_nb * G[j] * gamma[j] * inv[i] * su[i] * yu[c];",
+                       "const double ai = G[j] * gamma[j] * inv[i] * su[i] * yu[c];"),
+    "dec_s_of_branch0": ("const double ai = inv_nb * G[j] * gamma[j] * inv[i] * su[i] * yu[c];",
+                         "const double ai = inv_nb * G[j] * gamma[j] * inv[i] * su[0] * yu[c];"),
+    "dec_drop_inv": ("const double ai = inv_nb * G[j] * gamma[j] * inv[i] * su[i] * yu[c];",
+                     "const double ai = inv_nb * G[j] * gamma[j] * su[i] * yu[c];"),
+    "dec_norm_not_sqrt": ("norm[(size_t)t * U + u] = sqrt(sq);", "norm[(size_t)t * U + u] = sq;"),
+    "dec_branch_norm_of_total": ("bq[i] += ai * ai;", "bq[i] += a * a;"),
+    "dec_pi_unnormalised": ("total > 0.0 ? norm[(size_t)t * U + u] / total : 0.0;",
+                            "total > 0.0 ? norm[(size_t)t * U + u] : 0.0;"),
+    "dec_writer_token_transposed": ("const double *yu = Y + ((size_t)u * n + t) * D;",
+                                    "const double *yu = Y + ((size_t)t * U + u) * D;"),
+    "dec_a0_without_gate": ("a += inv_nb * G[j] * gamma[j] * inv[i] * R0t[j];",
+                            "a += inv_nb * gamma[j] * inv[i] * R0t[j];"),
 }
 
 
