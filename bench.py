@@ -40,7 +40,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gr", "reference"], default="gr")
-    ap.add_argument("--workload", default="prefill")
+    ap.add_argument("--workload", default=None,
+                    help="workload name (default: prefill; deep_stack with --decompose)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
@@ -49,6 +50,11 @@ def parse_args(argv=None):
     ap.add_argument("--backward", action="store_true",
                     help="time one sublayer's GR backward (gr_read_backward, then "
                          "gr_write_backward in place) instead of the fused forward step")
+    ap.add_argument("--decompose", action="store_true",
+                    help="time the contribution decomposition of a stack of --blocks GR blocks "
+                         "(every reader against all its writers) instead of the fused step")
+    ap.add_argument("--blocks", type=int, default=40,
+                    help="blocks of the decomposed stack (40: the pages' 780 block pairs)")
     ap.add_argument("--n-tokens", type=int, default=None,
                     help="run the workload's shape with this many tokens instead (small cases "
                          "for profiling; the line then reports no ncu traffic)")
@@ -593,6 +599,151 @@ def run_backward(args, w) -> None:
         dist.destroy_process_group()
 
 
+def decompose_bytes(w, blocks: int) -> int:
+    """Algorithmic HBM bytes of one decomposition of a stack of ``blocks`` GR blocks: for every
+    reader v = 1..blocks-1, its state and the initial state (4·D each, state dtype), its v
+    writers' outputs (D, state dtype) and write strengths (4 fp32), and its outputs per token
+    (v writer norms, 4v branch norms, v fractions and the initial state's share, fp32), plus
+    its parameters (fp32) once."""
+    es = w.state_bytes_per_elem()
+    D, r, N = w.d_model, w.rank, w.n_tokens
+    total = 0
+    for v in range(1, blocks):
+        total += N * (2 * 4 * D * es + v * (D * es + 16) + v * 4 * 6 + 4)
+        total += 4 * (4 * D + 2 * r * 4 * D + 4 * 4 * D)
+    return total
+
+
+def run_decompose(args, w) -> None:
+    """The contribution decomposition (eq auv and π) of a stack of --blocks GR blocks on the
+    workload's shape: the stack's states, write strengths and block outputs are made once by
+    the library's own forward chain (seeded y, fresh weights per block); one step decomposes
+    every reader v = 1..blocks-1 against its v writers and the initial state (all
+    blocks·(blocks-1)/2 ordered pairs), one gr_decompose launch per reader."""
+    import ctypes
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from stream_gated_residual_gb300 import gr
+    from stream_gated_residual_gb300 import workloads as wl
+    if w.dtype not in ("bf16", "f32"):
+        raise SystemExit("the decomposition takes bf16 or fp32 states")
+    L = args.blocks
+    if L < 2:
+        raise SystemExit("--blocks must be >= 2")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    gr.load()
+    wr = shard(w, rank)
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    N, D, r = w.n_tokens, w.d_model, w.rank
+
+    def dev_tensor(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    # the stack: states before every read, write strengths and outputs of every block
+    states = torch.empty((L, N, 4, D), dtype=tdt, device=dev)
+    Y = torch.empty((L, N, D), dtype=tdt, device=dev)
+    S = torch.empty((L, N, 4), dtype=torch.float32, device=dev)
+    params = []
+    R = dev_tensor(wl.make_state(wr))
+    R0 = R.clone()
+    x = torch.empty((N, D), dtype=tdt, device=dev)
+    for v in range(L):
+        p = {k: torch.from_numpy(a).to(dev) for k, a in wl.make_params(wr, v + 1).items()}
+        params.append(p)
+        P = gr.pack_params(p["gamma"], p["w_down"], p["w_up"], p["w_write"], tdt, w.eps)
+        if v == 0:
+            _, s = gr.read(R, P)
+        else:   # the write of block v-1, in place, then block v's read
+            _, s = gr.write_then_read(R, Y[v - 1], S[v - 1], P)
+        states[v].copy_(R)   # the state block v read
+        S[v].copy_(s)
+        Y[v].copy_(dev_tensor(wl.make_y(wr, v)))
+    torch.cuda.synchronize(dev)
+    outs = []
+    for v in range(1, L):
+        outs.append((torch.empty((N, v), dtype=torch.float32, device=dev),
+                     torch.empty((N, v, 4), dtype=torch.float32, device=dev),
+                     torch.empty((N, v), dtype=torch.float32, device=dev),
+                     torch.empty((N,), dtype=torch.float32, device=dev)))
+    lib = gr.load()
+    stream = torch.cuda.current_stream(dev)
+    shape = gr.make_shape(N, D, r, tdt, w.eps)
+    P_ = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    def step():
+        for v in range(1, L):
+            p = params[v]
+            o = outs[v - 1]
+            st = lib.gr_decompose(ctypes.byref(shape), P_(states[v]), P_(p["gamma"]),
+                                  P_(p["w_down"]), P_(p["w_up"]), P_(p["w_write"]), v, P_(Y),
+                                  P_(S), P_(R0), P_(o[0]), P_(o[1]), P_(o[2]), P_(o[3]),
+                                  ctypes.c_void_p(stream.cuda_stream))
+            if st != 0:
+                raise RuntimeError(f"gr_decompose: {gr.status_string(st)}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    props = torch.cuda.get_device_properties(dev)
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(str(getattr(props, "uuid", "") or ""))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if gr.device_status(clear=True) != 0:
+        raise RuntimeError("device status set during the decomposition")
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms_step = ms / args.steps
+    alg = decompose_bytes(w, L)
+    peaks = load_peaks()
+    peak = peaks["hbm_gbs"]
+    achieved = alg / (ms_step / 1e3) / 1e9
+    if rank == 0:
+        line = {
+            "metric": f"GR contribution decomposition tokens/s ({L * (L - 1) // 2} block pairs "
+                      f"of a {L}-block stack)",
+            "value": job_tokens_per_s(world, N, args.steps, ms / 1e3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded numpy PCG64; states from the library's "
+                                    "own forward chain; no dataset)",
+            "config": {"workload": f"{w.name} shape: N={N} tokens, D={D}, r={r}, "
+                                   f"{w.dtype} states; {L} blocks, readers 1..{L - 1} each "
+                                   f"against all earlier writers and the initial state",
+                       "n_tokens_per_gpu": N, "d_model": D, "rank": r, "state_dtype": w.dtype,
+                       "blocks": L, "l2": "inputs larger than L2 (writers' outputs "
+                                         f"{L * N * D * (2 if w.dtype == 'bf16' else 4) >> 20} "
+                                         "MiB), no flush",
+                       "pass": "decomposition (gr_decompose per reader)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": peaks["source"], "algorithmic_bytes_per_step": alg},
+            "gpu_launches": (L - 1) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def e2e_host_entry(args, w, world, dev, stream, tdt, R_h, y_h, sp_h, P) -> dict:
     """End to end through the host-buffer C entry: H2D of R, y, s_prev; D2H of R', x, s_next."""
     import numpy as np
@@ -662,6 +813,8 @@ def e2e_fp8(args, w, world, dev, stream, codes, scales, y, s_prev, x, s_next, fu
 def main(argv=None):
     args = parse_args(argv)
     from stream_gated_residual_gb300 import workloads as wl
+    if args.workload is None:
+        args.workload = "deep_stack" if args.decompose else "prefill"
     if args.workload not in wl.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; one of {sorted(wl.WORKLOADS)}")
     w = wl.WORKLOADS[args.workload]
@@ -673,6 +826,8 @@ def main(argv=None):
         run_reference(args, w)
     elif args.backward:
         run_backward(args, w)
+    elif args.decompose:
+        run_decompose(args, w)
     else:
         run_gr(args, w)
 

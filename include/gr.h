@@ -236,6 +236,31 @@ int gr_read_backward(const gr_shape* shape, const void* R, const float* gamma,
 int gr_write_backward(const gr_shape* shape, const float* dR_next, const void* y, const float* s,
                       float* dR, float* dy, float* ds, void* stream);
 
+/* ---- contribution decomposition (analysis) ----------------------------------------------------
+ * "【论文解读】 Qwen3.8 Flash Next", §二.6 (eq auv and the fractions π): GR never mixes branches,
+ * so the input of block v splits exactly into the initial state's share and one term per earlier
+ * writer u, a_{u→v} = ¼ Σ_i G_i^(v) ⊙ γ_i ⊙ s_i^(u) y^(u) / rms(R_i^(v)). For one reader v:
+ *   R        [N][4][D]  the state block v reads (R^(v)), in shape->state_dtype (GR_BF16/GR_F32)
+ *   gamma, w_down, w_up, w_write   block v's parameters, fp32, unpacked (as gr_read_backward);
+ *                      w_write is accepted for symmetry and not read (s plays no part here)
+ *   n_writers U >= 0, y [U][N][D] the writers' outputs (state dtype), s [U][N][4] fp32 their
+ *                      write strengths
+ *   R0       [N][4][D]  the initial state (state dtype), or NULL
+ * Outputs (fp32, overwritten; the gates are recomputed in fp32 from R):
+ *   norm        [N][U]     ‖a_{u→v}‖₂ over the token's D channels (required when U > 0)
+ *   branch_norm [N][U][4]  ‖a_{u→v,i}‖₂, branch i's share (or NULL)
+ *   pi          [N][U]     π_uv = ‖a_{u→v}‖ / Σ_u' ‖a_{u'→v}‖, per token; 0 where that sum is 0
+ *                          (or NULL)
+ *   a0_norm     [N]        ‖a_{0→v}‖₂, a_{0→v} = ¼ Σ_i G_i ⊙ γ_i ⊙ R0_i / rms(R_i) (required
+ *                          with R0, ignored without)
+ * All DEVICE pointers, 16-byte aligned; outputs must not overlap the inputs or each other.
+ * 0 <= U <= GR_MAX_WRITERS. Asynchronous on `stream`. Errors: as the other calls. */
+#define GR_MAX_WRITERS 65536
+int gr_decompose(const gr_shape* shape, const void* R, const float* gamma, const float* w_down,
+                 const float* w_up, const float* w_write, int32_t n_writers, const void* y,
+                 const float* s, const void* R0, float* norm, float* branch_norm, float* pi,
+                 float* a0_norm, void* stream);
+
 /* ---- FP8 branch state ------------------------------------------------------------------------
  * "【论文解读】 Qwen3.8 Flash Next", §二.7 stores the widened state in FP8 and fixes no format.
  * This library's FP8 state is two DEVICE arrays:

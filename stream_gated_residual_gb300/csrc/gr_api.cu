@@ -403,6 +403,46 @@ int gr_write_backward(const gr_shape* shape, const float* dR_next, const void* y
                                            static_cast<cudaStream_t>(stream)));
 }
 
+// ---- contribution decomposition -----------------------------------------------------------
+
+int gr_decompose(const gr_shape* shape, const void* R, const float* gamma, const float* w_down,
+                 const float* w_up, const float* w_write, int32_t n_writers, const void* y,
+                 const float* s, const void* R0, float* norm, float* branch_norm, float* pi,
+                 float* a0_norm, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if (n_writers < 0 || n_writers > GR_MAX_WRITERS) return GR_E_SHAPE;
+    if (!R || !gamma || !w_down || !w_up || !w_write) return GR_E_NULL;
+    const size_t U = size_t(n_writers);
+    if (U > 0 && (!y || !s || !norm)) return GR_E_NULL;
+    if (R0 && !a0_norm) return GR_E_NULL;
+    if (shape->n_tokens == 0 || (U == 0 && !R0)) return GR_OK;
+    const void* in[8] = {R, gamma, w_down, w_up, w_write, U ? y : nullptr, U ? s : nullptr, R0};
+    float* out[4] = {U ? norm : nullptr, U ? branch_norm : nullptr, U ? pi : nullptr,
+                     R0 ? a0_norm : nullptr};
+    for (const void* p : in)
+        if (p && !aligned16(p)) return GR_E_ALIGN;
+    for (const float* p : out)
+        if (p && !aligned16(p)) return GR_E_ALIGN;
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model), r = size_t(shape->rank);
+    const size_t K = kBranches * D, es = elem_size(shape->state_dtype);
+    const size_t in_n[8] = {N * K * es, K * 4, r * K * 4, r * K * 4, kBranches * K * 4,
+                            U * N * D * es, U * N * kBranches * 4, N * K * es};
+    const size_t out_n[4] = {N * U * 4, N * U * kBranches * 4, N * U * 4, N * 4};
+    for (int a = 0; a < 4; ++a) {
+        if (!out[a]) continue;
+        for (int b = 0; b < 8; ++b)
+            if (in[b] && overlaps(out[a], out_n[a], in[b], in_n[b])) return GR_E_ALIAS;
+        for (int b = a + 1; b < 4; ++b)
+            if (out[b] && overlaps(out[a], out_n[a], out[b], out_n[b])) return GR_E_ALIAS;
+    }
+    if ((st = check_device())) return st;
+    return status_of(launch_decompose(shape->n_tokens, shape->d_model, shape->rank, shape->eps,
+                                      shape->state_dtype, R, gamma, w_down, w_up, int(U),
+                                      U ? y : nullptr, U ? s : nullptr, R0, out[0], out[1],
+                                      out[2], out[3], static_cast<cudaStream_t>(stream)));
+}
+
 // ---- FP8 branch state ------------------------------------------------------------------------
 
 int gr_fp8_encode(const gr_shape* shape, const void* R, int32_t in_dtype, uint8_t* codes,

@@ -47,6 +47,14 @@ size_t fused_frag_bytes(int D, int r);
 bool tiled_supported(int D, int r);
 int64_t tiled_max_tokens();
 size_t tiled_frag_bytes(int D, int r);
+// Contribution decomposition at one reader (gr_decompose.cu): per token the writers' norms
+// [N][U], optional per-branch norms [N][U][4] and fractions [N][U], and with R0 the initial
+// state's share [N]. Parameters fp32 as in the backward; Y [U][N][D] in the state's dtype.
+cudaError_t launch_decompose(int64_t N, int D, int r, float eps, int dtype, const void* R,
+                             const float* gamma, const float* Wd, const float* Wu, int U,
+                             const void* Y, const float* S, const void* R0, float* norm,
+                             float* bnorm, float* pi, float* a0_norm, cudaStream_t st);
+
 // Concurrent split of a bf16 cluster-kernel shape (gr_split.cu): the tokens of the step that go
 // to the two-pass kernel (a multiple of 32; 0 = no split) and the SMs it gets (*free_sms).
 int64_t split_tokens(int64_t N, int D, int r, bool write, int* free_sms);

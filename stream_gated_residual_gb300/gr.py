@@ -80,6 +80,8 @@ def load() -> ctypes.CDLL:
         "gr_read_backward_workspace_size": ([S, sz], ctypes.c_int),
         "gr_read_backward": ([S] + [V] * 13 + [ctypes.c_size_t, V], ctypes.c_int),
         "gr_write_backward": ([S, V, V, V, V, V, V, V], ctypes.c_int),
+        "gr_decompose": ([S, V, V, V, V, V, ctypes.c_int32, V, V, V, V, V, V, V, V],
+                         ctypes.c_int),
         "gr_fp8_encode": ([S, V, ctypes.c_int32, V, V, V], ctypes.c_int),
         "gr_fp8_decode": ([S, V, V, V, ctypes.c_int32, V], ctypes.c_int),
         "gr_read_fp8": ([S, V, V, P, V, V, V], ctypes.c_int),
@@ -355,6 +357,55 @@ def write_backward(dR_next: torch.Tensor, y: torch.Tensor, s: torch.Tensor, stre
                                     _ptr(dR), _ptr(dy), _ptr(ds), _stream(stream)),
            "gr_write_backward")
     return dR, dy, ds
+
+
+# ---- contribution decomposition ---------------------------------------------------------------
+
+def decompose(R: torch.Tensor, gamma: torch.Tensor, w_down: torch.Tensor, w_up: torch.Tensor,
+              w_write: torch.Tensor, y: torch.Tensor | None, s: torch.Tensor | None,
+              R0: torch.Tensor | None = None, eps: float = 1e-6, branch_norm: bool = True,
+              pi: bool = True, stream=None) -> dict:
+    """gr_decompose at one reader: R [N,4,D] the state it reads, its fp32 parameters, the
+    writers' outputs y [U,N,D] (state dtype) and write strengths s [U,N,4] (fp32), optionally
+    the initial state R0 [N,4,D]. Returns fp32 tensors: norm [N,U], branch_norm [N,U,4] and pi
+    [N,U] (when asked), a0_norm [N] (with R0)."""
+    _dev(R, "R")
+    N, _, D = R.shape
+    r = w_down.shape[0]
+    shape = make_shape(N, D, r, R.dtype, eps)
+    for t, n in ((gamma, "gamma"), (w_down, "w_down"), (w_up, "w_up"), (w_write, "w_write")):
+        _dev(t, n)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{n} must be float32")
+    U = 0 if y is None else y.shape[0]
+    if U:
+        _dev(y, "y")
+        _dev(s, "s")
+        if y.dtype != R.dtype or tuple(y.shape) != (U, N, D) or tuple(s.shape) != (U, N, 4) \
+                or s.dtype != torch.float32:
+            raise ValueError("y must be [U, N, D] in the state dtype and s [U, N, 4] float32")
+    if R0 is not None:
+        _dev(R0, "R0")
+        if R0.dtype != R.dtype or R0.shape != R.shape:
+            raise ValueError("R0 must match R")
+    dev = R.device
+    out = {"norm": torch.empty((N, U), dtype=torch.float32, device=dev)}
+    if branch_norm:
+        out["branch_norm"] = torch.empty((N, U, 4), dtype=torch.float32, device=dev)
+    if pi:
+        out["pi"] = torch.empty((N, U), dtype=torch.float32, device=dev)
+    if R0 is not None:
+        out["a0_norm"] = torch.empty((N,), dtype=torch.float32, device=dev)
+
+    def p(k):
+        t = out.get(k)
+        return _ptr(t) if t is not None and t.numel() else None
+
+    _check(load().gr_decompose(
+        ctypes.byref(shape), _ptr(R), _ptr(gamma), _ptr(w_down), _ptr(w_up), _ptr(w_write), U,
+        _ptr(y) if U else None, _ptr(s) if U else None, _ptr(R0) if R0 is not None else None,
+        p("norm"), p("branch_norm"), p("pi"), p("a0_norm"), _stream(stream)), "gr_decompose")
+    return out
 
 
 # ---- FP8 branch state (e4m3 codes, one power-of-two exponent per 32-channel block) ------------

@@ -225,3 +225,26 @@ def test_backward_calls_validate_before_any_launch(lib):
                                  null) == E("GR_E_DEVICE")
     assert lib.gr_write_backward(ctypes.byref(sh), FAKE, FAKE2, FAKE3, FAKE4, FAKE, FAKE5,
                                  null) == E("GR_E_ALIAS")
+
+
+def test_decompose_validates_before_any_launch(lib):
+    E = header_constant
+    null = ctypes.c_void_p(None)
+    sh = _shape(n=64, d=256, r=16, dt=gr.GR_BF16)
+    # R, gamma, W_d, W_u, W_w, then (after U) y, s, R0, norm, branch_norm, pi, a0_norm
+    p = [ctypes.c_void_p(0x1000000 * (k + 1)) for k in range(12)]
+    call = lambda q, U=5, shape=sh: lib.gr_decompose(ctypes.byref(shape), *q[:5], U, *q[5:],
+                                                     null)
+    assert call(p) == E("GR_E_DEVICE")
+    assert call(p, U=-1) == E("GR_E_SHAPE")
+    assert call(p, U=E("GR_MAX_WRITERS") + 1) == E("GR_E_SHAPE")
+    assert call(p[:5] + [null] + p[6:]) == E("GR_E_NULL")                 # y
+    assert call(p[:8] + [null] + p[9:]) == E("GR_E_NULL")                 # norm
+    assert call(p[:11] + [null]) == E("GR_E_NULL")                        # R0 without a0_norm
+    assert call(p[:5] + [ctypes.c_void_p(0x6000008)] + p[6:]) == E("GR_E_ALIGN")
+    assert call(p[:8] + [p[5]] + p[9:]) == E("GR_E_ALIAS")                # norm on y
+    assert call(p[:9] + [p[8]] + p[10:]) == E("GR_E_ALIAS")               # branch_norm on norm
+    # optional outputs may be absent; no writers and no initial state: nothing to do
+    assert call(p[:9] + [null, null] + p[11:]) == E("GR_E_DEVICE")
+    assert call(p[:5] + [null] * 7, U=0) == 0
+    assert call(p, shape=_shape(n=64, d=256, r=16, dt=gr.GR_FP8)) == E("GR_E_DTYPE")
