@@ -9,7 +9,7 @@
 //   ‖a_{u→v}‖, ‖a_{u→v,i}‖ over the D channels,       π_uv = ‖a_{u→v}‖ / Σ_u' ‖a_{u'→v}‖
 //   a_{0→v}[c]     = ¼ Σ_i coef_i[c] R0_i[c]          (the initial state's share)
 //
-// One kernel, persistent, TB tokens per CTA at a time:
+// One kernel, persistent, TB tokens per CTA at a time (TB = 2 below rank 64, two CTAs per SM):
 //   1. the read's gates, recomputed as the backward does (squared sums, z = ¼ W_d vec R̂,
 //      h = SiLU(z), G = σ(W_u h)), into coef [TB][4D] fp32 in shared memory (the state rows are
 //      read twice, the second time from L2, so that a row of D = 12288 still fits);
@@ -31,8 +31,10 @@ constexpr int kSums = 5;             // Σ A², then Σ (coef_i y)² for the fou
 
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
 
+// 256 threads; two CTAs per SM below rank 64 (each thread then has 128 registers), so that one
+// CTA's gate recompute overlaps the other's writer pass.
 template <int RM>
-__host__ __device__ constexpr int dec_threads() { return RM > 32 ? 256 : 512; }
+__host__ __device__ constexpr int dec_threads() { return 256; }
 
 // Block sums of M per-thread values (NW warps); totals land in out[0..M).
 template <int M, int NW>
@@ -102,7 +104,7 @@ template <> struct Raw8<float> {
 };
 
 template <typename T, int RM, int TB>
-__global__ void __launch_bounds__(dec_threads<RM>())
+__global__ void __launch_bounds__(dec_threads<RM>(), RM > 32 ? 1 : 2)
 decompose_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
                  const float* __restrict__ gamma, const float* __restrict__ Wd,
                  const float* __restrict__ Wu, int U, const T* __restrict__ Y,
@@ -155,23 +157,22 @@ decompose_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
             float az[TB * RM];
 #pragma unroll
             for (int k = 0; k < TB * RM; ++k) az[k] = 0.f;
+#pragma unroll 2
+            for (int e = tid; e < K; e += NT) {
+                const int i = e / D;
+                const float ge = gamma[e];
+                float wd[RM];
 #pragma unroll
-            for (int i = 0; i < kBranches; ++i)
-                for (int c = tid; c < D; c += NT) {
-                    const int e = i * D + c;
-                    const float ge = gamma[e];
-                    float wd[RM];
+                for (int k = 0; k < RM; ++k) wd[k] = k < r ? Wd[size_t(k) * K + e] : 0.f;
 #pragma unroll
-                    for (int k = 0; k < RM; ++k) wd[k] = k < r ? Wd[size_t(k) * K + e] : 0.f;
+                for (int t2 = 0; t2 < TB; ++t2) {
+                    const float rv = t2 < nt ? to_f32(R[(t0 + t2) * K + e]) : 0.f;
+                    const float rh = ge * rv * inv[t2 * kBranches + i];
 #pragma unroll
-                    for (int t2 = 0; t2 < TB; ++t2) {
-                        const float rv = t2 < nt ? to_f32(R[(t0 + t2) * K + e]) : 0.f;
-                        const float rh = ge * rv * inv[t2 * kBranches + i];
-#pragma unroll
-                        for (int k = 0; k < RM; ++k)
-                            az[t2 * RM + k] = fmaf(wd[k], rh, az[t2 * RM + k]);
-                    }
+                    for (int k = 0; k < RM; ++k)
+                        az[t2 * RM + k] = fmaf(wd[k], rh, az[t2 * RM + k]);
                 }
+            }
             block_sum<TB * RM, NW>(az, red, tot);
             for (int q = tid; q < TB * RM; q += NT) {
                 const float z = (q % RM) < r ? 0.25f * tot[q] : 0.f;
@@ -179,13 +180,25 @@ decompose_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
             }
             __syncthreads();
         }
-        // 1c. coef = σ(W_u h) γ / rms
+        // 1c. coef = σ(W_u h) γ / rms (a row of W_u is r consecutive floats: 16-byte loads
+        //     when r is a multiple of 4)
+        const bool wu_vec = (r & 3) == 0;
+#pragma unroll 2
         for (int e = tid; e < K; e += NT) {
             const int i = e / D;
             const float ge = gamma[e];
             float wu[RM];
+            if (wu_vec) {
+                const float4* row = reinterpret_cast<const float4*>(Wu + size_t(e) * r);
 #pragma unroll
-            for (int k = 0; k < RM; ++k) wu[k] = k < r ? Wu[size_t(e) * r + k] : 0.f;
+                for (int k = 0; k < RM; k += 4) {
+                    const float4 q = k < r ? row[k / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    wu[k] = q.x; wu[k + 1] = q.y; wu[k + 2] = q.z; wu[k + 3] = q.w;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < RM; ++k) wu[k] = k < r ? Wu[size_t(e) * r + k] : 0.f;
+            }
 #pragma unroll
             for (int t2 = 0; t2 < TB; ++t2) {
                 float g = 0.f;
@@ -335,20 +348,17 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, const void* R, const fl
     return cudaGetLastError();
 }
 
-// Tokens per CTA: the most of 4, 2, 1 that the accumulators (TB·RM) and shared memory (the
-// fp32 coefficients, up to about 200 KB) allow.
+// Tokens per CTA: 2 below rank 64 when two tokens' fp32 coefficients fit in about 100 KB of
+// shared memory (two CTAs per SM), else 1.
 template <typename T, int RM>
 cudaError_t launch_rm(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
                       const float* Wd, const float* Wu, int U, const void* Y, const float* S,
                       const void* R0, float* norm, float* bnorm, float* pi, float* a0_norm,
                       cudaStream_t st) {
     const size_t row = size_t(kBranches) * D * 4;
-    const int tb_reg = RM <= 16 ? 4 : RM <= 32 ? 2 : 1;
-    const int tb_smem = row * 4 <= 200 * 1024 ? 4 : row * 2 <= 200 * 1024 ? 2 : 1;
+    const int tb_reg = RM <= 32 ? 2 : 1;
+    const int tb_smem = row * 2 <= 100 * 1024 ? 2 : 1;
     const int tb = tb_reg < tb_smem ? tb_reg : tb_smem;
-    if (tb >= 4 && RM <= 16)
-        return launch_t<T, RM, (RM <= 16 ? 4 : 1)>(N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0,
-                                                   norm, bnorm, pi, a0_norm, st);
     if (tb >= 2 && RM <= 32)
         return launch_t<T, RM, (RM <= 32 ? 2 : 1)>(N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0,
                                                    norm, bnorm, pi, a0_norm, st);
