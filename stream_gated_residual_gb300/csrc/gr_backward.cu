@@ -9,12 +9,13 @@
 //   dW_u = Σ_t dg ⊗ h,  dW_d = Σ_t dz ⊗ vec R̂ / n_r,  dW_w = Σ_t du ⊗ vec R̂ / n_r,
 //   dγ = Σ_t dR̂ ⊙ R inv.
 //
-// Two kernels. The per-token kernel (one CTA per token, the token's state row in shared memory
-// as fp32) recomputes the read's intermediates, writes dR, and leaves the per-token factors of
+// Two kernels. The per-token kernel (persistent, TB tokens per CTA at a time with their state
+// rows in shared memory in the state's type, so that each weight element loaded serves TB
+// tokens) recomputes the read's intermediates, writes dR, and leaves the per-token factors of
 // the parameter gradients in the caller's workspace: dg, vec R̂ and dR̂ ⊙ R inv ([N][4D] each)
 // and [h | dz/n_r | du/n_r | 1] ([N][2r+5]). The reduction kernel then forms each parameter
-// gradient as a sum over tokens of (small factor) × (long factor), a CTA per 256 columns and a
-// slice of the tokens, fp32 atomics into the zeroed outputs.
+// gradient as a sum over tokens of (small factor) × (long factor), a CTA per 256 columns and
+// 128 tokens, fp32 atomics into the zeroed outputs. W_u is transposed into the workspace first.
 #include <math.h>
 
 #include "gr_internal.h"
