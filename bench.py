@@ -93,8 +93,18 @@ def load_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained") or 0) or None,
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def tc_flops_per_token(w) -> int:
+    """Tensor-core arithmetic of one token on the large-rank path (FMA = 2 FLOP): the down
+    projection [W_d; W_w] (r + 4 outputs over 4·D inputs) and the up projection W_u (4·D outputs
+    over r inputs)."""
+    K = 4 * w.d_model
+    return 2 * (w.rank + 4) * K + 2 * K * w.rank
 
 
 def kernel_source_sha(kernel_path: str) -> str:
@@ -103,8 +113,11 @@ def kernel_source_sha(kernel_path: str) -> str:
     (gr_split.cu), which decides how many tokens each kernel gets."""
     from stream_gated_residual_gb300 import build as gbuild
     files = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
-             "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu"}
+             "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu",
+             "tc_bf16": "gr_rank_tc.cu"}
     names = [files[k] for k in kernel_path.split("+")]
+    if kernel_path == "tc_bf16":
+        names.append("gr_tc.cuh")
     if len(names) > 1:
         names.append("gr_split.cu")
     h = hashlib.sha256()
@@ -346,13 +359,19 @@ def run_gr(args, w) -> None:
     P = gr.pack_params(pt["gamma"], pt["w_down"], pt["w_up"], pt["w_write"], sdt, w.eps)
     path = gr.kernel_path(w.n_tokens, w.d_model, w.rank, sdt)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = len(path.split("+"))   # "fused_bf16+tiled_bf16": two kernels a step
+    # "fused_bf16+tiled_bf16": two kernels a step; the large-rank path: three
+    launches_per_step = 3 if path == "tc_bf16" else len(path.split("+"))
+    ws_need = 0 if fp8 else gr.step_workspace_size(w.n_tokens, w.d_model, w.rank, sdt)
+    ws = None
+    if ws_need:
+        wsb = torch.empty(ws_need + 256, dtype=torch.uint8, device=dev)
+        ws = wsb[(-wsb.data_ptr()) % 256:][:ws_need]
 
     def fused(sp, sn, st):
         if fp8:
             gr.write_then_read_fp8(codes, scales, y, sp, P, x=x, s_next=sn, stream=st)
         else:
-            gr.write_then_read(R, y, sp, P, x=x, s_next=sn, stream=st)
+            gr.write_then_read(R, y, sp, P, x=x, s_next=sn, stream=st, workspace=ws)
 
     def step(i):
         sp, sn = (s_a, s_b) if i % 2 == 0 else (s_b, s_a)
@@ -445,6 +464,20 @@ def run_gr(args, w) -> None:
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "kernel": path, "algorithmic_bytes_per_launch": alg_bytes,
                 "traffic": None if args.n_tokens is not None else profiled_traffic(path, w.name)}
+    if path == "tc_bf16":
+        # the pages' rank makes the read a dense contraction: against the bf16 tensor peak
+        # (sustained: the step is timed over a long loop), the HBM figures beside it
+        flops = w.n_tokens * tc_flops_per_token(w)
+        tflops = flops / (ms_step / 1e3) / 1e12
+        tpeak = peaks.get("bf16_tflops_sustained") or 1700.0
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": tflops / tpeak, "peak_source": peaks["source"] + " (bf16 sustained)",
+                    "kernel": path, "algorithmic_flops_per_step": flops,
+                    "hbm": {"achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": achieved / peaks["hbm_gbs"],
+                            "algorithmic_bytes_per_step": alg_bytes},
+                    "traffic": None if args.n_tokens is not None
+                    else profiled_traffic(path, w.name)}
 
     # bandwidth reference: single-stream x += y on [N, D]
     xr = torch.zeros((w.n_tokens, w.d_model), dtype=tdt, device=dev)
@@ -463,7 +496,14 @@ def run_gr(args, w) -> None:
     del xr, yr
 
     if fp8:
-        e2e = e2e_fp8(args, w, world, dev, stream, codes, scales, y, s_a, x, s_b, fused)
+        e2e = e2e_device_copies(args, w, world, dev, stream, (codes, scales, y, s_a),
+                                (codes, scales, x, s_b), s_a, s_b, fused,
+                                "gr_write_then_read_fp8 with pinned-host torch copies on the "
+                                "same stream")
+    elif path == "tc_bf16":
+        e2e = e2e_device_copies(args, w, world, dev, stream, (R, y, s_a), (R, x, s_b), s_a, s_b,
+                                fused, "gr_write_then_read_ws with pinned-host torch copies on "
+                                       "the same stream")
     else:
         e2e = e2e_host_entry(args, w, world, dev, stream, tdt, R_h, y_h, sp_h, P)
         del R
@@ -778,20 +818,22 @@ def e2e_host_entry(args, w, world, dev, stream, tdt, R_h, y_h, sp_h, P) -> dict:
             "api": "gr_write_then_read_host (pinned host buffers)"}
 
 
-def e2e_fp8(args, w, world, dev, stream, codes, scales, y, s_prev, x, s_next, fused) -> dict:
-    """End to end on the FP8 state: per step, pinned host copies of the codes, exponents, y and
-    s_prev go to the device, gr_write_then_read_fp8 runs, and the written codes and exponents,
-    x and s_next come back (torch copies on the same stream, not pipelined)."""
+def e2e_device_copies(args, w, world, dev, stream, ins, outs, s_prev, s_next, fused,
+                      api) -> dict:
+    """End to end through the device entry with host buffers: per step, pinned host copies of
+    the inputs `ins` go to the device, the step runs, and `outs` come back (torch copies on the
+    same stream, not pipelined). For the paths the host-buffer C entry does not take: the FP8
+    state and the large-rank path."""
     import torch
     import torch.distributed as dist
-    host = [t.cpu().pin_memory() for t in (codes, scales, y, s_prev)]
-    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (codes, scales, x, s_next)]
+    host = [t.cpu().pin_memory() for t in ins]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
 
     def one():
-        for h, d in zip(host, (codes, scales, y, s_prev)):
+        for h, d in zip(host, ins):
             d.copy_(h, non_blocking=True)
         fused(s_prev, s_next, stream)
-        for h, d in zip(outs, (codes, scales, x, s_next)):
+        for h, d in zip(hout, outs):
             h.copy_(d, non_blocking=True)
         stream.synchronize()
 
@@ -803,11 +845,10 @@ def e2e_fp8(args, w, world, dev, stream, codes, scales, y, s_prev, x, s_next, fu
     for _ in range(args.e2e_steps):
         one()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (codes, scales, y, s_prev))
-    d2h = sum(t.numel() * t.element_size() for t in (codes, scales, x, s_next))
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
     return {"value": job_tokens_per_s(world, w.n_tokens, args.e2e_steps, e2e_s), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "api": "gr_write_then_read_fp8 with pinned-host torch copies on the same stream"}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": api}
 
 
 def main(argv=None):

@@ -44,7 +44,9 @@ extern "C" {
 
 #define GR_API_VERSION 1
 #define GR_MAX_D 12288   /* largest d_model (one token's fp32 state row must fit on chip) */
-#define GR_MAX_RANK 64
+#define GR_MAX_RANK 64      /* largest rank of every path but the large-rank one            */
+#define GR_MAX_RANK_TC 448  /* largest rank of the large-rank tensor-core path (bf16 states,
+                               d_model a multiple of 64, rank a multiple of 8, rank >= 64)    */
 
 /* Status codes. */
 enum {
@@ -54,7 +56,7 @@ enum {
                            /* or n_branch != 4                                                 */
     GR_E_DTYPE = -3,       /* unknown state dtype                                               */
     GR_E_ALIGN = -4,       /* a device pointer is not 16-byte aligned                           */
-    GR_E_RANK = -5,        /* rank outside [1, 64]                                              */
+    GR_E_RANK = -5,        /* rank outside [1, 64], and outside the large-rank path's shapes    */
     GR_E_PARAMS = -6,      /* params not packed by gr_pack_params, or packed for another shape  */
     GR_E_SIZE = -7,        /* a caller-provided buffer is smaller than the call needs           */
     GR_E_ALIAS = -8,       /* an output overlaps an input in a way the call forbids             */
@@ -123,6 +125,31 @@ int gr_pack_params(const gr_shape* shape, const float* gamma, const float* w_dow
  * R [N][4][D] -> x [N][D] and s [N][4]. R is only read. x and s must not overlap R. */
 int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
             void* stream);
+
+/* ---- the pages' own rank, r = d/8 (large-rank path) ------------------------------------------
+ * "【论文解读】 Qwen3.8 Flash Next", §二.4 sets W_d ∈ R^{r × n_r·d} with r = d/8 (320 at d = 2560).
+ * bf16 states with d_model a multiple of 64 and a rank r with 64 <= r <= GR_MAX_RANK_TC,
+ * r % 8 == 0, run on the tcgen05 tensor cores ("tc_bf16" in gr_kernel_path): three launches
+ * (the write and each row's 1/rms; the down projection as a GEMM of the rms-scaled state with the
+ * packed [W_d; W_w]; the up projection as a GEMM with the gate and combine in its epilogue). Its
+ * numerics: the down projection's inputs are bf16(R'·inv_i) and the packed bf16 weights, h is
+ * rounded to bf16 for the up projection, W_u is bf16; fp32 accumulation throughout. It needs a
+ * device workspace between its launches, so these shapes take the _ws entries below; gr_read
+ * and gr_write_then_read return GR_E_SIZE for them and the host-buffer entries GR_E_RANK. */
+
+/* Bytes of device workspace a read or fused step of this shape needs: N·16 (each row's 1/rms)
+ * plus N·round_up(r, 64)·2 (h in bf16), each rounded up to 256, on the large-rank path; 0 for
+ * every other shape. */
+int gr_step_workspace_size(const gr_shape* shape, size_t* bytes);
+
+/* gr_read and gr_write_then_read with a caller-owned DEVICE workspace (256-byte aligned, at
+ * least gr_step_workspace_size bytes, not overlapping the call's other buffers; may be NULL
+ * with 0 bytes when the size is 0). Same contracts otherwise; every shape the library takes. */
+int gr_read_ws(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
+               void* workspace, size_t workspace_bytes, void* stream);
+int gr_write_then_read_ws(const gr_shape* shape, void* R, const void* y, const float* s_prev,
+                          const gr_params* next, void* x, float* s_next, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* The write (eq write) of a chain's last sublayer: R[t][i][:] += s[t][i] · y[t][:], in place. */
 int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void* stream);

@@ -87,7 +87,11 @@ int validate_shape(const gr_shape* s, bool fp8_ok = false) {
     } else if (s->state_dtype != GR_F32 && s->state_dtype != GR_BF16) {
         return GR_E_DTYPE;
     }
-    if (s->rank < 1 || s->rank > GR_MAX_RANK) return GR_E_RANK;
+    // ranks above GR_MAX_RANK only on the large-rank tensor-core path (bf16 states)
+    if (s->rank < 1 || s->rank > GR_MAX_RANK_TC) return GR_E_RANK;
+    if (s->rank > GR_MAX_RANK &&
+        !(s->state_dtype == GR_BF16 && rank_tc_supported(s->d_model, s->rank)))
+        return GR_E_RANK;
     if (!(s->eps >= 0.0f) || !isfinite(s->eps)) return GR_E_EPS;
     return GR_OK;
 }
@@ -126,15 +130,26 @@ bool use_fused(const gr_shape* s) {
            s->n_tokens <= fused_max_tokens();
 }
 
+// The large-rank tensor-core path (gr_rank_tc.cu) takes precedence over the generic kernel.
+bool use_rank_tc(const gr_shape* s) {
+    return s->state_dtype == GR_BF16 && rank_tc_supported(s->d_model, s->rank);
+}
+
 bool use_tiled(const gr_shape* s) {
     return s->state_dtype == GR_BF16 && !fused_supported(s->d_model, s->rank) &&
            tiled_supported(s->d_model, s->rank) && s->n_tokens <= tiled_max_tokens();
 }
 
 int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
-             const gr_params* p, void* x, float* s_out, cudaStream_t st) {
+             const gr_params* p, void* x, float* s_out, cudaStream_t st,
+             void* ws = nullptr, size_t ws_bytes = 0) {
     if (s->n_tokens == 0) return GR_OK;
     cudaError_t e;
+    if (use_rank_tc(s)) {
+        if (!ws || ws_bytes < rank_tc_workspace(s->n_tokens, s->rank)) return GR_E_SIZE;
+        return status_of(launch_rank_tc(s->n_tokens, s->d_model, s->rank, s->eps, R, y, s_prev,
+                                         p->packed, x, s_out, ws, st));
+    }
     int free_sms = 0;
     const int64_t n2 =
         use_fused(s) ? split_tokens(s->n_tokens, s->d_model, s->rank, y != nullptr, &free_sms)
@@ -169,6 +184,73 @@ int sm_count() {
 
 }  // namespace gr
 
+namespace gr {
+namespace {
+
+// The workspace of a step (large-rank path only): 256-byte aligned, big enough, and clear of the
+// step's other buffers.
+int check_step_ws(const gr_shape* s, const void* ws, size_t ws_bytes, const void* const* bufs,
+                  const size_t* sizes, int nbufs) {
+    if (!use_rank_tc(s)) return GR_OK;
+    const size_t need = rank_tc_workspace(s->n_tokens, s->rank);
+    if (!ws || ws_bytes < need) return GR_E_SIZE;
+    if (!aligned256(ws)) return GR_E_ALIGN;
+    for (int b = 0; b < nbufs; ++b)
+        if (overlaps(ws, need, bufs[b], sizes[b])) return GR_E_ALIAS;
+    return GR_OK;
+}
+
+int read_impl(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
+              void* ws, size_t ws_bytes, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if ((st = validate_params(shape, params))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!R || !x || !s) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(x) || !aligned16(s)) return GR_E_ALIGN;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es, nx = N * D * es, ns = N * kBranches * 4;
+    if (overlaps(x, nx, R, nR) || overlaps(s, ns, R, nR) || overlaps(x, nx, s, ns))
+        return GR_E_ALIAS;
+    const void* bufs[3] = {R, x, s};
+    const size_t sizes[3] = {nR, nx, ns};
+    if ((st = check_step_ws(shape, ws, ws_bytes, bufs, sizes, 3))) return st;
+    if ((st = check_device())) return st;
+    return run_step(shape, const_cast<void*>(R), nullptr, nullptr, params, x, s,
+                    static_cast<cudaStream_t>(stream), ws, ws_bytes);
+}
+
+int write_then_read_impl(const gr_shape* shape, void* R, const void* y, const float* s_prev,
+                         const gr_params* next, void* x, float* s_next, void* ws,
+                         size_t ws_bytes, void* stream) {
+    int st = validate_shape(shape);
+    if (st) return st;
+    if ((st = validate_params(shape, next))) return st;
+    if (shape->n_tokens == 0) return GR_OK;
+    if (!R || !y || !s_prev || !x || !s_next) return GR_E_NULL;
+    if (!aligned16(R) || !aligned16(y) || !aligned16(s_prev) || !aligned16(x) ||
+        !aligned16(s_next))
+        return GR_E_ALIGN;
+    const size_t es = elem_size(shape->state_dtype);
+    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
+    const size_t nR = N * kBranches * D * es, ny = N * D * es, ns = N * kBranches * 4;
+    if (overlaps(R, nR, y, ny) || overlaps(R, nR, s_prev, ns) || overlaps(x, ny, R, nR) ||
+        overlaps(s_next, ns, R, nR) || overlaps(x, ny, s_next, ns) ||
+        overlaps(x, ny, s_prev, ns) || overlaps(s_next, ns, y, ny) ||
+        (x != y && overlaps(x, ny, y, ny)) || (s_next != s_prev && overlaps(s_next, ns, s_prev, ns)))
+        return GR_E_ALIAS;
+    const void* bufs[5] = {R, y, s_prev, x, s_next};
+    const size_t sizes[5] = {nR, ny, ns, ny, ns};
+    if ((st = check_step_ws(shape, ws, ws_bytes, bufs, sizes, 5))) return st;
+    if ((st = check_device())) return st;
+    return run_step(shape, R, y, s_prev, next, x, s_next, static_cast<cudaStream_t>(stream), ws,
+                    ws_bytes);
+}
+
+}  // namespace
+}  // namespace gr
+
 using namespace gr;
 
 extern "C" {
@@ -198,6 +280,7 @@ const char* gr_kernel_path(const gr_shape* shape) {
     if (shape && shape->state_dtype == GR_FP8)
         return validate_fp8(shape, true) == GR_OK ? "tiled_fp8" : "invalid";
     if (validate_shape(shape) != GR_OK) return "invalid";
+    if (use_rank_tc(shape)) return "tc_bf16";
     if (use_fused(shape))
         return split_tokens(shape->n_tokens, shape->d_model, shape->rank, true, nullptr) > 0
                    ? "fused_bf16+tiled_bf16"
@@ -243,22 +326,22 @@ int gr_pack_params(const gr_shape* shape, const float* gamma, const float* w_dow
     return GR_OK;
 }
 
-int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
-            void* stream) {
+int gr_step_workspace_size(const gr_shape* shape, size_t* bytes) {
     int st = validate_shape(shape);
     if (st) return st;
-    if ((st = validate_params(shape, params))) return st;
-    if (shape->n_tokens == 0) return GR_OK;
-    if (!R || !x || !s) return GR_E_NULL;
-    if (!aligned16(R) || !aligned16(x) || !aligned16(s)) return GR_E_ALIGN;
-    const size_t es = elem_size(shape->state_dtype);
-    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
-    const size_t nR = N * kBranches * D * es, nx = N * D * es, ns = N * kBranches * 4;
-    if (overlaps(x, nx, R, nR) || overlaps(s, ns, R, nR) || overlaps(x, nx, s, ns))
-        return GR_E_ALIAS;
-    if ((st = check_device())) return st;
-    return run_step(shape, const_cast<void*>(R), nullptr, nullptr, params, x, s,
-                    static_cast<cudaStream_t>(stream));
+    if (!bytes) return GR_E_NULL;
+    *bytes = use_rank_tc(shape) ? rank_tc_workspace(shape->n_tokens, shape->rank) : 0;
+    return GR_OK;
+}
+
+int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
+            void* stream) {
+    return read_impl(shape, R, params, x, s, nullptr, 0, stream);
+}
+
+int gr_read_ws(const gr_shape* shape, const void* R, const gr_params* params, void* x, float* s,
+               void* workspace, size_t workspace_bytes, void* stream) {
+    return read_impl(shape, R, params, x, s, workspace, workspace_bytes, stream);
 }
 
 int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void* stream) {
@@ -279,24 +362,14 @@ int gr_write(const gr_shape* shape, void* R, const void* y, const float* s, void
 
 int gr_write_then_read(const gr_shape* shape, void* R, const void* y, const float* s_prev,
                        const gr_params* next, void* x, float* s_next, void* stream) {
-    int st = validate_shape(shape);
-    if (st) return st;
-    if ((st = validate_params(shape, next))) return st;
-    if (shape->n_tokens == 0) return GR_OK;
-    if (!R || !y || !s_prev || !x || !s_next) return GR_E_NULL;
-    if (!aligned16(R) || !aligned16(y) || !aligned16(s_prev) || !aligned16(x) ||
-        !aligned16(s_next))
-        return GR_E_ALIGN;
-    const size_t es = elem_size(shape->state_dtype);
-    const size_t N = size_t(shape->n_tokens), D = size_t(shape->d_model);
-    const size_t nR = N * kBranches * D * es, ny = N * D * es, ns = N * kBranches * 4;
-    if (overlaps(R, nR, y, ny) || overlaps(R, nR, s_prev, ns) || overlaps(x, ny, R, nR) ||
-        overlaps(s_next, ns, R, nR) || overlaps(x, ny, s_next, ns) ||
-        overlaps(x, ny, s_prev, ns) || overlaps(s_next, ns, y, ny) ||
-        (x != y && overlaps(x, ny, y, ny)) || (s_next != s_prev && overlaps(s_next, ns, s_prev, ns)))
-        return GR_E_ALIAS;
-    if ((st = check_device())) return st;
-    return run_step(shape, R, y, s_prev, next, x, s_next, static_cast<cudaStream_t>(stream));
+    return write_then_read_impl(shape, R, y, s_prev, next, x, s_next, nullptr, 0, stream);
+}
+
+int gr_write_then_read_ws(const gr_shape* shape, void* R, const void* y, const float* s_prev,
+                          const gr_params* next, void* x, float* s_next, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    return write_then_read_impl(shape, R, y, s_prev, next, x, s_next, workspace, workspace_bytes,
+                                stream);
 }
 
 int gr_read_fixed_gates(const gr_shape* shape, const void* R, const float* gamma,
@@ -333,6 +406,7 @@ int gr_residual_add_ref(int64_t n, int32_t dtype, const void* y, void* x, void* 
 int gr_read_backward_workspace_size(const gr_shape* shape, size_t* bytes) {
     int st = validate_shape(shape);
     if (st) return st;
+    if (shape->rank > GR_MAX_RANK) return GR_E_RANK;
     if (!bytes) return GR_E_NULL;
     *bytes = read_backward_workspace(shape->n_tokens, shape->d_model, shape->rank);
     return GR_OK;
@@ -345,6 +419,7 @@ int gr_read_backward(const gr_shape* shape, const void* R, const float* gamma,
                      void* stream) {
     int st = validate_shape(shape);
     if (st) return st;
+    if (shape->rank > GR_MAX_RANK) return GR_E_RANK;
     if (shape->n_tokens == 0) return GR_OK;
     const void* in[8] = {R, gamma, w_down, w_up, w_write, dx, ds, workspace};
     const void* out[5] = {dR, dgamma, dw_down, dw_up, dw_write};
@@ -411,6 +486,7 @@ int gr_decompose(const gr_shape* shape, const void* R, const float* gamma, const
                  float* a0_norm, void* stream) {
     int st = validate_shape(shape);
     if (st) return st;
+    if (shape->rank > GR_MAX_RANK) return GR_E_RANK;
     if (n_writers < 0 || n_writers > GR_MAX_WRITERS) return GR_E_SHAPE;
     if (!R || !gamma || !w_down || !w_up || !w_write) return GR_E_NULL;
     const size_t U = size_t(n_writers);
@@ -583,6 +659,7 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
     int st = validate_shape(shape);
     if (st) return st;
     if ((st = validate_params(shape, next))) return st;
+    if (use_rank_tc(shape)) return GR_E_RANK;   // the large-rank path has device entries only
     if (shape->n_tokens == 0) return GR_OK;
     if (!R_host || !y_host || !s_prev_host || !x_host || !s_next_host || !workspace)
         return GR_E_NULL;
@@ -682,6 +759,7 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
     int st = validate_shape(shape);
     if (st) return st;
     if ((st = validate_params(shape, next))) return st;
+    if (use_rank_tc(shape)) return GR_E_RANK;   // the large-rank path has device entries only
     if (shape->n_tokens == 0) return GR_OK;
     if (!R_host || !y_host || !s_prev_host || !x_host || !s_next_host) return GR_E_NULL;
     size_t need = 0;

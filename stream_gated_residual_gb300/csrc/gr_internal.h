@@ -18,6 +18,8 @@ constexpr int kBranches = 4;
 //   wdw     : W    [r+4][4D]                   rows 0..r-1 = W_d, rows r..r+3 = W_w
 //                                              (gamma folded on the bf16 path)
 //   wut     : W    [r][4D]                     W_u transposed
+//   wu      : bf16 [4D][r], W_u as given (each channel's r weights contiguous): only for the
+//             shapes of the large-rank tensor-core path (rank_tc_supported), else 0 bytes
 //   frag    : bf16 path only: the mma fragments of the weights (and gains) in the layout of the
 //             tensor-core kernel that serves the shape — per-CTA slices for the cluster kernel
 //             (shapes fused_supported() accepts, laid out in gr_fused_bf16.cu), else per-chunk
@@ -29,6 +31,7 @@ struct Layout {
     // bf16 shapes of the cluster kernel also carry the two-pass kernel's fragments, which the
     // two-pass kernel uses for the tokens it takes on the SMs the clusters leave idle
     size_t frag2, frag2_bytes;
+    size_t wu, wu_bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -67,6 +70,16 @@ cudaError_t launch_split_bf16(int64_t N, int64_t n2, int free_sms, int D, int r,
 // The two-pass kernel on an FP8 state also needs D % 128 == 0 and D <= 8192.
 bool tiled_fp8_supported(int D, int r);
 
+// Large-rank path on the tcgen05 tensor cores (gr_rank_tc.cu): bf16 states, D a multiple of 64,
+// 64 <= r <= 448 with r a multiple of 8. It needs rank_tc_workspace(N, r) bytes of device
+// workspace (inv [N][4] fp32, then h [N][rank_tc_padded(r)] bf16, each 256-byte aligned).
+bool rank_tc_supported(int D, int r);
+int rank_tc_padded(int r);
+size_t rank_tc_workspace(int64_t N, int r);
+cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const void* y,
+                           const float* s_prev, const void* packed, void* x, float* s_out,
+                           void* workspace, cudaStream_t st);
+
 inline Layout make_layout(int D, int r, int dtype) {
     Layout L{};
     const size_t K = size_t(kBranches) * D;
@@ -89,6 +102,9 @@ inline Layout make_layout(int D, int r, int dtype) {
                         : 0;
     L.frag2 = off;
     off = align256(off + L.frag2_bytes);
+    L.wu_bytes = dtype == GR_BF16 && rank_tc_supported(D, r) ? size_t(r) * K * 2 : 0;
+    L.wu = off;
+    off = align256(off + L.wu_bytes);
     L.total = off;
     return L;
 }

@@ -43,6 +43,15 @@ __global__ void pack_generic_kernel(int D, int r, const float* __restrict__ gamm
     }
 }
 
+// W_u as given ([4D][r], each channel's r weights contiguous), rounded to bf16: the B operand of
+// the large-rank path's up projection.
+__global__ void pack_wu_kernel(size_t n, const float* __restrict__ wu,
+                               __nv_bfloat16* __restrict__ out) {
+    for (size_t e = blockIdx.x * size_t(blockDim.x) + threadIdx.x; e < n;
+         e += size_t(gridDim.x) * blockDim.x)
+        out[e] = __float2bfloat16_rn(wu[e]);
+}
+
 }  // namespace
 
 // Fragment sections of the cluster kernel (gr_fused_bf16.cu) and the two-pass kernel
@@ -76,6 +85,12 @@ cudaError_t launch_pack(int D, int r, int dtype, const float* gamma, const float
     if (e != cudaSuccess) return e;
     if (L.frag2_bytes) {
         e = launch_pack_tiled(D, r, gamma, wd, wu, ww, base + L.frag2, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (L.wu_bytes) {
+        pack_wu_kernel<<<blocks, threads, 0, st>>>(size_t(r) * K, wu,
+                                                    reinterpret_cast<__nv_bfloat16*>(base + L.wu));
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (L.frag_bytes) {

@@ -68,6 +68,9 @@ def load() -> ctypes.CDLL:
         "gr_packed_size": ([S, sz], ctypes.c_int),
         "gr_pack_params": ([S, V, V, V, V, V, ctypes.c_size_t, P, V], ctypes.c_int),
         "gr_read": ([S, V, P, V, V, V], ctypes.c_int),
+        "gr_read_ws": ([S, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
+        "gr_step_workspace_size": ([S, sz], ctypes.c_int),
+        "gr_write_then_read_ws": ([S, V, V, V, P, V, V, V, ctypes.c_size_t, V], ctypes.c_int),
         "gr_write": ([S, V, V, V, V], ctypes.c_int),
         "gr_write_then_read": ([S, V, V, V, P, V, V, V], ctypes.c_int),
         "gr_read_fixed_gates": ([S, V, V, V, V, V], ctypes.c_int),
@@ -101,8 +104,9 @@ def status_string(status: int) -> str:
 
 
 def kernel_path(n_tokens: int, d_model: int, rank: int, dtype: torch.dtype) -> str:
-    """Which kernel a read or fused step of this shape runs ("fused_bf16", "tiled_bf16",
-    "tiled_fp8" for dtype FP8, or "generic")."""
+    """Which kernel a read or fused step of this shape runs ("fused_bf16",
+    "fused_bf16+tiled_bf16", "tiled_bf16", "tc_bf16" (the large-rank path), "tiled_fp8" for
+    dtype FP8, or "generic")."""
     return load().gr_kernel_path(ctypes.byref(make_shape(n_tokens, d_model, rank, dtype))).decode()
 
 
@@ -193,17 +197,47 @@ def _state_shape(R: torch.Tensor, params_or_rank, eps: float) -> Shape:
     return make_shape(R.shape[0], R.shape[2], rank, R.dtype, eps)
 
 
+def step_workspace_size(n_tokens: int, d_model: int, rank: int, dtype: torch.dtype) -> int:
+    """gr_step_workspace_size: device bytes a read or fused step of this shape needs (0 except on
+    the large-rank path)."""
+    need = ctypes.c_size_t(0)
+    shape = make_shape(n_tokens, d_model, rank, dtype)
+    _check(load().gr_step_workspace_size(ctypes.byref(shape), ctypes.byref(need)),
+           "gr_step_workspace_size")
+    return need.value
+
+
+def _step_ws(shape: Shape, device, workspace):
+    """(pointer, bytes) of the step's workspace: the caller's, else a fresh 256-byte aligned
+    buffer when the shape needs one."""
+    need = ctypes.c_size_t(0)
+    _check(load().gr_step_workspace_size(ctypes.byref(shape), ctypes.byref(need)),
+           "gr_step_workspace_size")
+    if workspace is not None:
+        _dev(workspace, "workspace")
+        return _ptr(workspace), workspace.numel() * workspace.element_size(), workspace
+    if need.value == 0:
+        return ctypes.c_void_p(None), 0, None
+    buf = torch.empty(need.value + 256, dtype=torch.uint8, device=device)
+    view = buf[(-buf.data_ptr()) % 256:][:need.value]
+    return _ptr(view), need.value, buf
+
+
 def read(R: torch.Tensor, params: Params, x: torch.Tensor | None = None,
-         s: torch.Tensor | None = None, stream=None):
-    """gr_read: R [N,4,D] -> (x [N,D], s [N,4] fp32)."""
+         s: torch.Tensor | None = None, stream=None, workspace: torch.Tensor | None = None):
+    """gr_read (through gr_read_ws): R [N,4,D] -> (x [N,D], s [N,4] fp32). The large-rank path
+    needs a device workspace: the caller's (256-byte aligned), else one allocated here."""
     shape = _state_shape(R, params, params.eps)
     N, _, D = R.shape
     x = torch.empty((N, D), dtype=R.dtype, device=R.device) if x is None else x
     s = torch.empty((N, 4), dtype=torch.float32, device=R.device) if s is None else s
     _dev(x, "x")
     _dev(s, "s")
-    _check(load().gr_read(ctypes.byref(shape), _ptr(R), params.ref(), _ptr(x), _ptr(s),
-                          _stream(stream)), "gr_read")
+    wp, wn, keep = _step_ws(shape, R.device, workspace)
+    _check(load().gr_read_ws(ctypes.byref(shape), _ptr(R), params.ref(), _ptr(x), _ptr(s), wp,
+                             wn, _stream(stream)), "gr_read")
+    if keep is not None and stream is not None:
+        keep.record_stream(stream)   # the allocator may hand it out again only after `stream`
     return x, s
 
 
@@ -219,8 +253,9 @@ def write(R: torch.Tensor, y: torch.Tensor, s: torch.Tensor, stream=None) -> tor
 
 def write_then_read(R: torch.Tensor, y: torch.Tensor, s_prev: torch.Tensor, params: Params,
                     x: torch.Tensor | None = None, s_next: torch.Tensor | None = None,
-                    stream=None):
-    """gr_write_then_read: R += s_prev_i y in place, then (x, s_next) = read(R, params)."""
+                    stream=None, workspace: torch.Tensor | None = None):
+    """gr_write_then_read (through gr_write_then_read_ws): R += s_prev_i y in place, then
+    (x, s_next) = read(R, params). Workspace as for read()."""
     shape = _state_shape(R, params, params.eps)
     N, _, D = R.shape
     x = torch.empty((N, D), dtype=R.dtype, device=R.device) if x is None else x
@@ -228,9 +263,12 @@ def write_then_read(R: torch.Tensor, y: torch.Tensor, s_prev: torch.Tensor, para
         else s_next
     for t, n in ((y, "y"), (s_prev, "s_prev"), (x, "x"), (s_next, "s_next")):
         _dev(t, n)
-    _check(load().gr_write_then_read(ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev),
-                                     params.ref(), _ptr(x), _ptr(s_next), _stream(stream)),
-           "gr_write_then_read")
+    wp, wn, keep = _step_ws(shape, R.device, workspace)
+    _check(load().gr_write_then_read_ws(ctypes.byref(shape), _ptr(R), _ptr(y), _ptr(s_prev),
+                                        params.ref(), _ptr(x), _ptr(s_next), wp, wn,
+                                        _stream(stream)), "gr_write_then_read")
+    if keep is not None and stream is not None:
+        keep.record_stream(stream)
     return x, s_next
 
 

@@ -79,6 +79,8 @@ WORKLOADS = {
     "deep_stack": Workload("deep_stack", 8192, 2048, 16, "bf16", y_std=0.1, n_sublayers=96),
     # prefill with the FP8 branch state (e4m3 codes + per-32-channel exponents; y, x bf16)
     "prefill_fp8": Workload("prefill_fp8", 16384, 4096, 16, "fp8", y_std=0.5),
+    # the pages' own rank: d = 2560 with r = d/8 = 320 (Digest §二.4), prefill-sized batch
+    "paper_rank": Workload("paper_rank", 16384, 2560, 320, "bf16", y_std=0.5),
     # skewed branch scales, 1% outlier channels x50, heavy-tailed y
     "large_skewed": Workload("large_skewed", 65536, 7168, 32, "bf16", y_std=0.5, y_kind="t3",
                              branch_scales=(0.1, 1.0, 10.0, 100.0), outlier_frac=0.01,

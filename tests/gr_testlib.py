@@ -76,9 +76,10 @@ def bf16_path_params(p: dict, w_up: str = "bf16") -> dict:
 
 
 def path_params(p: dict, kernel_path: str) -> dict:
-    """bf16_path_params for the kernel that serves a shape (gr.kernel_path's name): both
-    tensor-core kernels run the up projection in fp16, the generic kernel keeps bf16 W_u."""
-    return bf16_path_params(p, "bf16" if kernel_path == "generic" else "f16")
+    """bf16_path_params for the kernel that serves a shape (gr.kernel_path's name): the cluster
+    and two-pass kernels run the up projection in fp16, the generic kernel and the large-rank
+    path keep bf16 W_u."""
+    return bf16_path_params(p, "bf16" if kernel_path in ("generic", "tc_bf16") else "f16")
 
 
 def sample_rows(n: int, k: int, seed: int = 0) -> np.ndarray:

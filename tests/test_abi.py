@@ -127,12 +127,16 @@ def test_calls_validate_before_any_launch(lib):
     (4096, 32, gr.GR_BF16, "tiled_bf16"), (4104, 16, gr.GR_BF16, "generic"),
     (768, 16, gr.GR_BF16, "tiled_bf16"), (8192, 16, gr.GR_BF16, "tiled_bf16"),
     (64, 1, gr.GR_BF16, "tiled_bf16"), (4096, 33, gr.GR_BF16, "generic"),
-    (4096, 16, gr.GR_F32, "generic"), (8, 4, gr.GR_BF16, "generic")])
+    (4096, 16, gr.GR_F32, "generic"), (8, 4, gr.GR_BF16, "generic"),
+    (2560, 320, gr.GR_BF16, "tc_bf16"), (4096, 64, gr.GR_BF16, "tc_bf16"),
+    (1024, 448, gr.GR_BF16, "tc_bf16"), (4104, 64, gr.GR_BF16, "generic"),
+    (4096, 60, gr.GR_BF16, "generic"), (4096, 64, gr.GR_F32, "generic")])
 def test_kernel_path_selection(lib, D, r, dtype, path):
     """The cluster tensor-core kernel takes bf16 shapes whose width splits into 1..16 CTAs of 256
     channels (a power of two) with rank <= 16; the two-pass tensor-core kernel takes the other
     bf16 shapes with D a multiple of 64 and rank <= 32; every other valid shape (fp32 states
-    included) runs the generic kernel."""
+    included) runs the generic kernel; bf16 shapes with D a multiple of 64 and a rank of 64 … 448
+    (a multiple of 8) run the large-rank tensor-core path."""
     sh = _shape(n=100, d=D, r=r, dt=dtype)
     assert lib.gr_kernel_path(ctypes.byref(sh)).decode() == path
     assert lib.gr_kernel_path(ctypes.byref(_shape(d=12))).decode() == "invalid"
@@ -248,3 +252,51 @@ def test_decompose_validates_before_any_launch(lib):
     assert call(p[:9] + [null, null] + p[11:]) == E("GR_E_DEVICE")
     assert call(p[:5] + [null] * 7, U=0) == 0
     assert call(p, shape=_shape(n=64, d=256, r=16, dt=gr.GR_FP8)) == E("GR_E_DTYPE")
+
+
+def test_large_rank_validation(lib):
+    """Ranks above 64 exist only on the large-rank path (bf16, D % 64 == 0, r % 8 == 0,
+    r <= 448); its shapes need a step workspace: the workspace-free entries refuse them with
+    GR_E_SIZE, the host-buffer entries with GR_E_RANK, before any CUDA call."""
+    E = header_constant
+    null = ctypes.c_void_p(None)
+    assert E("GR_MAX_RANK_TC") == 448
+    need = ctypes.c_size_t(0)
+    tc = _shape(n=300, d=2560, r=320, dt=gr.GR_BF16)
+    assert lib.gr_step_workspace_size(ctypes.byref(tc), ctypes.byref(need)) == 0
+    assert need.value == (300 * 16 + 255) // 256 * 256 + (300 * 320 * 2 + 255) // 256 * 256
+    small = _shape(n=300, d=4096, r=16, dt=gr.GR_BF16)
+    assert lib.gr_step_workspace_size(ctypes.byref(small), ctypes.byref(need)) == 0
+    assert need.value == 0
+    for d, r, dt in ((2560, 512, gr.GR_BF16), (2560, 456, gr.GR_BF16), (2560, 100, gr.GR_BF16),
+                     (2568, 128, gr.GR_BF16), (2560, 128, gr.GR_F32), (2560, 128, gr.GR_FP8)):
+        bad = _shape(n=4, d=d, r=r, dt=dt)
+        assert lib.gr_step_workspace_size(ctypes.byref(bad), ctypes.byref(need)) in (
+            E("GR_E_RANK"), E("GR_E_SHAPE"), E("GR_E_DTYPE")), (d, r, dt)
+    # a packed-parameter struct for the shape (never dereferenced on the host)
+    st = gr.ParamsStruct()
+    st.tag, st.packed, st.d_model, st.n_branch, st.rank, st.state_dtype = (
+        gr.GR_PARAMS_TAG, FAKE.value, 2560, 4, 320, gr.GR_BF16)
+    R, x, s = (ctypes.c_void_p(0x1000000), ctypes.c_void_p(0x4000000), ctypes.c_void_p(0x5000000))
+    ws = ctypes.c_void_p(0x6000000)
+    assert lib.gr_read(ctypes.byref(tc), R, ctypes.byref(st), x, s, null) == E("GR_E_SIZE")
+    assert lib.gr_read_ws(ctypes.byref(tc), R, ctypes.byref(st), x, s, ws, 10**7,
+                          null) == E("GR_E_DEVICE")
+    assert lib.gr_read_ws(ctypes.byref(tc), R, ctypes.byref(st), x, s, ws, 100,
+                          null) == E("GR_E_SIZE")
+    assert lib.gr_read_ws(ctypes.byref(tc), R, ctypes.byref(st), x, s,
+                          ctypes.c_void_p(0x6000010), 10**7, null) == E("GR_E_ALIGN")
+    assert lib.gr_read_ws(ctypes.byref(tc), R, ctypes.byref(st), x, s, R, 10**7,
+                          null) == E("GR_E_ALIAS")
+    y = ctypes.c_void_p(0x3000000)
+    assert lib.gr_write_then_read(ctypes.byref(tc), R, y, s, ctypes.byref(st), x,
+                                  ctypes.c_void_p(0x5100000), null) == E("GR_E_SIZE")
+    assert lib.gr_write_then_read_ws(ctypes.byref(tc), R, y, s, ctypes.byref(st), x,
+                                     ctypes.c_void_p(0x5100000), ws, 10**7,
+                                     null) == E("GR_E_DEVICE")
+    assert lib.gr_write_then_read_host(ctypes.byref(tc), R, y, s, ctypes.byref(st), x,
+                                       ctypes.c_void_p(0x5100000), ws, 10**9,
+                                       null) == E("GR_E_RANK")
+    # the CUDA-core backward and decomposition stop at rank 64
+    assert lib.gr_read_backward_workspace_size(ctypes.byref(tc), ctypes.byref(need)) == \
+        E("GR_E_RANK")
