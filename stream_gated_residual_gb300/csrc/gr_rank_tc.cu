@@ -37,9 +37,11 @@ constexpr int kTile = 128;          // tokens per CTA: the MMA's M
 constexpr int kKc = 64;             // K elements per operand stage (128-byte rows)
 constexpr int kStageA = kTile * 128; // one 128-token × 64-channel bf16 stage
 constexpr int kGemmThreads = 192;   // down projection: producer, MMA, 4 scaling/epilogue warps
-constexpr int kUpThreads = 320;     // up projection: producer, MMA, 8 epilogue warps
+constexpr int kUpThreads = 352;     // up projection: producer, MMA, 8 epilogue warps, R' loader
 constexpr int kUpEpiWarps = 8;      // two per tensor-memory lane quadrant, 16 channels each
 constexpr int kCb = 32;             // channels per branch in an up-projection block
+constexpr int kPair = 2;            // CTAs of a cluster sharing each weight stage (TMA multicast)
+constexpr uint16_t kPairMask = 0x3;
 constexpr int kMaxRankTc = 448;     // r + 4 <= 512 accumulator columns; H fits shared memory
 
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + __expf(-a)); }
@@ -102,8 +104,8 @@ __host__ __device__ inline size_t down_stage_bytes(int n1) {
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
-down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW0,
-               const __grid_constant__ CUtensorMap tmW1, int64_t N, int D, int r, int n1,
+down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
+               int64_t N, int D, int r, int n1,
                int stages, const float* __restrict__ inv, __nv_bfloat16* __restrict__ h, int rp,
                float* __restrict__ s_out) {
     extern __shared__ uint8_t smraw[];
@@ -119,12 +121,13 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     const int64_t t0 = int64_t(blockIdx.x) * kTile;
     const int nk = kBranches * D / kKc, cpb = D / kKc;
     const uint32_t ncols = n1 > 256 ? 512 : 256;
+    const uint32_t crank = cluster_ctarank();   // 0 or 1: which half of each weight stage it loads
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&scaled[s], 4);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kPair);   // both CTAs' MMAs are done with the stage
         }
         mbar_init(acc_full, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -135,6 +138,7 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();   // the pair's barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
@@ -146,10 +150,12 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
                 if (kc >= stages && !mbar_wait(&empty[s], ((kc / stages) - 1) & 1)) break;
                 uint8_t* A = sm + s * sb;
                 uint8_t* B = A + 2 * kStageA;
+                const int half = n1 / kPair;
                 mbar_expect_tx(&full[s], bytes);
                 tma_load_3d(A, &tmR, (kc % cpb) * kKc, kc / cpb, int(t0), &full[s]);
-                tma_load_2d(B, &tmW0, kc * kKc, 0, &full[s]);
-                if (n1 > 256) tma_load_2d(B + 256 * 128, &tmW1, kc * kKc, 256, &full[s]);
+                // this CTA's half of the weight rows, delivered to both CTAs of the pair
+                tma_load_2d_mc(B + crank * half * 128, &tmW, kc * kKc, int(crank) * half,
+                               &full[s], kPairMask);
             }
         }
     } else if (warp == 1) {
@@ -179,7 +185,7 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
                         tc_mma(tmem + 256, al, b1, id1, 1u);
                     }
                 }
-                tc_commit(&empty[s]);
+                tc_commit_mc(&empty[s], kPairMask);
             }
             if (ok) tc_commit(acc_full);
         }
@@ -257,6 +263,7 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();   // neither CTA leaves while the other may still signal its barriers
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
@@ -264,18 +271,21 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
 }
 
 // ---- 3. up projection, gate and combine ------------------------------------------------------
-// Shared memory: H (rp/64 stages of 128 × 128 B), kUpStages B stages (4 branches × 32 rows ×
-// 128 B), two R' blocks (4 branches × 128 tokens × 32 channels bf16), then the barriers.
-constexpr int kUpStages = 3;
+// Shared memory: H (rp/64 stages of 128 × 128 B), nbs B stages (4 branches × 32 rows × 128 B),
+// nrb R' blocks (4 branches × 128 tokens × 32 channels bf16), then the barriers. A warp of its
+// own streams the R' blocks, up to nrb ahead of the epilogue, so that their HBM latency hides
+// behind the blocks before.
+constexpr int kUpMaxStages = 6;     // each CTA streams all of W_u: bytes in flight set its rate
+constexpr int kUpMaxR = 2;
 constexpr int kStageB = kBranches * kCb * 128;                 // 16 KB
 constexpr int kRBlock = kBranches * kTile * kCb * 2;           // 32 KB
-__host__ __device__ inline size_t up_smem_bytes(int rp) {
-    return size_t(rp / kKc) * kStageA + kUpStages * kStageB + 2 * kRBlock + 256;
+__host__ __device__ inline size_t up_smem_bytes(int rp, int nbs, int nrb) {
+    return size_t(rp / kKc) * kStageA + size_t(nbs) * kStageB + size_t(nrb) * kRBlock + 256;
 }
 
 __global__ void __launch_bounds__(kUpThreads, 1)
 up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmU,
-             const __grid_constant__ CUtensorMap tmR, int64_t N, int D, int rp,
+             const __grid_constant__ CUtensorMap tmR, int64_t N, int D, int rp, int nbs, int nrb,
              const float* __restrict__ gamma, const float* __restrict__ inv,
              __nv_bfloat16* __restrict__ x) {
     extern __shared__ uint8_t smraw[];
@@ -284,28 +294,31 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
     const int nkc = rp / kKc;
     uint8_t* H = sm;
     uint8_t* Bs = H + size_t(nkc) * kStageA;
-    uint8_t* Rb = Bs + kUpStages * kStageB;
-    uint64_t* h_full = reinterpret_cast<uint64_t*>(Rb + 2 * kRBlock);
+    uint8_t* Rb = Bs + size_t(nbs) * kStageB;
+    uint64_t* h_full = reinterpret_cast<uint64_t*>(Rb + size_t(nrb) * kRBlock);
     uint64_t* b_full = h_full + 1;
-    uint64_t* b_empty = b_full + kUpStages;
-    uint64_t* r_full = b_empty + kUpStages;
-    uint64_t* r_empty = r_full + 2;
-    uint64_t* t_full = r_empty + 2;
+    uint64_t* b_empty = b_full + kUpMaxStages;
+    uint64_t* r_full = b_empty + kUpMaxStages;
+    uint64_t* r_empty = r_full + kUpMaxR;
+    uint64_t* t_full = r_empty + kUpMaxR;
     uint64_t* t_empty = t_full + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(t_empty + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = int64_t(blockIdx.x) * kTile;
     const int nb = D / kCb;
+    const uint32_t crank = cluster_ctarank();   // 0 or 1: which two branches of a B stage it loads
 
     if (threadIdx.x == 0) {
         mbar_init(h_full, 1);
-        for (int s = 0; s < kUpStages; ++s) {
+        for (int s = 0; s < kUpMaxStages; ++s) {
             mbar_init(&b_full[s], 1);
-            mbar_init(&b_empty[s], 1);
+            mbar_init(&b_empty[s], kPair);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kUpMaxR; ++b) {
             mbar_init(&r_full[b], 1);
             mbar_init(&r_empty[b], kUpEpiWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(&t_full[b], 1);
             mbar_init(&t_empty[b], kUpEpiWarps);
         }
@@ -317,6 +330,7 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();   // the pair's barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
@@ -327,25 +341,32 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
                 tma_load_2d(H + kc * kStageA, &tmH, kc * kKc, int(t0), h_full);
             int it = 0;
             for (int cb = 0; cb < nb; ++cb) {
-                const int rb = cb & 1;
-                if (cb >= 2 && !mbar_wait(&r_empty[rb], ((cb >> 1) - 1) & 1)) break;
-                mbar_expect_tx(&r_full[rb], kRBlock);
-                for (int i = 0; i < kBranches; ++i)
-                    tma_load_3d(Rb + rb * kRBlock + i * (kTile * kCb * 2), &tmR, cb * kCb, i,
-                                int(t0), &r_full[rb]);
                 bool ok = true;
                 for (int kc = 0; kc < nkc; ++kc, ++it) {
-                    const int s = it % kUpStages;
-                    if (it >= kUpStages && !mbar_wait(&b_empty[s], ((it / kUpStages) - 1) & 1)) {
+                    const int s = it % nbs;
+                    if (it >= nbs && !mbar_wait(&b_empty[s], ((it / nbs) - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     mbar_expect_tx(&b_full[s], kStageB);
-                    for (int i = 0; i < kBranches; ++i)
-                        tma_load_2d(Bs + s * kStageB + i * (kCb * 128), &tmU, kc * kKc,
-                                    i * D + cb * kCb, &b_full[s]);
+                    // branches 2·crank, 2·crank + 1, delivered to both CTAs of the pair
+                    for (int i = 2 * int(crank); i < 2 * int(crank) + 2; ++i)
+                        tma_load_2d_mc(Bs + s * kStageB + i * (kCb * 128), &tmU, kc * kKc,
+                                       i * D + cb * kCb, &b_full[s], kPairMask);
                 }
                 if (!ok) break;
+            }
+        }
+    } else if (warp == 2 + kUpEpiWarps) {
+        // the R' blocks of the combine, up to nrb ahead
+        if (lane == 0) {
+            for (int cb = 0; cb < nb; ++cb) {
+                const int rb = cb % nrb;
+                if (cb >= nrb && !mbar_wait(&r_empty[rb], ((cb / nrb) - 1) & 1)) break;
+                mbar_expect_tx(&r_full[rb], kRBlock);
+                for (int i = 0; i < kBranches; ++i)
+                    tma_load_3d(Rb + rb * kRBlock + i * (kTile * kCb * 2), &tmR, cb * kCb, i,
+                                int(t0), &r_full[rb]);
             }
         }
     } else if (warp == 1) {
@@ -359,8 +380,8 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
                 if (!ok) break;
                 tc_fence_after();
                 for (int kc = 0; kc < nkc; ++kc, ++it) {
-                    const int s = it % kUpStages;
-                    ok = mbar_wait(&b_full[s], (it / kUpStages) & 1);
+                    const int s = it % nbs;
+                    ok = mbar_wait(&b_full[s], (it / nbs) & 1);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t a = smem_u32(H + kc * kStageA);
@@ -369,7 +390,7 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma(tmem + buf * (kBranches * kCb), sdesc_sw128(a + kk * 32),
                                sdesc_sw128(b + kk * 32), id, (kc | kk) != 0);
-                    tc_commit(&b_empty[s]);
+                    tc_commit_mc(&b_empty[s], kPairMask);
                 }
                 if (ok) tc_commit(&t_full[buf]);
             }
@@ -385,7 +406,8 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
         bool ok = true;
         for (int cb = 0; cb < nb && ok; ++cb) {
             const int buf = cb & 1;
-            ok = mbar_wait(&t_full[buf], (cb >> 1) & 1) && mbar_wait(&r_full[buf], (cb >> 1) & 1);
+            const int rb = cb % nrb;
+            ok = mbar_wait(&t_full[buf], (cb >> 1) & 1) && mbar_wait(&r_full[rb], (cb / nrb) & 1);
             if (!ok) break;
             tc_fence_after();
             // the four branches' 16 logits of this row, in flight together
@@ -401,7 +423,7 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
 #pragma unroll
             for (int i = 0; i < kBranches; ++i) {
                 const uint4* rr = reinterpret_cast<const uint4*>(
-                    Rb + buf * kRBlock + i * (kTile * kCb * 2) + row * (kCb * 2) + hh * (kH * 2));
+                    Rb + rb * kRBlock + i * (kTile * kCb * 2) + row * (kCb * 2) + hh * (kH * 2));
                 const float4* gm =
                     reinterpret_cast<const float4*>(gamma + size_t(i) * D + cb * kCb + hh * kH);
                 const float m = iv[i];
@@ -426,7 +448,7 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&t_empty[buf]);
-                mbar_arrive(&r_empty[buf]);
+                mbar_arrive(&r_empty[rb]);
             }
             if (t < N) {
                 uint4* xp = reinterpret_cast<uint4*>(x + t * D + cb * kCb + hh * kH);
@@ -443,6 +465,7 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -477,6 +500,25 @@ bool map_state(CUtensorMap* m, const void* R, int64_t N, int D, uint32_t box_ch,
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(R), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launch as clusters of kPair CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pairs(void (*kern)(KArgs...), unsigned grid, int threads, size_t smem,
+                         cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 }  // namespace
@@ -518,14 +560,14 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const unsigned tiles = unsigned((N + kTile - 1) / kTile);
+    // a whole number of CTA pairs (a pair's second tile may lie past N: TMA fills it with zeros
+    // and its rows are not written)
+    const unsigned tiles = unsigned((N + kTile - 1) / kTile + kPair - 1) / kPair * kPair;
     // 2. down projection
     {
-        CUtensorMap mR, mW0, mW1;
+        CUtensorMap mR, mW;
         if (!map_state(&mR, R, N, D, kKc, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !map_2d(&mW0, wdw, K, r + kBranches, size_t(K) * 2, kKc, n1 > 256 ? 256 : n1,
-                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !map_2d(&mW1, wdw, K, r + kBranches, size_t(K) * 2, kKc, n1 > 256 ? n1 - 256 : 16,
+            !map_2d(&mW, wdw, K, r + kBranches, size_t(K) * 2, kKc, n1 / kPair,
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const size_t sb = down_stage_bytes(n1);
@@ -537,9 +579,8 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        down_tc_kernel<<<tiles, kGemmThreads, smem, st>>>(mR, mW0, mW1, N, D, r, n1, stages, inv,
-                                                         h, rp, s_out);
-        e = cudaGetLastError();
+        e = launch_pairs(down_tc_kernel, tiles, kGemmThreads, smem, st, mR, mW, N, D, r, n1,
+                         stages, static_cast<const float*>(inv), h, rp, s_out);
         if (e != cudaSuccess) return e;
     }
     // 3. up projection, gate and combine
@@ -549,14 +590,19 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
             !map_2d(&mU, wu, r, K, size_t(r) * 2, kKc, kCb, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !map_state(&mR2, R, N, D, kCb, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
-        const size_t smem = 1024 + up_smem_bytes(rp);
+        // two R' blocks and as many weight stages (up to 6) as the shared memory holds
+        const int nrb = kUpMaxR;
+        const size_t cap = 232448 - 1024;
+        int nbs = kUpMaxStages;
+        while (nbs > 2 && up_smem_bytes(rp, nbs, nrb) > cap) --nbs;
+        if (up_smem_bytes(rp, nbs, nrb) > cap) return cudaErrorInvalidValue;
+        const size_t smem = 1024 + up_smem_bytes(rp, nbs, nrb);
         cudaError_t e = cudaFuncSetAttribute(up_tc_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        up_tc_kernel<<<tiles, kUpThreads, smem, st>>>(mH, mU, mR2, N, D, rp, gamma, inv,
-                                                       static_cast<__nv_bfloat16*>(x));
-        e = cudaGetLastError();
+        e = launch_pairs(up_tc_kernel, tiles, kUpThreads, smem, st, mH, mU, mR2, N, D, rp, nbs,
+                         nrb, gamma, static_cast<const float*>(inv), static_cast<__nv_bfloat16*>(x));
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -78,6 +78,27 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
         : "memory");
 }
 
+// ---- thread-block clusters: one TMA load delivered to several CTAs, one commit releasing them
+// The 2D tile lands at the same offset in every CTA of `mask` (cluster ranks), and each of them
+// gets the byte count on its mbarrier at the same offset as `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1,
+                                               uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// Arrives once on the mbarrier at `bar`'s offset in every CTA of `mask` when this thread's
+// earlier MMAs have completed.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
 // ---- epilogue loads: a warp reads 32 lanes (its quadrant: warp % 4) × 16 columns -------------
 // Without the wait: several loads may be in flight; tmem_wait_ld() before using any of them.
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
