@@ -102,8 +102,9 @@ const char* gr_status_string(int status);
  * tokens also runs on the two-pass kernel, concurrently, on the SMs the clusters leave idle;
  * this form needs the device, so without one the plain "fused_bf16" is reported),
  * "tiled_bf16" (two-pass tensor-core kernel: the other bf16 shapes with D % 64 == 0, r <= 32),
- * "tiled_fp8" (the two-pass kernel on an FP8 state), "generic" (one CTA per token), or
- * "invalid". Host only. */
+ * "tc_bf16" (the large-rank path on the tcgen05 tensor cores: bf16, D % 64 == 0,
+ * 64 <= r <= GR_MAX_RANK_TC, r % 8 == 0), "tiled_fp8" (the two-pass kernel on an FP8 state),
+ * "generic" (one CTA per token), or "invalid". Host only. */
 const char* gr_kernel_path(const gr_shape* shape);
 
 /* Bytes of device memory gr_pack_params needs for `shape` (host only; no CUDA call).
