@@ -69,10 +69,11 @@ def _case(N, D, r, dtype, U, seed=51, with_r0=True, zero_writer=None, weight_mul
                                            (37, 256, 16, "bf16", 7), (100, 1032, 32, "f32", 13),
                                            (17, 520, 64, "f32", 3), (64, 4096, 16, "bf16", 12),
                                            (33, 2048, 20, "bf16", 40), (9, 4096, 8, "f32", 5),
-                                           (7, 12288, 16, "bf16", 2), (3, 12288, 40, "f32", 4)])
+                                           (7, 12288, 16, "bf16", 2), (3, 12288, 40, "f32", 4),
+                                           (50, 256, 16, "bf16", 45), (70, 384, 32, "f32", 83)])
 def test_decompose_matches_oracle(N, D, r, dtype, U):
     """Every rank class and tokens-per-CTA choice, ragged token tiles and writer groups (U not a
-    multiple of 6), the widest D, both state types."""
+    multiple of 6, and U = 45 and 83), the widest D, both state types."""
     _case(N, D, r, dtype, U)
 
 
