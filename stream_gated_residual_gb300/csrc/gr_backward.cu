@@ -78,9 +78,11 @@ __host__ __device__ constexpr int bwd_threads() { return RM > 32 ? 256 : 512; }
 // RM: the largest rank of the instantiation (16, 32 or 64); TB: tokens per CTA at a time. Every
 // weight element a thread loads serves the TB tokens (the weights stream from L2 once per TB
 // tokens); the TB state rows sit in shared memory in the state's own type.
-template <typename T, int RM, int TB>
+// FULL: r == RM, so that every rank test below is a compile-time constant (the common case of a
+// rank that is itself 16, 32 or 64).
+template <typename T, int RM, int TB, bool FULL>
 __global__ void __launch_bounds__(bwd_threads<RM>())
-read_backward_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
+read_backward_kernel(int64_t N, int D, int r_arg, float eps, const T* __restrict__ R,
                      const float* __restrict__ gamma, const float* __restrict__ Wd,
                      const float* __restrict__ WuT, const float* __restrict__ Ww,
                      const float* __restrict__ dx, const float* __restrict__ ds,
@@ -90,6 +92,7 @@ read_backward_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R
     constexpr int M = RM + kBranches;
     constexpr int kBwdThreads = bwd_threads<RM>();
     constexpr int kBwdWarps = kBwdThreads / 32;
+    const int r = FULL ? RM : r_arg;
     extern __shared__ float smem[];
     const int K = kBranches * D;
     const int ss = 2 * r + kBranches + 1;                   // row stride of S
@@ -359,7 +362,7 @@ int grid_tokens(int64_t N) {
     return int(N < cap ? N : cap);
 }
 
-template <typename T, int RM, int TB>
+template <typename T, int RM, int TB, bool FULL>
 cudaError_t launch_rb_t(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
                         const float* Wd, const float* WuT, const float* Ww, const float* dx,
                         const float* ds, float* dR, float* DG, float* V, float* P, float* S,
@@ -370,7 +373,7 @@ cudaError_t launch_rb_t(int64_t N, int D, int r, float eps, const void* R, const
     const size_t smem =
         (size_t(TB) * K * sizeof(T) + 15) / 16 * 16 +
         (size_t(kBwdThreads / 32) * TB * M + 2 * TB * M + TB * RM + TB * kBranches) * 4;
-    auto kern = read_backward_kernel<T, RM, TB>;
+    auto kern = read_backward_kernel<T, RM, TB, FULL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
@@ -385,6 +388,19 @@ cudaError_t launch_rb_t(int64_t N, int D, int r, float eps, const void* R, const
     return cudaGetLastError();
 }
 
+// The full-rank instantiation when r == RM, else the general one.
+template <typename T, int RM, int TB>
+cudaError_t launch_rb_tb(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
+                         const float* Wd, const float* WuT, const float* Ww, const float* dx,
+                         const float* ds, float* dR, float* DG, float* V, float* P, float* S,
+                         cudaStream_t st) {
+    if (r == RM)
+        return launch_rb_t<T, RM, TB, true>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG,
+                                            V, P, S, st);
+    return launch_rb_t<T, RM, TB, false>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V,
+                                         P, S, st);
+}
+
 // The most tokens per CTA that the registers (TB·(RM+4) accumulators) and shared memory
 // (TB state rows, up to about 200 KB) allow: 4, 2 or 1.
 template <typename T, int RM>
@@ -397,13 +413,13 @@ cudaError_t launch_rb(int64_t N, int D, int r, float eps, const void* R, const f
     const int tb_smem = row * 4 <= 200 * 1024 ? 4 : row * 2 <= 200 * 1024 ? 2 : 1;
     const int tb = tb_reg < tb_smem ? tb_reg : tb_smem;
     if (tb >= 4 && RM <= 16)
-        return launch_rb_t<T, RM, (RM <= 16 ? 4 : 1)>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds,
-                                                      dR, DG, V, P, S, st);
+        return launch_rb_tb<T, RM, (RM <= 16 ? 4 : 1)>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx,
+                                                       ds, dR, DG, V, P, S, st);
     if (tb >= 2 && RM <= 32)
-        return launch_rb_t<T, RM, (RM <= 32 ? 2 : 1)>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds,
-                                                      dR, DG, V, P, S, st);
-    return launch_rb_t<T, RM, 1>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P, S,
-                                 st);
+        return launch_rb_tb<T, RM, (RM <= 32 ? 2 : 1)>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx,
+                                                       ds, dR, DG, V, P, S, st);
+    return launch_rb_tb<T, RM, 1>(N, D, r, eps, R, gamma, Wd, WuT, Ww, dx, ds, dR, DG, V, P, S,
+                                  st);
 }
 
 template <int MM>
