@@ -103,9 +103,10 @@ template <> struct Raw8<float> {
     __device__ __forceinline__ float get(int k) const { return k < 4 ? comp(a, k) : comp(b, k - 4); }
 };
 
-template <typename T, int RM, int TB>
+// FULL: r == RM, so that every rank test is a compile-time constant.
+template <typename T, int RM, int TB, bool FULL>
 __global__ void __launch_bounds__(dec_threads<RM>(), RM > 32 ? 1 : 2)
-decompose_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
+decompose_kernel(int64_t N, int D, int r_arg, float eps, const T* __restrict__ R,
                  const float* __restrict__ gamma, const float* __restrict__ Wd,
                  const float* __restrict__ Wu, int U, const T* __restrict__ Y,
                  const float* __restrict__ S, const T* __restrict__ R0,
@@ -114,6 +115,7 @@ decompose_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
     constexpr int NT = dec_threads<RM>();
     constexpr int NW = NT / 32;
     constexpr int TPT = NT / TB;            // threads per token in the writer pass
+    const int r = FULL ? RM : r_arg;
     constexpr int WPT = TPT / 32;           // warps per token
     extern __shared__ float smem[];
     const int K = kBranches * D;
@@ -322,7 +324,7 @@ decompose_kernel(int64_t N, int D, int r, float eps, const T* __restrict__ R,
     }
 }
 
-template <typename T, int RM, int TB>
+template <typename T, int RM, int TB, bool FULL>
 cudaError_t launch_t(int64_t N, int D, int r, float eps, const void* R, const float* gamma,
                      const float* Wd, const float* Wu, int U, const void* Y, const float* S,
                      const void* R0, float* norm, float* bnorm, float* pi, float* a0_norm,
@@ -332,7 +334,7 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, const void* R, const fl
     const size_t K = size_t(kBranches) * D;
     const size_t smem = (size_t(TB) * K + size_t(NT / 32) * RED + 2 * TB * RM +
                          TB * kBranches + TB * kGroup * kBranches + TB) * 4;
-    auto kern = decompose_kernel<T, RM, TB>;
+    auto kern = decompose_kernel<T, RM, TB, FULL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
@@ -360,10 +362,16 @@ cudaError_t launch_rm(int64_t N, int D, int r, float eps, const void* R, const f
     const int tb_smem = row * 2 <= 100 * 1024 ? 2 : 1;
     const int tb = tb_reg < tb_smem ? tb_reg : tb_smem;
     if (tb >= 2 && RM <= 32)
-        return launch_t<T, RM, (RM <= 32 ? 2 : 1)>(N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0,
-                                                   norm, bnorm, pi, a0_norm, st);
-    return launch_t<T, RM, 1>(N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0, norm, bnorm, pi,
-                              a0_norm, st);
+        return r == RM ? launch_t<T, RM, (RM <= 32 ? 2 : 1), true>(
+                             N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0, norm, bnorm, pi,
+                             a0_norm, st)
+                       : launch_t<T, RM, (RM <= 32 ? 2 : 1), false>(
+                             N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0, norm, bnorm, pi,
+                             a0_norm, st);
+    return r == RM ? launch_t<T, RM, 1, true>(N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0, norm,
+                                              bnorm, pi, a0_norm, st)
+                   : launch_t<T, RM, 1, false>(N, D, r, eps, R, gamma, Wd, Wu, U, Y, S, R0, norm,
+                                               bnorm, pi, a0_norm, st);
 }
 
 template <typename T>
