@@ -275,43 +275,71 @@ read_backward_kernel(int64_t N, int D, int r_arg, float eps, const T* __restrict
 // out rows m < M: Σ over this CTA's tokens of S[t][soff + m] · B[t][j], added atomically to
 // out0[m·K + j] (m < m0) or out1[(m − m0)·K + j]; or, transposed (one output), to
 // out0[j·M + m]. One column j per thread, 32 tokens' small factors staged in shared memory.
-template <int MM>
+template <int MM, int CW>
 __global__ void __launch_bounds__(kThreads)
 token_sum_kernel(int64_t N, int K, int M, const float* __restrict__ S, int s_stride, int soff,
                  const float* __restrict__ B, float* __restrict__ out0, float* __restrict__ out1,
                  int m0, bool transposed, int64_t tokens_per_cta) {
-    __shared__ float sS[32][MM];
-    const int j = blockIdx.x * kThreads + threadIdx.x;
+    // CW consecutive columns a thread (16- or 8-byte loads of the long factor), so that each
+    // shared-memory read of a small factor serves CW columns; rows padded to a multiple of 4
+    constexpr int MP = (MM + 3) / 4 * 4;
+    __shared__ __align__(16) float sS[32][MP];
+    const int j0 = (blockIdx.x * kThreads + threadIdx.x) * CW;
     const int64_t ta = int64_t(blockIdx.y) * tokens_per_cta;
     const int64_t tb = ta + tokens_per_cta < N ? ta + tokens_per_cta : N;
-    float acc[MM];
+    float acc[MM][CW];
 #pragma unroll
-    for (int m = 0; m < MM; ++m) acc[m] = 0.f;
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+        for (int c = 0; c < CW; ++c) acc[m][c] = 0.f;
     for (int64_t t0 = ta; t0 < tb; t0 += 32) {
         const int nt = int(tb - t0 < 32 ? tb - t0 : 32);
-        for (int e = threadIdx.x; e < nt * M; e += kThreads) {
-            const int tt = e / M, m = e - tt * M;
-            sS[tt][m] = S[(t0 + tt) * s_stride + soff + m];
+        for (int e = threadIdx.x; e < 32 * MP; e += kThreads) {
+            const int tt = e / MP, m = e - tt * MP;
+            sS[tt][m] = (tt < nt && m < M) ? S[(t0 + tt) * s_stride + soff + m] : 0.f;
         }
         __syncthreads();
-        if (j < K) {
+        if (j0 < K) {
 #pragma unroll 4
             for (int tt = 0; tt < nt; ++tt) {
-                const float b = B[(t0 + tt) * K + j];
+                float b[CW];
+                const float* bp = B + (t0 + tt) * K + j0;
+                if (CW == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(bp);
+                    b[0] = v.x; b[CW > 1 ? 1 : 0] = v.y; b[CW > 2 ? 2 : 0] = v.z;
+                    b[CW > 3 ? 3 : 0] = v.w;
+                } else if (CW == 2) {
+                    const float2 v = *reinterpret_cast<const float2*>(bp);
+                    b[0] = v.x; b[CW > 1 ? 1 : 0] = v.y;
+                } else {
+                    b[0] = *bp;
+                }
 #pragma unroll
-                for (int m = 0; m < MM; ++m)
-                    if (m < M) acc[m] = fmaf(sS[tt][m], b, acc[m]);
+                for (int m4 = 0; m4 < MP; m4 += 4) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(&sS[tt][m4]);
+                    const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (m4 + q < MM)
+#pragma unroll
+                            for (int c = 0; c < CW; ++c)
+                                acc[m4 + q][c] = fmaf(sv[q], b[c], acc[m4 + q][c]);
+                }
             }
         }
         __syncthreads();
     }
-    if (j < K) {
+    if (j0 < K) {
 #pragma unroll
         for (int m = 0; m < MM; ++m) {
             if (m < M) {
-                if (transposed) atomicAdd(&out0[size_t(j) * M + m], acc[m]);
-                else if (m < m0) atomicAdd(&out0[size_t(m) * K + j], acc[m]);
-                else atomicAdd(&out1[size_t(m - m0) * K + j], acc[m]);
+#pragma unroll
+                for (int c = 0; c < CW; ++c) {
+                    const int j = j0 + c;
+                    if (transposed) atomicAdd(&out0[size_t(j) * M + m], acc[m][c]);
+                    else if (m < m0) atomicAdd(&out0[size_t(m) * K + j], acc[m][c]);
+                    else atomicAdd(&out1[size_t(m - m0) * K + j], acc[m][c]);
+                }
             }
         }
     }
@@ -428,12 +456,14 @@ cudaError_t launch_sum(int64_t N, int K, int M, const float* S, int s_stride, in
                        cudaStream_t st) {
     // 128 tokens per CTA: thousands of CTAs keep enough loads of the long factor in flight
     // (a few CTAs walking thousands of tokens each were latency-bound); the cost is one atomic
-    // per output element and CTA row
-    const int gx = (K + kThreads - 1) / kThreads;
+    // per output element and CTA row. Columns per thread: 4 up to 20 small factors, 2 up to
+    // 40, else 1 (the accumulators are MM × CW registers).
+    constexpr int CW = MM <= 20 ? 4 : MM <= 40 ? 2 : 1;
+    const int gx = (K + kThreads * CW - 1) / (kThreads * CW);
     const int64_t per = 128;
     const int gy = int((N + per - 1) / per);
-    token_sum_kernel<MM><<<dim3(gx, gy), kThreads, 0, st>>>(N, K, M, S, s_stride, soff, B, out0,
-                                                            out1, m0, transposed, per);
+    token_sum_kernel<MM, CW><<<dim3(gx, gy), kThreads, 0, st>>>(
+        N, K, M, S, s_stride, soff, B, out0, out1, m0, transposed, per);
     return cudaGetLastError();
 }
 
