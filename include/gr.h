@@ -236,7 +236,7 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
  * The gradients of the read and the write by the chain rule through eq rms, eq gate, eq use_gate,
  * eq s and eq write ("【论文解读】 Qwen3.8 Flash Next", §二.4), in fp32 on CUDA cores. States (R,
  * y) in shape->state_dtype (GR_BF16 or GR_F32), parameters and every gradient fp32, all DEVICE
- * pointers, 16-byte aligned. */
+ * pointers, 16-byte aligned. Ranks 1 … GR_MAX_RANK (GR_E_RANK above). */
 
 /* Bytes of device workspace gr_read_backward needs: 3·N·4·D·4 bytes of per-token factors of
  * the parameter gradients, N·(2r+5)·4 more, and r·4·D·4 for W_u transposed, each part rounded
@@ -282,7 +282,8 @@ int gr_write_backward(const gr_shape* shape, const float* dR_next, const void* y
  *   a0_norm     [N]        ‖a_{0→v}‖₂, a_{0→v} = ¼ Σ_i G_i ⊙ γ_i ⊙ R0_i / rms(R_i) (required
  *                          with R0, ignored without)
  * All DEVICE pointers, 16-byte aligned; outputs must not overlap the inputs or each other.
- * 0 <= U <= GR_MAX_WRITERS. Asynchronous on `stream`. Errors: as the other calls. */
+ * 0 <= U <= GR_MAX_WRITERS; ranks 1 … GR_MAX_RANK (GR_E_RANK above). Asynchronous on
+ * `stream`. Errors: as the other calls. */
 #define GR_MAX_WRITERS 65536
 int gr_decompose(const gr_shape* shape, const void* R, const float* gamma, const float* w_down,
                  const float* w_up, const float* w_write, int32_t n_writers, const void* y,
