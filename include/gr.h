@@ -130,7 +130,8 @@ int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void*
 /* ---- the pages' own rank, r = d/8 (large-rank path) ------------------------------------------
  * "【论文解读】 Qwen3.8 Flash Next", §二.4 sets W_d ∈ R^{r × n_r·d} with r = d/8 (320 at d = 2560).
  * bf16 states with d_model a multiple of 64 and a rank r with 64 <= r <= GR_MAX_RANK_TC,
- * r % 8 == 0, run on the tcgen05 tensor cores ("tc_bf16" in gr_kernel_path): three launches
+ * r % 8 == 0 (and at most 2^31 - 2^16 tokens a call), run on the tcgen05 tensor cores
+ * ("tc_bf16" in gr_kernel_path): three launches
  * (the write and each row's 1/rms; the down projection as a GEMM of the rms-scaled state with the
  * packed [W_d; W_w]; the up projection as a GEMM with the gate and combine in its epilogue). Its
  * numerics: the down projection's inputs are bf16(R'·inv_i) and the packed bf16 weights, h is

@@ -130,7 +130,9 @@ bool use_fused(const gr_shape* s) {
            s->n_tokens <= fused_max_tokens();
 }
 
-// The large-rank tensor-core path (gr_rank_tc.cu) takes precedence over the generic kernel.
+// The large-rank tensor-core path (gr_rank_tc.cu) takes precedence over the generic kernel. Its
+// TMA coordinates are 32-bit: tokens up to kRankTcMaxTokens.
+constexpr int64_t kRankTcMaxTokens = 0x7fff0000;
 bool use_rank_tc(const gr_shape* s) {
     return s->state_dtype == GR_BF16 && rank_tc_supported(s->d_model, s->rank);
 }
@@ -146,6 +148,7 @@ int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
     if (s->n_tokens == 0) return GR_OK;
     cudaError_t e;
     if (use_rank_tc(s)) {
+        if (s->n_tokens > kRankTcMaxTokens) return GR_E_SHAPE;   // 32-bit TMA token coordinate
         if (!ws || ws_bytes < rank_tc_workspace(s->n_tokens, s->rank)) return GR_E_SIZE;
         return status_of(launch_rank_tc(s->n_tokens, s->d_model, s->rank, s->eps, R, y, s_prev,
                                          p->packed, x, s_out, ws, st));

@@ -1,0 +1,57 @@
+"""The bench's accounting on the CPU: the algorithmic bytes and flops it divides by, and the
+committed ncu summaries it takes `traffic` from (each must still describe the current kernel
+sources, else the bench would report a stale figure)."""
+import glob
+import os
+import re
+
+import pytest
+
+import bench
+from stream_gated_residual_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bytes_per_token_of_the_workloads():
+    # bf16 prefill: R in and out (4·D·2 each), y in and x out (D·2 each), s in and out (4·4 each)
+    assert bench.bytes_per_token(wl.WORKLOADS["prefill"]) == 2 * 4 * 4096 * 2 + 2 * 4096 * 2 + 32
+    # FP8 state: codes and block exponents in and out, y and x bf16
+    D = 4096
+    assert bench.bytes_per_token(wl.WORKLOADS["prefill_fp8"]) == \
+        2 * (4 * D + 4 * D // 32) + 2 * D * 2 + 32
+    assert bench.bytes_per_token(wl.WORKLOADS["tiny_fp32"]) == 2 * 4 * 256 * 4 + 2 * 256 * 4 + 32
+
+
+def test_flops_of_the_large_rank_and_backward_legs():
+    w = wl.WORKLOADS["paper_rank"]
+    K = 4 * w.d_model
+    assert bench.tc_flops_per_token(w) == 2 * (w.rank + 4) * K + 2 * K * w.rank
+    p = wl.WORKLOADS["prefill"]
+    Kp, r = 4 * p.d_model, p.rank
+    assert bench.backward_flops_per_token(p) == 2 * Kp * (6 * r + 13) + 16 * Kp
+
+
+def test_decomposition_bytes_count_every_pair():
+    w = wl.WORKLOADS["deep_stack"]
+    two = bench.decompose_bytes(w, 2)   # one reader with one writer
+    es, D, N, r = 2, w.d_model, w.n_tokens, w.rank
+    assert two == N * (2 * 4 * D * es + (D * es + 16) + 4 * 6 + 4) + \
+        4 * (4 * D + 2 * r * 4 * D + 4 * 4 * D)
+    assert bench.decompose_bytes(w, 40) > 39 * two   # the writers' share grows with the reader
+
+
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(ROOT, "profiles", "*__*.md"))))
+def test_committed_profiles_match_the_sources(path):
+    """A summary that carries a source hash and a DRAM figure is the one the bench reads for its
+    kernel path and workload; the hash must be that of the current sources."""
+    text = open(path).read()
+    m_s = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
+    m_b = re.search(r"^dram_bytes_per_launch:\s*(\d+)", text, re.M)
+    if not (m_s and m_b):
+        pytest.skip("launch list only (no traffic figure)")
+    kernel_path, workload = os.path.basename(path)[:-3].split("__")
+    assert workload in wl.WORKLOADS
+    assert m_s.group(1) == bench.kernel_source_sha(kernel_path), \
+        f"{os.path.basename(path)} describes sources that have changed since"
+    assert bench.profiled_traffic(kernel_path, workload) == int(m_b.group(1))
