@@ -114,7 +114,7 @@ def kernel_source_sha(kernel_path: str) -> str:
     from stream_gated_residual_gb300 import build as gbuild
     files = {"fused_bf16": "gr_fused_bf16.cu", "tiled_bf16": "gr_tiled_bf16.cu",
              "tiled_fp8": "gr_tiled_bf16.cu", "generic": "gr_generic.cu",
-             "tc_bf16": "gr_rank_tc.cu"}
+             "tc_bf16": "gr_rank_tc.cu", "decompose": "gr_decompose.cu"}
     names = [files[k] for k in kernel_path.split("+")]
     if kernel_path == "tc_bf16":
         names.append("gr_tc.cuh")
@@ -774,7 +774,9 @@ def run_decompose(args, w) -> None:
                                          "MiB), no flush",
                        "pass": "decomposition (gr_decompose per reader)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": None if args.n_tokens is not None or L != 40
+                         else profiled_traffic("decompose", w.name),
                          "peak_source": peaks["source"], "algorithmic_bytes_per_step": alg},
             "gpu_launches": (L - 1) * args.steps,
             "clocks": clocks,
