@@ -26,7 +26,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
+// σ(a) = 1/(1 + e^-a) with the fast exponential and division: a few ulp, far inside the fp32
+// bounds of these paths; 0 and 1 at the ends (1/inf = 0).
+__device__ __forceinline__ float sigm(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
 // Sums of the first m of M per-thread values over the block; the totals land in out[0..m).
 template <int M>

@@ -29,7 +29,9 @@ namespace {
 constexpr int kGroup = 6;            // writers per group: 5 sums each, 30 of a warp's 32 lanes
 constexpr int kSums = 5;             // Σ A², then Σ (coef_i y)² for the four branches
 
-__device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
+// σ(a) = 1/(1 + e^-a) with the fast exponential and division: a few ulp, far inside the fp32
+// bounds of these paths; 0 and 1 at the ends (1/inf = 0).
+__device__ __forceinline__ float sigm(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
 // 256 threads; two CTAs per SM below rank 64 (each thread then has 128 registers), so that one
 // CTA's gate recompute overlaps the other's writer pass.
