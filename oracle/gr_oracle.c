@@ -14,8 +14,9 @@
  *     eq write    R'_i = R_i + s_i y
  *   "Qwen3.8-Flash-Next 架构笔记 · 06 / RESIDUAL" (cbphcr.github.io), §2 and §3 (same
  *   formulas at n_r = 4).
- * Readings where the pages leave a point open (eps placement, multiplicative gain,
- * branch-major vec) are listed in the repository's SPEC file; eps is a parameter here.
+ * Where the pages leave a point open this file reads it as follows: eps inside the square
+ * root (1/sqrt(mean + eps)), a multiplicative gain γ, vec stacking the branches branch-major
+ * (index i·D + c); eps is a parameter here.
  *
  * Layouts, all row-major:
  *   R, R_out  [n][nb][D]      token, branch, channel
@@ -506,7 +507,7 @@ int gro_round_significand(int64_t n, int bits, double *v)
 
 /* ---- FP8 state (OCP e4m3 "e4m3fn" codes, one power-of-two scale per 32-channel block) ----
  * The pages name FP8 storage of the widened state ("【论文解读】 Qwen3.8 Flash Next", §二.7)
- * without a format; the repository's SPEC file, section "FP8 state", fixes the one used here.
+ * without a format; this file fixes the one used here, as follows.
  * An e4m3 code is sign | 4 exponent bits (bias 7) | 3 fraction bits; exponent field 0 holds
  * the subnormals m/8 · 2^-6; 0x7F and 0xFF are NaN; there are no infinities. */
 

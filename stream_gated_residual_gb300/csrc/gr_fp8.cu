@@ -1,7 +1,7 @@
 // FP8 branch state: encoding, decoding and the streaming write.
 //
 // The pages name FP8 storage of the widened state ("【论文解读】 Qwen3.8 Flash Next", §二.7) and
-// leave the format open. The library's format (its SPEC's FP8 section): e4m3 codes [N][4][D]
+// leave the format open. The library's format: e4m3 codes [N][4][D]
 // and one biased power-of-two exponent per 32 consecutive channels of a (token, branch) row,
 // scales [N][4][D/32], scale 2^(b - 127); a block's exponent is the smallest e with
 // max|v| <= 448·2^e, and codes are v/2^e rounded to the nearest e4m3 value, ties to even.

@@ -294,7 +294,7 @@ def pin_residual_add():
     assert np.array_equal(oracle.residual_add(a, b), a + b)
 
 
-# ---- backward (NEXT-3) --------------------------------------------------------------------------
+# ---- backward -----------------------------------------------------------------------------------
 
 def _fd_grad(f, A, h=1e-6):
     """Central finite differences of the scalar f() with respect to every entry of A."""
@@ -370,7 +370,7 @@ def pin_write_backward():
     assert _rel(_fd_grad(L, y), dy) < 1e-8 and _rel(_fd_grad(L, s), dsv) < 1e-8
 
 
-# ---- FP8 state (SPEC R21: e4m3 codes, one power-of-two scale per 32-channel block) ----------
+# ---- FP8 state (e4m3 codes, one power-of-two scale per 32-channel block) --------------------
 
 def _torch_e4m3_values():
     """Value of every e4m3 code by torch's float8_e4m3fn (a library conversion)."""
@@ -455,7 +455,7 @@ def pin_fp8_blocks_independent():
 
 def pin_fp8_write_then_read_error():
     """The FP8 fused step against the plain definition (fp64, no storage rounding) stays within
-    SPEC R22's bounds: R' within 2^-4, x and s within 2^-3 (per-row relative L2)."""
+    the FP8 bounds: R' within 2^-4, x and s within 2^-3 (per-row relative L2)."""
     rng = np.random.default_rng(151)
     n, nb, D, r = 16, 4, 128, 8
     R0 = rng.standard_normal((n, nb, D)).astype(np.float32)

@@ -1,4 +1,4 @@
-"""GPU parity of the backward (NEXT-3; SPEC R23/R24): gr_read_backward and gr_write_backward
+"""GPU parity of the backward : gr_read_backward and gr_write_backward
 through the C ABI against the fp64 oracle's chain-rule gradients (pinned by finite differences
 and by torch autograd), on the same stored inputs. Per-row relative L2 ≤ 1e-4; rows of a
 parameter gradient whose norm is below 1e-3 of the tensor's largest row are compared against

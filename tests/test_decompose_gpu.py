@@ -1,4 +1,4 @@
-"""GPU parity of the contribution decomposition (eq auv and π, Digest §二.6; SPEC R25/R26):
+"""GPU parity of the contribution decomposition (eq auv and π, Digest §二.6):
 gr_decompose through the C ABI against the fp64 oracle on the same stored inputs. Every norm,
 per-branch norm, π and the initial state's share within 1e-4 relative, with an absolute floor of
 1e-4 times the token's largest writer norm for terms far below it."""

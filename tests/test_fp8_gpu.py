@@ -1,11 +1,11 @@
-"""GPU parity of the FP8 branch state (e4m3 codes, one power-of-two exponent per 32-channel block;
-the library's SPEC R21) against the fp64 oracle, through the C ABI.
+"""GPU parity of the FP8 branch state (e4m3 codes, one power-of-two exponent per 32-channel block)
+against the fp64 oracle, through the C ABI.
 
 Codes and block exponents are integer results: they must match the oracle bit for bit
 (encode, write, fused write→read). x and s are compared per row with the storage-modelled oracle
 (the same stored FP8 state, the weights the two-pass kernel computes with) within the bf16
-path's bounds, and with the plain fp64 definition (no storage rounding at all) within R22's
-FP8 bounds."""
+path's bounds, and with the plain fp64 definition (no storage rounding at all) within the FP8
+bounds (R' 2^-4, x and s 2^-3)."""
 from __future__ import annotations
 
 import numpy as np
@@ -20,7 +20,7 @@ from stream_gated_residual_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-# SPEC R22: against the plain definition (R' at most one e4m3 rounding; x and s see it twice)
+# Against the plain definition (R' at most one e4m3 rounding; x and s see it twice)
 PLAIN_TOL_FP8 = {"R": 2.0 ** -4, "x": 2.0 ** -3, "s": 2.0 ** -3}
 
 
@@ -147,7 +147,7 @@ def test_read_only(D, r, N):
 
 @pytest.mark.parametrize("D,r,N", [(4096, 16, 200), (7168, 32, 200)])
 def test_plain_error_at_workload_weights(D, r, N):
-    """At the workloads' weight scale (N(0, 0.02), unit gains) x and s also stay within R22's
+    """At the workloads' weight scale (N(0, 0.02), unit gains) x and s also stay within the FP8
     bounds against the plain definition."""
     _fused_case(N, D, r, weight_mult=1.0, random_gamma=False)
 

@@ -1,10 +1,10 @@
 """GPU parity of the large-rank path (the pages' r = d/8; tcgen05 tensor cores) through the C
 ABI against the fp64 oracle. R' (the write) must match the storage-modelled oracle to the last
 bit; x and s are compared per row with the oracle run on the stored state and the path's bf16
-weights (SPEC R27: h is rounded to bf16 for the up projection and the tensor cores' fp32
+weights (h is rounded to bf16 for the up projection and the tensor cores' fp32
 accumulation over 4·D terms loses bits as D grows, which the oracle does not model: x within
 4e-3 as on the other bf16 paths, s within 5e-4), and, at the workloads' weight scale, with the
-plain fp64 definition within the bf16 bound (R17)."""
+plain fp64 definition within the bf16 bound."""
 from __future__ import annotations
 
 import numpy as np
