@@ -239,10 +239,16 @@ def cpu_baseline(w, target_s: float = 12.0) -> dict:
     probe = 64
     t = OracleInputs(w, probe).run(0, probe)
     n = int(max(probe, min(w.n_tokens, target_s * probe / max(t, 1e-9))))
-    t = OracleInputs(w, n).run(0, n)
-    return {"value": n / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    inp = OracleInputs(w, n)
+    t = inp.run(0, n)
+    # a workload the oracle finishes well inside the target is repeated, for a stable figure
+    reps = 1
+    while t < 0.8 * target_s and reps < 1000:
+        t += inp.run(0, n)
+        reps += 1
+    return {"value": reps * n / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"first {n} of {w.n_tokens} tokens of the {w.name} workload, one fused "
-                      f"write->read in fp64 ({t:.1f} s)"}
+                      f"write->read in fp64, {reps} time(s) ({t:.1f} s)"}
 
 
 def run_reference(args, w) -> None:
