@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import platform
 import json
 import os
 import re
@@ -246,9 +247,24 @@ def cpu_baseline(w, target_s: float = 12.0) -> dict:
     while t < 0.8 * target_s and reps < 1000:
         t += inp.run(0, n)
         reps += 1
-    return {"value": reps * n / t, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    # the same oracle on one core, on a sample sized for about 3 s
+    oracle.set_num_threads(1)
+    try:
+        t1 = OracleInputs(w, probe).run(0, probe)
+        n1 = int(max(1, min(n, 3.0 * probe / max(t1, 1e-9))))
+        t1, reps1 = inp.run(0, n1), 1
+        while t1 < 2.0 and reps1 < 1000:
+            t1 += inp.run(0, n1)
+            reps1 += 1
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": reps * n / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {n} of {w.n_tokens} tokens of the {w.name} workload, one fused "
-                      f"write->read in fp64, {reps} time(s) ({t:.1f} s)"}
+                      f"write->read in fp64, {reps} time(s) ({t:.1f} s)",
+            "host": f"{os.cpu_count()} logical CPUs, {platform.machine()}",
+            "single_core": {"value": reps1 * n1 / t1, "unit": UNIT, "cores": 1,
+                            "sample": f"first {n1} tokens, {reps1} time(s) ({t1:.1f} s)"}}
 
 
 def run_reference(args, w) -> None:
