@@ -142,9 +142,11 @@ bool use_tiled(const gr_shape* s) {
            tiled_supported(s->d_model, s->rank) && s->n_tokens <= tiled_max_tokens();
 }
 
+// allow_split = false keeps a cluster-kernel step on the cluster kernel alone: the concurrent
+// split needs the internal stream and events that gr_split.cu creates on first use.
 int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
              const gr_params* p, void* x, float* s_out, cudaStream_t st,
-             void* ws = nullptr, size_t ws_bytes = 0) {
+             void* ws = nullptr, size_t ws_bytes = 0, bool allow_split = true) {
     if (s->n_tokens == 0) return GR_OK;
     cudaError_t e;
     if (use_rank_tc(s)) {
@@ -155,8 +157,9 @@ int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
     }
     int free_sms = 0;
     const int64_t n2 =
-        use_fused(s) ? split_tokens(s->n_tokens, s->d_model, s->rank, y != nullptr, &free_sms)
-                     : 0;
+        use_fused(s) && allow_split
+            ? split_tokens(s->n_tokens, s->d_model, s->rank, y != nullptr, &free_sms)
+            : 0;
     if (n2 > 0)
         return status_of(launch_split_bf16(s->n_tokens, n2, free_sms, s->d_model, s->rank,
                                            s->eps, R, y, s_prev, p->packed, x, s_out, st));
@@ -796,7 +799,8 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
         cudaMemcpyAsync(dy, y_host, ny, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
         cudaMemcpyAsync(dsp, s_prev_host, ns, cudaMemcpyHostToDevice, cs) != cudaSuccess)
         return GR_E_CUDA;
-    st = run_step(shape, dR, dy, dsp, next, dx, dsn, cs);
+    // no concurrent split here: its internal stream and events would be created on first use
+    st = run_step(shape, dR, dy, dsp, next, dx, dsn, cs, nullptr, 0, false);
     if (st) return st;
     if (cudaMemcpyAsync(R_host, dR, nR, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
         cudaMemcpyAsync(x_host, dx, ny, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||

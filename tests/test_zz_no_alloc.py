@@ -1,6 +1,9 @@
 """gr_write_then_read_host_static (the host-buffer step staged through the library's fixed device
 workspace) against gr_write_then_read_host (caller-provided workspace): two fused steps in a
-row, each fed with the previous step's R' and s, give bit-identical results. The file is
+row, each fed with the previous step's R' and s, give bit-identical results. On a shape that
+gr_write_then_read_host splits between the cluster kernel and the two-pass kernel, the static
+entry runs the cluster kernel alone (the split's internal stream and events would be created on
+first use): R' is still bit-identical, x and s agree within the bf16 tolerance. The file is
 collected last on purpose, so the static entry also runs after every other test has used the
 library in the same process."""
 import ctypes
@@ -9,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from gr_testlib import params_to_torch, to_torch
+from gr_testlib import TOL, params_to_torch, rel_rows, to_torch
 from stream_gated_residual_gb300 import build as gbuild
 from stream_gated_residual_gb300 import gr
 from stream_gated_residual_gb300 import workloads as wl
@@ -36,10 +39,7 @@ def _two_steps(entry, w, R0, y0, y1, s0, P):
     return outs
 
 
-@pytest.mark.gpu
-@pytest.mark.parametrize("N,D,r,dtype", [(128, 4096, 16, "bf16"), (64, 256, 8, "f32"),
-                                         (333, 1024, 12, "bf16")])
-def test_static_workspace_entry_matches_workspace_entry(N, D, r, dtype):
+def _compare(N, D, r, dtype):
     w = wl.Workload("noalloc", N, D, r, dtype, y_std=0.5, seed=23)
     R0, s0 = wl.make_state(w), wl.make_s_prev(w)
     y0, y1 = wl.make_y(w, 0), wl.make_y(w, 1)
@@ -55,11 +55,38 @@ def test_static_workspace_entry_matches_workspace_entry(N, D, r, dtype):
     def static(R, y, s, P, x, sn):
         gr.write_then_read_host_static(R, y, s, P, x, sn)
 
+    split = gr.kernel_path(N, D, r, TDT[dtype]) == "fused_bf16+tiled_bf16"
     ref = _two_steps(with_workspace, w, R0, y0, y1, s0, P)
     got = _two_steps(static, w, R0, y0, y1, s0, P)
-    for (Ra, xa, sa), (Rb, xb, sb) in zip(ref, got):
-        assert torch.equal(Ra, Rb) and torch.equal(xa, xb) and torch.equal(sa, sb)
+    for i, ((Ra, xa, sa), (Rb, xb, sb)) in enumerate(zip(ref, got)):
+        if split and i > 0:
+            # the second write uses each entry's own s from the first step
+            assert rel_rows(Rb.float().numpy(), Ra.float().numpy()) <= TOL[dtype]
+        else:
+            assert torch.equal(Ra, Rb)
+        if split:
+            assert rel_rows(xb.float().numpy(), xa.float().numpy()) <= TOL[dtype]
+            assert rel_rows(sb.numpy(), sa.numpy()) <= TOL[dtype]
+        else:
+            assert torch.equal(xa, xb) and torch.equal(sa, sb)
     assert gr.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,D,r,dtype", [(128, 4096, 16, "bf16"), (64, 256, 8, "f32"),
+                                         (333, 1024, 12, "bf16")])
+def test_static_workspace_entry_matches_workspace_entry(N, D, r, dtype):
+    _compare(N, D, r, dtype)
+
+
+@pytest.mark.gpu
+def test_static_workspace_entry_past_the_split_threshold():
+    """1500 tokens at D = 1024 (18.5 MB of workspace) is past the split's token threshold at that
+    width. On a GB300 the clusters of 4 CTAs fill every SM there, so neither entry splits and
+    the results are bit-identical; on a device whose clusters leave SMs idle the host entry
+    splits, the static entry runs the cluster kernel alone, and x and s agree within the bf16
+    tolerance."""
+    _compare(1500, 1024, 16, "bf16")
 
 
 def test_static_workspace_entry_rejects_oversize_before_any_cuda_call():
