@@ -81,11 +81,11 @@ def test_static_workspace_entry_matches_workspace_entry(N, D, r, dtype):
 
 @pytest.mark.gpu
 def test_static_workspace_entry_past_the_split_threshold():
-    """1500 tokens at D = 1024 (18.5 MB of workspace) is past the split's token threshold at that
-    width. On a GB300 the clusters of 4 CTAs fill every SM there, so neither entry splits and
-    the results are bit-identical; on a device whose clusters leave SMs idle the host entry
-    splits, the static entry runs the cluster kernel alone, and x and s agree within the bf16
-    tolerance."""
+    """1500 tokens at D = 1024 (18.5 MB of workspace), past the split's first token bound at that
+    width (800). On a GB300 the split's time model keeps this shape, like every cluster-kernel
+    shape that fits the 32 MiB workspace, on the cluster kernel alone, so the results are
+    bit-identical; where the host entry does split, the static entry still runs the cluster
+    kernel alone, and x and s agree within the bf16 tolerance."""
     _compare(1500, 1024, 16, "bf16")
 
 
