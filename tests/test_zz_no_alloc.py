@@ -108,3 +108,32 @@ def test_static_workspace_entry_rejects_oversize_before_any_cuda_call():
     shape.n_tokens = 682
     assert L.gr_host_workspace_size(ctypes.byref(shape), ctypes.byref(need)) == 0
     assert need.value <= (32 << 20)
+
+
+def test_static_workspace_entry_validates_on_the_host():
+    """Missing pointers, overlapping host buffers and the large-rank shapes (device entries only)
+    are rejected before any CUDA call; an empty batch returns at once (no GPU needed)."""
+    gbuild.build()
+    L = gr.load()
+    shape = gr.Shape(64, 1024, 4, 16, gr.GR_BF16, 1e-6)
+    p = gr.ParamsStruct()
+    p.tag, p.packed = gr.GR_PARAMS_TAG, 0x1000
+    p.d_model, p.n_branch, p.rank, p.state_dtype = 1024, 4, 16, gr.GR_BF16
+    fake = [ctypes.c_void_p(0x1000000 * (i + 1)) for i in range(5)]
+
+    def call(sh, ptrs):
+        return L.gr_write_then_read_host_static(ctypes.byref(sh), ptrs[0], ptrs[1], ptrs[2],
+                                                ctypes.byref(p), ptrs[3], ptrs[4], None)
+
+    assert call(shape, [fake[0], None, fake[2], fake[3], fake[4]]) == -1       # GR_E_NULL
+    assert call(shape, [fake[0], fake[1], fake[2], fake[0], fake[4]]) == -8    # GR_E_ALIAS: x on R
+    assert call(shape, [fake[0], fake[1], fake[2], fake[1], fake[4]]) == -8    # x on y
+    assert call(shape, [fake[0], fake[1], fake[2], fake[3], fake[2]]) == -8    # s_next on s_prev
+    p.rank = 8
+    assert call(shape, fake) == -6                                             # GR_E_PARAMS
+    tc = gr.Shape(64, 2560, 4, 320, gr.GR_BF16, 1e-6)
+    p.d_model, p.rank = 2560, 320
+    assert call(tc, fake) == -5                                                # GR_E_RANK
+    empty = gr.Shape(0, 1024, 4, 16, gr.GR_BF16, 1e-6)
+    p.d_model, p.rank = 1024, 16
+    assert call(empty, [None] * 5) == 0
