@@ -218,9 +218,16 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
 
 /* gr_write_then_read_host without a caller-provided workspace: the same step on HOST buffers,
  * staged through a fixed device workspace of GR_STATIC_WORKSPACE_BYTES that the library holds
- * in a file-scope device array. The pages have no counterpart; it is a convenience form of
- * gr_write_then_read_host for small batches (decode) that allocates nothing: no cudaMalloc,
- * cudaFree, stream or event creation.
+ * in a file-scope device array. The pages have no counterpart. It serves callers that cannot
+ * allocate device memory themselves:
+ *   - a plain host program with no device allocator of its own (only host arrays to pass);
+ *   - a process whose device memory is already reserved by another allocator (a framework's
+ *     caching allocator, a serving engine's preallocated pool), where an extra cudaMalloc can
+ *     fail or fragment the pool;
+ *   - a latency-bound loop (decode), where cudaFree would synchronise the whole device.
+ * It calls no cudaMalloc or cudaFree and creates no stream or event; its device memory is
+ * fixed when the library is loaded and held by every device that loads it until the process
+ * exits.
  *   - Returns GR_E_SIZE, without touching anything, when gr_host_workspace_size(shape) exceeds
  *     GR_STATIC_WORKSPACE_BYTES (for example N > 682 tokens at D = 4096, bf16).
  *   - The first call on a device looks the workspace's device address up once

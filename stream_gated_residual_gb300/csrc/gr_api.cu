@@ -747,9 +747,12 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
 namespace gr {
 namespace {
 
-// The device workspace of gr_write_then_read_host_static: file scope, module lifetime, the same
-// layout gr_write_then_read_host uses in its caller-provided workspace. Nothing in it has to
-// start at zero: every byte a call reads was written earlier in the same call.
+// The device workspace of gr_write_then_read_host_static, the host-buffer step for callers that
+// cannot allocate device memory (a host program with no device allocator, a process whose
+// memory a pool already holds, a decode loop that cannot take cudaFree's device-wide
+// synchronisation): file scope, module lifetime, the same layout gr_write_then_read_host uses in
+// its caller-provided workspace. Nothing in it has to start at zero: every byte a call reads was
+// written earlier in the same call. Calls that overlap in time race on it.
 static __device__ __align__(256) unsigned char g_static_ws[GR_STATIC_WORKSPACE_BYTES];
 void* g_static_ws_addr[kMaxDevices];  // device address, looked up once per device
 std::mutex g_static_mu;

@@ -335,7 +335,11 @@ def write_then_read_host_static(R: torch.Tensor, y: torch.Tensor, s_prev: torch.
                                 params: Params, x: torch.Tensor, s_next: torch.Tensor,
                                 stream=None):
     """gr_write_then_read_host_static on CPU tensors (pinned for asynchronous copies), staged
-    through the library's fixed device workspace (GR_STATIC_WORKSPACE_BYTES)."""
+    through the library's fixed 32 MiB device workspace (GR_STATIC_WORKSPACE_BYTES), for callers
+    that cannot allocate device memory: a host program without a device allocator, a process
+    whose device memory a pool already holds, or a decode loop that cannot afford the device-wide
+    synchronisation of cudaFree. Nothing is allocated; shapes that need more than the workspace
+    raise GR_E_SIZE, and calls must not overlap in time (they share the workspace)."""
     for t, n in ((R, "R"), (y, "y"), (s_prev, "s_prev"), (x, "x"), (s_next, "s_next")):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous CPU tensor")

@@ -1,5 +1,8 @@
 """gr_write_then_read_host_static (the host-buffer step staged through the library's fixed device
-workspace) against gr_write_then_read_host (caller-provided workspace): two fused steps in a
+workspace, for callers that cannot allocate device memory: a host program with no device
+allocator, a process whose memory a pool already holds, a decode loop that cannot take
+cudaFree's device-wide synchronisation) against gr_write_then_read_host (caller-provided
+workspace): two fused steps in a
 row, each fed with the previous step's R' and s, give bit-identical results. On a shape that
 gr_write_then_read_host splits between the cluster kernel and the two-pass kernel, the static
 entry runs the cluster kernel alone (the split's internal stream and events would be created on
