@@ -1,6 +1,6 @@
-"""The bench's accounting on the CPU: the algorithmic bytes and flops it divides by, and the
+"""The bench's accounting on the CPU: the algorithmic bytes and flops it divides by, the
 committed ncu summaries it takes `traffic` from (each must still describe the current kernel
-sources, else the bench would report a stale figure)."""
+sources, else the bench would report a stale figure), and the reference arm's JSON line."""
 import glob
 import os
 import re
@@ -55,3 +55,28 @@ def test_committed_profiles_match_the_sources(path):
     assert m_s.group(1) == bench.kernel_source_sha(kernel_path), \
         f"{os.path.basename(path)} describes sources that have changed since"
     assert bench.profiled_traffic(kernel_path, workload) == int(m_b.group(1))
+
+
+@pytest.mark.parametrize("workload,extra", [("tiny_fp32", []), ("prefill", ["--n-tokens", "48"])])
+def test_reference_arm_prints_one_json_line(workload, extra):
+    """`bench.py --impl reference` times the fp64 oracle on the host cores (no GPU) and prints
+    one JSON line with the arm's keys: the same metric and unit as the CUDA arm, the oracle's
+    core count and sample, and an end-to-end figure that moves no bytes to or from a device."""
+    import json
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", workload, "--steps", "2", "--warmup", "1", *extra],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["metric"] == bench.METRIC
+    assert rec["unit"] == bench.UNIT and rec["value"] > 0 and rec["higher_is_better"] is True
+    assert rec["steps"] == 2 and rec["warmup"] == 1 and rec["dtype"] == "f64"
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == rec["value"]
+    e2e = rec["e2e"]
+    assert e2e["value"] == rec["value"] and e2e["unit"] == rec["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
