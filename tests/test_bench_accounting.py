@@ -80,3 +80,17 @@ def test_reference_arm_prints_one_json_line(workload, extra):
     e2e = rec["e2e"]
     assert e2e["value"] == rec["value"] and e2e["unit"] == rec["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    """The CUDA arm's `cpu_baseline`: the oracle on all host cores, repeated until its sample
+    covers the target time, and on one core; the thread count is restored afterwards."""
+    import oracle
+    oracle.build()
+    before = oracle.num_threads()
+    cb = bench.cpu_baseline(wl.WORKLOADS["tiny_fp32"], target_s=0.5)
+    assert oracle.num_threads() == before
+    assert cb["kind"] == "oracle" and cb["unit"] == bench.UNIT and cb["value"] > 0
+    assert cb["cores"] == before and "time(s)" in cb["sample"]
+    sc = cb["single_core"]
+    assert sc["cores"] == 1 and sc["value"] > 0 and sc["unit"] == bench.UNIT
