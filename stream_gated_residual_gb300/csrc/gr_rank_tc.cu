@@ -40,8 +40,6 @@ constexpr int kGemmThreads = 192;   // down projection: producer, MMA, 4 scaling
 constexpr int kUpThreads = 352;     // up projection: producer, MMA, 8 epilogue warps, R' loader
 constexpr int kUpEpiWarps = 8;      // two per tensor-memory lane quadrant, 16 channels each
 constexpr int kCb = 32;             // channels per branch in an up-projection block
-constexpr int kPair = 2;            // CTAs of a cluster sharing each weight stage (TMA multicast)
-constexpr uint16_t kPairMask = 0x3;
 constexpr int kMaxRankTc = 448;     // r + 4 <= 512 accumulator columns; H fits shared memory
 
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + __expf(-a)); }
@@ -121,13 +119,12 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     const int64_t t0 = int64_t(blockIdx.x) * kTile;
     const int nk = kBranches * D / kKc, cpb = D / kKc;
     const uint32_t ncols = n1 > 256 ? 512 : 256;
-    const uint32_t crank = cluster_ctarank();   // 0 or 1: which half of each weight stage it loads
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&scaled[s], 4);
-            mbar_init(&empty[s], kPair);   // both CTAs' MMAs are done with the stage
+            mbar_init(&empty[s], 1);   // the MMAs are done with the stage
         }
         mbar_init(acc_full, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -138,7 +135,6 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();   // the pair's barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
@@ -150,12 +146,11 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
                 if (kc >= stages && !mbar_wait(&empty[s], ((kc / stages) - 1) & 1)) break;
                 uint8_t* A = sm + s * sb;
                 uint8_t* B = A + 2 * kStageA;
-                const int half = n1 / kPair;
+                const int half = n1 / 2;   // a box holds at most 256 rows: two boxes
                 mbar_expect_tx(&full[s], bytes);
                 tma_load_3d(A, &tmR, (kc % cpb) * kKc, kc / cpb, int(t0), &full[s]);
-                // this CTA's half of the weight rows, delivered to both CTAs of the pair
-                tma_load_2d_mc(B + crank * half * 128, &tmW, kc * kKc, int(crank) * half,
-                               &full[s], kPairMask);
+                tma_load_2d(B, &tmW, kc * kKc, 0, &full[s]);
+                tma_load_2d(B + half * 128, &tmW, kc * kKc, half, &full[s]);
             }
         }
     } else if (warp == 1) {
@@ -185,7 +180,7 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
                         tc_mma(tmem + 256, al, b1, id1, 1u);
                     }
                 }
-                tc_commit_mc(&empty[s], kPairMask);
+                tc_commit(&empty[s]);
             }
             if (ok) tc_commit(acc_full);
         }
@@ -263,7 +258,6 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();   // neither CTA leaves while the other may still signal its barriers
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
@@ -306,13 +300,12 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = int64_t(blockIdx.x) * kTile;
     const int nb = D / kCb;
-    const uint32_t crank = cluster_ctarank();   // 0 or 1: which two branches of a B stage it loads
 
     if (threadIdx.x == 0) {
         mbar_init(h_full, 1);
         for (int s = 0; s < kUpMaxStages; ++s) {
             mbar_init(&b_full[s], 1);
-            mbar_init(&b_empty[s], kPair);
+            mbar_init(&b_empty[s], 1);
         }
         for (int b = 0; b < kUpMaxR; ++b) {
             mbar_init(&r_full[b], 1);
@@ -330,7 +323,6 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();   // the pair's barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
@@ -349,10 +341,9 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
                         break;
                     }
                     mbar_expect_tx(&b_full[s], kStageB);
-                    // branches 2·crank, 2·crank + 1, delivered to both CTAs of the pair
-                    for (int i = 2 * int(crank); i < 2 * int(crank) + 2; ++i)
-                        tma_load_2d_mc(Bs + s * kStageB + i * (kCb * 128), &tmU, kc * kKc,
-                                       i * D + cb * kCb, &b_full[s], kPairMask);
+                    for (int i = 0; i < kBranches; ++i)
+                        tma_load_2d(Bs + s * kStageB + i * (kCb * 128), &tmU, kc * kKc,
+                                    i * D + cb * kCb, &b_full[s]);
                 }
                 if (!ok) break;
             }
@@ -390,7 +381,7 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma(tmem + buf * (kBranches * kCb), sdesc_sw128(a + kk * 32),
                                sdesc_sw128(b + kk * 32), id, (kc | kk) != 0);
-                    tc_commit_mc(&b_empty[s], kPairMask);
+                    tc_commit(&b_empty[s]);
                 }
                 if (ok) tc_commit(&t_full[buf]);
             }
@@ -465,7 +456,6 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -502,22 +492,15 @@ bool map_state(CUtensorMap* m, const void* R, int64_t N, int D, uint32_t box_ch,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Launch as clusters of kPair CTAs along x.
+// Plain launch (no cluster): every CTA loads its own operands.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pairs(void (*kern)(KArgs...), unsigned grid, int threads, size_t smem,
+cudaError_t launch_plain(void (*kern)(KArgs...), unsigned grid, int threads, size_t smem,
                          cudaStream_t st, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kPair;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
@@ -560,14 +543,12 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // a whole number of CTA pairs (a pair's second tile may lie past N: TMA fills it with zeros
-    // and its rows are not written)
-    const unsigned tiles = unsigned((N + kTile - 1) / kTile + kPair - 1) / kPair * kPair;
+    const unsigned tiles = unsigned((N + kTile - 1) / kTile);
     // 2. down projection
     {
         CUtensorMap mR, mW;
         if (!map_state(&mR, R, N, D, kKc, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !map_2d(&mW, wdw, K, r + kBranches, size_t(K) * 2, kKc, n1 / kPair,
+            !map_2d(&mW, wdw, K, r + kBranches, size_t(K) * 2, kKc, n1 / 2,
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const size_t sb = down_stage_bytes(n1);
@@ -579,7 +560,7 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        e = launch_pairs(down_tc_kernel, tiles, kGemmThreads, smem, st, mR, mW, N, D, r, n1,
+        e = launch_plain(down_tc_kernel, tiles, kGemmThreads, smem, st, mR, mW, N, D, r, n1,
                          stages, static_cast<const float*>(inv), h, rp, s_out);
         if (e != cudaSuccess) return e;
     }
@@ -601,7 +582,7 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        e = launch_pairs(up_tc_kernel, tiles, kUpThreads, smem, st, mH, mU, mR2, N, D, rp, nbs,
+        e = launch_plain(up_tc_kernel, tiles, kUpThreads, smem, st, mH, mU, mR2, N, D, rp, nbs,
                          nrb, gamma, static_cast<const float*>(inv), static_cast<__nv_bfloat16*>(x));
         if (e != cudaSuccess) return e;
     }
