@@ -89,6 +89,34 @@ def workload_desc(w) -> str:
             f"r={w.rank}, {w.dtype} states, fp32 accumulation")
 
 
+def l2_policy(w, l2_bytes: int) -> tuple[bool, str]:
+    """Whether the timed steps flush L2, and the sentence that says so. Inputs at least twice
+    the L2 stream from HBM by themselves; smaller ones (decode) get the L2 flushed before every
+    step, outside that step's timed window."""
+    n, D = w.n_tokens, w.d_model
+    if w.dtype == "fp8":
+        state = n * 4 * (D + D // 32)
+    else:
+        state = n * 4 * D * w.state_bytes_per_elem()
+    io = 2 * n * D * (4 if w.dtype == "f32" else 2) + 2 * n * 16
+    in_bytes = state + io
+    if in_bytes < 2 * l2_bytes:
+        return True, (f"L2 flushed before every step ({2 * l2_bytes >> 20} MiB written; inputs "
+                      f"{in_bytes >> 20} MiB), per-step event windows")
+    return False, f"inputs larger than L2 (state {state >> 20} MiB), no flush"
+
+
+def bench_config(w, world: int, l2_note: str) -> dict:
+    """The `config` object of a bench line: the same keys and values in both arms for one
+    workload and world size, so that the two lines describe one workload."""
+    return {"workload": workload_desc(w), "n_tokens_per_gpu": w.n_tokens,
+            "d_model": w.d_model, "rank": w.rank, "n_branch": 4, "state_dtype": w.dtype,
+            "accumulate": "fp32", "parallelism": f"dp{world}", "l2": l2_note}
+
+
+L2_BYTES_DEFAULT = 126 << 20   # a GB300's L2, for a process that has no device to ask
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -267,6 +295,18 @@ def cpu_baseline(w, target_s: float = 12.0) -> dict:
                             "sample": f"first {n1} tokens, {reps1} time(s) ({t1:.1f} s)"}}
 
 
+def reference_l2_bytes() -> int:
+    """The L2 size the GPU arm's timing policy is decided with (asked of the device when one is
+    visible; the reference arm itself runs on the host cores)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(0).L2_cache_size) or L2_BYTES_DEFAULT
+    except Exception:   # noqa: BLE001 - no device: the default
+        pass
+    return L2_BYTES_DEFAULT
+
+
 def run_reference(args, w) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -296,8 +336,7 @@ def run_reference(args, w) -> None:
         "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * total / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": workload_desc(w), "n_tokens": w.n_tokens, "d_model": w.d_model,
-                   "rank": w.rank, "n_branch": 4, "step_sample_tokens": per_step},
+        "config": bench_config(w, args.gpus, l2_policy(w, reference_l2_bytes())[1]),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"{per_step} of the first {pool} tokens of the {w.name} "
@@ -324,6 +363,15 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def any_over_ranks(flag: bool, world: int, device=None) -> bool:
+    """True on every rank if any rank's flag is set: one decision that all ranks act on, so
+    that they all run the same collectives afterwards (a re-measurement is taken by every rank
+    or by none)."""
+    if world <= 1:
+        return bool(flag)
+    return max_over_ranks(1.0 if flag else 0.0, world, device) > 0.5
 
 
 def job_tokens_per_s(world: int, n_tokens_per_rank: int, steps: int, seconds: float) -> float:
@@ -407,14 +455,9 @@ def run_gr(args, w) -> None:
     uuid = str(getattr(props, "uuid", "") or "")
     # Inputs at least twice the L2 stream from HBM by themselves; smaller ones (decode) get the
     # L2 flushed before every step, outside that step's timed window.
-    l2_bytes = int(getattr(props, "L2_cache_size", 0) or (128 << 20))
-    in_bytes = sum(t.numel() * t.element_size() for t in (*state, y, x, s_a, s_b))
-    flush = in_bytes < 2 * l2_bytes
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT)
+    flush, l2_note = l2_policy(w, l2_bytes)
     fbuf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
-    l2_note = (f"L2 flushed before every step ({2 * l2_bytes >> 20} MiB written; inputs "
-               f"{in_bytes >> 20} MiB), per-step event windows" if flush else
-               f"inputs larger than L2 (state "
-               f"{sum(t.numel() * t.element_size() for t in state) >> 20} MiB), no flush")
 
     # The timed steps replay CUDA graphs of the same launches (no host work per step: the small
     # workloads are otherwise bound by the host's launch path). With the flush, one graph per
@@ -472,8 +515,9 @@ def run_gr(args, w) -> None:
         return ms, clocks
 
     ms, clocks = timed()
-    if BAD_REASONS & set(clocks["reasons"]):
-        ms, clocks = timed()  # one re-measurement
+    # one re-measurement, on every rank, if any rank saw a thermal or hardware slowdown
+    if any_over_ranks(bool(BAD_REASONS & set(clocks["reasons"])), world, dev):
+        ms, clocks = timed()
         clocks["remeasured"] = True
     ms_step = ms / args.steps
     tokens_per_s = job_tokens_per_s(world, w.n_tokens, args.steps, ms / 1e3)
@@ -542,11 +586,8 @@ def run_gr(args, w) -> None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded numpy PCG64; no dataset)",
-            "config": {"workload": workload_desc(w), "n_tokens_per_gpu": w.n_tokens,
-                       "d_model": w.d_model, "rank": w.rank, "n_branch": 4,
-                       "state_dtype": w.dtype, "accumulate": "fp32", "parallelism": f"dp{world}",
-                       "l2": l2_note,
-                       "launch": "host launches" if graphs is None else "CUDA graphs of the timed steps"},
+            "config": bench_config(w, world, l2_note),
+            "launch": "host launches" if graphs is None else "CUDA graphs of the timed steps",
             "hbm_gbs": achieved,
             "roofline": roofline,
             "bandwidth_reference": {"kernel": "gr_residual_add_ref (x += y, single stream)",

@@ -80,6 +80,23 @@ def test_reference_arm_prints_one_json_line(workload, extra):
     e2e = rec["e2e"]
     assert e2e["value"] == rec["value"] and e2e["unit"] == rec["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # the same config object as the CUDA arm's line for this workload at one GPU
+    w = wl.WORKLOADS[workload]
+    if extra:
+        w = w.scaled(n_tokens=int(extra[1]))
+    assert rec["config"] == bench.bench_config(w, 1, bench.l2_policy(w, bench.L2_BYTES_DEFAULT)[1])
+
+
+def test_l2_policy_flushes_only_inputs_below_twice_the_l2():
+    l2 = bench.L2_BYTES_DEFAULT
+    for name, flush in [("decode", True), ("tiny_fp32", True), ("prefill", False),
+                        ("large_skewed", False), ("prefill_fp8", False)]:
+        f, note = bench.l2_policy(wl.WORKLOADS[name], l2)
+        assert f is flush, name
+        assert note.startswith("L2 flushed" if flush else "inputs larger than L2"), name
+    # the deep-stack sublayer: 8192 tokens of a [4, 2048] bf16 state (128 MiB) plus y, x, s
+    f, _ = bench.l2_policy(wl.WORKLOADS["deep_stack"], l2)
+    assert f is True
 
 
 def test_cpu_baseline_reports_all_cores_and_one_core():

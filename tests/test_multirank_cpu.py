@@ -27,8 +27,12 @@ def _rank_main(rank, world, port, out_dir):
         w = bench.shard(wl.WORKLOADS["tiny_fp32"], rank)
         R = wl.make_state(w)
         ms = bench.max_over_ranks(10.0 + rank, world)
+        # a slowdown seen by one rank only: every rank decides to re-measure
+        again = bench.any_over_ranks(rank == 1, world)
+        neither = bench.any_over_ranks(False, world)
         tps = bench.job_tokens_per_s(world, w.n_tokens, 7, ms / 1e3)
-        np.savez(os.path.join(out_dir, f"rank{rank}.npz"), R=R, seed=w.seed, ms=ms, tps=tps)
+        np.savez(os.path.join(out_dir, f"rank{rank}.npz"), R=R, seed=w.seed, ms=ms, tps=tps,
+                 again=again, neither=neither)
     finally:
         dist.destroy_process_group()
 
@@ -45,8 +49,10 @@ def test_two_rank_sharding_and_timing(tmp_path):
     for x in r:
         assert float(x["ms"]) == 11.0                        # the slowest rank's time
         assert float(x["tps"]) == pytest.approx(world * base.n_tokens * 7 / 0.011)
+        assert bool(x["again"]) is True and bool(x["neither"]) is False
 
 
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.job_tokens_per_s(1, 100, 10, 2.0) == 500.0
+    assert bench.any_over_ranks(True, 1) is True and bench.any_over_ranks(False, 1) is False
