@@ -16,14 +16,29 @@ _LOCK = threading.Lock()
 _LIB = None
 
 
+def _stamp() -> str:
+    import hashlib
+    import platform
+    h = hashlib.sha256(platform.machine().encode())
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile gr_oracle.c into a shared library beside it (gcc, OpenMP, no fast-math)."""
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+    """Compile gr_oracle.c into a shared library beside it (gcc, OpenMP, no fast-math). A
+    library built from other sources or on another machine is rebuilt."""
+    stamp = _SO + ".stamp"
+    fresh = (os.path.exists(_SO) and os.path.exists(stamp)
+             and open(stamp).read().strip() == _stamp())
+    if force or not fresh:
         tmp = _SO + f".{os.getpid()}.tmp"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
                "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _SO)
+        with open(stamp, "w") as f:
+            f.write(_stamp() + "\n")
     return _SO
 
 

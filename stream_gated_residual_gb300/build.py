@@ -7,7 +7,9 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 
@@ -18,6 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libgr_gb300.so")
+STAMP = LIB + ".stamp"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -40,11 +43,25 @@ def _deps() -> list[str]:
     return sources() + headers + [os.path.join(INCLUDE, "gr.h"), os.path.abspath(__file__)]
 
 
+def source_stamp(extra_flags: list[str] | None = None) -> str:
+    """Hash of everything the library is built from (sources, headers, this script, the flags)
+    and of the machine it is built on: a library built elsewhere, or from other sources, never
+    counts as up to date."""
+    h = hashlib.sha256()
+    h.update(platform.machine().encode())
+    h.update(" ".join(ARCH + NVCC_FLAGS + list(extra_flags or [])).encode())
+    for p in sorted(_deps()):
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == source_stamp()
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
@@ -74,6 +91,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(source_stamp(extra_flags) + "\n")
     return LIB
 
 
