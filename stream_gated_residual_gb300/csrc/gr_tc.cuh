@@ -1,7 +1,7 @@
 // tcgen05 wrappers (5th-generation tensor cores, sm_100-family): tensor-memory allocation, the
 // shared-memory matrix descriptor, the instruction descriptor of kind::f16, the MMA, its commit to
-// an mbarrier, and the tensor-memory loads of the epilogue. Inline PTX, per the PTX ISA's
-// tcgen05 chapter; included after gr_ptx.cuh by the units that issue tcgen05 MMAs.
+// an mbarrier, and the tensor-memory loads and stores. Inline PTX, per the PTX ISA's tcgen05
+// chapter; included after gr_ptx.cuh by the units that use tensor memory.
 #pragma once
 
 #include <stdint.h>
@@ -78,27 +78,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
         : "memory");
 }
 
-// ---- thread-block clusters: one TMA load delivered to several CTAs, one commit releasing them
-// The 2D tile lands at the same offset in every CTA of `mask` (cluster ranks), and each of them
-// gets the byte count on its mbarrier at the same offset as `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1,
-                                               uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-// Arrives once on the mbarrier at `bar`'s offset in every CTA of `mask` when this thread's
-// earlier MMAs have completed.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 // ---- epilogue loads: a warp reads 32 lanes (its quadrant: warp % 4) × 16 columns -------------
 // Without the wait: several loads may be in flight; tmem_wait_ld() before using any of them.
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
@@ -120,6 +99,20 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
+}
+// A warp writes 32 lanes (its quadrant) × 16 columns: thread l's r[k] to lane (taddr's lane
+// + l), column (taddr's column + k). tmem_wait_st() before anything relies on the values.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
