@@ -15,14 +15,17 @@
 //   * A thread-block cluster of C = D/256 CTAs splits the channels: CTA q owns channels
 //     [256q, 256q+256) of every branch.
 //   * Tiles of 16 tokens (the mma M dimension) arrive by TMA (zero fill past N): R in 64-channel
-//     boxes with 128-byte swizzle into a 4-buffer ring, y in 32-channel boxes with 64-byte
+//     boxes with 128-byte swizzle into a 5-buffer ring, y in 32-channel boxes with 64-byte
 //     swizzle (so the A warps' reads of token rows g and g+1 hit different banks) and s_prev
-//     into a 2-buffer ring.
+//     into a 2-buffer ring. A tile's chain (load, write, exchange, combine, store) is several
+//     times the period at which tiles complete, so the depth of the R ring and of the exchange
+//     buffers sets the rate: both are as deep as shared memory allows.
 //   * 16 warps in two roles that run concurrently on different tiles:
 //     - A warps (8): warp a owns branch a%4 and 128 channels (half a/4). They form R' (written
 //       back in place into the R buffer, from where a TMA store takes it to HBM), the
 //       per-branch sums of squares (diagonal of R'·R'ᵀ on the tensor cores) and the down
-//       projections (W_d, W_w with gamma folded, mma fragments resident in shared memory); sum
+//       projections (W_d, W_w with gamma folded; the mma fragments are resident in tensor
+//       memory, which this kernel uses as storage only, so shared memory holds the ring); sum
 //       the two halves; and send each token's row sums with st.async to its owner CTA.
 //     - B warps (8): the CTA's owned token slots of each tile go round the B warps; for each
 //       the warp gathers the token's row sums from every CTA, forms inv, h and s with warp
@@ -39,6 +42,7 @@
 
 #include "gr_internal.h"
 #include "gr_ptx.cuh"
+#include "gr_tc.cuh"
 
 namespace gr {
 
@@ -54,8 +58,12 @@ static_assert(kAW % 4 == 0 && kBW % 4 == 0, "roles are whole warpgroups");
 static_assert(kAW * kARegs + kBW * kBRegs == (kAW + kBW) * kLaunchRegs, "register split");
 constexpr int kAThreads = kAW * 32;
 constexpr int kDq = 256;                    // channels per branch per CTA
-constexpr int kRStages = 4, kYStages = 2;
-constexpr int kXStages = 3;                 // slots of the row-sum and h/inv exchange buffers
+constexpr int kRStages = 5, kYStages = 2;
+constexpr int kXStages = 4;                 // slots of the row-sum and h/inv exchange buffers
+constexpr int kMbSlots = 32;                // 8-byte slots of the mbarrier area
+// Tensor memory: the A warps' down-projection fragments, 16 columns per (A warp, 32-channel
+// chunk) in the warp's lane quadrant (warp % 4); A warps a and a + 4 share a quadrant.
+constexpr int kTmemCols = 128;
 constexpr int kBoxCh = 64;                  // channels per TMA box (128 bytes: the swizzle span)
 constexpr int kColBlocks = kDq / kBoxCh;    // 4 boxes per row slice
 constexpr int kRBoxBytes = kBoxCh * 4 * kT * 2;        // [16 tok][4 br][64 ch] bf16 = 8 KB
@@ -84,9 +92,10 @@ struct FusedShape {
     int off_gam, off_r, off_y, off_s, off_red, off_recv, off_bcast, off_mbar, smem_bytes;
 };
 
-// Packed fragment slice of one CTA: down | up | gamma. Shared memory: down | gamma | R ring
-// (1024-aligned) | y ring | s_prev ring | red | recv[3] | bcast[3] | mbarriers. The up
-// fragments go to the B warps' registers straight from global memory.
+// Packed fragment slice of one CTA: down | up | gamma. Shared memory: gamma | R ring
+// (1024-aligned) | y ring | s_prev ring | red | recv[4] | bcast[4] | mbarriers. The down
+// fragments go to tensor memory and the up fragments to the B warps' registers, both straight
+// from global memory.
 __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     FusedShape s{};
     s.C = D / kDq;
@@ -104,7 +113,7 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     s.red_bytes = kT * s.red_stride * 4;
     s.recv_bytes = s.C * ((kT / s.C) * 4 * s.rw + 4) * 4;   // per source: its rows + 4 pad
     s.bcast_bytes = kT * s.nb4 * 4;
-    s.off_gam = s.down_bytes;
+    s.off_gam = 0;
     s.off_r = round_up(s.off_gam + s.gam_bytes, 1024);
     s.off_y = s.off_r + kRStages * kRBufBytes;
     s.off_s = s.off_y + kYStages * kYBufBytes;
@@ -112,7 +121,7 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
     s.off_recv = s.off_red + round_up(s.red_bytes, 16);
     s.off_bcast = s.off_recv + kXStages * round_up(s.recv_bytes, 16);
     s.off_mbar = s.off_bcast + kXStages * round_up(s.bcast_bytes, 16);
-    s.smem_bytes = s.off_mbar + round_up(8 * 24, 16);
+    s.smem_bytes = s.off_mbar + round_up(8 * kMbSlots, 16);
     return s;
 }
 
@@ -120,12 +129,13 @@ __host__ __device__ inline FusedShape fused_shape(int D, int r) {
 constexpr int kMbRFull = 0;                        // [4] R tile landed (TMA)
 constexpr int kMbRReady = kMbRFull + kRStages;     // [4] R' written back (8 A-warp arrivals)
 constexpr int kMbREmpty = kMbRReady + kRStages;    // [4] B warps done with the R buffer (8)
-constexpr int kMbYFull = kMbREmpty + kRStages;     // [3] y and s_prev landed (TMA)
-constexpr int kMbWeights = kMbYFull + kYStages;    // weights landed
-constexpr int kMbRecv = kMbWeights + 1;            // [3] row sums from every CTA (owner)
-constexpr int kMbBcast = kMbRecv + kXStages;       // [3] h and inv from every owner
+constexpr int kMbYFull = kMbREmpty + kRStages;     // [2] y and s_prev landed (TMA)
+constexpr int kMbWeights = kMbYFull + kYStages;    // gamma landed
+constexpr int kMbRecv = kMbWeights + 1;            // [4] row sums from every CTA (owner)
+constexpr int kMbBcast = kMbRecv + kXStages;       // [4] h and inv from every owner
 constexpr int kMbCount = kMbBcast + kXStages;
-static_assert(kMbCount * 8 + kRStages * 4 <= 24 * 8, "mbarrier area holds 24 slots");
+// mbarriers, then the per-buffer counters (rdone), then the tensor-memory base address
+static_assert(kMbCount * 8 + kRStages * 4 + 4 <= kMbSlots * 8, "mbarrier area");
 
 // Named barrier among the A warps only.
 __device__ __forceinline__ void a_sync() {
@@ -156,6 +166,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S.off_mbar);
     // per R buffer: count of B warps done with it (the eighth of each round refills it)
     uint32_t* rdone = reinterpret_cast<uint32_t*>(mbar + kMbCount);
+    uint32_t* tslot = rdone + kRStages;   // tensor-memory base (written by tcgen05.alloc)
     auto rbuf = [&](int k) { return smem + S.off_r + int(k % kRStages) * kRBufBytes; };
     auto ybuf = [&](int k) { return smem + S.off_y + int(k % kYStages) * kYBufBytes; };
     auto sbuf = [&](int k) { return smem + S.off_s + int(k % kYStages) * kSBufBytes; };
@@ -166,6 +177,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         return reinterpret_cast<float*>(smem + S.off_bcast + p * round_up(S.bcast_bytes, 16));
     };
 
+    if (warp == 0) {
+        tmem_alloc(tslot, kTmemCols);
+        tmem_relinquish();
+    }
     if (tid == 0) {
         for (int i = 0; i < kMbCount; ++i) {
             const bool eight = (i >= kMbRReady && i < kMbRReady + kRStages) ||
@@ -175,7 +190,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         for (int i = 0; i < kRStages; ++i) rdone[i] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
 
     // TMA of the k-th local tile's R slice: one 4-D box {64 ch, 4 br, 16 tok, 4 blocks} = the
     // CTA's 256 channels as four 64-channel blocks (one thread).
@@ -201,8 +219,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
     };
 
     if (tid == 0) {
-        mbar_expect_tx(&mbar[kMbWeights], uint32_t(S.down_bytes + S.gam_bytes));
-        bulk_g2s(smem, slice, uint32_t(S.down_bytes), &mbar[kMbWeights]);
+        mbar_expect_tx(&mbar[kMbWeights], uint32_t(S.gam_bytes));
         bulk_g2s(smem + S.off_gam, slice + S.down_bytes + S.up_bytes, uint32_t(S.gam_bytes),
                  &mbar[kMbWeights]);
     }
@@ -235,8 +252,26 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             s_off[u] = (int(crank) * (tpc * 4 * rw + 4) + slot * 4 * rw + 4 * rem4) * 4;
             s_own[u] = owner;
         }
-        mbar_wait(&mbar[kMbWeights], 0);
-        const uint4* s_down = reinterpret_cast<const uint4*>(smem);
+        // this warp's down fragments into its tensor-memory columns: 16 per 32-channel chunk
+        // j4, units (n-tile j, lane) at columns 4j .. 4j+3 (zero past the real n-tiles)
+        const uint32_t ta = tmem + (uint32_t((a & 3) * 32) << 16) + uint32_t((a >> 2) * 64);
+        {
+            const uint4* gdown = reinterpret_cast<const uint4*>(slice);
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                uint32_t v[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                    const bool last_half = (j == NTD - 1) && S.half_last;
+                    if (j < NTD && (!last_half || lane < 16))
+                        b = gdown[(a * 4 + j4) * S.upb + j * 32 + lane];
+                    v[4 * j] = b.x, v[4 * j + 1] = b.y, v[4 * j + 2] = b.z, v[4 * j + 3] = b.w;
+                }
+                tmem_st16(ta + uint32_t(j4 * 16), v);
+            }
+            tmem_wait_st();
+        }
         float* red = reinterpret_cast<float*>(smem + S.off_red);   // [kT][kAW][rw], padded
         for (int k = 0; k < nlocal; ++k) {
             const int p = int(k % kXStages);
@@ -298,6 +333,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             float acc[NTD][4], sq0[4], sq1[4];
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
+                uint32_t bw[16];   // this chunk's down fragments, from tensor memory
+                tmem_ld16_nowait(ta + uint32_t(j4 * 16), bw);
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     const uint32_t a0 = Rp[0][j4][2 * ks], a1 = Rp[1][j4][2 * ks];
@@ -310,11 +347,11 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                         mma_bf16(sq1, a0, a1, a2, a3, a1, a3);
                     }
                 }
+                tmem_wait_ld(bw);
 #pragma unroll
                 for (int j = 0; j < NTD; ++j) {
-                    uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                    const bool last_half = (j == NTD - 1) && S.half_last;
-                    if (!last_half || lane < 16) b = s_down[(a * 4 + j4) * S.upb + j * 32 + lane];
+                    const uint4 b = make_uint4(bw[4 * j], bw[4 * j + 1], bw[4 * j + 2],
+                                               bw[4 * j + 3]);
                     if (j4 == 0)
                         mma_bf16_z(acc[j], Rp[0][j4][0], Rp[1][j4][0], Rp[0][j4][1], Rp[1][j4][1],
                                    b.x, b.y);
@@ -326,8 +363,8 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 }
             }
             // Before the row sums of tile k leave, every owner must be done with the exchange
-            // slot of tile k-3 and this CTA's B warps with its h/inv slot: both follow from
-            // the local combine of tile k-3 (it needed h from every owner).
+            // slot of tile k-4 and this CTA's B warps with its h/inv slot: both follow from
+            // the local combine of tile k-4 (it needed h from every owner).
             if (k >= kXStages)
                 mbar_wait(&mbar[kMbREmpty + int((k - kXStages) % kRStages)],
                           uint32_t(((k - kXStages) / kRStages) & 1));
@@ -362,6 +399,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             }
             a_sync();  // red is free again
         }
+        tc_fence_before();   // this warp's tensor-memory loads are done before the dealloc
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBRegs));
         // =============================== B warps ===========================================
@@ -462,7 +500,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         };
 
         // Up projection (eq gate), gates, combine (eq use_gate) and x for local tile k; then the
-        // R buffer is released and refilled with tile k+4.
+        // R buffer is released and refilled with tile k+5.
         auto combine = [&](int k) {
             const int t0 = (cid + k * ncl) * kT;
             const int p = int(k % kXStages);
@@ -563,7 +601,7 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                         f2_to_bf2(mul2(eighth, xacc2[row][2])), f2_to_bf2(mul2(eighth, xacc2[row][3])));
                 }
             }
-            // refill: the last B warp done with this buffer loads R of tile k+4 into it (lane 0);
+            // refill: the last B warp done with this buffer loads R of tile k+5 into it (lane 0);
             // no other warp waits for it
             if (k + kRStages < nlocal) {
                 uint32_t last = 0;
@@ -596,6 +634,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
         if (WRITE && b == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     cluster_sync();  // no CTA leaves while shared::cluster traffic to it may be in flight
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
 // Fragment section: for CTA slice q, [down | up | gamma].
