@@ -63,7 +63,9 @@ enum {
     GR_E_CUDA = -9,        /* a CUDA launch or copy failed                                      */
     GR_E_DEVICE = -10,     /* no usable CUDA device (this build runs on sm_103a only)           */
     GR_E_EPS = -11,        /* eps negative or not finite                                        */
-    GR_E_TIMEOUT = -12     /* a kernel's bounded device-side wait ran out (see gr_device_status) */
+    GR_E_TIMEOUT = -12,    /* a kernel's bounded device-side wait ran out (see gr_device_status) */
+    GR_E_NOMEM = -13       /* the device could not commit the fixed workspace of
+                              gr_write_then_read_host_static (its memory is taken)               */
 };
 
 /* Storage dtype of R, y and x. GR_FP8 is the FP8 branch state (see the FP8 section below): R is
@@ -225,13 +227,18 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
  *     caching allocator, a serving engine's preallocated pool), where an extra cudaMalloc can
  *     fail or fragment the pool;
  *   - a latency-bound loop (decode), where cudaFree would synchronise the whole device.
- * It calls no cudaMalloc or cudaFree and creates no stream or event; its device memory is
- * fixed when the library is loaded and held by every device that loads it until the process
- * exits.
+ * It calls no cudaMalloc or cudaFree and creates no stream or event. Its device memory is a
+ * fixed-size array, held by every device that loads it until the process exits. When the device
+ * commits that memory depends on CUDA's module loading: with lazy loading (the default) at the
+ * first call of this entry on the device, with CUDA_MODULE_LOADING=EAGER when the library's
+ * module loads with the context. A process whose allocator takes the device's memory first
+ * should therefore make one call (or set EAGER) before its pool grows.
  *   - Returns GR_E_SIZE, without touching anything, when gr_host_workspace_size(shape) exceeds
  *     GR_STATIC_WORKSPACE_BYTES (for example N > 682 tokens at D = 4096, bf16).
  *   - The first call on a device looks the workspace's device address up once
- *     (cudaGetSymbolAddress); make that first call outside any stream capture.
+ *     (cudaGetSymbolAddress); make that first call outside any stream capture. If the device
+ *     cannot commit the memory there, the call returns GR_E_NOMEM (GR_E_CUDA for any other
+ *     failure), clears the CUDA runtime's error, touches nothing, and the next call tries again.
  *   - Shapes that the device entries split between the cluster kernel and the two-pass kernel
  *     (gr_kernel_path "fused_bf16+tiled_bf16") run on the cluster kernel alone here: the split
  *     uses an internal stream and events that would be created on first use. Their R' is

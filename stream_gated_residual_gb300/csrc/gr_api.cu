@@ -278,6 +278,7 @@ const char* gr_status_string(int status) {
         case GR_E_DEVICE: return "no usable sm_103 CUDA device";
         case GR_E_EPS: return "eps negative or not finite";
         case GR_E_TIMEOUT: return "a bounded device-side wait ran out";
+        case GR_E_NOMEM: return "the device could not commit the library's fixed workspace";
         default: return "unknown status";
     }
 }
@@ -785,10 +786,15 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
     const int dev = current_device();
     {
         std::lock_guard<std::mutex> lock(g_static_mu);
-        if (!g_static_ws_addr[dev] &&
-            cudaGetSymbolAddress(&g_static_ws_addr[dev], g_static_ws) != cudaSuccess) {
-            g_static_ws_addr[dev] = nullptr;
-            return GR_E_CUDA;
+        if (!g_static_ws_addr[dev]) {
+            // under lazy module loading (CUDA's default) this is where the device commits the
+            // array's memory; a device whose memory is taken fails here with an allocation error
+            const cudaError_t e = cudaGetSymbolAddress(&g_static_ws_addr[dev], g_static_ws);
+            if (e != cudaSuccess) {
+                g_static_ws_addr[dev] = nullptr;
+                cudaGetLastError();   // not a sticky error: clear it for the caller's next call
+                return e == cudaErrorMemoryAllocation ? GR_E_NOMEM : GR_E_CUDA;
+            }
         }
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.gr_api_version() == header_constant("GR_API_VERSION")
-    for code in range(0, -13, -1):
+    for code in range(0, -14, -1):
         s = gr.status_string(code)
         assert s and s != "unknown status", code
     assert gr.status_string(-99) == "unknown status"
