@@ -125,9 +125,13 @@ def test_decode_full():
 @pytest.mark.parametrize("mult", [10.0, 50.0])
 def test_decode_sharp_gates_and_random_gamma(mult):
     """Weights x10 (gate logits spread over several units, G and s far from 1/2 and 1) and x50
-    (gates saturated at 0 or 1), with non-unit gains. Against the plain definition the rounding
-    of the stored state moves a saturated s by a relative amount equal to the absolute error of
-    its logit, so only the storage-modelled comparison bounds these cases."""
+    (gates saturated at 0 or 1), with non-unit gains. Against the plain definition, the bf16
+    rounding of the stored state and of the folded weights moves each logit u by an absolute
+    amount that grows with its spread, and where s = 2σ(u) is far from 1 it moves by that amount
+    relative to itself: measured at x10, s is 2.8e-2 from the plain definition (R' 1.7e-3, x
+    4.0e-3), past the 2e-2 bound, and more at x50. Only the storage-modelled comparison, which
+    sees the same stored values and weights, bounds these cases; the x5 sweeps of the kernels
+    below meet the plain bound as well (s up to 1.8e-2 at D = 7168)."""
     w = wl.WORKLOADS["decode"]
     check(w, *fused_case(w, weight_mult=mult, random_gamma=True), plain_too=False)
 
@@ -277,7 +281,7 @@ def test_fused_kernel_shapes(D, r, N):
     """Every cluster size (D = 256 … 4096 → 1 … 16 CTAs), ranks 1 … 16, ragged last tiles."""
     w = wl.Workload("fused", N, D, r, "bf16", y_std=0.5, seed=13)
     assert gr.kernel_path(N, D, r, torch.bfloat16) == "fused_bf16"
-    check(w, *fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    check(w, *fused_case(w, random_gamma=True, weight_mult=5.0))
     assert gr.device_status(clear=True) == 0
 
 
@@ -309,7 +313,7 @@ def test_tiled_kernel_shapes(D, r, N):
     16-token half is empty), and more tiles than SMs (N = 10000)."""
     w = wl.Workload("tiled", N, D, r, "bf16", y_std=0.5, seed=29)
     assert gr.kernel_path(N, D, r, torch.bfloat16) == "tiled_bf16"
-    check(w, *fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    check(w, *fused_case(w, random_gamma=True, weight_mult=5.0))
     assert gr.device_status(clear=True) == 0
 
 
@@ -343,7 +347,7 @@ def test_split_cluster_and_two_pass(N, write):
     assert gr.kernel_path(N, D, r, torch.bfloat16) == "fused_bf16+tiled_bf16"
     w = wl.Workload("split", N, D, r, "bf16", y_std=0.5, seed=37)
     if write:
-        check(w, *fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+        check(w, *fused_case(w, random_gamma=True, weight_mult=5.0))
     else:
         R = wl.make_state(w)
         p = wl.make_params(w, 1, weight_mult=5.0)

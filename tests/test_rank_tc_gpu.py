@@ -45,7 +45,7 @@ def test_fused_step(N, D, r):
     and a single token; sharp weights (x5) and random gains."""
     w = wl.Workload("tc", N, D, r, "bf16", y_std=0.5, seed=47)
     assert gr.kernel_path(N, D, r, torch.bfloat16) == "tc_bf16"
-    _check(*fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    _check(*fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=True)
     assert gr.device_status(clear=True) == 0
 
 
