@@ -40,6 +40,8 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "gr_internal.h"
 #include "gr_ptx.cuh"
 #include "gr_tc.cuh"
@@ -553,6 +555,11 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
             const float4 iv1 = *reinterpret_cast<const float4*>(bc + (g + 8) * nb4);
             const float inv0s[4] = {iv0.x, iv0.y, iv0.z, iv0.w};
             const float inv1s[4] = {iv1.x, iv1.y, iv1.z, iv1.w};
+            // SCALED: some token row of the warp was scaled down (ea or eb > 0) and its logits
+            // are scaled back; otherwise every scale is 1 and the code path has no multiplies
+            // for it (the same result: a product with 1 is exact)
+            auto gate_combine = [&](auto scaled) {
+                constexpr bool SCALED = decltype(scaled)::value;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float inv0 = inv0s[i], inv1 = inv1s[i];
@@ -571,10 +578,12 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 for (int j = 0; j < 4; ++j) {
                     float c[4];
                     mma_f16_z(c, ah[0], ah[1], ah[2], ah[3], wu[i * 4 + j].x, wu[i * 4 + j].y);
-                    c[0] *= ua;
-                    c[1] *= ua;
-                    c[2] *= ub;
-                    c[3] *= ub;
+                    if constexpr (SCALED) {
+                        c[0] *= ua;
+                        c[1] *= ua;
+                        c[2] *= ub;
+                        c[3] *= ub;
+                    }
                     const uint64_t gm2 = f2(gm[2 * j], gm[2 * j + 1]);
                     const uint64_t u0 = mul2(gm2, bf2_to_f2(q0[j]));   // γ·R' (row g)
                     const uint64_t u1 = mul2(gm2, bf2_to_f2(q1[j]));   // γ·R' (row g+8)
@@ -585,6 +594,9 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                     xacc2[1][j] = fma2(inv1_2, w1, xacc2[1][j]);
                 }
             }
+            };
+            if (__all_sync(0xffffffffu, (ea | eb) == 0)) gate_combine(std::false_type{});
+            else gate_combine(std::true_type{});
             // the buffer is released only after the TMA store has read it
             if (WRITE && b == 0 && lane == 0)
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

@@ -39,6 +39,8 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "gr_internal.h"
 #include "gr_ptx.cuh"
 
@@ -506,6 +508,7 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
         // ---------------------------------- pass 2 --------------------------------------------
         uint32_t ah[KSU][4];     // fp16 A fragments of the scaled h
         uint64_t unscale_a, unscale_b;   // 2^e of tokens g and g+8, as fp32 pairs
+        bool unit_scale;                 // every row of the warp unscaled (e = 0)
         {
             const float* ha = hbuf + (16 * mt2 + g) * C::kHP;
             const float* hb = ha + 8 * C::kHP;
@@ -534,6 +537,7 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             const float ua = __int_as_float((127 + ea) << 23), ub = __int_as_float((127 + eb) << 23);
             unscale_a = f2(ua, ua);
             unscale_b = f2(ub, ub);
+            unit_scale = __all_sync(0xffffffffu, (ea | eb) == 0);
 #pragma unroll
             for (int ks = 0; ks < KSU; ++ks)
 #pragma unroll
@@ -549,6 +553,11 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             inv2[i][1] = invb[i * kTT + 16 * mt2 + g + 8];
         }
         const int ch = co * 8 + 2 * q;   // this thread's channel pair within the chunk
+        // SCALED: some token row of the warp was scaled down and its logits are scaled back;
+        // otherwise every scale is 1 and the chunk loop has no multiplies for it (a product
+        // with 1 is exact, so both paths give the same result)
+        auto pass2 = [&](auto scaled) {
+        constexpr bool SCALED = decltype(scaled)::value;
         for (int jj = 0; jj < J; ++jj) {
             const int j = J - 1 - jj;
             const int st = sr.st;
@@ -600,9 +609,11 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
                 }
                 const uint64_t ra = mul2(rpa, mul2(g2, f2(inv2[i][0], inv2[i][0])));
                 const uint64_t rbv = mul2(rpb, mul2(g2, f2(inv2[i][1], inv2[i][1])));
-                float a0, a1, b0, b1;
-                unf2(mul2(f2(cg4[i][0], cg4[i][1]), unscale_a), a0, a1);
-                unf2(mul2(f2(cg4[i][2], cg4[i][3]), unscale_b), b0, b1);
+                float a0 = cg4[i][0], a1 = cg4[i][1], b0 = cg4[i][2], b1 = cg4[i][3];
+                if constexpr (SCALED) {
+                    unf2(mul2(f2(a0, a1), unscale_a), a0, a1);
+                    unf2(mul2(f2(b0, b1), unscale_b), b0, b1);
+                }
                 const uint64_t ta = add2(f2(tanh_approx(a0), tanh_approx(a1)), one2);
                 const uint64_t tb = add2(f2(tanh_approx(b0), tanh_approx(b1)), one2);
                 xa = fma2(ta, ra, xa);
@@ -625,6 +636,9 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
             wr.next();
             ++xc;
         }
+        };
+        if (unit_scale) pass2(std::false_type{});
+        else pass2(std::true_type{});
     }
     if (lane == 0) bulk_wait_all();
 }
