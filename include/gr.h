@@ -240,9 +240,9 @@ int gr_write_then_read_host(const gr_shape* shape, void* R_host, const void* y_h
  *     cannot commit the memory there, the call returns GR_E_NOMEM (GR_E_CUDA for any other
  *     failure), clears the CUDA runtime's error, touches nothing, and the next call tries again.
  *   - Shapes that the device entries split between the cluster kernel and the two-pass kernel
- *     (gr_kernel_path "fused_bf16+tiled_bf16") run on the cluster kernel alone here: the split
- *     uses an internal stream and events that would be created on first use. Their R' is
- *     bit-identical to gr_write_then_read_host's; x and s agree within the bf16 tolerance.
+ *     (gr_kernel_path "fused_bf16+tiled_bf16") run on the cluster kernel alone here (on a GB300
+ *     no shape that fits the workspace is split anyway). Their R' is bit-identical to
+ *     gr_write_then_read_host's; x and s agree within the bf16 tolerance.
  *   - Nothing in the workspace has to start at zero (each call writes all it reads).
  *   - All calls on a device share the one workspace: calls that overlap in time (on different
  *     streams or host threads) race on it. Run them one after another.

@@ -142,8 +142,8 @@ bool use_tiled(const gr_shape* s) {
            tiled_supported(s->d_model, s->rank) && s->n_tokens <= tiled_max_tokens();
 }
 
-// allow_split = false keeps a cluster-kernel step on the cluster kernel alone: the concurrent
-// split needs the internal stream and events that gr_split.cu creates on first use.
+// allow_split = false keeps a cluster-kernel step on the cluster kernel alone (the host entries'
+// chunks, which are below the split's token threshold anyway).
 int run_step(const gr_shape* s, void* R, const void* y, const float* s_prev,
              const gr_params* p, void* x, float* s_out, cudaStream_t st,
              void* ws = nullptr, size_t ws_bytes = 0, bool allow_split = true) {
@@ -808,7 +808,7 @@ int gr_write_then_read_host_static(const gr_shape* shape, void* R_host, const vo
         cudaMemcpyAsync(dy, y_host, ny, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
         cudaMemcpyAsync(dsp, s_prev_host, ns, cudaMemcpyHostToDevice, cs) != cudaSuccess)
         return GR_E_CUDA;
-    // no concurrent split here: its internal stream and events would be created on first use
+    // the cluster kernel alone (no shape that fits the workspace reaches the split's threshold)
     st = run_step(shape, dR, dy, dsp, next, dx, dsn, cs, nullptr, 0, false);
     if (st) return st;
     if (cudaMemcpyAsync(R_host, dR, nR, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||

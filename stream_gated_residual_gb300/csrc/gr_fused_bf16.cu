@@ -152,6 +152,10 @@ gr_fused_kernel(const __grid_constant__ CUtensorMap tm_R, const __grid_constant_
                 int N, int D, int r, float eps, const float* __restrict__ s_prev, const char* __restrict__ frag,
                 __nv_bfloat16* __restrict__ x, float* __restrict__ s_out) {
     extern __shared__ __align__(1024) char smem[];
+    // This CTA is resident: a programmatic dependent (the split's two-pass share) may take the
+    // SMs that the clusters leave free once every CTA of the grid is, and only then, so that it
+    // cannot occupy an SM a cluster needs.
+    dep_launch_dependents();
     const FusedShape S = fused_shape(D, r);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q4 = lane & 3;
@@ -743,6 +747,7 @@ bool make_map_y(CUtensorMap* m, const void* y, int64_t N, int D) {
 
 struct ClusterCache {
     int max_clusters[2][4][5];  // [WRITE][NTD][log2 C], 0 = not queried
+    int smem_set[2][4];         // [WRITE][NTD]: dynamic shared memory granted (attributes set)
 };
 ClusterCache g_cluster_cache[64];
 
@@ -753,16 +758,22 @@ template <bool WRITE, int NTD>
 cudaError_t prepare_t(const FusedShape& S, cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr,
                       int& max_clusters) {
     auto kern = gr_fused_kernel<WRITE, NTD>;
-    // the register split assumes this launch size; anything else could stall setmaxnreg.inc
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S.smem_bytes);
-    if (e != cudaSuccess) return e;
-    if (S.C > 8) {
+    ClusterCache& cc = g_cluster_cache[dev & 63];
+    // the attributes are checked and set once per device and instantiation (the largest shared
+    // memory so far), not on every launch
+    if (cc.smem_set[WRITE ? 1 : 0][NTD] < S.smem_bytes) {
+        // the register split assumes this launch size; anything else could stall setmaxnreg.inc
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S.smem_bytes);
+        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
+        cc.smem_set[WRITE ? 1 : 0][NTD] = S.smem_bytes;
     }
     cfg = cudaLaunchConfig_t{};
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -773,11 +784,9 @@ cudaError_t prepare_t(const FusedShape& S, cudaLaunchConfig_t& cfg, cudaLaunchAt
     cfg.numAttrs = 1;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = size_t(S.smem_bytes);
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     int lc = 0;
     while ((1 << lc) < S.C) ++lc;
-    int& maxc = g_cluster_cache[dev & 63].max_clusters[WRITE ? 1 : 0][NTD][lc];
+    int& maxc = cc.max_clusters[WRITE ? 1 : 0][NTD][lc];
     if (maxc == 0) {
         cfg.gridDim = dim3(unsigned(S.C * 64));
         int n = 0;

@@ -128,9 +128,11 @@ cudaError_t launch_fused_bf16(int64_t N, int D, int r, float eps, void* R, const
 // Two-pass bf16 tensor-core kernel (write then read, or read only when y == nullptr).
 // max_ctas > 0 caps the grid (the SMs left to it); the fragments come from the section the
 // packed buffer has for the two-pass kernel (frag, or frag2 on a cluster-kernel shape).
+// programmatic: launched as the programmatic dependent of the preceding launch on `st` (it
+// starts once that grid's CTAs are all resident, and finishes only after that grid).
 cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
                               const float* s_prev, const void* packed, void* x, float* s_out,
-                              cudaStream_t st, int max_ctas = 0);
+                              cudaStream_t st, int max_ctas = 0, bool programmatic = false);
 
 // The two-pass kernel on an FP8 state (codes [N][4][D], block exponents [N][4][D/32]); y and x
 // bf16; read only when y == nullptr.

@@ -79,6 +79,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         }
     }
 }
+// Programmatic dependent launch: a grid launched as the programmatic dependent of this one may
+// start once every CTA of this grid has executed launch_dependents (or exited); the dependent's
+// dep_wait returns once this grid has completed and its memory operations are visible. Both are
+// no-ops when the launch has no such dependency.
+__device__ __forceinline__ void dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
     asm volatile(

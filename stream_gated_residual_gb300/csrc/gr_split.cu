@@ -1,9 +1,9 @@
 // Concurrent split of a large cluster-kernel step. The cluster kernel fills only the SMs its
 // resident clusters take (7 clusters of 16 = 112 of 152 SMs at D = 4096); the two-pass kernel
-// takes a share of the tokens on the rest, on an internal stream forked from the caller's stream
-// and joined back to it.
-#include <mutex>
-
+// takes a share of the tokens on the rest. Both go on the caller's stream: the two-pass kernel is
+// the cluster kernel's programmatic dependent, so its CTAs start only once every cluster is
+// resident (they cannot take an SM a cluster needs) and its grid completes only after the
+// cluster kernel's (work after the call waits for both).
 #include "gr_internal.h"
 
 namespace gr {
@@ -17,25 +17,6 @@ namespace {
 // 115 µs at D = 4096). At the prefill shape this gives 2560 of 16384 tokens to 40 SMs, the best
 // split measured there.
 constexpr double kTiledTilePerChannel = 0.0122;
-
-constexpr int kMaxDevices = 64;
-
-struct SplitPipe {
-    std::mutex mu;
-    bool ready = false;
-    cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-SplitPipe g_split[kMaxDevices];
-
-cudaError_t split_pipe_init(SplitPipe& sp) {
-    if (sp.ready) return cudaSuccess;
-    cudaError_t e = cudaStreamCreateWithFlags(&sp.aux, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sp.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sp.join, cudaEventDisableTiming);
-    if (e == cudaSuccess) sp.ready = true;
-    return e;
-}
 
 }  // namespace
 
@@ -69,16 +50,7 @@ int64_t split_tokens(int64_t n_tokens, int D, int r, bool write, int* free_sms) 
 cudaError_t launch_split_bf16(int64_t N, int64_t n2, int free_sms, int D, int r, float eps,
                               void* R, const void* y, const float* s_prev, const void* packed,
                               void* x, float* s_out, cudaStream_t st) {
-    // tokens [0, n1) on the cluster kernel (caller's stream), [n1, N) on the two-pass kernel
-    // (internal stream), which waits for the work already on the caller's stream and which the
-    // caller's stream waits for afterwards
-    int d = 0;
-    cudaError_t e = cudaGetDevice(&d);
-    if (e != cudaSuccess) return e;
-    if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
-    SplitPipe& sp = g_split[d];
-    std::lock_guard<std::mutex> lock(sp.mu);
-    if ((e = split_pipe_init(sp)) != cudaSuccess) return e;
+    // tokens [0, n1) on the cluster kernel, [n1, N) on the two-pass kernel, both on `st`
     const int64_t n1 = N - n2;
     const size_t Dz = size_t(D);
     char* R2 = static_cast<char*>(R) + size_t(n1) * kBranches * Dz * 2;
@@ -86,15 +58,9 @@ cudaError_t launch_split_bf16(int64_t N, int64_t n2, int free_sms, int D, int r,
     const float* sp2 = s_prev ? s_prev + size_t(n1) * kBranches : nullptr;
     char* x2 = static_cast<char*>(x) + size_t(n1) * Dz * 2;
     float* so2 = s_out + size_t(n1) * kBranches;
-    if ((e = cudaEventRecord(sp.fork, st)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(sp.aux, sp.fork, 0)) != cudaSuccess)
-        return e;
-    e = launch_fused_bf16(n1, D, r, eps, R, y, s_prev, packed, x, s_out, st);
-    if (e == cudaSuccess)
-        e = launch_tiled_bf16(n2, D, r, eps, R2, y2, sp2, packed, x2, so2, sp.aux, free_sms);
+    cudaError_t e = launch_fused_bf16(n1, D, r, eps, R, y, s_prev, packed, x, s_out, st);
     if (e != cudaSuccess) return e;
-    if ((e = cudaEventRecord(sp.join, sp.aux)) != cudaSuccess) return e;
-    return cudaStreamWaitEvent(st, sp.join, 0);
+    return launch_tiled_bf16(n2, D, r, eps, R2, y2, sp2, packed, x2, so2, st, free_sms, true);
 }
 
 }  // namespace gr

@@ -641,6 +641,9 @@ gr_tiled_kernel(const __grid_constant__ CUtensorMap tm_R,   // R/R' loads, box {
         else pass2(std::true_type{});
     }
     if (lane == 0) bulk_wait_all();
+    // As the programmatic dependent of a cluster-kernel launch (the concurrent split), this grid
+    // completes only after that grid has: work after the call in the stream then follows both.
+    dep_wait();
 }
 
 // ---- packing ---------------------------------------------------------------------------------
@@ -742,10 +745,14 @@ bool make_map_nd(CUtensorMap* m, const void* p, int64_t N, int D, int box_ch, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Largest dynamic shared memory already granted to each instantiation, per device (the attribute
+// is set once, not on every launch).
+template <bool WRITE, int NTD, int KSU, bool FP8> int g_smem_set[64];
+
 template <bool WRITE, int NTD, int KSU, bool FP8>
 cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, uint8_t* scales, const void* y,
                      const float* s_prev, const char* frag, void* x, float* s_out,
-                     cudaStream_t st, int max_ctas) {
+                     cudaStream_t st, int max_ctas, bool programmatic) {
     using C = TiledCfg<NTD, KSU, FP8>;
     CUtensorMap mR, mRs, my, mx;
     memset(&mRs, 0, sizeof(mRs));
@@ -757,24 +764,42 @@ cudaError_t launch_t(int64_t N, int D, int r, float eps, void* R, uint8_t* scale
     if (!make_map_nd(&mx, x, N, D, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
     auto kern = gr_tiled_kernel<WRITE, NTD, KSU, FP8>;
     const int smem = C::smem_bytes(D);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    int& granted = g_smem_set<WRITE, NTD, KSU, FP8>[dev & 63];
+    if (granted < smem) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        granted = smem;
+    }
     const int64_t ntiles = (N + kTT - 1) / kTT;
     int64_t grid = ntiles < sm_count() ? ntiles : sm_count();
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-    kern<<<unsigned(grid), kThreadsT, smem, st>>>(mR, mRs, my, mx, int(N), D, r, eps, s_prev,
-                                                  frag, s_out, scales);
-    return cudaGetLastError();
+    // as a programmatic dependent of the preceding launch on the stream (the split's cluster
+    // kernel): its CTAs start once that grid's CTAs are all resident, and it finishes after it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreadsT);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, mR, mRs, my, mx, int(N), D, r, eps, s_prev, frag,
+                              s_out, scales);
 }
 
 template <int NTD, int KSU, bool FP8>
 cudaError_t launch_k(int64_t N, int D, int r, float eps, void* R, uint8_t* scales, const void* y,
                      const float* s_prev, const char* frag, void* x, float* s_out,
-                     cudaStream_t st, int max_ctas = 0) {
+                     cudaStream_t st, int max_ctas = 0, bool programmatic = false) {
     return y ? launch_t<true, NTD, KSU, FP8>(N, D, r, eps, R, scales, y, s_prev, frag, x, s_out,
-                                             st, max_ctas)
+                                             st, max_ctas, programmatic)
              : launch_t<false, NTD, KSU, FP8>(N, D, r, eps, R, scales, y, s_prev, frag, x, s_out,
-                                              st, max_ctas);
+                                              st, max_ctas, programmatic);
 }
 
 }  // namespace
@@ -821,7 +846,7 @@ cudaError_t launch_pack_tiled(int D, int r, const float* gamma, const float* wd,
 
 cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const void* y,
                               const float* s_prev, const void* packed, void* x, float* s_out,
-                              cudaStream_t st, int max_ctas) {
+                              cudaStream_t st, int max_ctas, bool programmatic) {
     if (!tiled_supported(D, r) || N < 1 || N > tiled_max_tokens()) return cudaErrorInvalidValue;
     const Layout L = make_layout(D, r, GR_BF16);
     const char* frag = static_cast<const char*>(packed) + (L.frag2_bytes ? L.frag2 : L.frag);
@@ -829,9 +854,9 @@ cudaError_t launch_tiled_bf16(int64_t N, int D, int r, float eps, void* R, const
     tiled_cfg(r, ntd, ksu);
     if (ntd == 3)
         return launch_k<3, 1, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st,
-                                     max_ctas);
+                                     max_ctas, programmatic);
     return launch_k<5, 2, false>(N, D, r, eps, R, nullptr, y, s_prev, frag, x, s_out, st,
-                                 max_ctas);
+                                 max_ctas, programmatic);
 }
 
 bool tiled_fp8_supported(int D, int r) {

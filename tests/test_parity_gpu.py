@@ -340,7 +340,8 @@ def test_tiled_read_only(D, r, N):
 @pytest.mark.parametrize("N,write", [(8192, True), (16384, False)])
 def test_split_cluster_and_two_pass(N, write):
     """A large step on a cluster-kernel shape (D = 4096, r = 16) also runs a share of its tokens
-    on the two-pass kernel, on the SMs the clusters leave idle and on a second stream: every row
+    on the two-pass kernel, on the SMs the clusters leave idle (its programmatic dependent on the
+    same stream): every row
     (both shares and the boundary between them) against the oracle, for the fused step and for
     the read alone, with sharp gates and random gains."""
     D, r = 4096, 16

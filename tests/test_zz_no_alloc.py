@@ -5,8 +5,8 @@ cudaFree's device-wide synchronisation) against gr_write_then_read_host (caller-
 workspace): two fused steps in a
 row, each fed with the previous step's R' and s, give bit-identical results. On a shape that
 gr_write_then_read_host splits between the cluster kernel and the two-pass kernel, the static
-entry runs the cluster kernel alone (the split's internal stream and events would be created on
-first use): R' is still bit-identical, x and s agree within the bf16 tolerance. The file is
+entry runs the cluster kernel alone: R' is still bit-identical, x and s agree within the bf16
+tolerance. The file is
 collected last on purpose, so the static entry also runs after every other test has used the
 library in the same process. Beside the comparison with the other host entry, the static entry's
 two chained steps are checked directly against the fp64 oracle's chain of the same two steps
