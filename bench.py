@@ -488,6 +488,10 @@ def run_gr(args, w) -> None:
         torch.cuda.synchronize(dev)
         sampler = ClockSampler(uuid)
         sampler.start()
+        # The GPU idled while the sampler started. Untimed steps (as many as the warm-up) are
+        # queued right before the first timed event, so that the window opens on a busy GPU.
+        for i in range(max(1, args.warmup)):
+            step(i)
         if flush:
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
@@ -667,6 +671,7 @@ def run_backward(args, w) -> None:
         dist.barrier()
     sampler = ClockSampler(str(getattr(props, "uuid", "") or ""))
     sampler.start()
+    step()   # untimed, queued right before the window: it opens on a busy GPU
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -804,6 +809,7 @@ def run_decompose(args, w) -> None:
         dist.barrier()
     sampler = ClockSampler(str(getattr(props, "uuid", "") or ""))
     sampler.start()
+    step()   # untimed, queued right before the window: it opens on a busy GPU
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
