@@ -134,16 +134,19 @@ int gr_read(const gr_shape* shape, const void* R, const gr_params* params, void*
  * bf16 states with d_model a multiple of 64 and a rank r with 64 <= r <= GR_MAX_RANK_TC,
  * r % 8 == 0 (and at most 2^31 - 2^16 tokens a call), run on the tcgen05 tensor cores
  * ("tc_bf16" in gr_kernel_path): three launches
- * (the write and each row's 1/rms; the down projection as a GEMM of the rms-scaled state with the
- * packed [W_d; W_w]; the up projection as a GEMM with the gate and combine in its epilogue). Its
- * numerics: the down projection's inputs are bf16(R'·inv_i) and the packed bf16 weights, h is
- * rounded to bf16 for the up projection, W_u is bf16; fp32 accumulation throughout. It needs a
- * device workspace between its launches, so these shapes take the _ws entries below; gr_read
- * and gr_write_then_read return GR_E_SIZE for them and the host-buffer entries GR_E_RANK. */
+ * (the write with each branch's projection [W_d; W_w]·γ_i of its unscaled stored rows, as a GEMM
+ * a (128-token tile, branch); the per-token gates, which apply each branch's 1/rms to those
+ * projections; the up projection as a GEMM with the gate and combine in its epilogue). Its
+ * numerics: the down projection's inputs are the stored bf16 rows and the packed bf16 weights,
+ * the 1/rms factors are applied afterwards in fp32, h is rounded to bf16 for the up projection,
+ * W_u is bf16; fp32 accumulation throughout. It needs a device workspace between its launches,
+ * so these shapes take the _ws entries below; gr_read and gr_write_then_read return GR_E_SIZE
+ * for them and the host-buffer entries GR_E_RANK. */
 
-/* Bytes of device workspace a read or fused step of this shape needs: N·16 (each row's 1/rms)
- * plus N·round_up(r, 64)·2 (h in bf16), each rounded up to 256, on the large-rank path; 0 for
- * every other shape. */
+/* Bytes of device workspace a read or fused step of this shape needs on the large-rank path, each
+ * part rounded up to 256: N·16 (each row's 1/rms), N·round_up(r, 64)·2 (h in bf16),
+ * N·16·round_up(r + 4, 4) (the four branches' r + 4 projections in fp32) and N·16 (each row's
+ * sum of squares); 0 for every other shape. */
 int gr_step_workspace_size(const gr_shape* shape, size_t* bytes);
 
 /* gr_read and gr_write_then_read with a caller-owned DEVICE workspace (256-byte aligned, at

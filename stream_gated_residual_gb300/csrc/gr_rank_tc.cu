@@ -1,30 +1,28 @@
 // The read at the pages' own rank, r = d/8 ("【论文解读】 Qwen3.8 Flash Next", §二.4: W_d is
 // r × n_r·d with r = d/8), on the 5th-generation tensor cores (tcgen05, accumulators in tensor
 // memory, operands staged by TMA). At r in the hundreds the read is a dense contraction of about
-// 4·r·4D flops a token, as much arithmetic as memory traffic, so the projections run as two
-// GEMMs and everything else rides in their prologue and epilogue:
+// 4·r·4D flops a token, as much arithmetic as memory traffic, so the projections run as GEMMs
+// and everything else rides in their prologue and epilogue:
 //
-//   1. rownorm_kernel   eq write (R' = R + s_prev·y, stored bf16, as gr_write computes it) and
-//                       the stored row's inv_i = 1/√(mean R'_i² + eps) into the workspace;
-//                       one warp per (token, branch) row.
-//   2. down_tc_kernel   [z | u] = [W_d; W_w]·γ ⊙ vec(R' ⊙ inv) for 128 tokens a CTA: TMA brings
-//                       R' and the packed bf16 rows of [W_d; W_w] (γ folded) 64 channels at a
-//                       time; four warps scale their token rows of each R' stage by inv_i in
-//                       shared memory (eq rms), split into bf16 hi + lo; one thread issues the
-//                       MMAs of both halves into a 128 × (r+4) fp32 accumulator in tensor memory;
-//                       the epilogue writes h = SiLU(z/4) as bf16 into the workspace and
-//                       s = 2σ(u/4) (eq gate, eq s).
-//   3. up_tc_kernel     g = W_u h for 128 tokens × 4 branches × 32 channels a step (eq gate), two
-//                       accumulators in tensor memory so the MMAs of one channel block overlap
-//                       the epilogue of the previous one; the epilogue forms G = σ(g) and
-//                       x = ¼ Σ_i G_i γ_i inv_i R'_i from a TMA copy of the block's R' (eq
-//                       use_gate).
+//   1. write_down_tc_kernel  one CTA per (128-token tile, branch i): the write R'_i = R_i +
+//                            s_i·y (eq write, stored bf16, back to HBM by TMA store) stage by
+//                            stage, each row's sum of squares, and the branch's projection
+//                            P_i = [W_d; W_w]^(i)·γ_i R'_i of the unscaled stored rows (exact in
+//                            bf16: one bf16 MMA) into a (r+4)-column fp32 accumulator in tensor
+//                            memory; P_i and the sums of squares go to the step workspace.
+//   2. gates_kernel          per token: inv_i = 1/√(ssq_i/D + eps) (eq rms), z and u = ¼ Σ_i
+//                            inv_i P_i (eq gate, eq s: the normalisation is linear, so it can
+//                            follow the contraction), h = SiLU(z) as bf16, s = 2σ(u).
+//   3. up_tc_kernel          g = W_u h for 128 tokens × 4 branches × 32 channels a step (eq gate),
+//                            two accumulators in tensor memory so the MMAs of one channel block
+//                            overlap the epilogue of the previous one; the epilogue forms G = σ(g)
+//                            and x = ¼ Σ_i G_i γ_i inv_i R'_i from a TMA copy of the block's R'
+//                            (eq use_gate).
 //
-// Warp roles of both GEMM kernels (192 threads): warp 0 issues the TMA loads, warp 1 owns the
-// tensor memory and issues the MMAs, warps 2-5 (one per tensor-memory lane quadrant) scale and
-// run the epilogue. Every mbarrier wait is bounded; a wait that runs out records a status bit
-// and the kernel finishes without the work.
+// Every mbarrier wait is bounded; a wait that runs out records a status bit and the kernel
+// finishes without the work.
 #include <math.h>
+#include <string.h>
 
 #include "gr_internal.h"
 #include "gr_ptx.cuh"
@@ -36,7 +34,6 @@ namespace {
 constexpr int kTile = 128;          // tokens per CTA: the MMA's M
 constexpr int kKc = 64;             // K elements per operand stage (128-byte rows)
 constexpr int kStageA = kTile * 128; // one 128-token × 64-channel bf16 stage
-constexpr int kGemmThreads = 192;   // down projection: producer, MMA, 4 scaling/epilogue warps
 constexpr int kUpThreads = 352;     // up projection: producer, MMA, 8 epilogue warps, R' loader
 constexpr int kUpEpiWarps = 8;      // two per tensor-memory lane quadrant, 16 channels each
 constexpr int kCb = 32;             // channels per branch in an up-projection block
@@ -48,83 +45,49 @@ __device__ __forceinline__ float sigm_fast(float a) {
     return fmaf(0.5f, tanh_approx(0.5f * a), 0.5f);
 }
 
-// ---- 1. eq write and the stored row's 1/rms --------------------------------------------------
-__global__ void __launch_bounds__(256)
-rownorm_kernel(int64_t N, int D, float eps, __nv_bfloat16* __restrict__ R,
-               const __nv_bfloat16* __restrict__ y, const float* __restrict__ s_prev,
-               float* __restrict__ inv) {
-    const int lane = threadIdx.x & 31;
-    const int64_t rows = N * kBranches;
-    const int d8 = D / 8;
-    for (int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5); row < rows;
-         row += int64_t(gridDim.x) * 8) {
-        const int64_t t = row / kBranches;
-        uint4* Rr = reinterpret_cast<uint4*>(R + row * D);
-        const uint4* yr = y ? reinterpret_cast<const uint4*>(y + t * D) : nullptr;
-        const float s = y ? s_prev[row] : 0.f;
-        float ss = 0.f;
-        for (int c = lane; c < d8; c += 32) {
-            uint4 q = Rr[c];
-            uint32_t w[4] = {q.x, q.y, q.z, q.w};
-            if (y) {
-                const uint4 yq = __ldg(yr + c);
-                const uint32_t yw[4] = {yq.x, yq.y, yq.z, yq.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float lo = fmaf(s, __uint_as_float(yw[k] << 16),
-                                          __uint_as_float(w[k] << 16));
-                    const float hi = fmaf(s, __uint_as_float(yw[k] & 0xffff0000u),
-                                          __uint_as_float(w[k] & 0xffff0000u));
-                    w[k] = pack_bf2(lo, hi);
-                }
-                Rr[c] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float lo = __uint_as_float(w[k] << 16);
-                const float hi = __uint_as_float(w[k] & 0xffff0000u);
-                ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) inv[row] = rsqrtf(ss / float(D) + eps);
-    }
-}
-
-// ---- 2. down projection --------------------------------------------------------------------
-// Shared memory: `stages` × {A_hi, A_lo: 128 rows × 128 B each, B: n1 rows × 128 B}, then the
-// barriers. The state rows arrive in A_hi; the scaling warps leave hi = bf16(R'·inv) there and the
-// rounding residual lo = bf16(R'·inv − hi) in A_lo, and both go through the MMA (the split keeps
-// the down projection's inputs to about 2^-16 relative instead of bf16's 2^-8).
-__host__ __device__ inline size_t down_stage_bytes(int n1) {
+// ---- 1. eq write and each branch's down projection -----------------------------------------
+// One CTA per (128-token tile, branch i): the write R'_i = R_i + s_i·y (eq write, stored bf16)
+// stage by stage, each row's sum of squares, and the branch's projection of the UNSCALED stored
+// rows, P_i = [W_d; W_w]^(i)·γ_i R'_i, on the tensor cores. R' is exact in bf16, so one bf16
+// MMA carries it; the 1/rms factor is applied afterwards in fp32 (kernel 2), which is why each
+// branch needs an accumulator of its own (a CTA of its own). R' leaves by TMA store.
+//
+// Shared memory: `stages` × {A: 128 rows × 128 B (R, then R' in place), Y: 128 × 128 B,
+// B: n1 rows × 128 B}, then the barriers. Warps: 0 producer, 1 MMA issuer (owns the tensor
+// memory), 2-5 the write and the epilogue (one per lane quadrant, thread = token row), 6 the R'
+// stores (the stage is free once its MMAs are done and its store has read it).
+constexpr int kWdThreads = 224;
+__host__ __device__ inline size_t wd_stage_bytes(int n1) {
     return 2 * kStageA + size_t(n1) * 128;
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
-down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
-               int64_t N, int D, int r, int n1,
-               int stages, const float* __restrict__ inv, __nv_bfloat16* __restrict__ h, int rp,
-               float* __restrict__ s_out) {
+template <bool WRITE>
+__global__ void __launch_bounds__(kWdThreads, 1)
+write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
+                     const __grid_constant__ CUtensorMap tmY,
+                     const __grid_constant__ CUtensorMap tmW, int64_t N, int D, int r, int n1,
+                     int stages, const float* __restrict__ s_prev, float* __restrict__ P, int ps,
+                     float* __restrict__ ssq) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) &
                                              ~uintptr_t(1023));
-    const size_t sb = down_stage_bytes(n1);
+    const size_t sb = wd_stage_bytes(n1);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + stages * sb);
-    uint64_t* scaled = full + 4;
-    uint64_t* empty = scaled + 4;
+    uint64_t* written = full + 4;
+    uint64_t* empty = written + 4;
     uint64_t* acc_full = empty + 4;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t0 = int64_t(blockIdx.x) * kTile;
-    const int nk = kBranches * D / kKc, cpb = D / kKc;
+    const int64_t t0 = int64_t(blockIdx.x >> 2) * kTile;
+    const int ib = int(blockIdx.x & 3);
+    const int nk = D / kKc;
     const uint32_t ncols = n1 > 256 ? 512 : 256;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&scaled[s], 4);
-            mbar_init(&empty[s], 1);   // the MMAs are done with the stage
+            mbar_init(&written[s], 4);
+            mbar_init(&empty[s], WRITE ? 2 : 1);   // the MMAs' commit (+ the store's read)
         }
         mbar_init(acc_full, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -140,17 +103,18 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint32_t bytes = uint32_t(kStageA + size_t(n1) * 128);   // what TMA brings
+            const uint32_t bytes = uint32_t(kStageA + (WRITE ? kStageA : 0) + size_t(n1) * 128);
+            const int half = n1 / 2;   // a box holds at most 256 rows: two boxes
             for (int kc = 0; kc < nk; ++kc) {
                 const int s = kc % stages;
                 if (kc >= stages && !mbar_wait(&empty[s], ((kc / stages) - 1) & 1)) break;
                 uint8_t* A = sm + s * sb;
                 uint8_t* B = A + 2 * kStageA;
-                const int half = n1 / 2;   // a box holds at most 256 rows: two boxes
                 mbar_expect_tx(&full[s], bytes);
-                tma_load_3d(A, &tmR, (kc % cpb) * kKc, kc / cpb, int(t0), &full[s]);
-                tma_load_2d(B, &tmW, kc * kKc, 0, &full[s]);
-                tma_load_2d(B + half * 128, &tmW, kc * kKc, half, &full[s]);
+                tma_load_3d(A, &tmR, kc * kKc, ib, int(t0), &full[s]);
+                if (WRITE) tma_load_2d(A + kStageA, &tmY, kc * kKc, int(t0), &full[s]);
+                tma_load_2d(B, &tmW, ib * D + kc * kKc, 0, &full[s]);
+                tma_load_2d(B + half * 128, &tmW, ib * D + kc * kKc, half, &full[s]);
             }
         }
     } else if (warp == 1) {
@@ -160,100 +124,97 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
             bool ok = true;
             for (int kc = 0; kc < nk && ok; ++kc) {
                 const int s = kc % stages;
-                // the stage's TMA bytes (weights too) and the scaled state rows
+                // the stage's TMA bytes (weights too) and the rows the write warps left in place
                 ok = mbar_wait(&full[s], (kc / stages) & 1) &&
-                     mbar_wait(&scaled[s], (kc / stages) & 1);
+                     mbar_wait(&written[s], (kc / stages) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t a = smem_u32(sm + s * sb), b = a + 2 * kStageA;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t acc = (kc | kk) != 0;
-                    const uint64_t ah = sdesc_sw128(a + kk * 32);
-                    const uint64_t al = sdesc_sw128(a + kStageA + kk * 32);
-                    const uint64_t b0 = sdesc_sw128(b + kk * 32);
-                    tc_mma(tmem, ah, b0, id0, acc);
-                    tc_mma(tmem, al, b0, id0, 1u);
-                    if (n1 > 256) {
-                        const uint64_t b1 = sdesc_sw128(b + 256 * 128 + kk * 32);
-                        tc_mma(tmem + 256, ah, b1, id1, acc);
-                        tc_mma(tmem + 256, al, b1, id1, 1u);
-                    }
+                    const uint64_t ad = sdesc_sw128(a + kk * 32);
+                    tc_mma(tmem, ad, sdesc_sw128(b + kk * 32), id0, acc);
+                    if (n1 > 256)
+                        tc_mma(tmem + 256, ad, sdesc_sw128(b + 256 * 128 + kk * 32), id1, acc);
                 }
                 tc_commit(&empty[s]);
             }
             if (ok) tc_commit(acc_full);
         }
+    } else if (warp == 6) {
+        // R' of each stage to HBM once the write warps have left it in place
+        if (WRITE && lane == 0) {
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % stages;
+                if (!mbar_wait(&written[s], (kc / stages) & 1)) break;
+                tma_store_3d(&tmR, sm + s * sb, kc * kKc, ib, int(t0));
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(&empty[s]);
+            }
+            bulk_wait_all();
+        }
     } else {
         // warps 2-5: lane quadrant q; thread row = token t0 + 32q + lane
         const int q = warp & 3, row = q * 32 + lane;
         const int64_t t = t0 + row;
-        float iv[kBranches];
-#pragma unroll
-        for (int i = 0; i < kBranches; ++i) iv[i] = t < N ? inv[t * kBranches + i] : 0.f;
+        const float sv = (WRITE && t < N) ? s_prev[t * kBranches + ib] : 0.f;
+        float ss = 0.f;
         bool ok = true;
         for (int kc = 0; kc < nk && ok; ++kc) {
             const int s = kc % stages;
             ok = mbar_wait(&full[s], (kc / stages) & 1);
             if (!ok) break;
-            const int i = kc / cpb;
-            const float m = i == 0 ? iv[0] : i == 1 ? iv[1] : i == 2 ? iv[2] : iv[3];
             uint8_t* rp8 = sm + s * sb + row * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 // logical chunk j sits at j ^ (row & 7): eight rows hit eight bank groups
                 const int off = (j ^ (row & 7)) * 16;
-                uint4* p = reinterpret_cast<uint4*>(rp8 + off);
-                const uint4 v = *p;
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t hi[4], lo[4];
+                uint4 v = *reinterpret_cast<const uint4*>(rp8 + off);
+                uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                if (WRITE) {
+                    const uint4 yv = *reinterpret_cast<const uint4*>(rp8 + kStageA + off);
+                    const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = fmaf(sv, __uint_as_float(yw[k] << 16),
+                                              __uint_as_float(w[k] << 16));
+                        const float hi = fmaf(sv, __uint_as_float(yw[k] & 0xffff0000u),
+                                              __uint_as_float(w[k] & 0xffff0000u));
+                        w[k] = pack_bf2(lo, hi);
+                    }
+                    *reinterpret_cast<uint4*>(rp8 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float a0 = __uint_as_float(w[k] << 16) * m;
-                    const float a1 = __uint_as_float(w[k] & 0xffff0000u) * m;
-                    hi[k] = pack_bf2(a0, a1);
-                    lo[k] = pack_bf2(a0 - __uint_as_float(hi[k] << 16),
-                                     a1 - __uint_as_float(hi[k] & 0xffff0000u));
+                    const float lo = __uint_as_float(w[k] << 16);
+                    const float hi = __uint_as_float(w[k] & 0xffff0000u);
+                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
                 }
-                *p = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(rp8 + kStageA + off) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            fence_proxy_async_smem();
+            if (WRITE) fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&scaled[s]);
+            if (lane == 0) mbar_arrive(&written[s]);
         }
-        // epilogue: h = SiLU(z/4) (bf16, zero in the padding up to rp), s = 2σ(u/4)
+        // epilogue: the branch's r + 4 projections of this row, and its sum of squares
         if (ok) ok = mbar_wait(acc_full, 0);
         tc_fence_after();
         if (ok) {
-            const int ncol = n1 > rp ? n1 : rp;
-            for (int c0 = 0; c0 < ncol; c0 += 16) {
+            // every lane takes part in the warp's tensor-memory loads (a row past N included);
+            // only rows of real tokens are stored
+            float* Prow = P + (t * kBranches + ib) * size_t(ps);
+            for (int c0 = 0; c0 < n1; c0 += 16) {
                 float v[16];
-                if (c0 < n1) {
-                    tmem_ld16(tmem + (uint32_t(q * 32) << 16) + c0, v);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                }
+                tmem_ld16(tmem + (uint32_t(q * 32) << 16) + c0, v);
                 if (t >= N) continue;
-                float hv[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = c0 + j;
-                    const float z = 0.25f * v[j];
-                    hv[j] = col < r ? z * sigm(z) : 0.f;
-                    if (col >= r && col < r + kBranches)
-                        s_out[t * kBranches + (col - r)] = 2.0f * sigm(z);
-                }
-                if (c0 < rp) {
-                    uint4* hp = reinterpret_cast<uint4*>(h + t * rp + c0);
-                    hp[0] = make_uint4(pack_bf2(hv[0], hv[1]), pack_bf2(hv[2], hv[3]),
-                                       pack_bf2(hv[4], hv[5]), pack_bf2(hv[6], hv[7]));
-                    hp[1] = make_uint4(pack_bf2(hv[8], hv[9]), pack_bf2(hv[10], hv[11]),
-                                       pack_bf2(hv[12], hv[13]), pack_bf2(hv[14], hv[15]));
-                }
+                for (int k4 = 0; k4 < 4; ++k4)
+                    if (c0 + 4 * k4 < ps)
+                        *reinterpret_cast<float4*>(Prow + c0 + 4 * k4) =
+                            make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
             }
+            if (t < N) ssq[t * kBranches + ib] = ss;
         }
     }
     tc_fence_before();
@@ -261,6 +222,35 @@ down_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ 
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
+    }
+}
+
+// ---- 2. eq rms, eq gate (z, h) and eq s from the branches' projections ---------------------------
+// One warp per token: inv_i = 1/√(ssq_i/D + eps), z = ¼ Σ_i inv_i P_i[0, r), u = ¼ Σ_i inv_i
+// P_i[r, r+4); h = SiLU(z) as bf16 (zero up to rp), s = 2σ(u), and inv for the up projection.
+__global__ void __launch_bounds__(256)
+gates_kernel(int64_t N, int D, int r, int rp, int ps, float eps, const float* __restrict__ P,
+             const float* __restrict__ ssq, __nv_bfloat16* __restrict__ h,
+             float* __restrict__ inv, float* __restrict__ s_out) {
+    const int lane = threadIdx.x & 31;
+    for (int64_t t = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5); t < N;
+         t += int64_t(gridDim.x) * 8) {
+        float iv[kBranches];
+#pragma unroll
+        for (int i = 0; i < kBranches; ++i)
+            iv[i] = rsqrtf(ssq[t * kBranches + i] / float(D) + eps);
+        if (lane < kBranches) inv[t * kBranches + lane] = iv[lane];
+        const float* Pt = P + t * kBranches * size_t(ps);
+        for (int k = lane; k < rp || k < r + kBranches; k += 32) {
+            float z = 0.f;
+            if (k < r + kBranches) {
+#pragma unroll
+                for (int i = 0; i < kBranches; ++i) z = fmaf(iv[i], Pt[i * size_t(ps) + k], z);
+                z *= 0.25f;
+            }
+            if (k < rp) h[t * rp + k] = __float2bfloat16_rn(k < r ? z * sigm(z) : 0.f);
+            if (k >= r && k < r + kBranches) s_out[t * kBranches + (k - r)] = 2.0f * sigm(z);
+        }
     }
 }
 
@@ -513,8 +503,14 @@ bool rank_tc_supported(int D, int r) {
 
 int rank_tc_padded(int r) { return (r + kKc - 1) / kKc * kKc; }
 
+// Floats per (token, branch) row of the branches' projections: r + 4, rounded to 16 bytes.
+static int rank_tc_pstride(int r) { return (r + kBranches + 3) / 4 * 4; }
+
+// inv [N][4] fp32 | h [N][rp] bf16 | P [N][4][ps] fp32 | ssq [N][4] fp32
 size_t rank_tc_workspace(int64_t N, int r) {
-    return align256(size_t(N) * kBranches * 4) + align256(size_t(N) * rank_tc_padded(r) * 2);
+    return align256(size_t(N) * kBranches * 4) + align256(size_t(N) * rank_tc_padded(r) * 2) +
+           align256(size_t(N) * kBranches * rank_tc_pstride(r) * 4) +
+           align256(size_t(N) * kBranches * 4);
 }
 
 cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const void* y,
@@ -526,42 +522,49 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
     const float* gamma = reinterpret_cast<const float*>(base + L.gamma32);
     const void* wdw = base + L.wdw;
     const void* wu = base + L.wu;
-    float* inv = static_cast<float*>(workspace);
-    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) +
-                                                        align256(size_t(N) * kBranches * 4));
     const int rp = rank_tc_padded(r);
+    const int ps = rank_tc_pstride(r);
+    char* wsb = static_cast<char*>(workspace);
+    float* inv = reinterpret_cast<float*>(wsb);
+    wsb += align256(size_t(N) * kBranches * 4);
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(wsb);
+    wsb += align256(size_t(N) * rp * 2);
+    float* P = reinterpret_cast<float*>(wsb);
+    wsb += align256(size_t(N) * kBranches * ps * 4);
+    float* ssq = reinterpret_cast<float*>(wsb);
     const int n1 = (r + kBranches + 15) / 16 * 16;
     const int K = kBranches * D;
 
-    // 1. write and row norms
-    {
-        const int64_t blocks = (N * kBranches + 7) / 8;
-        const int64_t cap = int64_t(sm_count()) * 8;
-        rownorm_kernel<<<unsigned(blocks < cap ? blocks : cap), 256, 0, st>>>(
-            N, D, eps, static_cast<__nv_bfloat16*>(R), static_cast<const __nv_bfloat16*>(y),
-            s_prev, inv);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     const unsigned tiles = unsigned((N + kTile - 1) / kTile);
-    // 2. down projection
+    // 1. the write and each branch's down projection: a CTA per (tile, branch)
     {
-        CUtensorMap mR, mW;
+        CUtensorMap mR, mY, mW;
+        memset(&mY, 0, sizeof(mY));
         if (!map_state(&mR, R, N, D, kKc, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            (y && !map_2d(&mY, y, D, N, size_t(D) * 2, kKc, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) ||
             !map_2d(&mW, wdw, K, r + kBranches, size_t(K) * 2, kKc, n1 / 2,
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        const size_t sb = down_stage_bytes(n1);
+        const size_t sb = wd_stage_bytes(n1);
         int stages = int((232448 - 1024 - 256) / sb);   // within 227 KB with alignment, barriers
         stages = stages > 4 ? 4 : stages;
         if (stages < 2) return cudaErrorInvalidValue;
         const size_t smem = 1024 + stages * sb + 256;
-        cudaError_t e = cudaFuncSetAttribute(down_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto kern = y ? write_down_tc_kernel<true> : write_down_tc_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        e = launch_plain(down_tc_kernel, tiles, kGemmThreads, smem, st, mR, mW, N, D, r, n1,
-                         stages, static_cast<const float*>(inv), h, rp, s_out);
+        e = launch_plain(kern, tiles * kBranches, kWdThreads, smem, st, mR, mY, mW, N, D, r, n1,
+                         stages, s_prev, P, ps, ssq);
+        if (e != cudaSuccess) return e;
+    }
+    // 2. inv, z, u, h and s per token
+    {
+        const int64_t blocks = (N + 7) / 8;
+        const int64_t cap = int64_t(sm_count()) * 8;
+        gates_kernel<<<unsigned(blocks < cap ? blocks : cap), 256, 0, st>>>(
+            N, D, r, rp, ps, eps, P, ssq, h, inv, s_out);
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     // 3. up projection, gate and combine

@@ -264,7 +264,9 @@ def test_large_rank_validation(lib):
     need = ctypes.c_size_t(0)
     tc = _shape(n=300, d=2560, r=320, dt=gr.GR_BF16)
     assert lib.gr_step_workspace_size(ctypes.byref(tc), ctypes.byref(need)) == 0
-    assert need.value == (300 * 16 + 255) // 256 * 256 + (300 * 320 * 2 + 255) // 256 * 256
+    a256 = lambda n: (n + 255) // 256 * 256
+    # 1/rms | h (bf16, r rounded up to 64) | the r + 4 projections of each branch (fp32) | ssq
+    assert need.value == a256(300 * 16) + a256(300 * 320 * 2) + a256(300 * 16 * 324) + a256(300 * 16)
     small = _shape(n=300, d=4096, r=16, dt=gr.GR_BF16)
     assert lib.gr_step_workspace_size(ctypes.byref(small), ctypes.byref(need)) == 0
     assert need.value == 0
