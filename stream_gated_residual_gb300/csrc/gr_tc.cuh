@@ -70,6 +70,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] · B[smem]ᵀ: A's row m in lane m, two 16-bit elements of consecutive k in
+// each 32-bit column (the lower k in the low half), so one K = 16 step reads 8 columns.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrives once on `bar` when every MMA this thread issued before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile(
@@ -120,6 +130,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     tmem_wait_ld(r);
 #pragma unroll
     for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+// ---- a bounded wait that never suspends ---------------------------------------------------------
+// For producers that share a warp (lanes with waits of their own): a suspending try_wait would
+// stop the whole warp. Spins on test_wait; records bit 0 of the status word if it runs out.
+__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n"
+            " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (clock64() - t0 > kWaitLimit) {
+            atomicOr(&g_wait_status, 1u);
+            return false;
+        }
+    }
 }
 
 // ---- TMA store of a 3-D box (the large-rank path's R' tiles) ---------------------------------
