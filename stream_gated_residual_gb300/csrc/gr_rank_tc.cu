@@ -453,11 +453,14 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CU
                         const int c = v8 * 8 + 2 * k;
                         const float w0 = gv[2 * k] * __uint_as_float(w[k] << 16);
                         const float w1 = gv[2 * k + 1] * __uint_as_float(w[k] & 0xffff0000u);
-                        acc[c] = fmaf(m, fmaf(w0, tanh_approx(__uint_as_float(g[i][c])), w0),
-                                      acc[c]);
-                        acc[c + 1] =
-                            fmaf(m, fmaf(w1, tanh_approx(__uint_as_float(g[i][c + 1])), w1),
-                                 acc[c + 1]);
+                        // tanh of both logits in one MUFU op on an f16 pair (2^-11 of the logit,
+                        // far inside the bf16 rounding of x); the epilogue is bound by that unit
+                        uint32_t th =
+                            pack_h2(__uint_as_float(g[i][c]), __uint_as_float(g[i][c + 1]));
+                        asm("tanh.approx.f16x2 %0, %0;" : "+r"(th));
+                        const float2 tf = __half22float2(*reinterpret_cast<const __half2*>(&th));
+                        acc[c] = fmaf(m, fmaf(w0, tf.x, w0), acc[c]);
+                        acc[c + 1] = fmaf(m, fmaf(w1, tf.y, w1), acc[c + 1]);
                     }
                 }
             }
