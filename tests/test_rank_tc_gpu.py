@@ -49,6 +49,19 @@ def test_fused_step(N, D, r):
     assert gr.device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("N,D,r", [(4000, 512, 64), (20000, 256, 64)])
+def test_tile_rows_and_waves(N, D, r):
+    """Token tiles shorter than the MMA's 128 rows, sized to fill whole waves of SMs: 4000
+    tokens give the write pass tiles of about 106 rows (the rows past a tile's own are loaded,
+    never stored) and 20000 tokens run the up projection in two waves of 66-row tiles; every
+    row against the oracle, so a row stored twice or never, or a neighbour's rows leaking into
+    a tile, fails."""
+    w = wl.Workload("tcrows", N, D, r, "bf16", y_std=0.5, seed=73)
+    assert gr.kernel_path(N, D, r, torch.bfloat16) == "tc_bf16"
+    _check(*fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    assert gr.device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("N,D,r", [(200, 2560, 320), (64, 1024, 64)])
 def test_workload_weights_against_plain_definition(N, D, r):
     """At the workloads' weight scale (N(0, 0.02), unit gains) also within the bf16 bound of
