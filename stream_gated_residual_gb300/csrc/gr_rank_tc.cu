@@ -39,20 +39,26 @@ constexpr int kMaxRankTc = 448;     // r + 4 <= 512 accumulator columns; H fits 
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
 // ---- 1. eq write and each branch's down projection -----------------------------------------
-// One CTA per (tile, branch i): the write R'_i = R_i + s_i·y (eq write, stored bf16)
-// stage by stage, each row's sum of squares, and the branch's projection of the UNSCALED stored
-// rows, P_i = [W_d; W_w]^(i)·γ_i R'_i, on the tensor cores. R' is exact in bf16, so one bf16
-// MMA carries it; the 1/rms factor is applied afterwards in fp32 (kernel 2), which is why each
-// branch needs an accumulator of its own (a CTA of its own). R' leaves by TMA store.
-// A tile is `rows` <= 128 tokens, chosen by the host so that the grid fills whole waves of SMs;
+// Units of work are (tile, branch i): the write R'_i = R_i + s_i·y (eq write, stored bf16) stage
+// by stage, each row's sum of squares, and the branch's projection of the UNSCALED stored rows,
+// P_i = [W_d; W_w]^(i)·γ_i R'_i, on the tensor cores. R' is exact in bf16, so one bf16 MMA
+// carries it; the 1/rms factor is applied afterwards in fp32 (kernel 2), which is why each branch
+// needs an accumulator of its own. R' leaves by TMA store.
+// A persistent grid: CTA c takes units c, c + G, c + 2G, ... (G a multiple of 4, so the four
+// branch units of a tile run side by side and share y through L2), and one ring of stages runs
+// through all of them: the next unit's loads, writes and stores go on while four warps of their
+// own drain the previous unit's accumulator and store its P rows; only the next unit's first
+// MMA waits for that drain.
+// A tile is `rows` <= 128 tokens, chosen by the host so that the units fill whole waves of SMs;
 // the MMA always spans 128 rows: the rows past the tile's own (the next tile's tokens, or past N)
 // are loaded but never stored, and their accumulator rows are dropped.
 //
 // Shared memory: `stages` × {A: 128 rows × 128 B (R, then R' in place), Y: 128 × 128 B,
-// B: n1 rows × 128 B}, then the barriers. Warps: 0 producer, 1 MMA issuer (owns the tensor
-// memory), 2-5 the write and the epilogue (one per lane quadrant, thread = token row), 6 the R'
-// stores (the stage is free once its MMAs are done and its store has read it).
-constexpr int kWdThreads = 224;
+// B: n1 rows × 128 B}, then the barriers and two 128-float buffers of row sums of squares.
+// Warps: 0 producer, 1 MMA issuer (owns the tensor memory), 2-5 the write (one per lane quadrant,
+// thread = token row), 6 the R' stores (a stage is free once its MMAs are done and its store has
+// read it), 7-10 the epilogue (one per lane quadrant).
+constexpr int kWdThreads = 352;
 __host__ __device__ inline size_t wd_stage_bytes(int n1) {
     return 2 * kStageA + size_t(n1) * 128;
 }
@@ -63,7 +69,7 @@ write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
                      const __grid_constant__ CUtensorMap tmS,
                      const __grid_constant__ CUtensorMap tmY,
                      const __grid_constant__ CUtensorMap tmW, int64_t N, int D, int r, int n1,
-                     int stages, int rows, const float* __restrict__ s_prev,
+                     int stages, int rows, int units, const float* __restrict__ s_prev,
                      float* __restrict__ P, int ps, float* __restrict__ ssq) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) &
@@ -72,13 +78,20 @@ write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + stages * sb);
     uint64_t* written = full + 4;
     uint64_t* empty = written + 4;
-    uint64_t* acc_full = empty + 4;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* acc_full = empty + 4;      // [2]: a unit's MMAs are done
+    uint64_t* acc_empty = acc_full + 2;  // the epilogue has read the accumulator
+    uint64_t* ss_full = acc_empty + 1;   // [2]: a unit's sums of squares are in ssbuf
+    uint64_t* ss_empty = ss_full + 2;    // [2]: the epilogue has read them
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(ss_empty + 2);
+    float* ssbuf = reinterpret_cast<float*>(sm + stages * sb + 256);   // [2][128]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t0 = int64_t(blockIdx.x >> 2) * rows;
-    const int ib = int(blockIdx.x & 3);
     const int nk = D / kKc;
     const uint32_t ncols = n1 > 256 ? 512 : 256;
+    const int G = int(gridDim.x);
+    const int nu = units > int(blockIdx.x) ? (units - int(blockIdx.x) + G - 1) / G : 0;
+    // unit j of this CTA: tile and branch, and the tile's first token
+    auto unit_ib = [&](int j) { return (int(blockIdx.x) + j * G) & 3; };
+    auto unit_t0 = [&](int j) { return int64_t((int(blockIdx.x) + j * G) >> 2) * rows; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
@@ -86,7 +99,12 @@ write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
             mbar_init(&written[s], 4);
             mbar_init(&empty[s], WRITE ? 2 : 1);   // the MMAs' commit (+ the store's read)
         }
-        mbar_init(acc_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&ss_full[b], 4);
+            mbar_init(&ss_empty[b], 4);
+        }
+        mbar_init(acc_empty, 4);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -102,16 +120,24 @@ write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
         if (lane == 0) {
             const uint32_t bytes = uint32_t(kStageA + (WRITE ? kStageA : 0) + size_t(n1) * 128);
             const int half = n1 / 2;   // a box holds at most 256 rows: two boxes
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % stages;
-                if (kc >= stages && !mbar_wait(&empty[s], ((kc / stages) - 1) & 1)) break;
-                uint8_t* A = sm + s * sb;
-                uint8_t* B = A + 2 * kStageA;
-                mbar_expect_tx(&full[s], bytes);
-                tma_load_3d(A, &tmR, kc * kKc, ib, int(t0), &full[s]);
-                if (WRITE) tma_load_2d(A + kStageA, &tmY, kc * kKc, int(t0), &full[s]);
-                tma_load_2d(B, &tmW, ib * D + kc * kKc, 0, &full[s]);
-                tma_load_2d(B + half * 128, &tmW, ib * D + kc * kKc, half, &full[s]);
+            bool ok = true;
+            for (int j = 0; j < nu && ok; ++j) {
+                const int ib = unit_ib(j);
+                const int t0 = int(unit_t0(j));
+                for (int kc = 0; kc < nk; ++kc) {
+                    const int g = j * nk + kc, s = g % stages;
+                    if (g >= stages && !mbar_wait(&empty[s], ((g / stages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* A = sm + s * sb;
+                    uint8_t* B = A + 2 * kStageA;
+                    mbar_expect_tx(&full[s], bytes);
+                    tma_load_3d(A, &tmR, kc * kKc, ib, t0, &full[s]);
+                    if (WRITE) tma_load_2d(A + kStageA, &tmY, kc * kKc, t0, &full[s]);
+                    tma_load_2d(B, &tmW, ib * D + kc * kKc, 0, &full[s]);
+                    tma_load_2d(B + half * 128, &tmW, ib * D + kc * kKc, half, &full[s]);
+                }
             }
         }
     } else if (warp == 1) {
@@ -119,87 +145,64 @@ write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
             const uint32_t id0 = idesc_bf16_f32(kTile, n1 > 256 ? 256 : n1);
             const uint32_t id1 = idesc_bf16_f32(kTile, n1 > 256 ? n1 - 256 : 16);
             bool ok = true;
-            for (int kc = 0; kc < nk && ok; ++kc) {
-                const int s = kc % stages;
-                // the stage's TMA bytes (weights too) and the rows the write warps left in place
-                ok = mbar_wait(&full[s], (kc / stages) & 1) &&
-                     mbar_wait(&written[s], (kc / stages) & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t a = smem_u32(sm + s * sb), b = a + 2 * kStageA;
+            for (int j = 0; j < nu && ok; ++j) {
+                // the previous unit's accumulator has been read out
+                if (j > 0) ok = mbar_wait(acc_empty, (j - 1) & 1);
+                for (int kc = 0; kc < nk && ok; ++kc) {
+                    const int g = j * nk + kc, s = g % stages;
+                    // the stage's TMA bytes (weights too) and the rows the write warps left in
+                    // place
+                    ok = mbar_wait(&full[s], (g / stages) & 1) &&
+                         mbar_wait(&written[s], (g / stages) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a = smem_u32(sm + s * sb), b = a + 2 * kStageA;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t acc = (kc | kk) != 0;
-                    const uint64_t ad = sdesc_sw128(a + kk * 32);
-                    tc_mma(tmem, ad, sdesc_sw128(b + kk * 32), id0, acc);
-                    if (n1 > 256)
-                        tc_mma(tmem + 256, ad, sdesc_sw128(b + 256 * 128 + kk * 32), id1, acc);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = (kc | kk) != 0;
+                        const uint64_t ad = sdesc_sw128(a + kk * 32);
+                        tc_mma(tmem, ad, sdesc_sw128(b + kk * 32), id0, acc);
+                        if (n1 > 256)
+                            tc_mma(tmem + 256, ad, sdesc_sw128(b + 256 * 128 + kk * 32), id1, acc);
+                    }
+                    tc_commit(&empty[s]);
                 }
-                tc_commit(&empty[s]);
+                if (ok) tc_commit(&acc_full[j & 1]);
             }
-            if (ok) tc_commit(acc_full);
         }
     } else if (warp == 6) {
         // R' of each stage to HBM once the write warps have left it in place. (Keeping two stores
         // in flight hands each stage back one stage later, which costs the ring a stage: slower.)
         if (WRITE && lane == 0) {
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % stages;
-                if (!mbar_wait(&written[s], (kc / stages) & 1)) break;
-                tma_store_3d(&tmS, sm + s * sb, kc * kKc, ib, int(t0));
-                bulk_commit();
-                bulk_wait_read<0>();
-                mbar_arrive(&empty[s]);
+            bool ok = true;
+            for (int j = 0; j < nu && ok; ++j) {
+                const int ib = unit_ib(j);
+                const int t0 = int(unit_t0(j));
+                for (int kc = 0; kc < nk; ++kc) {
+                    const int g = j * nk + kc, s = g % stages;
+                    if (!mbar_wait(&written[s], (g / stages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tma_store_3d(&tmS, sm + s * sb, kc * kKc, ib, t0);
+                    bulk_commit();
+                    bulk_wait_read<0>();
+                    mbar_arrive(&empty[s]);
+                }
             }
             bulk_wait_all();
         }
-    } else {
-        // warps 2-5: lane quadrant q; thread row = token t0 + 32q + lane
+    } else if (warp >= 7) {
+        // warps 7-10: the epilogue of each unit, lane quadrant q, thread row = token t0 + 32q + lane
         const int q = warp & 3, row = q * 32 + lane;
-        const int64_t t = t0 + row;
-        const bool mine = row < rows && t < N;   // the tile's own token (the rest are ignored)
-        const float sv = (WRITE && mine) ? s_prev[t * kBranches + ib] : 0.f;
-        float ss = 0.f;
         bool ok = true;
-        for (int kc = 0; kc < nk && ok; ++kc) {
-            const int s = kc % stages;
-            ok = mbar_wait(&full[s], (kc / stages) & 1);
+        for (int j = 0; j < nu && ok; ++j) {
+            const int ib = unit_ib(j);
+            const int64_t t = unit_t0(j) + row;
+            const bool mine = row < rows && t < N;
+            ok = mbar_wait(&acc_full[j & 1], (j >> 1) & 1);
             if (!ok) break;
-            uint8_t* rp8 = sm + s * sb + row * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                // logical chunk j sits at j ^ (row & 7): eight rows hit eight bank groups
-                const int off = (j ^ (row & 7)) * 16;
-                uint4 v = *reinterpret_cast<const uint4*>(rp8 + off);
-                uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                if (WRITE) {
-                    const uint4 yv = *reinterpret_cast<const uint4*>(rp8 + kStageA + off);
-                    const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float lo = fmaf(sv, __uint_as_float(yw[k] << 16),
-                                              __uint_as_float(w[k] << 16));
-                        const float hi = fmaf(sv, __uint_as_float(yw[k] & 0xffff0000u),
-                                              __uint_as_float(w[k] & 0xffff0000u));
-                        w[k] = pack_bf2(lo, hi);
-                    }
-                    *reinterpret_cast<uint4*>(rp8 + off) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float lo = __uint_as_float(w[k] << 16);
-                    const float hi = __uint_as_float(w[k] & 0xffff0000u);
-                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-                }
-            }
-            if (WRITE) fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&written[s]);
-        }
-        // epilogue: the branch's r + 4 projections of this row, and its sum of squares
-        if (ok) ok = mbar_wait(acc_full, 0);
-        tc_fence_after();
-        if (ok) {
+            tc_fence_after();
             // every lane takes part in the warp's tensor-memory loads (a row past N included);
             // only rows of real tokens are stored
             float* Prow = P + (t * kBranches + ib) * size_t(ps);
@@ -213,7 +216,67 @@ write_down_tc_kernel(const __grid_constant__ CUtensorMap tmR,
                         *reinterpret_cast<float4*>(Prow + c0 + 4 * k4) =
                             make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
             }
-            if (mine) ssq[t * kBranches + ib] = ss;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+            ok = mbar_wait(&ss_full[j & 1], (j >> 1) & 1);
+            if (!ok) break;
+            if (mine) ssq[t * kBranches + ib] = ssbuf[(j & 1) * 128 + row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ss_empty[j & 1]);
+        }
+    } else {
+        // warps 2-5: the write; lane quadrant q; thread row = token t0 + 32q + lane
+        const int q = warp & 3, row = q * 32 + lane;
+        bool ok = true;
+        for (int j = 0; j < nu && ok; ++j) {
+            const int ib = unit_ib(j);
+            const int64_t t = unit_t0(j) + row;
+            const bool mine = row < rows && t < N;   // the tile's own token (the rest are ignored)
+            const float sv = (WRITE && mine) ? s_prev[t * kBranches + ib] : 0.f;
+            float ss = 0.f;
+            for (int kc = 0; kc < nk && ok; ++kc) {
+                const int g = j * nk + kc, s = g % stages;
+                ok = mbar_wait(&full[s], (g / stages) & 1);
+                if (!ok) break;
+                uint8_t* rp8 = sm + s * sb + row * 128;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    // logical chunk jj sits at jj ^ (row & 7): eight rows hit eight bank groups
+                    const int off = (jj ^ (row & 7)) * 16;
+                    uint4 v = *reinterpret_cast<const uint4*>(rp8 + off);
+                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    if (WRITE) {
+                        const uint4 yv = *reinterpret_cast<const uint4*>(rp8 + kStageA + off);
+                        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float lo = fmaf(sv, __uint_as_float(yw[k] << 16),
+                                                  __uint_as_float(w[k] << 16));
+                            const float hi = fmaf(sv, __uint_as_float(yw[k] & 0xffff0000u),
+                                                  __uint_as_float(w[k] & 0xffff0000u));
+                            w[k] = pack_bf2(lo, hi);
+                        }
+                        *reinterpret_cast<uint4*>(rp8 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = __uint_as_float(w[k] << 16);
+                        const float hi = __uint_as_float(w[k] & 0xffff0000u);
+                        ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                    }
+                }
+                if (WRITE) fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&written[s]);
+            }
+            if (!ok) break;
+            // the unit's sums of squares to the epilogue (its buffer free again two units on)
+            if (j >= 2) ok = mbar_wait(&ss_empty[j & 1], ((j >> 1) - 1) & 1);
+            if (!ok) break;
+            ssbuf[(j & 1) * 128 + row] = ss;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ss_full[j & 1]);
         }
     }
     tc_fence_before();
@@ -596,7 +659,7 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
     const int K = kBranches * D;
 
     const int64_t sms = sm_count();
-    // 1. the write and each branch's down projection: a CTA per (tile, branch)
+    // 1. the write and each branch's down projection: units (tile, branch) on a persistent grid
     {
         const int rows = rank_tc_tile_rows(N, kBranches, sms);
         const unsigned tiles = unsigned((N + rows - 1) / rows);
@@ -609,16 +672,22 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const size_t sb = wd_stage_bytes(n1);
-        int stages = int((232448 - 1024 - 256) / sb);   // within 227 KB with alignment, barriers
+        // the stages, then 256 bytes of barriers and two 512-byte buffers of sums of squares
+        int stages = int((232448 - 1024 - 1280) / sb);
         stages = stages > 4 ? 4 : stages;
         if (stages < 2) return cudaErrorInvalidValue;
-        const size_t smem = 1024 + stages * sb + 256;
+        const size_t smem = 1024 + stages * sb + 1280;
         auto kern = y ? write_down_tc_kernel<true> : write_down_tc_kernel<false>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        e = launch_plain(kern, tiles * kBranches, kWdThreads, smem, st, mR, mS, mY, mW, N, D, r,
-                         n1, stages, rows, s_prev, P, ps, ssq);
+        // a persistent grid: a multiple of 4 CTAs (the branch units of a tile side by side)
+        const int units = int(tiles) * kBranches;
+        int grid = int(sms) / kBranches * kBranches;
+        grid = grid < 4 ? 4 : grid;
+        grid = grid > units ? units : grid;
+        e = launch_plain(kern, unsigned(grid), kWdThreads, smem, st, mR, mS, mY, mW, N, D, r,
+                         n1, stages, rows, units, s_prev, P, ps, ssq);
         if (e != cudaSuccess) return e;
     }
     // 2. inv, z, u, h and s per token
