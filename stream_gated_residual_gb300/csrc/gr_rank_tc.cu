@@ -4,12 +4,12 @@
 // 4·r·4D flops a token, as much arithmetic as memory traffic, so the projections run as GEMMs
 // and everything else rides in their prologue and epilogue:
 //
-//   1. write_down_tc_kernel  one CTA per (tile of <= 128 tokens, branch i): the write R'_i = R_i +
-//                            s_i·y (eq write, stored bf16, back to HBM by TMA store) stage by
-//                            stage, each row's sum of squares, and the branch's projection
-//                            P_i = [W_d; W_w]^(i)·γ_i R'_i of the unscaled stored rows (exact in
-//                            bf16: one bf16 MMA) into a (r+4)-column fp32 accumulator in tensor
-//                            memory; P_i and the sums of squares go to the step workspace.
+//   1. write_down_tc_kernel  units of (tile of <= 128 tokens, branch i) on a persistent grid: the
+//                            write R'_i = R_i + s_i·y (eq write, stored bf16, back to HBM by TMA
+//                            store) stage by stage, each row's sum of squares, and the branch's
+//                            projection P_i = [W_d; W_w]^(i)·γ_i R'_i of the unscaled stored rows
+//                            (exact in bf16: one bf16 MMA) into a (r+4)-column fp32 accumulator in
+//                            tensor memory; P_i and the sums of squares go to the step workspace.
 //   2. gates_kernel          per token: inv_i = 1/√(ssq_i/D + eps) (eq rms), z and u = ¼ Σ_i
 //                            inv_i P_i (eq gate, eq s: the normalisation is linear, so it can
 //                            follow the contraction), h/2 = ½ SiLU(z) as bf16, s = 2σ(u).
