@@ -31,10 +31,12 @@
 namespace gr {
 namespace {
 
-constexpr int kTile = 128;          // tokens per CTA: the MMA's M
+constexpr int kTile = 128;          // the MMAs' M: rows of a tile (its tokens are up to this many)
 constexpr int kKc = 64;             // K elements per operand stage (128-byte rows)
-constexpr int kStageA = kTile * 128; // one 128-token × 64-channel bf16 stage
-constexpr int kMaxRankTc = 448;     // r + 4 <= 512 accumulator columns; H fits shared memory
+constexpr int kStageA = kTile * 128; // one 128-row × 64-channel bf16 stage
+// r + 4 <= 512 accumulator columns in the write pass; h/2 (r/2 columns, r rounded up to 64)
+// beside the up projection's 256-column accumulator in its 512
+constexpr int kMaxRankTc = 448;
 
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
