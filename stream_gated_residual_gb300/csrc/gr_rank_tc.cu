@@ -298,6 +298,11 @@ __global__ void __launch_bounds__(256)
 gates_kernel(int64_t N, int D, int r, int rp, int ps, float eps, const float* __restrict__ P,
              const float* __restrict__ ssq, __nv_bfloat16* __restrict__ h,
              float* __restrict__ inv, float* __restrict__ s_out) {
+    // the write pass's P and ssq are complete and visible past this wait; once every CTA of this
+    // one-wave grid has passed it, the up projection (whose own R' loads need that grid, not this
+    // one) may launch and start its weight and R' loads while these CTAs finish
+    dep_wait();
+    dep_launch_dependents();
     const int lane = threadIdx.x & 31;
     for (int64_t t = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5); t < N;
          t += int64_t(gridDim.x) * 8) {
@@ -449,6 +454,8 @@ up_tc_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CU
     } else {
         // warps 2-17: lane quadrant q = warp % 4, 16-channel quarter hq of each 64-channel block
         // (in R' half block hq / 2, at its 16-channel half hq % 2)
+        // h and inv come from the gates kernel, this launch's programmatic predecessor
+        dep_wait();
         const int q = warp & 3, hq = (warp - 2) >> 2, row = q * 32 + lane;
         constexpr int kH = 16;
         const int64_t t = t0 + row;
@@ -594,15 +601,22 @@ bool map_nd(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* p,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Plain launch (no cluster): every CTA loads its own operands.
+// Plain launch (no cluster): every CTA loads its own operands. `programmatic`: launched as the
+// programmatic dependent of the preceding launch on the stream (it may start before that one
+// ends; it waits with dep_wait before it reads that launch's results).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_plain(void (*kern)(KArgs...), unsigned grid, int threads, size_t smem,
-                         cudaStream_t st, Args... args) {
+                         cudaStream_t st, bool programmatic, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
@@ -688,17 +702,21 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
         int grid = int(sms) / kBranches * kBranches;
         grid = grid < 4 ? 4 : grid;
         grid = grid > units ? units : grid;
-        e = launch_plain(kern, unsigned(grid), kWdThreads, smem, st, mR, mS, mY, mW, N, D, r,
-                         n1, stages, rows, units, s_prev, P, ps, ssq);
+        e = launch_plain(kern, unsigned(grid), kWdThreads, smem, st, false, mR, mS, mY, mW, N, D,
+                         r, n1, stages, rows, units, s_prev, P, ps, ssq);
         if (e != cudaSuccess) return e;
     }
     // 2. inv, z, u, h and s per token
     {
+        // a programmatic dependent of the write pass, which triggers nothing: the gates CTAs start
+        // as the write pass's leave (triggered at the write pass's start, CTAs parked beside it
+        // made the step 10 µs slower). One wave (8 CTAs of 256 threads an SM), so that every CTA
+        // passes its dep_wait, and triggers the up projection's launch, without waiting for
+        // another CTA to leave.
         const int64_t blocks = (N + 7) / 8;
         const int64_t cap = sms * 8;
-        gates_kernel<<<unsigned(blocks < cap ? blocks : cap), 256, 0, st>>>(
-            N, D, r, rp, ps, eps, P, ssq, h, inv, s_out);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_plain(gates_kernel, unsigned(blocks < cap ? blocks : cap), 256, 0,
+                                     st, true, N, D, r, rp, ps, eps, P, ssq, h, inv, s_out);
         if (e != cudaSuccess) return e;
     }
     // 3. up projection, gate and combine
@@ -739,8 +757,8 @@ cudaError_t launch_rank_tc(int64_t N, int D, int r, float eps, void* R, const vo
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
-        e = launch_plain(up_tc_kernel, tiles, kUpThreads, smem, st, mU, mR2, mG, N, D, rp, nbs,
-                         nrb, rows, static_cast<const __nv_bfloat16*>(h),
+        e = launch_plain(up_tc_kernel, tiles, kUpThreads, smem, st, true, mU, mR2, mG, N, D, rp,
+                         nbs, nrb, rows, static_cast<const __nv_bfloat16*>(h),
                          static_cast<const float*>(inv), static_cast<__nv_bfloat16*>(x));
         if (e != cudaSuccess) return e;
     }
