@@ -132,3 +132,27 @@ def test_paper_rank_full_size_sampled():
                                      rng.choice(w.n_tokens, 1022, replace=False)]))
     _check(*fused_case(w, rows=rows), plain_too=True)
     assert gr.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("N,D,r", [(20000, 256, 64), (3000, 2560, 320)])
+def test_repeatable(N, D, r):
+    """The same step on the same inputs, three times: R', x and s bit-identical. The order in which
+    CTAs finish changes from run to run and must not reach the result (no sum depends on it).
+    20000 tokens give each write-pass CTA several units, 3000 one."""
+    w = wl.Workload("tcrep", N, D, r, "bf16", y_std=0.5, seed=79)
+    R0 = to_torch(wl.make_state(w))
+    y = to_torch(wl.make_y(w))
+    sp = torch.from_numpy(wl.make_s_prev(w)).cuda()
+    t = params_to_torch(wl.make_params(w, 1, 5.0))
+    P = gr.pack_params(t["gamma"], t["w_down"], t["w_up"], t["w_write"], torch.bfloat16, w.eps)
+    outs = []
+    for _ in range(3):
+        Rt = R0.clone()
+        x, s = gr.write_then_read(Rt, y, sp, P)
+        torch.cuda.synchronize()
+        outs.append((Rt, x, s))
+    for Rt, x, s in outs[1:]:
+        assert torch.equal(Rt, outs[0][0])
+        assert torch.equal(x, outs[0][1])
+        assert torch.equal(s, outs[0][2])
+    assert gr.device_status(clear=True) == 0
