@@ -55,10 +55,10 @@ def test_tile_rows_and_waves(N, D, r):
     tokens give the write pass tiles of about 106 rows (the rows past a tile's own are loaded,
     never stored) and 20000 tokens run the up projection in two waves of 66-row tiles; every
     row against the oracle, so a row stored twice or never, or a neighbour's rows leaking into
-    a tile, fails."""
+    a tile, fails; against the plain definition too (about 3e-3 on a GB300)."""
     w = wl.Workload("tcrows", N, D, r, "bf16", y_std=0.5, seed=73)
     assert gr.kernel_path(N, D, r, torch.bfloat16) == "tc_bf16"
-    _check(*fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=False)
+    _check(*fused_case(w, random_gamma=True, weight_mult=5.0), plain_too=True)
     assert gr.device_status(clear=True) == 0
 
 
